@@ -1,0 +1,429 @@
+#!/usr/bin/env python3
+"""Benchmark of the QSA hot path on one GB300 (or N independent replicas).
+
+One step = one decode verify window of QSA attention: block scores -> top-k
+-> split-KV chunk attention -> log-sum-exp merge (four launches), on the
+workload "5 rows (4 drafts + 1), 24 q heads / 4 KV heads, head_dim 128,
+32,768 filled int8 K/V cells, 64-cell blocks, top-k 4,096 cells, 64-cell
+chunks".  The metric is decode KV GB/s: the algorithmic bytes a window must
+read (every filled K code and scale for the scores, plus the union of the
+selected visible cells' K+V codes and scales for the attention) per second.
+L2 (129 MB) is flushed by writing a 256 MB buffer before every timed step,
+outside the timed events.
+
+The prompt side (2,048 queries against 32,768 cells, 24/4 heads, int8 K/V,
+on the tensor cores) is reported in the "prompt" object of the same line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (plain FP64 numpy, the build's
+correctness reference) on this machine's host cores, on a bounded sample of the
+same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+# The oracle legs run single-threaded (reported as cores = 1).
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "QSA attn: decode KV GB/s (% HBM peak); prompt int8 TOPS (% peak)"
+WORKLOAD = ("decode verify window: 5 rows, 24 q heads / 4 KV heads, head_dim 128, 32,768 int8 K/V cells, "
+            "64-cell blocks, top-k 4,096 cells, 64-cell chunks")
+PROMPT_WORKLOAD = "prompt chunk: 2,048 queries at 30,720..32,767 over 32,768 int8 K/V cells, 24/4 heads"
+L2_FLUSH_BYTES = 256 << 20
+K_ROW, KS_ROW, V_ROW, VS_ROW = 128, 8, 128, 8
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def algorithmic_bytes(case, ids, n_sel):
+    """(a1 bytes, a3 bytes) of one window: every filled K code + scale once; the union over rows
+    of each pool's selected visible cells, K+V codes + scales, once per KV head."""
+    a1 = sum(p.n_filled * p.n_kv_heads * (K_ROW + KS_ROW) for p in case.pools)
+    a3 = 0
+    for pi, pool in enumerate(case.pools):
+        cells = set()
+        for t in range(case.n_rows):
+            if case.row_pool[t] != pi:
+                continue
+            sel = np.asarray(ids[t][: n_sel[t]])
+            cells.update(sel[sel <= case.row_pos[t]].tolist())
+        a3 += len(cells) * pool.n_kv_heads * (K_ROW + KS_ROW + V_ROW + VS_ROW)
+    return a1, a3
+
+
+def prompt_flops(case, call):
+    """(issued, logical) FLOPs of one prompt call: unmasked (query, cell) pairs x q heads x
+    2 products x 2 * 128 FLOP, issued twice (fp16 hi and lo parts of the non-code operand)."""
+    _, n_q, pos0 = call
+    pairs = sum(pos0 + i + 1 for i in range(n_q)) * case.n_q_heads
+    logical = pairs * 2 * 2 * 128
+    return 2 * logical, logical
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) != 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def kernel_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged since."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            d = json.load(f)[kernel]
+        src = os.path.join(ROOT, "sparse_selection_attention_gb300", "csrc", d["source"])
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        return int(d["dram_bytes_per_launch"]) if sha == d["source_sha"] else None
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------ distributed
+
+def dist_init():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return 0, 1, 0
+    import torch
+    import torch.distributed as dist
+    rank, local = int(os.environ["RANK"]), int(os.environ.get("LOCAL_RANK", "0"))
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    if backend == "nccl":
+        torch.cuda.set_device(local)
+    dist.init_process_group(backend=backend)
+    return rank, ws, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU oracle legs
+
+def oracle_window_seconds(case, budget_s: float):
+    """Times the oracle's full decode window repeatedly for about budget_s seconds."""
+    import oracle as O
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        O.decode_window(case)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            return el / reps, reps
+
+
+def cpu_baseline(case, bytes_per_window, budget_s=12.0):
+    sec, reps = oracle_window_seconds(case, budget_s)
+    return {"value": bytes_per_window / sec / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"full decode window (all 4 steps, 5 rows) x {reps}, {sec * 1e3:.0f} ms each, FP64 numpy"}
+
+
+def prompt_cpu_baseline(pcase, call, flops_issued, budget_s=8.0):
+    import oracle as O
+    rng = np.random.default_rng(0)
+    i0, n_q, pos0 = call
+    rows, t0 = [], time.perf_counter()
+    q = pcase.q[i0:i0 + n_q]
+    while time.perf_counter() - t0 < budget_s:
+        r = int(rng.integers(0, n_q))
+        O.prompt_attention(pcase.pool, q, pos0, rows=[r])
+        rows.append(r)
+    el = time.perf_counter() - t0
+    pairs = sum(pos0 + r + 1 for r in rows) * pcase.n_q_heads
+    per_pair = flops_issued / (sum(pos0 + i + 1 for i in range(n_q)) * pcase.n_q_heads)
+    return {"value": pairs * per_pair / el / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": f"{len(rows)} random query rows of the 2,048-query call, all heads, FP64 numpy"}
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args):
+    import torch
+
+    import sparse_selection_attention_gb300 as qsa
+
+    rank, ws, local = dist_init()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    hbm_peak, tc_peak, peak_src = peaks()
+
+    case = W.verify_window()
+    pools = [qsa.DevicePool.upload(p, dev) for p in case.pools]
+    win = qsa.DecodeWindow(pools, case.row_pool, case.n_q_heads, case.block_cells, case.k_cells, case.chunk_cells,
+                           n_chunks=case.n_chunks, max_blocks=case.max_blocks, device=dev)
+    q = torch.from_numpy(case.q).to(dev)
+    row_pos = torch.from_numpy(case.row_pos).to(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(args.warmup):
+        win.run(q, row_pos)
+    torch.cuda.synchronize()
+    ids = win.ids.cpu().numpy()
+    n_sel = win.n_sel.cpu().numpy()
+    a1, a3 = algorithmic_bytes(case, [ids[t] for t in range(case.n_rows)], n_sel)
+    bytes_step = a1 + a3
+
+    # ---- device-timed steps, per-kernel events on the launching stream
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for k in range(K):
+            flush.zero_()
+            e = ev[k]
+            e[0].record(stream)
+            qsa.block_scores(win.pools, win.row_pool, q, win.block_cells, win.scores)
+            e[1].record(stream)
+            qsa.topk(win.scores, win.n_filled, win.block_cells, win.k_cells, win.ids, win.n_sel)
+            e[2].record(stream)
+            qsa.decode_attn(win.pools, win.row_pool, q, row_pos, win.ids, win.n_sel, win.k_cells, win.chunk_cells,
+                            win.n_chunks, win.partials)
+            e[3].record(stream)
+            qsa.attn_merge(win.partials, win.n_sel, win.n_rows, win.n_q_heads, win.chunk_cells, win.n_chunks,
+                           win.out, win.lse)
+            e[4].record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+    per = np.array([[ev[k][j].elapsed_time(ev[k][j + 1]) for j in range(4)] for k in range(K)])  # ms
+    step_ms = float(per.sum(axis=1).mean())
+    step_ms = max_over_ranks(step_ms, ws)
+    names = ["block_scores", "topk", "decode_attn", "attn_merge"]
+    kern_ms = per.mean(axis=0)
+    value = bytes_step * ws / (step_ms * 1e-3) / 1e9
+
+    dom = int(np.argmax(kern_ms))
+    dom_bytes = {0: a1, 2: a3}.get(dom)
+    roofline = None
+    if dom_bytes is not None:
+        ach = dom_bytes / (kern_ms[dom] * 1e-3) / 1e9
+        roofline = {"kernel": names[dom], "bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
+                    "frac": ach / hbm_peak, "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes": dom_bytes,
+                    "traffic": kernel_traffic(names[dom])}
+    kernels = {}
+    for j, n in enumerate(names):
+        d = {"us": float(kern_ms[j] * 1e3), "share": float(kern_ms[j] / kern_ms.sum())}
+        b = {0: a1, 2: a3}.get(j)
+        if b is not None:
+            d["algorithmic_bytes"] = b
+            d["GB/s"] = b / (kern_ms[j] * 1e-3) / 1e9
+            d["frac_hbm"] = d["GB/s"] / hbm_peak
+        kernels[n] = d
+
+    # ---- end to end through the public API with pinned host buffers
+    q_h = torch.from_numpy(case.q).pin_memory()
+    pos_h = torch.from_numpy(case.row_pos).pin_memory()
+    out_h = torch.empty(win.out.shape, dtype=torch.float32).pin_memory()
+    lse_h = torch.empty(win.lse.shape, dtype=torch.float32).pin_memory()
+    q_d = torch.empty_like(q)
+    pos_d = torch.empty_like(row_pos)
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    torch.cuda.synchronize()
+    for k in range(K):
+        flush.zero_()
+        e2e_ev[k][0].record(stream)
+        q_d.copy_(q_h, non_blocking=True)
+        pos_d.copy_(pos_h, non_blocking=True)
+        win.run(q_d, pos_d)
+        out_h.copy_(win.out, non_blocking=True)
+        lse_h.copy_(win.lse, non_blocking=True)
+        e2e_ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = float(np.mean([a.elapsed_time(b) for a, b in e2e_ev]))
+    e2e_ms = max_over_ranks(e2e_ms, ws)
+    h2d = q_h.numel() * 4 + pos_h.numel() * 4
+    d2h = out_h.numel() * 4 + lse_h.numel() * 4
+
+    # ---- prompt side
+    prompt = None
+    if not args.no_prompt:
+        pcase = W.prompt_int8()
+        call = pcase.calls[0]
+        ppool = qsa.DevicePool.upload(pcase.pool, dev)
+        pq = torch.from_numpy(pcase.q).to(dev)
+        pout = torch.empty((call[1], pcase.n_q_heads, 128), device=dev)
+        plse = torch.empty((call[1], pcase.n_q_heads), device=dev)
+        for _ in range(2):
+            qsa.prompt_attn(ppool, pq, call[2], pout, plse)
+        torch.cuda.synchronize()
+        P = max(3, args.steps // 10)
+        pev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(P)]
+        for k in range(P):
+            flush.zero_()
+            pev[k][0].record(stream)
+            qsa.prompt_attn(ppool, pq, call[2], pout, plse)
+            pev[k][1].record(stream)
+        torch.cuda.synchronize()
+        if qsa.get_device_error() != 0:
+            raise RuntimeError("prompt kernel reported a device error")
+        p_ms = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in pev])), ws)
+        issued, logical = prompt_flops(pcase, call)
+        ach = issued / (p_ms * 1e-3) / 1e12
+        prompt = {"workload": PROMPT_WORKLOAD, "ms_per_call": p_ms, "value": ach * ws, "unit": "TFLOP/s",
+                  "logical_TFLOP/s": logical / (p_ms * 1e-3) / 1e12 * ws, "dtype": "f16 (exact int8 codes)",
+                  "roofline": {"kernel": "prompt_attn", "bound": "tensor", "achieved": ach, "peak": tc_peak,
+                               "unit": "TFLOP/s", "frac": ach / tc_peak,
+                               "peak_source": f"{peak_src} bf16_tflops (fp16 dense rate = bf16)",
+                               "traffic": kernel_traffic("prompt_attn")}}
+        if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+            prompt["cpu_baseline"] = prompt_cpu_baseline(pcase, call, issued)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
+        "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded; shapes of the pages' workloads)",
+        "config": {"workload": WORKLOAD, "rows": case.n_rows, "q_heads": case.n_q_heads, "kv_heads": 4,
+                   "cells": 32768, "k_cells": case.k_cells, "chunk_cells": case.chunk_cells,
+                   "bytes_per_step": bytes_step, "scores_bytes": a1, "attention_union_bytes": a3,
+                   "l2": "flushed (256 MB write) before every timed step, outside the events",
+                   "parallelism": f"{ws} independent replica(s)" if ws > 1 else "1 GPU"},
+        "frac_of_hbm_peak": value / ws / hbm_peak,
+        "roofline": roofline,
+        "kernels": kernels,
+        "e2e": {"value": bytes_step * ws / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 4 * K,
+        "clocks": clocks.summary(),
+        "prompt": prompt,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(case, bytes_step)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    case = W.verify_window()
+    import oracle as O
+    res = O.decode_window(case)
+    a1, a3 = algorithmic_bytes(case, res["ids"], res["n_sel"])
+    bytes_step = a1 + a3
+    for _ in range(args.warmup):
+        O.decode_window(case)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        O.decode_window(case)
+    el = time.perf_counter() - t0
+    ms = el / args.steps * 1e3
+    value = bytes_step / (ms * 1e-3) / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded; shapes of the pages' workloads)",
+        "config": {"workload": WORKLOAD, "bytes_per_step": bytes_step},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "full decode window per step (block scores, full-sort top-k, chunk partials, "
+                                   "merge; FP64 numpy, one thread)"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prompt", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

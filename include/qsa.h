@@ -1,0 +1,228 @@
+/*
+ * qsa.h -- C ABI of the GB300 (sm_103a) QSA attention library.
+ *
+ * QSA ("sparse selection") attention reads a paged KV cache whose K and V are
+ * stored as int8 codes (or int8 K with 4-bit V) with one fp32 scale per
+ * (cell, KV head, dim group).  The decode side scores 64-cell blocks, keeps
+ * the cells of the top-scoring blocks, runs split-KV attention over them in
+ * chunks and merges the chunks by log-sum-exp.  The prompt side runs causal
+ * attention of a chunk of many queries over the whole cached context.
+ *
+ * Sources (pull-request pages of the "Strata" inference engine):
+ *   #1888  "QSA decode attention: split each query's cells across blocks on
+ *           the int8 mma path" -- Summary, What changed.
+ *   #2075  "QSA decode attention: PR #540's two-cells-per-step chunk kernel on
+ *           every CUDA card and a bounded merge" -- Summary, Bit for bit.
+ *   #600   "qsa_prompt_attn: tensor-core kernel for Volta" -- description.
+ *   #2806  "sycl: decode QSA selection and attention in fewer, shorter
+ *           launches" -- Summary (switch table), What changed.
+ *   #1367  "prompt attention: STRATA_PROMPT_ATTN_IMMA=1 - the int8-KV kernel
+ *           on INT8 tensor cores" -- What it does.
+ *
+ * Conventions shared by every call
+ *   - Memory is owned by the caller.  Pointers marked (dev) are device
+ *     pointers on the current CUDA device, (host) are host pointers read
+ *     before the call returns.  No call allocates device memory.
+ *   - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
+ *     stream.  Work is enqueued asynchronously on it.
+ *   - Arguments are validated on the host before anything is enqueued.  Any
+ *     status other than QSA_OK means nothing was enqueued, except
+ *     QSA_ERR_CUDA, which reports a failed launch (as #1888 What changed:
+ *     the launcher returns without launching when it cannot serve a call).
+ *   - head_dim is 128.  K scales cover 64-dim groups; int8 V scales 64-dim
+ *     groups, 4-bit V scales 32-dim groups.
+ *   - Results are deterministic: the same inputs and sizes give the same bits
+ *     on every run (fixed reduction orders; #2075 Bit for bit).
+ */
+#ifndef QSA_GB300_H
+#define QSA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  QSA_OK = 0,
+  QSA_ERR_ARG = 1,          /* invalid argument (null pointer, bad size, misaligned) */
+  QSA_ERR_UNSUPPORTED = 2,  /* valid request outside this build's limits */
+  QSA_ERR_SCRATCH = 3,      /* caller's scratch buffer is too small */
+  QSA_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+  QSA_ERR_DEVICE = 5        /* a kernel reported an error through the device error word */
+} qsa_status;
+
+/* Limits of this build (host-validated). */
+#define QSA_HEAD_DIM 128
+#define QSA_MAX_POOLS 4          /* pool sets per launch (#2806 What changed: up to four) */
+#define QSA_MAX_DECODE_ROWS 32   /* rows of one decode window */
+#define QSA_MAX_GROUP 8          /* q heads per KV head on the decode side */
+#define QSA_MAX_TOPK_BLOCKS 32768
+
+/*
+ * One slot's paged KV pool.  All pointers (dev), 16-byte aligned, caller-owned.
+ *   k_codes    int8   [n_pages][n_kv_heads][page_cells][128]
+ *   v_codes    v_bits 8: int8 [n_pages][n_kv_heads][page_cells][128]
+ *              v_bits 4: uint8 [n_pages][n_kv_heads][page_cells][64]; byte j
+ *              holds dim 2j in its low nibble and dim 2j+1 in its high nibble,
+ *              nibble = code + 8 (code in [-8, 7])
+ *   k_scales   fp32   [n_pages][n_kv_heads][page_cells][2]   (64-dim groups)
+ *   v_scales   fp32   [n_pages][n_kv_heads][page_cells][128 / v_group],
+ *              v_group = 64 (v_bits 8) or 32 (v_bits 4)
+ *   page_table int32  [ceil(capacity / page_cells)] logical -> physical page
+ * Logical cell c is at physical page page_table[c / page_cells], offset
+ * c % page_cells.  Cells 0 .. n_filled-1 hold data; others are never read.
+ * (Per-(cell, KV head, 64-dim group) scales: #600 description; paged pool and
+ * one pool per slot: #2806 Summary.)
+ */
+typedef struct {
+  const int8_t* k_codes;
+  const void* v_codes;
+  const float* k_scales;
+  const float* v_scales;
+  const int32_t* page_table;
+  int32_t n_filled;
+  int32_t capacity;
+  int32_t page_cells;   /* multiple of 64 */
+  int32_t n_kv_heads;   /* 1..16 */
+  int32_t head_dim;     /* must be 128 */
+  int32_t v_bits;       /* 8 or 4 */
+} qsa_pool;
+
+/*
+ * qsa_block_scores -- decode block scores of every row of a window, one
+ * launch over all slots' pools (#2806 Summary: scores once per slot; a
+ * block's (query, head) sums reduced together).
+ *   S[t,b] = sum_h (1/n_b) sum_{c in b} sum_{g in G(h)} q[t,g] . K[c,h] / sqrt(128)
+ * where block b holds logical cells [b*B, min((b+1)*B, n_filled)), n_b of
+ * them, K[c,h,d] = kcode * kscale[c,h,d/64], and q head g reads KV head
+ * g / (n_q_heads / n_kv_heads).  (The pages name the step but print no
+ * formula; this is the library's stated definition.)
+ *   pools      (host) [n_pools] descriptors, 1 <= n_pools <= QSA_MAX_POOLS
+ *   row_pool   (host) int32 [n_rows]: pool index of each row
+ *   q          (dev)  fp32 [n_rows][n_q_heads][128]
+ *   scores     (dev)  fp32 [n_rows][max_blocks]; entries b < ceil(n_filled/B)
+ *              of each row's pool are written, the rest are left untouched
+ *   block_cells B in {32, 64, 128, 256}, dividing every pool's page_cells
+ *   max_blocks >= ceil(n_filled / B) of every row's pool
+ * Errors: QSA_ERR_ARG on null/misaligned pointers or bad sizes;
+ * QSA_ERR_UNSUPPORTED past the limits above.
+ */
+qsa_status qsa_block_scores(const qsa_pool* pools, int n_pools, const int32_t* row_pool,
+                            const float* q, int n_rows, int n_q_heads, int block_cells,
+                            float* scores, int max_blocks, void* stream);
+
+/*
+ * qsa_topk -- per row, the cells of the k_cells / B highest-scoring blocks,
+ * in ascending cell id (#2806 Summary: one top-k per window; radix digits on
+ * integer keys, so the ids are the same whatever the kernel).
+ * Order: score descending, ties by block id ascending; -0.0 equals +0.0; a
+ * NaN score ranks below -inf.  Blocks are those b < ceil(n_filled[t] / B).
+ *   scores     (dev)  fp32 [n_rows][max_blocks]
+ *   n_filled   (host) int32 [n_rows]: filled cells of each row's pool
+ *   ids        (dev)  int32 [n_rows][k_cells]: entries [0, n_sel[t]) written
+ *   n_sel      (dev)  int32 [n_rows]: number of ids of each row
+ *   k_cells    multiple of block_cells, >= 0
+ * Errors: QSA_ERR_ARG (bad sizes, k_cells not a multiple of block_cells);
+ * QSA_ERR_UNSUPPORTED when ceil(n_filled/B) > QSA_MAX_TOPK_BLOCKS.
+ */
+qsa_status qsa_topk(const float* scores, int max_blocks, const int32_t* n_filled, int n_rows,
+                    int block_cells, int k_cells, int32_t* ids, int32_t* n_sel, void* stream);
+
+/*
+ * Partials of the decode attention (caller scratch).  For n_rows rows,
+ * n_q_heads heads and n_chunks chunks per (row, head) the buffer holds
+ *   float ml[n_rows][n_q_heads][n_chunks][2]      (m, l) of each chunk
+ *   float o [n_rows][n_q_heads][n_chunks][128]    unnormalised sum p * V
+ * back to back (o starts at byte offset 8 * n_rows * n_q_heads * n_chunks).
+ * An empty chunk (no visible cell) has m = -inf, l = 0, o = 0.
+ */
+size_t qsa_decode_partials_bytes(int n_rows, int n_q_heads, int n_chunks);
+
+/*
+ * qsa_decode_attn -- split-KV chunk attention over the selected cells
+ * (#2075 Summary: chunk kernel over the selection, empty chunks marked;
+ * #1888 Summary: one query's cells split among blocks, ~2 blocks per SM).
+ * Chunk j of row t is ids[t][j*C .. min((j+1)*C, n_sel[t])).  For every q
+ * head g and chunk j < ceil(n_sel[t] / C), over the chunk's cells c with
+ * c <= row_pos[t]:
+ *   z_c = q[t,g] . K[c, kv(g)] / sqrt(128),  m = max z,  l = sum exp(z - m),
+ *   o = sum exp(z - m) V[c, kv(g)]
+ * with V[c,h,d] = vcode * vscale[c,h,d/v_group].  Chunks at or past
+ * ceil(n_sel[t] / C) are not written.
+ *   pools, row_pool  as qsa_block_scores
+ *   q          (dev)  fp32 [n_rows][n_q_heads][128]
+ *   row_pos    (dev)  int32 [n_rows]: each row's own cell (causal, inclusive)
+ *   ids        (dev)  int32 [n_rows][k_cells], ids < the row pool's n_filled
+ *   n_sel      (dev)  int32 [n_rows], 0 <= n_sel <= k_cells
+ *   chunk_cells C: multiple of 16, 16 <= C <= 1024
+ *   n_chunks   chunks per (row, head) in the partials, >= ceil(k_cells / C)
+ *   partials   (dev)  scratch, partials_bytes >= qsa_decode_partials_bytes()
+ * Errors: QSA_ERR_ARG, QSA_ERR_UNSUPPORTED (group > QSA_MAX_GROUP, rows >
+ * QSA_MAX_DECODE_ROWS), QSA_ERR_SCRATCH (partials too small).
+ */
+qsa_status qsa_decode_attn(const qsa_pool* pools, int n_pools, const int32_t* row_pool,
+                           const float* q, const int32_t* row_pos, const int32_t* ids,
+                           const int32_t* n_sel, int n_rows, int n_q_heads, int k_cells,
+                           int chunk_cells, int n_chunks, void* partials, size_t partials_bytes,
+                           void* stream);
+
+/*
+ * qsa_attn_merge -- log-sum-exp merge of the chunk partials in chunk order,
+ * visiting only chunks j < ceil(n_sel[t] / C) and skipping empty ones
+ * (#1888 What changed: splits merged in split order; #2075 Summary:
+ * attn_merge_v2 skips chunks marked empty; #2806 Summary: the merge folds
+ * only the chunks its selection reaches).
+ *   M = max m_j, L = sum l_j exp(m_j - M), out = sum o_j exp(m_j - M) / L,
+ *   lse = M + ln L; no live chunk: out = 0, lse = -inf.
+ *   partials   (dev)  as written by qsa_decode_attn with the same sizes
+ *   n_sel      (dev)  int32 [n_rows]
+ *   out        (dev)  fp32 [n_rows][n_q_heads][128]
+ *   lse        (dev)  fp32 [n_rows][n_q_heads], may be NULL
+ */
+qsa_status qsa_attn_merge(const void* partials, const int32_t* n_sel, int n_rows, int n_q_heads,
+                          int chunk_cells, int n_chunks, float* out, float* lse, void* stream);
+
+/*
+ * qsa_prompt_attn -- causal attention of a chunk of n_q queries over the
+ * cached context, on the tensor cores (#1367 What it does: both products on
+ * the tensor cores with an exact split of the non-code operand; #600
+ * description: a chunk of queries against the whole context).
+ * Query i sits at position q_pos0 + i and sees cells 0 .. q_pos0 + i:
+ *   out[i,g] = sum_c softmax_c(q[i,g] . K[c,kv(g)] / sqrt(128)) V[c,kv(g)]
+ *   lse[i,g] = ln sum_c exp(...)
+ *   pool       (host) one descriptor; page_cells multiple of 64
+ *   q          (dev)  fp32 [n_q][n_q_heads][128]
+ *   out        (dev)  fp32 [n_q][n_q_heads][128]
+ *   lse        (dev)  fp32 [n_q][n_q_heads], may be NULL
+ *   q_pos0 >= 0, q_pos0 + n_q <= pool->n_filled
+ * Errors: QSA_ERR_ARG, QSA_ERR_UNSUPPORTED (n_q_heads / n_kv_heads > 128).
+ * A kernel whose internal wait runs out sets the device error word (see
+ * qsa_get_device_error) and leaves its outputs incomplete.
+ */
+qsa_status qsa_prompt_attn(const qsa_pool* pool, const float* q, int n_q, int q_pos0,
+                           int n_q_heads, float* out, float* lse, void* stream);
+
+/*
+ * qsa_get_device_error -- synchronises `stream`, then reads and clears the
+ * device error word of the current device.  *code = 0 when no kernel
+ * reported an error; otherwise a nonzero code (1 = a bounded wait inside
+ * the prompt kernel ran out).  Returns QSA_ERR_DEVICE when *code != 0.
+ */
+qsa_status qsa_get_device_error(int32_t* code, void* stream);
+
+/* Test hook: limit, in nanoseconds, of each bounded wait inside the kernels
+ * (default 2e9).  0 makes the first wait give up at once, which exercises the
+ * error path without a hang.  Affects later launches on all devices. */
+void qsa_set_wait_limit_ns(uint64_t ns);
+
+const char* qsa_status_str(qsa_status s);
+
+/* ABI version of this header (major * 100 + minor). */
+int qsa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QSA_GB300_H */

@@ -1,0 +1,261 @@
+// C ABI of the QSA library: host-side validation and launches.
+//
+// Every entry point validates all host-visible arguments before it enqueues
+// anything; a non-OK status (other than QSA_ERR_CUDA) means nothing was
+// enqueued ("#1888 QSA decode attention", What changed: the launcher returns
+// without launching when it cannot serve the call).
+#include <cstdio>
+#include <mutex>
+#include <vector>
+
+#include "kernels.h"
+
+namespace qsa {
+
+namespace {
+unsigned long long g_wait_limit_ns = 2000000000ull;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct DeviceInfo {
+  int sms = 0;
+  int smem_optin = 0;
+};
+
+DeviceInfo& device_info() {
+  static std::mutex mu;
+  static std::vector<DeviceInfo> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(mu);
+  if ((int)cache.size() <= dev) cache.resize(dev + 1);
+  DeviceInfo& d = cache[dev];
+  if (d.sms == 0) {
+    cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (d.sms <= 0) d.sms = 1;
+  }
+  return d;
+}
+
+qsa_status check_pool(const qsa_pool& p, bool need_v) {
+  if (!p.k_codes || !p.k_scales || !p.page_table || (need_v && (!p.v_codes || !p.v_scales))) return QSA_ERR_ARG;
+  if (!aligned16(p.k_codes) || !aligned16(p.k_scales) || (need_v && (!aligned16(p.v_codes) || !aligned16(p.v_scales))))
+    return QSA_ERR_ARG;
+  if (p.head_dim != QSA_HEAD_DIM) return QSA_ERR_UNSUPPORTED;
+  if (p.v_bits != 8 && p.v_bits != 4) return QSA_ERR_ARG;
+  if (p.page_cells <= 0 || p.page_cells % 64 != 0) return QSA_ERR_ARG;
+  if (p.n_kv_heads < 1 || p.n_kv_heads > 16) return QSA_ERR_UNSUPPORTED;
+  if (p.capacity < 0 || p.n_filled < 0 || p.n_filled > p.capacity) return QSA_ERR_ARG;
+  return QSA_OK;
+}
+
+PoolDev to_dev(const qsa_pool& p) {
+  PoolDev d;
+  d.k_codes = p.k_codes;
+  d.v_codes = static_cast<const uint8_t*>(p.v_codes);
+  d.k_scales = p.k_scales;
+  d.v_scales = p.v_scales;
+  d.page_table = p.page_table;
+  d.n_filled = p.n_filled;
+  d.page_cells = p.page_cells;
+  d.v_bits = p.v_bits;
+  return d;
+}
+
+// Shared checks of the pool set and row mapping of a decode window.
+qsa_status check_window(const qsa_pool* pools, int n_pools, const int32_t* row_pool, int n_rows,
+                        int n_q_heads, bool need_v) {
+  if (!pools || !row_pool) return QSA_ERR_ARG;
+  if (n_pools < 1 || n_pools > QSA_MAX_POOLS) return QSA_ERR_UNSUPPORTED;
+  if (n_rows < 1) return QSA_ERR_ARG;
+  if (n_rows > QSA_MAX_DECODE_ROWS) return QSA_ERR_UNSUPPORTED;
+  for (int i = 0; i < n_pools; ++i) {
+    const qsa_status s = check_pool(pools[i], need_v);
+    if (s != QSA_OK) return s;
+    if (pools[i].n_kv_heads != pools[0].n_kv_heads) return QSA_ERR_ARG;
+  }
+  for (int t = 0; t < n_rows; ++t)
+    if (row_pool[t] < 0 || row_pool[t] >= n_pools) return QSA_ERR_ARG;
+  const int Hkv = pools[0].n_kv_heads;
+  if (n_q_heads < 1 || n_q_heads % Hkv != 0) return QSA_ERR_ARG;
+  if (n_q_heads / Hkv > QSA_MAX_GROUP) return QSA_ERR_UNSUPPORTED;
+  return QSA_OK;
+}
+
+qsa_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return QSA_OK;
+  fprintf(stderr, "qsa: CUDA error %s\n", cudaGetErrorString(e));
+  return QSA_ERR_CUDA;
+}
+
+}  // namespace
+
+int device_sm_count() { return device_info().sms; }
+int device_max_smem_optin() { return device_info().smem_optin; }
+unsigned long long wait_limit_ns() { return g_wait_limit_ns; }
+void set_wait_limit_ns(unsigned long long ns) { g_wait_limit_ns = ns; }
+
+}  // namespace qsa
+
+using namespace qsa;
+
+extern "C" {
+
+qsa_status qsa_block_scores(const qsa_pool* pools, int n_pools, const int32_t* row_pool, const float* q,
+                            int n_rows, int n_q_heads, int block_cells, float* scores, int max_blocks,
+                            void* stream) {
+  qsa_status s = check_window(pools, n_pools, row_pool, n_rows, n_q_heads, false);
+  if (s != QSA_OK) return s;
+  if (!q || !scores) return QSA_ERR_ARG;
+  if (block_cells != 32 && block_cells != 64 && block_cells != 128 && block_cells != 256) return QSA_ERR_ARG;
+  ScoresParams p{};
+  p.n_pools = n_pools;
+  p.unit_begin[0] = 0;
+  for (int i = 0; i < n_pools; ++i) {
+    if (pools[i].page_cells % block_cells != 0) return QSA_ERR_ARG;
+    const int nb = (pools[i].n_filled + block_cells - 1) / block_cells;
+    if (nb > max_blocks) return QSA_ERR_ARG;
+    p.pools[i] = to_dev(pools[i]);
+    p.unit_begin[i + 1] = p.unit_begin[i] + nb;
+  }
+  p.total_units = p.unit_begin[n_pools];
+  for (int t = 0; t < n_rows; ++t) p.row_pool[t] = row_pool[t];
+  p.n_rows = n_rows;
+  p.n_q_heads = n_q_heads;
+  p.n_kv_heads = pools[0].n_kv_heads;
+  p.block_cells = block_cells;
+  p.max_blocks = max_blocks;
+  p.q = q;
+  p.scores = scores;
+  if (block_scores_smem_bytes(n_rows, p.n_kv_heads) > (size_t)device_max_smem_optin()) return QSA_ERR_UNSUPPORTED;
+  return from_cuda(launch_block_scores(p, static_cast<cudaStream_t>(stream)));
+}
+
+qsa_status qsa_topk(const float* scores, int max_blocks, const int32_t* n_filled, int n_rows, int block_cells,
+                    int k_cells, int32_t* ids, int32_t* n_sel, void* stream) {
+  if (!scores || !n_filled || !ids || !n_sel) return QSA_ERR_ARG;
+  if (n_rows < 1) return QSA_ERR_ARG;
+  if (n_rows > QSA_MAX_DECODE_ROWS) return QSA_ERR_UNSUPPORTED;
+  if (block_cells < 1 || k_cells < 0 || k_cells % block_cells != 0) return QSA_ERR_ARG;
+  TopkParams p{};
+  int max_nb = 1;
+  for (int t = 0; t < n_rows; ++t) {
+    if (n_filled[t] < 0) return QSA_ERR_ARG;
+    const int nb = (n_filled[t] + block_cells - 1) / block_cells;
+    if (nb > max_blocks) return QSA_ERR_ARG;
+    if (nb > QSA_MAX_TOPK_BLOCKS) return QSA_ERR_UNSUPPORTED;
+    max_nb = nb > max_nb ? nb : max_nb;
+    p.n_filled[t] = n_filled[t];
+  }
+  p.scores = scores;
+  p.max_blocks = max_blocks;
+  p.n_rows = n_rows;
+  p.block_cells = block_cells;
+  p.k_cells = k_cells;
+  p.ids = ids;
+  p.n_sel = n_sel;
+  if (topk_smem_bytes(max_nb) > (size_t)device_max_smem_optin()) return QSA_ERR_UNSUPPORTED;
+  return from_cuda(launch_topk(p, max_nb, static_cast<cudaStream_t>(stream)));
+}
+
+size_t qsa_decode_partials_bytes(int n_rows, int n_q_heads, int n_chunks) {
+  if (n_rows <= 0 || n_q_heads <= 0 || n_chunks <= 0) return 0;
+  return sizeof(float) * (size_t)n_rows * n_q_heads * n_chunks * (2 + QSA_HEAD_DIM);
+}
+
+qsa_status qsa_decode_attn(const qsa_pool* pools, int n_pools, const int32_t* row_pool, const float* q,
+                           const int32_t* row_pos, const int32_t* ids, const int32_t* n_sel, int n_rows,
+                           int n_q_heads, int k_cells, int chunk_cells, int n_chunks, void* partials,
+                           size_t partials_bytes, void* stream) {
+  qsa_status s = check_window(pools, n_pools, row_pool, n_rows, n_q_heads, true);
+  if (s != QSA_OK) return s;
+  if (!q || !row_pos || !ids || !n_sel || !partials) return QSA_ERR_ARG;
+  if (!aligned16(partials)) return QSA_ERR_ARG;
+  if (k_cells < 0 || chunk_cells < 16 || chunk_cells > 1024 || chunk_cells % 16 != 0) return QSA_ERR_ARG;
+  const int need_chunks = (k_cells + chunk_cells - 1) / chunk_cells;
+  if (n_chunks < need_chunks || n_chunks < 1) return QSA_ERR_ARG;
+  if (partials_bytes < qsa_decode_partials_bytes(n_rows, n_q_heads, n_chunks)) return QSA_ERR_SCRATCH;
+  AttnParams p{};
+  for (int i = 0; i < n_pools; ++i) p.pools[i] = to_dev(pools[i]);
+  for (int t = 0; t < n_rows; ++t) p.row_pool[t] = row_pool[t];
+  p.q = q;
+  p.row_pos = row_pos;
+  p.ids = ids;
+  p.n_sel = n_sel;
+  p.n_rows = n_rows;
+  p.n_q_heads = n_q_heads;
+  p.n_kv_heads = pools[0].n_kv_heads;
+  p.k_cells = k_cells;
+  p.chunk_cells = chunk_cells;
+  p.n_chunks = n_chunks;
+  p.ml = static_cast<float*>(partials);
+  p.o = p.ml + (size_t)n_rows * n_q_heads * n_chunks * 2;
+  return from_cuda(launch_decode_attn(p, static_cast<cudaStream_t>(stream)));
+}
+
+qsa_status qsa_attn_merge(const void* partials, const int32_t* n_sel, int n_rows, int n_q_heads,
+                          int chunk_cells, int n_chunks, float* out, float* lse, void* stream) {
+  if (!partials || !n_sel || !out) return QSA_ERR_ARG;
+  if (n_rows < 1 || n_q_heads < 1 || n_chunks < 1) return QSA_ERR_ARG;
+  if (n_rows > QSA_MAX_DECODE_ROWS) return QSA_ERR_UNSUPPORTED;
+  if (chunk_cells < 16 || chunk_cells > 1024 || chunk_cells % 16 != 0) return QSA_ERR_ARG;
+  MergeParams p{};
+  p.ml = static_cast<const float*>(partials);
+  p.o = p.ml + (size_t)n_rows * n_q_heads * n_chunks * 2;
+  p.n_sel = n_sel;
+  p.n_rows = n_rows;
+  p.n_q_heads = n_q_heads;
+  p.chunk_cells = chunk_cells;
+  p.n_chunks = n_chunks;
+  p.out = out;
+  p.lse = lse;
+  return from_cuda(launch_attn_merge(p, static_cast<cudaStream_t>(stream)));
+}
+
+qsa_status qsa_prompt_attn(const qsa_pool* pool, const float* q, int n_q, int q_pos0, int n_q_heads, float* out,
+                           float* lse, void* stream) {
+  if (!pool || !q || !out) return QSA_ERR_ARG;
+  qsa_status s = check_pool(*pool, true);
+  if (s != QSA_OK) return s;
+  if (n_q < 0 || q_pos0 < 0 || (long long)q_pos0 + n_q > pool->n_filled) return QSA_ERR_ARG;
+  if (n_q_heads < 1 || n_q_heads % pool->n_kv_heads != 0) return QSA_ERR_ARG;
+  if (n_q_heads / pool->n_kv_heads > 128) return QSA_ERR_UNSUPPORTED;
+  if (n_q == 0) return QSA_OK;
+  PromptParams p{};
+  p.pool = to_dev(*pool);
+  p.n_kv_heads = pool->n_kv_heads;
+  p.n_q_heads = n_q_heads;
+  p.n_q = n_q;
+  p.q_pos0 = q_pos0;
+  p.q = q;
+  p.out = out;
+  p.lse = lse;
+  p.wait_limit_ns = wait_limit_ns();
+  return from_cuda(launch_prompt_attn(p, static_cast<cudaStream_t>(stream)));
+}
+
+qsa_status qsa_get_device_error(int32_t* code, void* stream) {
+  if (!code) return QSA_ERR_ARG;
+  const qsa_status s = from_cuda(read_and_clear_device_error(code, static_cast<cudaStream_t>(stream)));
+  if (s != QSA_OK) return s;
+  return *code ? QSA_ERR_DEVICE : QSA_OK;
+}
+
+void qsa_set_wait_limit_ns(uint64_t ns) { set_wait_limit_ns(ns); }
+
+const char* qsa_status_str(qsa_status s) {
+  switch (s) {
+    case QSA_OK: return "ok";
+    case QSA_ERR_ARG: return "invalid argument";
+    case QSA_ERR_UNSUPPORTED: return "unsupported by this build";
+    case QSA_ERR_SCRATCH: return "scratch buffer too small";
+    case QSA_ERR_CUDA: return "CUDA error";
+    case QSA_ERR_DEVICE: return "device error word set";
+  }
+  return "unknown status";
+}
+
+int qsa_abi_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,66 @@
+// Kernel parameter blocks and launchers (internal to the library).
+#pragma once
+
+#include "common.cuh"
+
+namespace qsa {
+
+struct ScoresParams {
+  PoolDev pools[QSA_MAX_POOLS];
+  int unit_begin[QSA_MAX_POOLS + 1];  // prefix sums of each pool's block count
+  int row_pool[QSA_MAX_DECODE_ROWS];
+  int n_pools, total_units;
+  int n_rows, n_q_heads, n_kv_heads, block_cells, max_blocks;
+  const float* q;
+  float* scores;
+};
+
+struct TopkParams {
+  const float* scores;
+  int max_blocks;
+  int n_filled[QSA_MAX_DECODE_ROWS];
+  int n_rows, block_cells, k_cells;
+  int32_t* ids;
+  int32_t* n_sel;
+};
+
+struct AttnParams {
+  PoolDev pools[QSA_MAX_POOLS];
+  int row_pool[QSA_MAX_DECODE_ROWS];
+  const float* q;
+  const int32_t* row_pos;
+  const int32_t* ids;
+  const int32_t* n_sel;
+  int n_rows, n_q_heads, n_kv_heads, k_cells, chunk_cells, n_chunks;
+  float* ml;  // [n_rows][n_q_heads][n_chunks][2]
+  float* o;   // [n_rows][n_q_heads][n_chunks][128]
+};
+
+struct MergeParams {
+  const float* ml;
+  const float* o;
+  const int32_t* n_sel;
+  int n_rows, n_q_heads, chunk_cells, n_chunks;
+  float* out;
+  float* lse;
+};
+
+struct PromptParams {
+  PoolDev pool;
+  int n_kv_heads, n_q_heads, n_q, q_pos0;
+  const float* q;
+  float* out;
+  float* lse;
+  unsigned long long wait_limit_ns;
+};
+
+size_t block_scores_smem_bytes(int n_rows, int n_kv_heads);
+size_t topk_smem_bytes(int max_nb);
+cudaError_t launch_block_scores(const ScoresParams& p, cudaStream_t stream);
+cudaError_t launch_topk(const TopkParams& p, int max_nb, cudaStream_t stream);
+cudaError_t launch_decode_attn(const AttnParams& p, cudaStream_t stream);
+cudaError_t launch_attn_merge(const MergeParams& p, cudaStream_t stream);
+cudaError_t launch_prompt_attn(const PromptParams& p, cudaStream_t stream);
+cudaError_t read_and_clear_device_error(int32_t* code, cudaStream_t stream);
+
+}  // namespace qsa

@@ -1,0 +1,106 @@
+"""The C-ABI library loads, exports every symbol include/qsa.h declares, and its
+host-side validation rejects bad calls before anything is enqueued.  No test
+here launches a kernel or needs a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sparse_selection_attention_gb300 as qsa
+from sparse_selection_attention_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return qsa.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "qsa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qsa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("qsa_block_scores", "qsa_topk", "qsa_decode_attn", "qsa_attn_merge", "qsa_prompt_attn"):
+        assert n in names
+    assert sorted(qsa.EXPORTS) == sorted(names)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_pure_host_calls(lib):
+    assert qsa.abi_version() == 100
+    assert qsa.status_str(qsa.QSA_ERR_SCRATCH) == "scratch buffer too small"
+    assert qsa.decode_partials_bytes(5, 24, 64) == 4 * 5 * 24 * 64 * 130
+    assert qsa.decode_partials_bytes(0, 24, 64) == 0
+
+
+def _pool(**kw):
+    base = dict(k_codes=16, v_codes=32, k_scales=48, v_scales=64, page_table=80, n_filled=100, capacity=256,
+                page_cells=256, n_kv_heads=4, head_dim=128, v_bits=8)
+    base.update(kw)
+    return qsa.QsaPoolC(*[base[f] for f, _ in qsa.QsaPoolC._fields_])
+
+
+def _scores_call(lib, pools, row_pool, R=2, Hq=24, B=64, q=16, scores=32, max_blocks=4):
+    arr = (qsa.QsaPoolC * len(pools))(*pools)
+    rp = (ctypes.c_int32 * len(row_pool))(*row_pool)
+    return lib.qsa_block_scores(arr, len(pools), rp, q, R, Hq, B, scores, max_blocks, None)
+
+
+def test_block_scores_validation(lib):
+    ok_pool = _pool()
+    assert _scores_call(lib, [_pool(k_codes=None)], [0, 0]) == qsa.QSA_ERR_ARG
+    assert _scores_call(lib, [_pool(k_codes=17)], [0, 0]) == qsa.QSA_ERR_ARG          # misaligned
+    assert _scores_call(lib, [_pool(head_dim=64)], [0, 0]) == qsa.QSA_ERR_UNSUPPORTED
+    assert _scores_call(lib, [ok_pool], [0, 1]) == qsa.QSA_ERR_ARG                     # row -> missing pool
+    assert _scores_call(lib, [ok_pool], [0, 0], Hq=25) == qsa.QSA_ERR_ARG              # Hq % Hkv
+    assert _scores_call(lib, [ok_pool], [0, 0], Hq=40) == qsa.QSA_ERR_UNSUPPORTED      # group 10 > 8
+    assert _scores_call(lib, [ok_pool], [0, 0], B=48) == qsa.QSA_ERR_ARG
+    assert _scores_call(lib, [ok_pool], [0, 0], max_blocks=1) == qsa.QSA_ERR_ARG        # 2 blocks needed
+    assert _scores_call(lib, [ok_pool] * 5, [0, 0]) == qsa.QSA_ERR_UNSUPPORTED          # > 4 pools
+
+
+def test_topk_validation(lib):
+    nf = (ctypes.c_int32 * 2)(100, 200)
+    assert lib.qsa_topk(16, 4, nf, 2, 64, 100, 32, 48, None) == qsa.QSA_ERR_ARG    # k not multiple of B
+    assert lib.qsa_topk(16, 3, nf, 2, 64, 128, 32, 48, None) == qsa.QSA_ERR_ARG    # 4 blocks > max_blocks 3
+    assert lib.qsa_topk(None, 4, nf, 2, 64, 128, 32, 48, None) == qsa.QSA_ERR_ARG
+    big = (ctypes.c_int32 * 1)(64 * 40000)
+    assert lib.qsa_topk(16, 40000, big, 1, 64, 128, 32, 48, None) == qsa.QSA_ERR_UNSUPPORTED
+    many = (ctypes.c_int32 * 33)(*([100] * 33))
+    assert lib.qsa_topk(16, 4, many, 33, 64, 128, 32, 48, None) == qsa.QSA_ERR_UNSUPPORTED
+
+
+def test_decode_attn_validation(lib):
+    pools = (qsa.QsaPoolC * 1)(_pool())
+    rp = (ctypes.c_int32 * 2)(0, 0)
+    need = qsa.decode_partials_bytes(2, 24, 4)
+    args = lambda **kw: [pools, 1, rp, 16, 32, 48, 64, 2, 24, kw.get("k", 256), kw.get("C", 64),
+                         kw.get("n", 4), kw.get("part", 80), kw.get("nbytes", need), None]
+    assert lib.qsa_decode_attn(*args(nbytes=need - 4)) == qsa.QSA_ERR_SCRATCH
+    assert lib.qsa_decode_attn(*args(n=3)) == qsa.QSA_ERR_ARG          # fewer chunks than k / C
+    assert lib.qsa_decode_attn(*args(C=40)) == qsa.QSA_ERR_ARG
+    assert lib.qsa_decode_attn(*args(part=84)) == qsa.QSA_ERR_ARG      # misaligned scratch
+    assert lib.qsa_decode_attn(*args(part=None)) == qsa.QSA_ERR_ARG
+    assert lib.qsa_attn_merge(None, 16, 2, 24, 64, 4, 32, None, None) == qsa.QSA_ERR_ARG
+    assert lib.qsa_attn_merge(16, 16, 2, 24, 40, 4, 32, None, None) == qsa.QSA_ERR_ARG
+
+
+def test_prompt_validation(lib):
+    pool = _pool(n_filled=1000, capacity=1024)
+    assert lib.qsa_prompt_attn(ctypes.byref(pool), 16, 100, 950, 24, 32, None, None) == qsa.QSA_ERR_ARG
+    assert lib.qsa_prompt_attn(ctypes.byref(pool), 16, 100, -1, 24, 32, None, None) == qsa.QSA_ERR_ARG
+    assert lib.qsa_prompt_attn(ctypes.byref(pool), 16, 100, 0, 26, 32, None, None) == qsa.QSA_ERR_ARG
+    bad = _pool(page_cells=96)
+    assert lib.qsa_prompt_attn(ctypes.byref(bad), 16, 10, 0, 24, 32, None, None) == qsa.QSA_ERR_ARG
+    assert lib.qsa_prompt_attn(ctypes.byref(pool), 16, 0, 0, 24, 32, None, None) == qsa.QSA_OK   # nothing to do

@@ -1,0 +1,112 @@
+"""GPU parity of the tensor-core prompt attention against the FP64 oracle,
+through the C ABI: small ragged cases in full, the two full-size prompt
+workloads on sampled rows, the cross-path identity with decode, and the
+bounded-wait error path (a wait limit of 0 makes the kernel give up at its
+first wait, report through the device error word and leave the context
+usable; no fault, trap or hang is involved)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import sparse_selection_attention_gb300 as qsa
+import workloads as W
+from _parity import assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+def run_prompt(case, call):
+    i0, n, pos0 = call
+    pool = qsa.DevicePool.upload(case.pool)
+    q = torch.from_numpy(np.ascontiguousarray(case.q[i0:i0 + n])).cuda()
+    out = torch.full((n, case.n_q_heads, 128), float("nan"), device="cuda")
+    lse = torch.full((n, case.n_q_heads), float("nan"), device="cuda")
+    qsa.prompt_attn(pool, q, pos0, out, lse)
+    torch.cuda.synchronize()
+    assert qsa.get_device_error() == 0
+    return out.cpu().numpy(), lse.cpu().numpy()
+
+
+@pytest.mark.parametrize("n_ctx,n_q,Hq,Hkv,v_bits,page_cells", [
+    (700, 150, 24, 4, 8, 256),     # G = 6: 21 queries per CTA, ragged last CTA and tile
+    (513, 40, 8, 2, 4, 64),        # 4-bit V, G = 4
+    (64, 64, 2, 1, 8, 64),         # one tile, queries from position 0
+    (1000, 37, 6, 6, 8, 128),      # G = 1
+    (333, 333, 16, 1, 4, 64),      # G = 16, whole context is the prompt
+])
+def test_small_prompt_full(n_ctx, n_q, Hq, Hkv, v_bits, page_cells):
+    case = W.prompt_case(name="p", seed=n_ctx + n_q, n_ctx=n_ctx, n_q=n_q, n_q_heads=Hq, n_kv_heads=Hkv,
+                         v_bits=v_bits, page_cells=page_cells, capacity=n_ctx + 200)
+    out, lse = run_prompt(case, case.calls[0])
+    ref_out, ref_lse = O.prompt_attention(case.pool, case.q, case.calls[0][2])
+    assert_close(out, ref_out, "out")
+    assert_close(lse, ref_lse, "lse")
+
+
+def _sample_rows(n_q, k, seed):
+    rng = np.random.default_rng(seed)
+    rows = set(rng.choice(n_q, size=k, replace=False).tolist()) | {0, 1, n_q - 1}
+    return sorted(rows)
+
+
+def test_prompt_int8_full_size_sampled():
+    """2,048 queries against 32,768 cells, 24/4 heads (the prompt workload of the bench)."""
+    case = W.prompt_int8()
+    out, lse = run_prompt(case, case.calls[0])
+    rows = _sample_rows(2048, 40, 0)
+    ref_out, ref_lse = O.prompt_attention(case.pool, case.q, case.calls[0][2], rows=rows)
+    assert_close(out[rows], ref_out, "out")
+    assert_close(lse[rows], ref_lse, "lse")
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+
+
+def test_prompt_k8v4_last_call_sampled():
+    """8,192 queries against 131,072 cells in four calls; the last call checked on sampled rows."""
+    case = W.prompt_k8v4()
+    call = case.calls[-1]
+    out, lse = run_prompt(case, call)
+    rows = _sample_rows(call[1], 24, 1)
+    q_call = case.q[call[0]:call[0] + call[1]]
+    ref_out, ref_lse = O.prompt_attention(case.pool, q_call, call[2], rows=rows)
+    assert_close(out[rows], ref_out, "out")
+    assert_close(lse[rows], ref_lse, "lse")
+    assert np.isfinite(out).all()
+
+
+def test_prompt_row_equals_decode_with_all_cells():
+    """Cross-path: a prompt row at position p equals decode with top-k = all cells at p."""
+    case = W.prompt_case(name="x", seed=21, n_ctx=640, n_q=5, n_q_heads=24, n_kv_heads=4)
+    out, lse = run_prompt(case, case.calls[0])
+    dcase = W.DecodeCase("x", [case.pool], np.zeros(5, np.int32), case.q, np.arange(635, 640, dtype=np.int32),
+                         24, 64, 640, 64, 10, 10)
+    from _parity import upload_case
+    win, q, row_pos = upload_case(dcase)
+    win.run(q, row_pos)
+    torch.cuda.synchronize()
+    assert_close(out, win.out.cpu().numpy(), "prompt vs decode out")
+    assert_close(lse, win.lse.cpu().numpy(), "prompt vs decode lse")
+
+
+def test_prompt_deterministic():
+    case = W.prompt_case(name="d", seed=2, n_ctx=900, n_q=100, n_q_heads=24, n_kv_heads=4)
+    a = run_prompt(case, case.calls[0])
+    b = run_prompt(case, case.calls[0])
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_bounded_wait_reports_and_context_survives():
+    case = W.prompt_case(name="w", seed=4, n_ctx=300, n_q=30, n_q_heads=8, n_kv_heads=2)
+    pool = qsa.DevicePool.upload(case.pool)
+    q = torch.from_numpy(case.q).cuda()
+    out = torch.zeros((30, 8, 128), device="cuda")
+    try:
+        qsa.set_wait_limit_ns(0)
+        qsa.prompt_attn(pool, q, case.calls[0][2], out)
+        assert qsa.get_device_error() == 1
+    finally:
+        qsa.set_wait_limit_ns(2_000_000_000)
+    assert qsa.get_device_error() == 0          # read-and-clear
+    out2, lse2 = run_prompt(case, case.calls[0])  # the context is still usable
+    ref_out, _ = O.prompt_attention(case.pool, case.q, case.calls[0][2])
+    assert_close(out2, ref_out, "out after error path")
