@@ -204,6 +204,32 @@ qsa_status qsa_attn_merge(const void* partials, const int32_t* n_sel, int n_rows
 qsa_status qsa_prompt_attn(const qsa_pool* pool, const float* q, int n_q, int q_pos0,
                            int n_q_heads, float* out, float* lse, void* stream);
 
+/* Size of the library-owned scratch of qsa_decode_attn_noalloc (8 MiB). */
+#define QSA_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * qsa_decode_attn_noalloc -- qsa_decode_attn followed by qsa_attn_merge, for
+ * callers that cannot allocate device memory: it takes inputs and outputs
+ * only and keeps the chunk partials in a fixed array of
+ * QSA_NOALLOC_SCRATCH_BYTES that the library owns on every GPU it is loaded
+ * on (held until the process exits).  The pages have no counterpart of this
+ * call; it exists for engines whose device memory is all reserved up front
+ * and for plugins whose interface carries no allocator.
+ *   Arguments as qsa_decode_attn and qsa_attn_merge, with
+ *   n_chunks = ceil(k_cells / chunk_cells) (at least 1).
+ *   Requires n_rows * n_q_heads * n_chunks * 130 * 4 <= QSA_NOALLOC_SCRATCH_BYTES,
+ *   else QSA_ERR_SCRATCH with nothing enqueued.  No cudaMalloc / cudaFree.
+ *   The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   All calls share the one array: calls that overlap on the GPU (other
+ *   streams, other threads) race on it and must be serialised by the caller.
+ *   Nothing in it needs clearing between calls.
+ */
+qsa_status qsa_decode_attn_noalloc(const qsa_pool* pools, int n_pools, const int32_t* row_pool,
+                                   const float* q, const int32_t* row_pos, const int32_t* ids,
+                                   const int32_t* n_sel, int n_rows, int n_q_heads, int k_cells,
+                                   int chunk_cells, float* out, float* lse, void* stream);
+
 /*
  * qsa_get_device_error -- synchronises `stream`, then reads and clears the
  * device error word of the current device.  *code = 0 when no kernel

@@ -25,7 +25,9 @@ MAX_DECODE_ROWS = 32
 EXPORTS = [
     "qsa_block_scores", "qsa_topk", "qsa_decode_partials_bytes", "qsa_decode_attn", "qsa_attn_merge",
     "qsa_prompt_attn", "qsa_get_device_error", "qsa_set_wait_limit_ns", "qsa_status_str", "qsa_abi_version",
+    "qsa_decode_attn_noalloc",
 ]
+NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class QsaError(RuntimeError):
@@ -64,6 +66,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qsa_decode_attn.argtypes = [pool_p, i, i32p, p, p, p, p, i, i, i, i, i, p, sz, p]
     lib.qsa_attn_merge.argtypes = [p, p, i, i, i, i, p, p, p]
     lib.qsa_prompt_attn.argtypes = [pool_p, p, i, i, i, p, p, p]
+    lib.qsa_decode_attn_noalloc.argtypes = [pool_p, i, i32p, p, p, p, p, i, i, i, i, p, p, p]
     lib.qsa_get_device_error.argtypes = [i32p, p]
     lib.qsa_set_wait_limit_ns.argtypes = [u64]
     lib.qsa_set_wait_limit_ns.restype = None
@@ -71,7 +74,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qsa_status_str.restype = ctypes.c_char_p
     lib.qsa_abi_version.argtypes = []
     for name in ("qsa_block_scores", "qsa_topk", "qsa_decode_attn", "qsa_attn_merge", "qsa_prompt_attn",
-                 "qsa_get_device_error", "qsa_abi_version"):
+                 "qsa_get_device_error", "qsa_abi_version", "qsa_decode_attn_noalloc"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -173,6 +176,20 @@ def prompt_attn(pool: DevicePool, q: torch.Tensor, q_pos0: int, out: torch.Tenso
     pc = pool.c()
     _check(load().qsa_prompt_attn(ctypes.byref(pc), _ptr(q), n_q, q_pos0, Hq, _ptr(out), _ptr(lse),
                                   _stream(stream)), "qsa_prompt_attn")
+
+
+def decode_attn_noalloc(pools: Sequence[DevicePool], row_pool: Sequence[int], q: torch.Tensor,
+                        row_pos: torch.Tensor, ids: torch.Tensor, n_sel: torch.Tensor, k_cells: int,
+                        chunk_cells: int, out: torch.Tensor, lse: Optional[torch.Tensor] = None,
+                        stream=None) -> None:
+    """Chunk attention + merge with the library's own fixed scratch, for callers that cannot allocate
+    device memory (an engine whose memory is all reserved up front, a plugin with no allocator).
+    Calls that overlap on the GPU share that scratch and race; the first call on a device should come
+    before any stream capture."""
+    R, Hq, _ = q.shape
+    _check(load().qsa_decode_attn_noalloc(_pools_c(pools), len(pools), _i32_array(row_pool), _ptr(q),
+                                          _ptr(row_pos), _ptr(ids), _ptr(n_sel), R, Hq, k_cells, chunk_cells,
+                                          _ptr(out), _ptr(lse), _stream(stream)), "qsa_decode_attn_noalloc")
 
 
 def get_device_error(stream=None) -> int:

@@ -18,7 +18,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libqsa_gb300.so")
-SOURCES = ["api.cu", "block_scores.cu", "topk.cu", "decode_attn.cu", "prompt_attn.cu"]
+SOURCES = ["api.cu", "block_scores.cu", "topk.cu", "decode_attn.cu", "prompt_attn.cu", "noalloc.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in ("common.cuh", "kernels.h", "tc.cuh")] + [
     os.path.join(ROOT, "include", "qsa.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -1,0 +1,48 @@
+"""The decode attention entry point that allocates nothing.
+
+Some callers cannot lend the library a scratch buffer: an engine that
+reserves all device memory up front for its KV pool, or a plugin whose
+interface carries only input and output pointers.  qsa_decode_attn_noalloc
+serves them with a fixed scratch array the library owns.  These tests call it
+through the C ABI twice in a row and compare each result with the existing
+entry points (qsa_decode_attn + qsa_attn_merge with a caller buffer), within
+the tolerance the other parity tests use.  This file is collected last."""
+import numpy as np
+import pytest
+import torch
+
+import sparse_selection_attention_gb300 as qsa
+import workloads as W
+from _parity import assert_close, upload_case
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("make", [W.verify_window, W.batched_long_context, W.tiny_dense_decode])
+def test_noalloc_matches_caller_scratch_twice(make):
+    case = make()
+    win, q, row_pos = upload_case(case)
+    win.run(q, row_pos)            # caller-scratch path: scores, top-k, attention, merge
+    torch.cuda.synchronize()
+    ref_out, ref_lse = win.out.cpu().numpy(), win.lse.cpu().numpy()
+    for _ in range(2):
+        out = torch.full_like(win.out, float("nan"))
+        lse = torch.full_like(win.lse, float("nan"))
+        qsa.decode_attn_noalloc(win.pools, win.row_pool, q, row_pos, win.ids, win.n_sel, case.k_cells,
+                                case.chunk_cells, out, lse)
+        torch.cuda.synchronize()
+        assert_close(out.cpu().numpy(), ref_out, "noalloc out")
+        assert_close(lse.cpu().numpy(), ref_lse, "noalloc lse")
+
+
+def test_noalloc_refuses_windows_past_its_scratch():
+    case = W.verify_window()
+    win, q, row_pos = upload_case(case)
+    win.run(q, row_pos)
+    torch.cuda.synchronize()
+    out = torch.zeros_like(win.out)
+    # 16-cell chunks of 4,096 cells: 5 x 24 x 256 x 520 B > 8 MiB
+    with pytest.raises(qsa.QsaError) as err:
+        qsa.decode_attn_noalloc(win.pools, win.row_pool, q, row_pos, win.ids, win.n_sel, case.k_cells, 16, out)
+    assert err.value.status == qsa.QSA_ERR_SCRATCH
+    assert torch.count_nonzero(out) == 0
