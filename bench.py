@@ -8,8 +8,9 @@ workload "5 rows (4 drafts + 1), 24 q heads / 4 KV heads, head_dim 128,
 chunks".  The metric is decode KV GB/s: the algorithmic bytes a window must
 read (every filled K code and scale for the scores, plus the union of the
 selected visible cells' K+V codes and scales for the attention) per second.
-L2 (129 MB) is flushed by writing a 256 MB buffer before every timed step,
-outside the timed events.
+L2 (129 MB) is flushed before every timed step, outside the timed events, by
+writing a 256 MB buffer and then reading another 256 MB buffer (so the dirty
+lines of the write are already written back when the step starts).
 
 The prompt side (2,048 queries against 32,768 cells, 24/4 heads, int8 K/V,
 on the tensor cores) is reported in the "prompt" object of the same line.
@@ -88,6 +89,7 @@ class ClockSampler:
     """nvidia-smi clock / throttle samples while the timed region runs."""
     FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    INTERVAL_MS = 20
 
     def __init__(self, index: int):
         self.index = index
@@ -98,7 +100,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", str(self.INTERVAL_MS)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except Exception:
@@ -108,6 +110,11 @@ class ClockSampler:
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append(line.strip())
+
+    def wait_first_sample(self, timeout_s: float = 5.0):
+        t0 = time.time()
+        while self.proc is not None and not self.lines and time.time() - t0 < timeout_s:
+            time.sleep(0.02)
 
     def __exit__(self, *a):
         if self.proc is not None:
@@ -220,6 +227,12 @@ def prompt_cpu_baseline(pcase, call, flops_issued, budget_s=8.0):
 
 # ------------------------------------------------------------------ our arm
 
+def gpu_sleep(us: float = 400.0):
+    """Keeps the GPU busy for about `us` microseconds (outside any timed event)."""
+    import torch
+    torch.cuda._sleep(int(us * 2.1e3))
+
+
 def run_ours(args):
     import torch
 
@@ -237,11 +250,20 @@ def run_ours(args):
     q = torch.from_numpy(case.q).to(dev)
     row_pos = torch.from_numpy(case.row_pos).to(dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    clean = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush_l2():
+        """Writes 256 MB (evicts L2), then reads another 256 MB so that the dirty lines are written
+        back before the timed work starts (it then finds a cold, clean L2)."""
+        flush.zero_()
+        clean.sum()
     stream = torch.cuda.current_stream(dev)
 
+    clocks = ClockSampler(local).__enter__()
     for _ in range(args.warmup):
         win.run(q, row_pos)
     torch.cuda.synchronize()
+    clocks.wait_first_sample()
     ids = win.ids.cpu().numpy()
     n_sel = win.n_sel.cpu().numpy()
     a1, a3 = algorithmic_bytes(case, [ids[t] for t in range(case.n_rows)], n_sel)
@@ -252,23 +274,21 @@ def run_ours(args):
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
     barrier(ws)
     torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
-        for k in range(K):
-            flush.zero_()
-            e = ev[k]
-            e[0].record(stream)
-            qsa.block_scores(win.pools, win.row_pool, q, win.block_cells, win.scores)
-            e[1].record(stream)
-            qsa.topk(win.scores, win.n_filled, win.block_cells, win.k_cells, win.ids, win.n_sel)
-            e[2].record(stream)
-            qsa.decode_attn(win.pools, win.row_pool, q, row_pos, win.ids, win.n_sel, win.k_cells, win.chunk_cells,
-                            win.n_chunks, win.partials)
-            e[3].record(stream)
-            qsa.attn_merge(win.partials, win.n_sel, win.n_rows, win.n_q_heads, win.chunk_cells, win.n_chunks,
-                           win.out, win.lse)
-            e[4].record(stream)
-        torch.cuda.synchronize()
-        barrier(ws)
+    for k in range(K):
+        flush_l2()
+        gpu_sleep()   # the GPU idles here, outside the events, while the CPU enqueues the whole step
+        e = ev[k]
+        e[0].record(stream)
+        win.scores_step(q)
+        e[1].record(stream)
+        win.topk_step()
+        e[2].record(stream)
+        win.attn_step(q, row_pos)
+        e[3].record(stream)
+        win.merge_step()
+        e[4].record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
     per = np.array([[ev[k][j].elapsed_time(ev[k][j + 1]) for j in range(4)] for k in range(K)])  # ms
     step_ms = float(per.sum(axis=1).mean())
     step_ms = max_over_ranks(step_ms, ws)
@@ -304,7 +324,7 @@ def run_ours(args):
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     torch.cuda.synchronize()
     for k in range(K):
-        flush.zero_()
+        flush_l2()
         e2e_ev[k][0].record(stream)
         q_d.copy_(q_h, non_blocking=True)
         pos_d.copy_(pos_h, non_blocking=True)
@@ -330,10 +350,10 @@ def run_ours(args):
         for _ in range(2):
             qsa.prompt_attn(ppool, pq, call[2], pout, plse)
         torch.cuda.synchronize()
-        P = max(3, args.steps // 10)
+        P = max(3, min(20, args.steps // 10))
         pev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(P)]
         for k in range(P):
-            flush.zero_()
+            flush_l2()
             pev[k][0].record(stream)
             qsa.prompt_attn(ppool, pq, call[2], pout, plse)
             pev[k][1].record(stream)
@@ -352,6 +372,7 @@ def run_ours(args):
         if rank == 0 and ws == 1 and not args.no_cpu_baseline:
             prompt["cpu_baseline"] = prompt_cpu_baseline(pcase, call, issued)
 
+    clocks.__exit__()
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
         "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
@@ -359,7 +380,7 @@ def run_ours(args):
         "config": {"workload": WORKLOAD, "rows": case.n_rows, "q_heads": case.n_q_heads, "kv_heads": 4,
                    "cells": 32768, "k_cells": case.k_cells, "chunk_cells": case.chunk_cells,
                    "bytes_per_step": bytes_step, "scores_bytes": a1, "attention_union_bytes": a3,
-                   "l2": "flushed (256 MB write) before every timed step, outside the events",
+                   "l2": "flushed before every timed step, outside the events: 256 MB write, then 256 MB read",
                    "parallelism": f"{ws} independent replica(s)" if ws > 1 else "1 GPU"},
         "frac_of_hbm_peak": value / ws / hbm_peak,
         "roofline": roofline,
@@ -411,7 +432,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -58,7 +58,7 @@ typedef enum {
 #define QSA_MAX_POOLS 4          /* pool sets per launch (#2806 What changed: up to four) */
 #define QSA_MAX_DECODE_ROWS 32   /* rows of one decode window */
 #define QSA_MAX_GROUP 8          /* q heads per KV head on the decode side */
-#define QSA_MAX_TOPK_BLOCKS 32768
+#define QSA_MAX_TOPK_BLOCKS 16384
 
 /*
  * One slot's paged KV pool.  All pointers (dev), 16-byte aligned, caller-owned.
@@ -101,7 +101,7 @@ typedef struct {
  * formula; this is the library's stated definition.)
  *   pools      (host) [n_pools] descriptors, 1 <= n_pools <= QSA_MAX_POOLS
  *   row_pool   (host) int32 [n_rows]: pool index of each row
- *   q          (dev)  fp32 [n_rows][n_q_heads][128]
+ *   q          (dev)  fp32 [n_rows][n_q_heads][128], 16-byte aligned
  *   scores     (dev)  fp32 [n_rows][max_blocks]; entries b < ceil(n_filled/B)
  *              of each row's pool are written, the rest are left untouched
  *   block_cells B in {32, 64, 128, 256}, dividing every pool's page_cells
@@ -152,7 +152,7 @@ size_t qsa_decode_partials_bytes(int n_rows, int n_q_heads, int n_chunks);
  * with V[c,h,d] = vcode * vscale[c,h,d/v_group].  Chunks at or past
  * ceil(n_sel[t] / C) are not written.
  *   pools, row_pool  as qsa_block_scores
- *   q          (dev)  fp32 [n_rows][n_q_heads][128]
+ *   q          (dev)  fp32 [n_rows][n_q_heads][128], 16-byte aligned
  *   row_pos    (dev)  int32 [n_rows]: each row's own cell (causal, inclusive)
  *   ids        (dev)  int32 [n_rows][k_cells], ids < the row pool's n_filled
  *   n_sel      (dev)  int32 [n_rows], 0 <= n_sel <= k_cells
@@ -193,8 +193,8 @@ qsa_status qsa_attn_merge(const void* partials, const int32_t* n_sel, int n_rows
  *   out[i,g] = sum_c softmax_c(q[i,g] . K[c,kv(g)] / sqrt(128)) V[c,kv(g)]
  *   lse[i,g] = ln sum_c exp(...)
  *   pool       (host) one descriptor; page_cells multiple of 64
- *   q          (dev)  fp32 [n_q][n_q_heads][128]
- *   out        (dev)  fp32 [n_q][n_q_heads][128]
+ *   q          (dev)  fp32 [n_q][n_q_heads][128], 16-byte aligned
+ *   out        (dev)  fp32 [n_q][n_q_heads][128], 16-byte aligned
  *   lse        (dev)  fp32 [n_q][n_q_heads], may be NULL
  *   q_pos0 >= 0, q_pos0 + n_q <= pool->n_filled
  * Errors: QSA_ERR_ARG, QSA_ERR_UNSUPPORTED (n_q_heads / n_kv_heads > 128).

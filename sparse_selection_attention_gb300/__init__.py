@@ -231,16 +231,42 @@ class DecodeWindow:
         self.out = torch.zeros((R, self.n_q_heads, HEAD_DIM), dtype=torch.float32, device=device)
         self.lse = torch.zeros((R, self.n_q_heads), dtype=torch.float32, device=device)
 
+        # ctypes arguments that do not change between steps, built once.
+        self._c_pools = _pools_c(pools)
+        self._c_row_pool = _i32_array(self.row_pool)
+        self._c_n_filled = _i32_array(self.n_filled)
+        self._nbytes = nbytes
+
+    def scores_step(self, q: torch.Tensor, stream=None) -> None:
+        _check(load().qsa_block_scores(self._c_pools, len(self.pools), self._c_row_pool, _ptr(q), self.n_rows,
+                                       self.n_q_heads, self.block_cells, self.scores.data_ptr(), self.max_blocks,
+                                       _stream(stream)), "qsa_block_scores")
+
+    def topk_step(self, stream=None) -> None:
+        _check(load().qsa_topk(self.scores.data_ptr(), self.max_blocks, self._c_n_filled, self.n_rows,
+                               self.block_cells, self.k_cells, self.ids.data_ptr(), self.n_sel.data_ptr(),
+                               _stream(stream)), "qsa_topk")
+
+    def attn_step(self, q: torch.Tensor, row_pos: torch.Tensor, stream=None) -> None:
+        _check(load().qsa_decode_attn(self._c_pools, len(self.pools), self._c_row_pool, _ptr(q), _ptr(row_pos),
+                                      self.ids.data_ptr(), self.n_sel.data_ptr(), self.n_rows, self.n_q_heads,
+                                      self.k_cells, self.chunk_cells, self.n_chunks, self.partials.data_ptr(),
+                                      self._nbytes, _stream(stream)), "qsa_decode_attn")
+
+    def merge_step(self, stream=None) -> None:
+        _check(load().qsa_attn_merge(self.partials.data_ptr(), self.n_sel.data_ptr(), self.n_rows, self.n_q_heads,
+                                     self.chunk_cells, self.n_chunks, self.out.data_ptr(), self.lse.data_ptr(),
+                                     _stream(stream)), "qsa_attn_merge")
+
     def run(self, q: torch.Tensor, row_pos: torch.Tensor, stream=None) -> None:
-        block_scores(self.pools, self.row_pool, q, self.block_cells, self.scores, stream)
-        topk(self.scores, self.n_filled, self.block_cells, self.k_cells, self.ids, self.n_sel, stream)
+        """block scores -> top-k -> chunk attention -> merge, enqueued on one stream."""
+        self.scores_step(q, stream)
+        self.topk_step(stream)
         self.attend(q, row_pos, stream)
 
     def attend(self, q: torch.Tensor, row_pos: torch.Tensor, stream=None) -> None:
-        decode_attn(self.pools, self.row_pool, q, row_pos, self.ids, self.n_sel, self.k_cells, self.chunk_cells,
-                    self.n_chunks, self.partials, stream)
-        attn_merge(self.partials, self.n_sel, self.n_rows, self.n_q_heads, self.chunk_cells, self.n_chunks,
-                   self.out, self.lse, stream)
+        self.attn_step(q, row_pos, stream)
+        self.merge_step(stream)
 
     def partial_views(self):
         """(ml [R, Hq, n_chunks, 2], o [R, Hq, n_chunks, 128]) views of the partials buffer."""

@@ -5,7 +5,9 @@
 // enqueued ("#1888 QSA decode attention", What changed: the launcher returns
 // without launching when it cannot serve the call).
 #include <cstdio>
+#include <map>
 #include <mutex>
+#include <utility>
 #include <vector>
 
 #include "kernels.h"
@@ -92,6 +94,20 @@ qsa_status from_cuda(cudaError_t e) {
 }  // namespace
 
 int device_sm_count() { return device_info().sms; }
+
+cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<int, const void*>, size_t> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  size_t& cur = done[{dev, kernel}];
+  if (bytes <= cur) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) cur = bytes;
+  return e;
+}
 int device_max_smem_optin() { return device_info().smem_optin; }
 unsigned long long wait_limit_ns() { return g_wait_limit_ns; }
 void set_wait_limit_ns(unsigned long long ns) { g_wait_limit_ns = ns; }
@@ -107,7 +123,7 @@ qsa_status qsa_block_scores(const qsa_pool* pools, int n_pools, const int32_t* r
                             void* stream) {
   qsa_status s = check_window(pools, n_pools, row_pool, n_rows, n_q_heads, false);
   if (s != QSA_OK) return s;
-  if (!q || !scores) return QSA_ERR_ARG;
+  if (!q || !scores || !aligned16(q)) return QSA_ERR_ARG;
   if (block_cells != 32 && block_cells != 64 && block_cells != 128 && block_cells != 256) return QSA_ERR_ARG;
   ScoresParams p{};
   p.n_pools = n_pools;
@@ -128,7 +144,10 @@ qsa_status qsa_block_scores(const qsa_pool* pools, int n_pools, const int32_t* r
   p.max_blocks = max_blocks;
   p.q = q;
   p.scores = scores;
-  if (block_scores_smem_bytes(n_rows, p.n_kv_heads) > (size_t)device_max_smem_optin()) return QSA_ERR_UNSUPPORTED;
+  if (!block_scores_supported(p.n_kv_heads, block_cells)) return QSA_ERR_UNSUPPORTED;
+  p.q_rows_per_batch = block_scores_q_rows_per_batch(n_rows, n_q_heads, p.n_kv_heads, block_cells);
+  if (block_scores_smem_bytes(n_rows, n_q_heads, p.n_kv_heads, block_cells) > (size_t)device_max_smem_optin())
+    return QSA_ERR_UNSUPPORTED;
   return from_cuda(launch_block_scores(p, static_cast<cudaStream_t>(stream)));
 }
 
@@ -171,7 +190,7 @@ qsa_status qsa_decode_attn(const qsa_pool* pools, int n_pools, const int32_t* ro
   qsa_status s = check_window(pools, n_pools, row_pool, n_rows, n_q_heads, true);
   if (s != QSA_OK) return s;
   if (!q || !row_pos || !ids || !n_sel || !partials) return QSA_ERR_ARG;
-  if (!aligned16(partials)) return QSA_ERR_ARG;
+  if (!aligned16(partials) || !aligned16(q)) return QSA_ERR_ARG;
   if (k_cells < 0 || chunk_cells < 16 || chunk_cells > 1024 || chunk_cells % 16 != 0) return QSA_ERR_ARG;
   const int need_chunks = (k_cells + chunk_cells - 1) / chunk_cells;
   if (n_chunks < need_chunks || n_chunks < 1) return QSA_ERR_ARG;
@@ -215,7 +234,7 @@ qsa_status qsa_attn_merge(const void* partials, const int32_t* n_sel, int n_rows
 
 qsa_status qsa_prompt_attn(const qsa_pool* pool, const float* q, int n_q, int q_pos0, int n_q_heads, float* out,
                            float* lse, void* stream) {
-  if (!pool || !q || !out) return QSA_ERR_ARG;
+  if (!pool || !q || !out || !aligned16(q) || !aligned16(out)) return QSA_ERR_ARG;
   qsa_status s = check_pool(*pool, true);
   if (s != QSA_OK) return s;
   if (n_q < 0 || q_pos0 < 0 || (long long)q_pos0 + n_q > pool->n_filled) return QSA_ERR_ARG;

@@ -51,5 +51,8 @@ __device__ __forceinline__ float warp_max(float v) {
 // Host-side helpers shared by the launchers.
 int device_sm_count();
 int device_max_smem_optin();
+// Raises a kernel's dynamic shared memory limit to at least `bytes` on the
+// current device; the attribute call is made only when the limit grows.
+cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes);
 
 }  // namespace qsa

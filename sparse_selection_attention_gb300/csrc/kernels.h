@@ -11,6 +11,7 @@ struct ScoresParams {
   int row_pool[QSA_MAX_DECODE_ROWS];
   int n_pools, total_units;
   int n_rows, n_q_heads, n_kv_heads, block_cells, max_blocks;
+  int q_rows_per_batch;   // rows of q staged in shared memory at a time
   const float* q;
   float* scores;
 };
@@ -54,7 +55,9 @@ struct PromptParams {
   unsigned long long wait_limit_ns;
 };
 
-size_t block_scores_smem_bytes(int n_rows, int n_kv_heads);
+size_t block_scores_smem_bytes(int n_rows, int n_q_heads, int n_kv_heads, int block_cells);
+bool block_scores_supported(int n_kv_heads, int block_cells);
+int block_scores_q_rows_per_batch(int n_rows, int n_q_heads, int n_kv_heads, int block_cells);
 size_t topk_smem_bytes(int max_nb);
 cudaError_t launch_block_scores(const ScoresParams& p, cudaStream_t stream);
 cudaError_t launch_topk(const TopkParams& p, int max_nb, cudaStream_t stream);

@@ -516,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const PromptPa
 }  // namespace
 
 cudaError_t launch_prompt_attn(const PromptParams& p, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(prompt_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(prompt_attn_kernel), (size_t)kSmemBytes);
   if (e != cudaSuccess) return e;
   const int G = p.n_q_heads / p.n_kv_heads;
   const int qpc = kM / G;

@@ -10,19 +10,22 @@
 // One CTA per row holds all of the row's keys in shared memory.  Four radix
 // passes of 8 bits (most significant first) find the threshold key T: each
 // pass histograms the digit of the keys still matching the prefix (integer
-// shared atomics: the counts do not depend on their order) and one warp scans
-// the 256 bins from the top to find the digit holding the k-th key.  Blocks
+// shared atomics, aggregated per warp over lanes with equal digits, since
+// scores of one row share their leading bits; the counts do not depend on
+// their order) and one warp scans the 256 bins from the top to find the digit
+// holding the k-th key.  Blocks
 // with key > T are taken, then the lowest-id blocks with key == T.  Two
 // CTA-wide prefix sums over blocks in id order give each chosen block its
-// rank j; every block but the row's last holds exactly B cells, so rank j
-// writes its cells at ids[j*B ..].
+// rank j and a slot in a shared list; every block but the row's last holds
+// exactly B cells, so the CTA then writes the ids coalesced: chosen block j
+// fills ids[j*B ..].
 #include "kernels.h"
 
 namespace qsa {
 
 namespace {
 
-constexpr int kThreads = 1024;
+constexpr int kMaxThreads = 1024;
 
 __device__ __forceinline__ uint32_t score_key(float x) {
   if (x != x) return 0u;                 // NaN ranks below every number
@@ -33,7 +36,7 @@ __device__ __forceinline__ uint32_t score_key(float x) {
 
 // Exclusive CTA-wide prefix sum of one int per thread; also returns the total.
 __device__ __forceinline__ int cta_exclusive_scan(int v, int* warp_tot, int& total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, n_warps = blockDim.x >> 5;
   int inc = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -43,7 +46,7 @@ __device__ __forceinline__ int cta_exclusive_scan(int v, int* warp_tot, int& tot
   if (lane == 31) warp_tot[warp] = inc;
   __syncthreads();
   if (warp == 0) {
-    int w = warp_tot[lane];
+    int w = lane < n_warps ? warp_tot[lane] : 0;
     int wi = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -60,7 +63,8 @@ __device__ __forceinline__ int cta_exclusive_scan(int v, int* warp_tot, int& tot
   return base;
 }
 
-__global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
+__global__ void __launch_bounds__(kMaxThreads) topk_kernel(const TopkParams p) {
+  const int kThreads = blockDim.x;
   extern __shared__ uint32_t keys[];
   __shared__ int hist[256];
   __shared__ int warp_tot[33];
@@ -93,9 +97,14 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
       const int shift = 24 - 8 * pass;
       for (int i = tid; i < 256; i += kThreads) hist[i] = 0;
       __syncthreads();
-      for (int b = tid; b < nb; b += kThreads) {
-        const uint32_t k = keys[b];
-        if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 0xFF], 1);
+      for (int b0 = 0; b0 < nb; b0 += kThreads) {   // warp-uniform trip count
+        const int b = b0 + tid;
+        const uint32_t k = b < nb ? keys[b] : 0u;
+        const bool live = b < nb && (k & mask) == prefix;
+        const unsigned lm = __ballot_sync(0xffffffffu, live);
+        const int digit = live ? (int)((k >> shift) & 0xFF) : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, digit) & lm;
+        if (live && (__ffs(peers) - 1) == (tid & 31)) atomicAdd(&hist[digit], __popc(peers));
       }
       __syncthreads();
       if (tid < 32) {
@@ -156,37 +165,39 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
     }
   }
   const int rank0 = cta_exclusive_scan(chosen, warp_tot, total);
-  bool last_chosen = false;
+  int* sel = reinterpret_cast<int*>(keys + nb);   // chosen block ids in ascending order
   {
     int e = eq_base, j = rank0;
     for (int b = b0; b < b1; ++b) {
       const uint32_t k = keys[b];
       bool c = take_all || k > T;
       if (!take_all && k == T) { c = e < need; ++e; }
-      if (!c) continue;
-      const int n_b = min(B, n_filled - b * B);
-      int32_t* dst = ids + (size_t)j * B;
-      for (int i = 0; i < n_b; ++i) dst[i] = b * B + i;
-      ++j;
-      if (b == nb - 1) last_chosen = true;
+      if (c) sel[j++] = b;
     }
   }
-  // Only the row's last block can hold fewer than B cells.
-  if (b0 <= nb - 1 && nb - 1 < b1) {
+  __syncthreads();
+  // Every block but the row's last holds B cells, so chosen block j fills ids[j*B ..].
+  for (int idx = tid; idx < kb * B; idx += kThreads) {
+    const int cell = sel[idx / B] * B + idx % B;
+    if (cell < n_filled) ids[idx] = cell;
+  }
+  if (tid == 0) {
     const int n_last = n_filled - (nb - 1) * B;
-    p.n_sel[t] = kb * B - (last_chosen ? (B - n_last) : 0);
+    p.n_sel[t] = kb * B - (sel[kb - 1] == nb - 1 ? (B - n_last) : 0);
   }
 }
 
 }  // namespace
 
-size_t topk_smem_bytes(int max_nb) { return sizeof(uint32_t) * (size_t)max_nb; }
+size_t topk_smem_bytes(int max_nb) { return 2 * sizeof(uint32_t) * (size_t)max_nb; }
 
 cudaError_t launch_topk(const TopkParams& p, int max_nb, cudaStream_t stream) {
   const size_t smem = topk_smem_bytes(max_nb);
-  cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(topk_kernel), (size_t)smem);
   if (e != cudaSuccess) return e;
-  topk_kernel<<<p.n_rows, kThreads, smem, stream>>>(p);
+  // About two keys per thread, 128..1024 threads.
+  const int threads = min(kMaxThreads, max(128, ((max_nb + 1) / 2 + 31) / 32 * 32));
+  topk_kernel<<<p.n_rows, threads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
