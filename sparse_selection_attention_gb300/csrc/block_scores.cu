@@ -1,22 +1,25 @@
 // Decode block scores (qsa_block_scores).
 //
-// S[t,b] = sum_h (1/n_b) sum_{c in b} sum_{g in G(h)} q[t,g] . K[c,h] / sqrt(D).
-// The score is linear in K, so a block is read once per window: the kernel
-// forms the fp32 per-dim block sum ksum[h][d] = sum_c kcode*kscale of each KV
-// head, then dots it with qbar[t][h][d] = sum_{g in G(h)} q[t,g,d] for every
-// row of the block's pool ("#2806 sycl: decode QSA selection and attention in
-// fewer, shorter launches", Summary: a block's (query, head) sums are reduced
-// together; scores run once per slot).  HBM-bound: every filled K code and
-// scale is read exactly once per call.
+// S[t,b] = sum_h (1/n_b) sum_{c in b} sum_{g in G(h)} q[t,g] . K[c,h] / sqrt(D)
+//        = sum_h (1/n_b) sum_{c in b} sum_grp kscale[c,h,grp] (qbar[t,h] . kcode[c,h])_grp / sqrt(D),
+// qbar[t,h] = sum_{g in G(h)} q[t,g]: the group's q heads are summed once, and
+// a block is read once per window for all of its slot's rows ("#2806 sycl:
+// decode QSA selection and attention in fewer, shorter launches", Summary: a
+// block's (query, head) sums are reduced together; scores once per slot).
+// HBM-bound: every filled K code and scale is read exactly once per call.
 //
-// A persistent grid of one 512-thread CTA per SM walks the (pool, block)
-// units, several units at a time when a unit needs fewer than 512 threads.
-// Thread (head h, 16-dim slice dq, cell group cg) accumulates 8 cells
-// cg + (B/8) k in registers; the int8 codes become fp32 through the exponent
-// bias (2^23 + 128 + code is exact, so subtracting 2^23 + 128 gives the code).
-// The next units' loads are in flight while the current ones are reduced.
-// Reductions run in a fixed order (cells in order, lane butterflies over 4
-// cell groups, then warps in index order): bitwise reproducible.
+// The per-(cell, row) dot products run on mma.sync m16n8k16: A = K codes of
+// 16 cells (int8 -> fp16, exact), B = qbar 2^f of 8 rows split into fp16
+// hi + lo (both accumulate into one fp32 sum), one accumulator per 64-dim
+// K-scale group.  A persistent grid of one 512-thread CTA per SM walks the
+// (pool, block) units; warp task = (unit, KV head, 16-cell m-tile).  Each
+// thread loads the 64 code bytes of its two cells with four 16-byte loads,
+// straight into registers, and the next unit's loads are in flight while the
+// current one is reduced.  The epilogue weights each cell by its K scales,
+// reduces over cells (lane butterfly), then over the unit's m-tiles and heads
+// with a fixed butterfly: bitwise reproducible.
+#include <cuda_fp16.h>
+
 #include "kernels.h"
 
 namespace qsa {
@@ -24,199 +27,297 @@ namespace qsa {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kCellsPerThread = 8;
+constexpr int kWarps = kThreads / 32;
+constexpr int kTpwMax = 2;   // warp tasks per warp per iteration
+constexpr int kNtMax = 4;    // 8-row n-tiles (rows <= 32)
 
-struct Slice {
-  uint4 codes[kCellsPerThread];
-  float scale[kCellsPerThread];
-  int pi, n_b, b;
+__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+// Two bytes of a biased word (code + 128) -> exact fp16 pair of the codes.
+__device__ __forceinline__ uint32_t byte_pair_h2(uint32_t u, uint32_t sel) {
+  return h2u(__hsub2(u2h(__byte_perm(u, 0x64646464u, sel)), u2h(0x64806480u)));
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ float pow2i(int e) { return __int_as_float((127 + max(-126, min(127, e))) << 23); }
+
+__host__ __device__ inline int round4(int x) { return (x + 3) & ~3; }
+
+// One warp task's operands: codes of cells cb+g and cb+g+8 (dims 64 grp + 16 tq .. +15) and scales.
+struct TaskData {
+  uint4 c[2][2];   // [cell a/b][K-scale group]
+  float2 ks[2];
+};
+
+struct TaskRef {
+  int u_s, h, mt;   // unit slot, KV head, m-tile
   bool live;
 };
 
-// Unit us of super-unit su: pool, block, and this thread's 8 code slices.
-__device__ __forceinline__ void load_slice(const ScoresParams& p, int unit, bool active, Slice& s) {
-  const int B = p.block_cells, Hkv = p.n_kv_heads;
-  s.live = active && unit < p.total_units;
-  if (!s.live) return;
+__device__ __forceinline__ int pool_of(const ScoresParams& p, int unit) {
   int pi = 0;
   while (pi + 1 < p.n_pools && unit >= p.unit_begin[pi + 1]) ++pi;
+  return pi;
+}
+
+__device__ __forceinline__ void load_task(const ScoresParams& p, int unit, const TaskRef& r, TaskData& d) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, tq = lane & 3;
+  const int B = p.block_cells;
+  const int pi = pool_of(p, unit);
   const PoolDev& pool = p.pools[pi];
   const int b = unit - p.unit_begin[pi];
   const int cell0 = b * B;
   const int n_b = min(B, pool.n_filled - cell0);
   const int page = __ldg(pool.page_table + cell0 / pool.page_cells);
-  const int off0 = cell0 % pool.page_cells;
-  const int i = threadIdx.x % (Hkv * B);
-  const int dq = i & 7, ncg = B / 8, cg = (i >> 3) % ncg, h = (i >> 3) / ncg;
-  const long long slot0 = ((long long)page * Hkv + h) * pool.page_cells + off0;
+  const long long slot0 = ((long long)page * p.n_kv_heads + r.h) * pool.page_cells + cell0 % pool.page_cells;
 #pragma unroll
-  for (int k = 0; k < kCellsPerThread; ++k) {
-    const int c = cg + ncg * k;
+  for (int ab = 0; ab < 2; ++ab) {
+    const int c = 16 * r.mt + g + 8 * ab;
     if (c < n_b) {
-      s.codes[k] = __ldg(reinterpret_cast<const uint4*>(pool.k_codes + (slot0 + c) * kD) + dq);
-      s.scale[k] = __ldg(pool.k_scales + (slot0 + c) * 2 + (dq >> 2));
+      const uint4* src = reinterpret_cast<const uint4*>(pool.k_codes + (slot0 + c) * kD);
+      d.c[ab][0] = __ldg(src + tq);
+      d.c[ab][1] = __ldg(src + 4 + tq);
+      d.ks[ab] = __ldg(reinterpret_cast<const float2*>(pool.k_scales) + slot0 + c);
     } else {
-      s.codes[k] = make_uint4(0u, 0u, 0u, 0u);
-      s.scale[k] = 0.f;
+      d.c[ab][0] = d.c[ab][1] = make_uint4(0u, 0u, 0u, 0u);
+      d.ks[ab] = make_float2(0.f, 0.f);
     }
   }
-  s.pi = pi;
-  s.n_b = n_b;
-  s.b = b;
 }
 
-// Byte j of a biased word (code + 128) -> exact float of the code.
-__device__ __forceinline__ float biased_byte_to_f32(uint32_t u, int j) {
-  return __int_as_float(__byte_perm(u, 0x4B000000u, 0x7540 | j)) - 8388736.0f;
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int w) {
+  return w == 0 ? v.x : (w == 1 ? v.y : (w == 2 ? v.z : v.w));
 }
 
+template <int kMaxNt, int kMaxTpw>
 __global__ void __launch_bounds__(kThreads, 1) block_scores_kernel(const ScoresParams p) {
-  extern __shared__ float smem[];
-  const int Hkv = p.n_kv_heads;
-  const int G = p.n_q_heads / Hkv;
-  const int B = p.block_cells;
-  const int U = Hkv * B;                   // threads per unit
-  const int upi = kThreads / U;            // units per iteration
-  const int wph = B / 32;                  // warps per head (4 cell groups each)
-  float* qbar = smem;                                  // [n_rows][Hkv][128]
-  float* red = qbar + p.n_rows * Hkv * kD;             // [upi][Hkv][wph][128]
-  float* ksum = red + upi * Hkv * wph * kD;            // [upi][Hkv][128]
-  const int tid = threadIdx.x, lane = tid & 31;
-  const int us = tid / U;                  // unit slot of this thread
-  const bool active = us < upi;
-  const int i = tid % U;
-  const int dq = i & 7, h = (i >> 3) / (B / 8), wl = ((i >> 3) % (B / 8)) / 4;
+  extern __shared__ __align__(16) float smem[];
+  const int Hkv = p.n_kv_heads, G = p.n_q_heads / Hkv, B = p.block_cells;
+  const int R = p.n_rows, NT = (R + 7) / 8;
+  const int tpu = Hkv * (B / 16);                 // warp tasks per unit (<= 32)
+  const int upi = max(1, kWarps / tpu);           // units per iteration
+  const int tpw = (upi * tpu + kWarps - 1) / kWarps;
+  // smem: B fragments [Hkv][NT][8 k-steps][32 lanes] uint4, 1/f [R][Hkv] (padded to 4), partial sums
+  // [upi][tpu][NT*8], then the staging area for q rows.
+  uint4* bfrag = reinterpret_cast<uint4*>(smem);
+  float* inv_f = reinterpret_cast<float*>(bfrag + Hkv * NT * 8 * 32);
+  float* part = inv_f + round4(R * Hkv);
+  float* qstage = part + upi * tpu * NT * 8;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, tq = lane & 3;
   const int n_super = (p.total_units + upi - 1) / upi;
-
   if ((int)blockIdx.x >= n_super) return;
-  Slice cur, nxt;
-  load_slice(p, blockIdx.x * upi + us, active, cur);
 
-  // q -> shared memory in one coalesced pass (every load in flight at once), then
-  // qbar[t][h][d] = sum over the group's q heads, in head order.
+  TaskRef ref[kMaxTpw];
+#pragma unroll
+  for (int k = 0; k < kMaxTpw; ++k) {
+    const int ti = warp + kWarps * k;
+    ref[k].live = k < tpw && ti < upi * tpu;
+    ref[k].u_s = ti / tpu;
+    ref[k].h = (ti % tpu) / (B / 16);
+    ref[k].mt = ti % (B / 16);
+  }
+  TaskData cur[kMaxTpw], nxt[kMaxTpw];
+#pragma unroll
+  for (int k = 0; k < kMaxTpw; ++k) {
+    const int unit = blockIdx.x * upi + ref[k].u_s;
+    if (ref[k].live && unit < p.total_units) load_task(p, unit, ref[k], cur[k]);
+  }
+
+  // ---- qbar 2^f per (row, head), split fp16 hi/lo, laid out as this kernel's B fragments.
   {
-    float* qs = red;   // the work area is free until the first unit is reduced
     const int row_floats = p.n_q_heads * kD;
-    const int rb = p.q_rows_per_batch;
-    for (int r0 = 0; r0 < p.n_rows; r0 += rb) {
-      const int nr = min(rb, p.n_rows - r0);
+    for (int r0 = 0; r0 < R; r0 += p.q_rows_per_batch) {
+      const int nr = min(p.q_rows_per_batch, R - r0);
       const float4* q4 = reinterpret_cast<const float4*>(p.q + (size_t)r0 * row_floats);
-      for (int k = tid; k < nr * row_floats / 4; k += kThreads) reinterpret_cast<float4*>(qs)[k] = __ldg(q4 + k);
+      for (int k = tid; k < nr * row_floats / 4; k += kThreads) reinterpret_cast<float4*>(qstage)[k] = __ldg(q4 + k);
       __syncthreads();
-      for (int k = tid; k < nr * Hkv * kD; k += kThreads) {
-        const int t = k / (Hkv * kD), hh = (k / kD) % Hkv, d = k % kD;
-        const float* qg = qs + (size_t)t * row_floats + hh * G * kD + d;
-        float s = 0.f;
-        for (int g = 0; g < G; ++g) s += qg[(size_t)g * kD];
-        qbar[(size_t)r0 * Hkv * kD + k] = s;
+      // One warp per (row, head): qbar in registers (4 dims per lane), max |qbar| -> 2^f.
+      for (int rh = warp; rh < nr * Hkv; rh += kWarps) {
+        const int tr = rh / Hkv, h = rh % Hkv, t = r0 + tr;
+        const float* qg = qstage + (size_t)tr * row_floats + h * G * kD;
+        float v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float s = 0.f;
+          for (int gg = 0; gg < G; ++gg) s += qg[gg * kD + 4 * lane + i];
+          v[i] = s;
+        }
+        float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+        amax = warp_max(amax);
+        int e = 0;
+        if (amax > 0.f) frexpf(amax, &e);
+        const int fe = amax > 0.f ? max(-126, min(127, 7 - e)) : 0;
+        const float f = pow2i(fe);
+        if (lane == 0) inv_f[t * Hkv + h] = pow2i(-fe);
+        // dims 4 lane .. +3 = 64 grp + 16 tq' + 4 s' .. : k-step 4 grp + s', fragment lane (row % 8, tq')
+        const int d0 = 4 * lane, grp = d0 >> 6, tqp = (d0 >> 4) & 3, sp = (d0 >> 2) & 3;
+        const int s = 4 * grp + sp, nt = t >> 3, gp = t & 7;
+        const __half2 h01 = __floats2half2_rn(v[0] * f, v[1] * f), h23 = __floats2half2_rn(v[2] * f, v[3] * f);
+        const float2 b01 = __half22float2(h01), b23 = __half22float2(h23);
+        const __half2 l01 = __floats2half2_rn(v[0] * f - b01.x, v[1] * f - b01.y);
+        const __half2 l23 = __floats2half2_rn(v[2] * f - b23.x, v[3] * f - b23.y);
+        bfrag[((h * NT + nt) * 8 + s) * 32 + gp * 4 + tqp] = make_uint4(h2u(h01), h2u(h23), h2u(l01), h2u(l23));
       }
       __syncthreads();
     }
+    for (int k = tid; k < Hkv * 8 * 32; k += kThreads) {   // rows R .. NT*8-1: zero fragments
+      const int h = k / 256, s = (k / 32) % 8, ln = k % 32, row = (NT - 1) * 8 + (ln >> 2);
+      if (row >= R) bfrag[((h * NT + NT - 1) * 8 + s) * 32 + ln] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    __syncthreads();
   }
 
   for (int su = blockIdx.x; su < n_super; su += gridDim.x) {
     const bool more = su + (int)gridDim.x < n_super;
-    if (more) load_slice(p, (su + gridDim.x) * upi + us, active, nxt);
-    else nxt.live = false;
-
-    if (active) {   // warp-uniform: U is a multiple of 32
-      float acc[16];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) acc[j] = 0.f;
-      if (cur.live) {
+    for (int k = 0; k < kMaxTpw; ++k) {
+      const int unit = (su + gridDim.x) * upi + ref[k].u_s;
+      if (more && ref[k].live && unit < p.total_units) load_task(p, unit, ref[k], nxt[k]);
+    }
 #pragma unroll
-        for (int k = 0; k < kCellsPerThread; ++k) {
-          const uint32_t w[4] = {cur.codes[k].x ^ 0x80808080u, cur.codes[k].y ^ 0x80808080u,
-                                 cur.codes[k].z ^ 0x80808080u, cur.codes[k].w ^ 0x80808080u};
+    for (int k = 0; k < kMaxTpw; ++k) {
+      const int unit = su * upi + ref[k].u_s;
+      if (!ref[k].live || unit >= p.total_units) continue;   // warp-uniform
+      const int h = ref[k].h;
+      float d[kMaxNt][2][4];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) acc[j] = fmaf(biased_byte_to_f32(w[j >> 2], j & 3), cur.scale[k], acc[j]);
+      for (int nt = 0; nt < kMaxNt; ++nt)
+#pragma unroll
+        for (int gr = 0; gr < 2; ++gr)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) d[nt][gr][i] = 0.f;
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const int gr = s >> 2, w = s & 3;
+        const uint32_t wa = word_of(cur[k].c[0][gr], w) ^ 0x80808080u;
+        const uint32_t wb = word_of(cur[k].c[1][gr], w) ^ 0x80808080u;
+        uint32_t a[4];
+        a[0] = byte_pair_h2(wa, 0x4140);
+        a[2] = byte_pair_h2(wa, 0x4342);
+        a[1] = byte_pair_h2(wb, 0x4140);
+        a[3] = byte_pair_h2(wb, 0x4342);
+#pragma unroll
+        for (int nt = 0; nt < kMaxNt; ++nt) {
+          if (nt < NT) {
+            const uint4 bf = bfrag[((h * NT + nt) * 8 + s) * 32 + lane];
+            mma16816(d[nt][gr], a, bf.x, bf.y);
+            mma16816(d[nt][gr], a, bf.z, bf.w);
+          }
         }
       }
+      // Weight each cell by its K scales, sum the two cells, reduce over the 8 cell pairs.
+      const float2 ka = cur[k].ks[0], kb = cur[k].ks[1];
+      const int ti = ref[k].u_s * tpu + h * (B / 16) + ref[k].mt;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], 8);
-        acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], 16);
-      }
-      if (lane < 8) {
-        float4* dst = reinterpret_cast<float4*>(red + ((us * Hkv + h) * wph + wl) * kD + dq * 16);
-        dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-        dst[2] = make_float4(acc[8], acc[9], acc[10], acc[11]);
-        dst[3] = make_float4(acc[12], acc[13], acc[14], acc[15]);
+      for (int nt = 0; nt < kMaxNt; ++nt) {
+        if (nt < NT) {
+          float e0 = fmaf(ka.y, d[nt][1][0], ka.x * d[nt][0][0]);
+          e0 += fmaf(kb.y, d[nt][1][2], kb.x * d[nt][0][2]);
+          float e1 = fmaf(ka.y, d[nt][1][1], ka.x * d[nt][0][1]);
+          e1 += fmaf(kb.y, d[nt][1][3], kb.x * d[nt][0][3]);
+#pragma unroll
+          for (int o = 4; o < 32; o <<= 1) {
+            e0 += __shfl_xor_sync(0xffffffffu, e0, o);
+            e1 += __shfl_xor_sync(0xffffffffu, e1, o);
+          }
+          if (g == 0) {
+            const int row = nt * 8 + 2 * tq;
+            part[ti * NT * 8 + row] = row < R ? e0 * inv_f[row * Hkv + h] : 0.f;
+            part[ti * NT * 8 + row + 1] = row + 1 < R ? e1 * inv_f[(row + 1) * Hkv + h] : 0.f;
+          }
+        }
       }
     }
     __syncthreads();
-    for (int k = tid; k < upi * Hkv * kD; k += kThreads) {
-      const int uh = k / kD, d = k % kD;
-      float s = 0.f;
-      for (int w = 0; w < wph; ++w) s += red[(uh * wph + w) * kD + d];
-      ksum[k] = s;
-    }
-    __syncthreads();
-    // Dots: warp -> (unit slot, row) pairs of rows in the unit's pool.
-    for (int pr = tid >> 5; pr < upi * p.n_rows; pr += kThreads / 32) {
-      const int u_s = pr / p.n_rows, t = pr % p.n_rows;
+    // S[t, b]: one warp per (unit slot, row); lane l holds the unit's task l (<= 32 tasks), then a
+    // fixed butterfly over the lanes.
+    for (int pr = warp; pr < upi * R; pr += kWarps) {
+      const int u_s = pr / R, t = pr % R;
       const int unit = su * upi + u_s;
       if (unit >= p.total_units) continue;
-      int pi = 0;
-      while (pi + 1 < p.n_pools && unit >= p.unit_begin[pi + 1]) ++pi;
+      const int pi = pool_of(p, unit);
       if (p.row_pool[t] != pi) continue;
-      const int b = unit - p.unit_begin[pi];
-      const int n_b = min(B, p.pools[pi].n_filled - b * B);
-      float s = 0.f;
-      for (int hh = 0; hh < Hkv; ++hh) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int d = lane + 32 * j;
-          s = fmaf(qbar[(t * Hkv + hh) * kD + d], ksum[(u_s * Hkv + hh) * kD + d], s);
-        }
-      }
+      float s = lane < tpu ? part[(u_s * tpu + lane) * NT * 8 + t] : 0.f;
       s = warp_sum(s);
-      if (lane == 0) p.scores[(size_t)t * p.max_blocks + b] = s * (kInvSqrtD / (float)n_b);
+      if (lane == 0) {
+        const int b = unit - p.unit_begin[pi];
+        const int n_b = min(B, p.pools[pi].n_filled - b * B);
+        p.scores[(size_t)t * p.max_blocks + b] = s * (kInvSqrtD / (float)n_b);
+      }
     }
-    if (more) cur = nxt;
+    if (more) {
+#pragma unroll
+      for (int k = 0; k < kMaxTpw; ++k) cur[k] = nxt[k];
+    }
     __syncthreads();
   }
 }
 
-}  // namespace
-
-// Floats of the work area: the reduction buffers, or at least one row of q (staged there first).
-static size_t block_scores_work_floats(int n_rows, int n_q_heads, int n_kv_heads, int block_cells) {
-  const int upi = kThreads / (n_kv_heads * block_cells);
-  size_t work = (size_t)upi * n_kv_heads * (block_cells / 32) * kD + (size_t)upi * n_kv_heads * kD;
-  const size_t q_row = (size_t)n_q_heads * kD;
-  const size_t q_all = q_row * n_rows;
-  const size_t want = q_all < 16384 ? q_all : (q_row > 16384 ? q_row : 16384);   // up to 64 KB of q at once
-  return work > want ? work : want;
+// Floats of the q staging area: up to 16K floats (64 KB), at least one row of q.
+size_t q_stage_floats(int n_rows, int n_q_heads) {
+  const size_t row = (size_t)n_q_heads * kD, all = row * n_rows;
+  return all < 16384 ? all : (row > 16384 ? row : 16384);
 }
 
+}  // namespace
+
 int block_scores_q_rows_per_batch(int n_rows, int n_q_heads, int n_kv_heads, int block_cells) {
-  const size_t area = block_scores_work_floats(n_rows, n_q_heads, n_kv_heads, block_cells);
-  const int rb = (int)(area / ((size_t)n_q_heads * kD));
+  (void)n_kv_heads;
+  (void)block_cells;
+  const int rb = (int)(q_stage_floats(n_rows, n_q_heads) / ((size_t)n_q_heads * kD));
   return rb < 1 ? 1 : (rb > n_rows ? n_rows : rb);
 }
 
 size_t block_scores_smem_bytes(int n_rows, int n_q_heads, int n_kv_heads, int block_cells) {
-  return sizeof(float) * ((size_t)n_rows * n_kv_heads * kD +
-                          block_scores_work_floats(n_rows, n_q_heads, n_kv_heads, block_cells));
+  const int NT = (n_rows + 7) / 8;
+  const int tpu = n_kv_heads * (block_cells / 16);
+  const int upi = tpu >= kWarps ? 1 : kWarps / tpu;
+  return 16 * (size_t)n_kv_heads * NT * 8 * 32 +
+         4 * ((size_t)round4(n_rows * n_kv_heads) + (size_t)upi * tpu * NT * 8) + 4 * q_stage_floats(n_rows, n_q_heads);
 }
 
 bool block_scores_supported(int n_kv_heads, int block_cells) {
-  return n_kv_heads * block_cells <= kThreads && block_cells == kCellsPerThread * (block_cells / 8) &&
-         (n_kv_heads * block_cells) % 32 == 0 && block_cells >= 32;
+  const int tpu = n_kv_heads * (block_cells / 16);
+  const int upi = tpu >= kWarps ? 1 : kWarps / tpu;
+  return block_cells % 16 == 0 && tpu <= 32 && (upi * tpu + kWarps - 1) / kWarps <= kTpwMax;
+}
+
+template <int NT, int TPW>
+static cudaError_t launch_variant(const ScoresParams& p, size_t smem, int grid, cudaStream_t stream) {
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(block_scores_kernel<NT, TPW>), smem);
+  if (e != cudaSuccess) return e;
+  block_scores_kernel<NT, TPW><<<grid, kThreads, smem, stream>>>(p);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_block_scores(const ScoresParams& p, cudaStream_t stream) {
-  const size_t smem = block_scores_smem_bytes(p.n_rows, p.n_q_heads, p.n_kv_heads, p.block_cells);
   if (p.total_units == 0) return cudaSuccess;
-  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(block_scores_kernel), (size_t)smem);
-  if (e != cudaSuccess) return e;
-  const int upi = kThreads / (p.n_kv_heads * p.block_cells);
+  const int nt = (p.n_rows + 7) / 8;
+  if (nt > kNtMax) return cudaErrorInvalidValue;
+  const size_t smem = block_scores_smem_bytes(p.n_rows, p.n_q_heads, p.n_kv_heads, p.block_cells);
+  const int tpu = p.n_kv_heads * (p.block_cells / 16);
+  const int upi = max(1, kWarps / tpu);
+  const int tpw = (upi * tpu + kWarps - 1) / kWarps;
   const int n_super = (p.total_units + upi - 1) / upi;
   const int grid = min(n_super, device_sm_count());
-  block_scores_kernel<<<grid, kThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  const int ntv = nt == 1 ? 1 : (nt == 2 ? 2 : 4);
+  if (tpw == 1) {
+    if (ntv == 1) return launch_variant<1, 1>(p, smem, grid, stream);
+    if (ntv == 2) return launch_variant<2, 1>(p, smem, grid, stream);
+    return launch_variant<4, 1>(p, smem, grid, stream);
+  }
+  if (ntv == 1) return launch_variant<1, 2>(p, smem, grid, stream);
+  if (ntv == 2) return launch_variant<2, 2>(p, smem, grid, stream);
+  return launch_variant<4, 2>(p, smem, grid, stream);
 }
 
 }  // namespace qsa

@@ -63,6 +63,18 @@ def test_small_ragged(fill, page_cells, Hq, Hkv, k, C, v_bits):
     run_and_check(case)
 
 
+@pytest.mark.parametrize("rows_per_slot,Hq,Hkv,B", [
+    (10, 16, 8, 64),    # 20 rows (three 8-row tiles), 8 KV heads: two warp tasks per warp
+    (6, 8, 2, 128),     # 12 rows, 128-cell blocks
+    (4, 32, 4, 32),     # 8 rows, 32-cell blocks, 8 q heads per KV head
+])
+def test_many_rows_and_block_sizes(rows_per_slot, Hq, Hkv, B):
+    case = W.decode_case(name="wide", seed=rows_per_slot * B + Hkv, fills=[2000, 1500], capacity=2048,
+                         rows_per_slot=rows_per_slot, n_q_heads=Hq, n_kv_heads=Hkv, k_cells=4 * B,
+                         chunk_cells=64, block_cells=B, page_cells=256, bias_prob=0.05)
+    run_and_check(case)
+
+
 def test_rows_with_masked_cells_and_two_pools():
     """Rows early in the context: selected cells past a row's position are masked; a chunk whose cells
     are all masked is empty; the merge skips it."""
