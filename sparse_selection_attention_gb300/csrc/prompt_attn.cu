@@ -517,55 +517,58 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const PromptPa
 
 namespace ws {
 
-// Warp-specialised prompt attention for int8 V (see the file comment for the
-// arithmetic).  Roles of the 16 warps of a CTA:
-//   warp 0      one thread issues the bulk copies of each 64-cell K/V tile into
-//               a 3-stage ring of raw staging buffers;
-//   warp 1      one thread issues every tcgen05.mma: S(i) = Q K(i)^T into one
-//               of two tensor-memory S slots, then P += W(i-1) V(i-1) with W
-//               read from tensor memory;
-//   warps 4-7   convert raw tiles into fp16 operands (2-stage ring): K (K-major)
-//               and V transposed, plus the per-cell scales and the tile's
-//               V-scale power of two;
-//   warps 8-15  softmax, two threads per row (32 cells each): logits, running
-//               max (lazy, threshold 2^8), p, and W = p * vscale * 2^k split
-//               into fp16 hi/lo, written back over S(i) in tensor memory.
-// QK of tile i+1 overlaps the softmax of tile i and P.V of tile i-1.  P
-// accumulates at most kFoldEvery tiles in tensor memory; it is then folded
-// into O with fp32 FMAs (O = O * factor + P), and also whenever a row's
-// running max or the V-scale exponent changes, so that P always holds tiles
-// of one reference.  Every mbarrier wait is bounded; a wait that runs out
-// sets the device error word and every role stops at its next wait.
+// Warp-specialised prompt attention for int8 V.  Roles of the 16 warps:
+//   warp 0      one thread issues the bulk copies of each 64-cell K/V tile (codes and scales) into a
+//               3-stage ring of raw staging buffers;
+//   warp 1      issues every tcgen05.mma (one thread): S(i) = Q K(i)^T, with Q (hi and lo) held in
+//               tensor memory, into one of two S slots; then P += W(i-1) V(i-1), W read from the S
+//               slot it was written over;
+//   warps 4-7   convert raw tiles into fp16 operands in a 3-stage ring: K and V keep their stored
+//               [cell][dim] order (K is the K-major B operand of S = Q K^T, V the MN-major B operand
+//               of P = W V), plus the tile's K scales and V scales times a power of two 2^k;
+//   warps 8-15  softmax, two threads per row (warps w and w+4 share rows, 32 cells and 64 output
+//               dims each): logits, running max (rescaled lazily, past 2^8), p, and
+//               W = p * vscale * 2^k split into fp16 hi + lo, stored over S(i).
+// S(i+1) overlaps the softmax of tile i and P.V of tile i-1.  P holds at most kFoldEvery tiles in
+// tensor memory: a warp folds its rows' P into the fp32 output O in shared memory (O = O * factor + P)
+// and zeroes P whenever one of its rows changes its running max, when the V-scale exponent changes,
+// and every kFoldEvery tiles, so that P only ever holds tiles of one reference per row.  The only
+// thread barrier in the loop joins the two warps of a row pair; every other hand-off is an mbarrier
+// with a bounded wait.  A wait that runs out sets the device error word; every role then stops at
+// its next wait and the CTA drains its copies and MMAs before it exits.
 constexpr int kThreads = 512;
 constexpr int kM = 128;
 constexpr int kN = 64;
 constexpr int kRawStages = 3;
 constexpr int kFoldEvery = 8;
-constexpr int kQhi = 0, kQlo = 32768;                     // 2 K-blocks x [128 rows][128 B] each
-constexpr int kOp0 = 65536, kOpBytes = 32768;             // per op stage: K [2][64][128 B], V^T [128][128 B]
+// Tensor memory columns (512 allocated).
+constexpr uint32_t kTQ = 0;     // Q of dim group g: hi at 64g, lo at 64g + 32 (fp16 pairs)
+constexpr uint32_t kTS = 128;   // S slot s at 128 + 128s: S_g at +64g (fp32); W_g hi at +64g, lo at +64g+32
+constexpr uint32_t kTP = 384;   // P: output dim d at 384 + d (fp32)
+// Shared memory map (offsets from a 1024-byte aligned base).
+constexpr int kO = 0;                                   // O [128 dims][128 rows] fp32
+constexpr int kOpStages = 3;
+constexpr int kOp0 = 65536, kOpBytes = 32768;           // op stage: K, V as [dim group][64 cells][128 B]
 constexpr int kOpK = 0, kOpV = 16384;
-constexpr int kRaw0 = kOp0 + 2 * kOpBytes, kRawBytes = 17408;   // raw K 8 KB, V 8 KB, ks 512 B, vs 512 B
+constexpr int kRaw0 = kOp0 + kOpStages * kOpBytes, kRawBytes = 17408;   // raw K 8 KB, V 8 KB, ks, vs 512 B
 constexpr int kRK = 0, kRV = 8192, kRKs = 16384, kRVs = 16896;
-constexpr int kAux0 = kRaw0 + kRawStages * kRawBytes, kAuxBytes = 1088;   // per op stage: ks, vsp, info
-constexpr int kAuxKs = 0, kAuxVs = 512, kAuxInfo = 1024;
-constexpr int kRed = kAux0 + 2 * kAuxBytes;               // tile maxima [2 halves][128], l [2][128]
-constexpr int kCtl = kRed + 2048;                         // barriers and control words
-constexpr int kSmemBytes = kCtl + 512 + 1024;             // + alignment slack
+constexpr int kAux0 = kRaw0 + kRawStages * kRawBytes, kAuxBytes = 1088;   // per op stage
+constexpr int kAuxKs = 0, kAuxVs = 512, kAuxInfo = 1024;                  // ks [2][64], vs [2][64], k, changed
+constexpr int kRed = kAux0 + kOpStages * kAuxBytes;             // row maxima [2][2][128], row sums [2][128], flags [2][8]
+constexpr int kRedMax = 0, kRedSum = 512, kRedFlag = 768;   // in 4-byte words
+constexpr int kCtl = kRed + 4096;
+constexpr int kSmemBytes = kCtl + 512 + 1024;           // + alignment slack
 
-// Barrier indices.
-constexpr int RAW_FULL = 0, RAW_EMPTY = 3, OP_FULL = 6, OP_EMPTY = 8, S_FULL = 10, S_EMPTY = 12, W_FULL = 14,
-              PV_DONE = 16, N_BARS = 17;
-// Control words (ints) after the barriers.
-constexpr int C_ABORT = 0, C_TMEM = 1, C_PVACC = 2 /* [2] */, C_FOLD = 4 /* [2] */, C_GO_SM = 6 /* [2] */,
-              C_GO_CV = 8 /* [2] */, C_GO_FD = 10 /* [2] */, C_GO_EP = 12, C_ISSUED = 13, C_LAST_BAR = 14,
-              C_LAST_PAR = 15, N_CTL = 16;
+constexpr int RAW_FULL = 0, RAW_EMPTY = 3, OP_FULL = 6, OP_EMPTY = 9, S_FULL = 12, S_EMPTY = 14, W_FULL = 16,
+              N_BARS = 18;
+constexpr int C_ABORT = 0, C_TMEM = 1, C_ISSUED = 2, C_LAST_BAR = 3, C_LAST_PAR = 4, N_CTL = 5;
 
 struct Ctl {
   uint32_t bars;
   volatile int* w;
 };
 
-// Bounded wait that gives up at once once the CTA has aborted.
+// Bounded wait on a phase; gives up at once when the CTA has already aborted.
 __device__ __forceinline__ bool wait_b(const Ctl& c, int bar, uint32_t parity, uint64_t limit_ns) {
   const uint32_t b = c.bars + 8 * bar;
   if (limit_ns == 0) {
@@ -586,16 +589,49 @@ __device__ __forceinline__ bool wait_b(const Ctl& c, int bar, uint32_t parity, u
   }
 }
 
-// Acquire side of a phase that another thread of the role has already seen complete.
-__device__ __forceinline__ void acquire(const Ctl& c, int bar, uint32_t parity) {
-  tc::mbar_wait(c.bars + 8 * bar, parity, 2000000000ull);
-}
-
 __device__ __forceinline__ void arrive(const Ctl& c, int bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(c.bars + 8 * bar) : "memory");
 }
 
 __device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + max(-126, min(127, e))) << 23); }
+
+// Packed fp32 pairs (round to nearest, like the scalar operations).
+__device__ __forceinline__ uint64_t pk(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float2 upk(uint64_t r) {
+  float2 v;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+  return v;
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// 2^x (hardware approximation; 2^-inf = +0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// (a, b) -> fp16 pairs hi, lo with hi + lo = (a, b) to ~2^-21 relative (|a|, |b| < 65504): hi keeps
+// the top 11 significant bits (exact in fp16 down to 2^-14), lo = x - hi exactly in fp32, rounded.
+__device__ __forceinline__ void split_pair(uint64_t ab, uint32_t& hi, uint32_t& lo) {
+  const float2 v = upk(ab);
+  const float ha = __uint_as_float(__float_as_uint(v.x) & 0xFFFFE000u);
+  const float hb = __uint_as_float(__float_as_uint(v.y) & 0xFFFFE000u);
+  const float2 rem = upk(ffma2(pk(ha, hb), pk(-1.f, -1.f), ab));
+  hi = h2_bits(__floats2half2_rn(ha, hb));
+  lo = h2_bits(__floats2half2_rn(rem.x, rem.y));
+}
 
 __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const PromptParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -618,20 +654,22 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
   c.bars = sbase + kCtl;
   c.w = reinterpret_cast<volatile int*>(smem + kCtl + 8 * N_BARS);
   float* red = reinterpret_cast<float*>(smem + kRed);
+  volatile int* wflag = reinterpret_cast<volatile int*>(red + kRedFlag);
 
   if (tid == 0) {
     for (int s = 0; s < kRawStages; ++s) {
       tc::mbar_init(c.bars + 8 * (RAW_FULL + s), 1);
       tc::mbar_init(c.bars + 8 * (RAW_EMPTY + s), 4);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kOpStages; ++s) {
       tc::mbar_init(c.bars + 8 * (OP_FULL + s), 4);
       tc::mbar_init(c.bars + 8 * (OP_EMPTY + s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       tc::mbar_init(c.bars + 8 * (S_FULL + s), 1);
       tc::mbar_init(c.bars + 8 * (S_EMPTY + s), 1);
       tc::mbar_init(c.bars + 8 * (W_FULL + s), 8);
     }
-    tc::mbar_init(c.bars + 8 * PV_DONE, 1);
     tc::mbar_fence_init();
     for (int i = 0; i < N_CTL; ++i) c.w[i] = 0;
   }
@@ -641,17 +679,20 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
   tc::fence_after_sync();
   const uint32_t tmem = static_cast<uint32_t>(c.w[C_TMEM]);
 
-  // ---- softmax threads: row r (lane quarter of the warp), half h (32 cells, 64 dims).
+  // Softmax threads: row r of the CTA (TMEM lane r), half h (cells 32h.., output dims 64h..).
   const bool is_sm = warp >= 8;
-  const int r = 32 * (warp & 3) + lane;
+  const int quarter = warp & 3;
+  const int r = 32 * quarter + lane;
   const int half = (warp - 8) >> 2;
   const int qi = q_begin + r / G;
   const bool row_valid = (r < QPC * G) && (qi < q_end);
   const int head = kvh * G + (r % G);
   const int pos = row_valid ? p.q_pos0 + qi : p.q_pos0;
+  const uint32_t tl = tmem + ((uint32_t)(32 * quarter) << 16);
   float lambda = 0.f;
   if (is_sm) {
-    // Q row scaled by a power of two (max |q 2^f| in [64, 128)), this half's 64 dims split hi/lo.
+    // Q row scaled by a power of two f (max |q f| in [64, 128)); dim group `half` split hi/lo into
+    // tensor memory, element pairs packed two per column.
     const float4* q4 = reinterpret_cast<const float4*>(p.q + ((size_t)qi * p.n_q_heads + head) * kD);
     float amax = 0.f;
     if (row_valid) {
@@ -664,26 +705,25 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
     if (amax > 0.f) frexpf(amax, &e);
     const int fexp = amax > 0.f ? max(-126, min(127, 7 - e)) : 0;
     const float f = pow2f(fexp);
-    for (int cch = 0; cch < 8; ++cch) {
-      float x[8];
-      if (row_valid) {
-        const float4 a = __ldg(q4 + 16 * half + 2 * cch), b = __ldg(q4 + 16 * half + 2 * cch + 1);
-        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-      } else {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) x[k] = 0.f;
+    for (int part = 0; part < 2; ++part) {
+      uint32_t hi[16], lo[16];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (row_valid) v = __ldg(q4 + 16 * half + 8 * part + k);
+        split2(v.x * f, v.y * f, hi[2 * k], lo[2 * k]);
+        split2(v.z * f, v.w * f, hi[2 * k + 1], lo[2 * k + 1]);
       }
-      uint32_t hi[4], lo[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) split2(x[2 * k] * f, x[2 * k + 1] * f, hi[k], lo[k]);
-      const int off = half * 16384 + sw128(r, cch);
-      *reinterpret_cast<uint4*>(smem + kQhi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4*>(smem + kQlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      tc::tmem_st16(tl + kTQ + 64 * half + 16 * part, hi);
+      tc::tmem_st16(tl + kTQ + 64 * half + 32 + 16 * part, lo);
     }
+    tc::tmem_wait_st();
     lambda = kLog2e * kInvSqrtD * pow2f(-fexp);
   }
-  tc::fence_proxy_async_smem();
+  tc::fence_before_sync();
   __syncthreads();
+  tc::fence_after_sync();
 
   // =========================================================== producer
   if (warp == 0) {
@@ -708,160 +748,128 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
     }
   }
   // =========================================================== MMA issuer
+  // The whole warp runs the loop and waits; one elected lane issues (converged issue keeps the
+  // operands in uniform registers).  Descriptors step by 32-bit adds on their low word.
   else if (warp == 1) {
-    if (lane == 0) {
-      const uint32_t idesc_s = tc::idesc_f16_f32(kM, kN);
-      const uint32_t idesc_o = tc::idesc_f16_f32(kM, 64);
-      int last_bar = -1;
-      uint32_t last_par = 0;
-      bool ok = true;
-      for (int i = 0; i <= n_tiles && ok; ++i) {
-        if (i < n_tiles) {
-          const int sl = i & 1;
-          ok = wait_b(c, OP_FULL + sl, (i >> 1) & 1, limit);
-          if (ok && i >= 2) ok = wait_b(c, S_EMPTY + sl, ((i - 2) >> 1) & 1, limit);
-          if (!ok) break;
-          tc::fence_after_sync();
-          const uint32_t kop = sbase + kOp0 + sl * kOpBytes + kOpK;
+    const uint32_t idesc = tc::idesc_f16_f32(kM, 64);
+    const uint32_t idesc_v = tc::idesc_f16_f32_bmn(kM, 64);
+    const uint32_t d_hi = tc::sw128_desc_hi();
+    const uint32_t k_lo0 = tc::sw128_desc_lo(sbase + kOp0 + kOpK, 16);
+    const uint32_t v_lo0 = tc::sw128_desc_lo(sbase + kOp0 + kOpV, 8192);
+    int last_bar = -1;
+    uint32_t last_par = 0;
+    for (int i = 0; i <= n_tiles; ++i) {
+      if (i < n_tiles) {
+        const int sl = i & 1, os = i % kOpStages;
+        bool ok = wait_b(c, OP_FULL + os, (i / kOpStages) & 1, limit);
+        if (ok && i >= 2) ok = wait_b(c, S_EMPTY + sl, ((i - 2) >> 1) & 1, limit);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        tc::fence_after_sync();
+        if (tc::elect_one()) {
+          const uint32_t k_lo = k_lo0 + (uint32_t)(os * (kOpBytes >> 4));
+          const uint32_t d = tmem + kTS + 128 * sl;
 #pragma unroll
           for (int g = 0; g < 2; ++g) {
-            const uint64_t ah = tc::sw128_desc(sbase + kQhi + g * 16384);
-            const uint64_t al = tc::sw128_desc(sbase + kQlo + g * 16384);
-            const uint64_t bk = tc::sw128_desc(kop + g * 8192);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              tc::mma_f16(tmem + sl * 128 + g * kN, ah + 2 * kk, bk + 2 * kk, idesc_s, kk > 0);
-              tc::mma_f16(tmem + sl * 128 + g * kN, al + 2 * kk, bk + 2 * kk, idesc_s, 1);
+              const uint32_t b_lo = k_lo + (uint32_t)((g * 8192 + kk * 32) >> 4);
+              tc::mma_f16_tmem_a_w(d + 64 * g, tmem + kTQ + 64 * g + 8 * kk, b_lo, d_hi, idesc, kk > 0 ? 1u : 0u);
+              tc::mma_f16_tmem_a_w(d + 64 * g, tmem + kTQ + 64 * g + 32 + 8 * kk, b_lo, d_hi, idesc, 1u);
             }
           }
           tc::mma_commit(c.bars + 8 * (S_FULL + sl));
-          last_bar = S_FULL + sl;
-          last_par = (i >> 1) & 1;
         }
-        if (i >= 1) {
-          const int j = i - 1, sj = j & 1;
-          if (!wait_b(c, W_FULL + sj, (j >> 1) & 1, limit)) { ok = false; break; }
-          tc::fence_after_sync();
-          const uint32_t acc = c.w[C_PVACC + sj];
-          const uint32_t vop = sbase + kOp0 + sj * kOpBytes + kOpV;
+        __syncwarp();
+        last_bar = S_FULL + sl;
+        last_par = (i >> 1) & 1;
+      }
+      if (i >= 1) {
+        const int j = i - 1, sj = j & 1, oj = j % kOpStages;
+        if (!__all_sync(0xffffffffu, wait_b(c, W_FULL + sj, (j >> 1) & 1, limit))) break;
+        tc::fence_after_sync();
+        if (tc::elect_one()) {
+          const uint32_t v_lo = v_lo0 + (uint32_t)(oj * (kOpBytes >> 4));
+          const uint32_t aw = tmem + kTS + 128 * sj;
+          const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
           for (int g = 0; g < 2; ++g) {
-            const uint64_t bv = tc::sw128_desc(vop + g * 64 * 128);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              const uint32_t aw = tmem + sj * 128 + (2 * g) * 32 + 8 * kk;
-              tc::mma_f16_tmem_a(tmem + 256 + g * 64, aw, bv + 2 * kk, idesc_o, (kk > 0 || acc) ? 1u : 0u);
-              tc::mma_f16_tmem_a(tmem + 256 + g * 64, aw + 32, bv + 2 * kk, idesc_o, 1u);
+              const uint32_t b_lo = v_lo + (uint32_t)((g * 8192 + kk * 2048) >> 4);
+              tc::mma_f16_tmem_a_w(tmem + kTP + 64 * g, aw + 64 * g + 8 * kk, b_lo, d_hi, idesc_v, kk > 0 ? 1u : acc0);
+              tc::mma_f16_tmem_a_w(tmem + kTP + 64 * g, aw + 64 * g + 32 + 8 * kk, b_lo, d_hi, idesc_v, 1u);
             }
           }
           tc::mma_commit(c.bars + 8 * (S_EMPTY + sj));
-          tc::mma_commit(c.bars + 8 * (OP_EMPTY + sj));
-          tc::mma_commit(c.bars + 8 * PV_DONE);
-          last_bar = PV_DONE;
-          last_par = j & 1;
+          tc::mma_commit(c.bars + 8 * (OP_EMPTY + oj));
         }
+        __syncwarp();
+        last_bar = OP_EMPTY + oj;
+        last_par = (j / kOpStages) & 1;
       }
+    }
+    if (lane == 0) {
       c.w[C_LAST_BAR] = last_bar;
       c.w[C_LAST_PAR] = (int)last_par;
     }
   }
   // =========================================================== converters
   else if (warp >= 4 && warp < 8) {
+    const int cw = warp - 4;
     const int ct = tid - 128;   // 0..127
-    int k_ref = 0;              // V-scale exponent reference (identical in the 4 warps)
+    int k_ref = 0;              // V-scale exponent reference (the same in the 4 warps)
     for (int i = 0; i < n_tiles; ++i) {
-      const int rs = i % kRawStages, os = i & 1;
-      if (ct == 0) {
-        bool ok = wait_b(c, RAW_FULL + rs, (i / kRawStages) & 1, limit);
-        if (ok && i >= 2) ok = wait_b(c, OP_EMPTY + os, ((i - 2) >> 1) & 1, limit);
-        c.w[C_GO_CV + (i & 1)] = ok && !c.w[C_ABORT];
-      }
-      tc::named_barrier(2, 128);
-      if (!c.w[C_GO_CV + (i & 1)]) break;
-      if (ct != 0) {
-        acquire(c, RAW_FULL + rs, (i / kRawStages) & 1);
-        if (i >= 2) acquire(c, OP_EMPTY + os, ((i - 2) >> 1) & 1);
-      }
+      const int rs = i % kRawStages, os = i % kOpStages;
+      bool ok = wait_b(c, RAW_FULL + rs, (i / kRawStages) & 1, limit);
+      if (ok && i >= kOpStages) ok = wait_b(c, OP_EMPTY + os, ((i / kOpStages) - 1) & 1, limit);
+      if (!__all_sync(0xffffffffu, ok)) break;
       const uint8_t* raw = smem + kRaw0 + rs * kRawBytes;
       uint8_t* op = smem + kOp0 + os * kOpBytes;
       uint8_t* aux = smem + kAux0 + os * kAuxBytes;
       const int cell0 = i * kN;
-      // K codes -> fp16, K-major [cell][dim] in two 64-dim blocks.
+      // K and V codes -> fp16 in their stored order: [dim group][cell][64 dims, 128 B], 128-byte
+      // swizzle (cells 16cw..16cw+15; thread: one cell, one dim group, of K and of V).
       {
         const int cc = ct >> 1, hf = ct & 1;
-        const uint8_t* src = raw + kRK + cc * 128 + hf * 64;
-        uint8_t* dst = op + kOpK + hf * 8192;
 #pragma unroll
-        for (int s4 = 0; s4 < 4; ++s4) {
-          const int i4 = (s4 + cc) & 3;
-          const uint4 v = *reinterpret_cast<const uint4*>(src + i4 * 16);
-          uint32_t hh[8];
-          s8x4_to_h2x2(v.x, hh[0], hh[1]);
-          s8x4_to_h2x2(v.y, hh[2], hh[3]);
-          s8x4_to_h2x2(v.z, hh[4], hh[5]);
-          s8x4_to_h2x2(v.w, hh[6], hh[7]);
-          *reinterpret_cast<uint4*>(dst + sw128(cc, 2 * i4)) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
-          *reinterpret_cast<uint4*>(dst + sw128(cc, 2 * i4 + 1)) = make_uint4(hh[4], hh[5], hh[6], hh[7]);
-        }
-      }
-      // V codes -> fp16 transposed [dim][cell].
-      {
-        const int dq = ct & 31, co = ct >> 5;
-#pragma unroll
-        for (int oi = 0; oi < 2; ++oi) {
-          const int oct = co + 4 * oi;
-          uint32_t w[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            w[k] = *reinterpret_cast<const uint32_t*>(raw + kRV + (8 * oct + k) * 128 + 4 * dq) ^ 0x80808080u;
-          uint4 out[4];
-          uint32_t a[4], b[4];
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            a[kk] = __byte_perm(w[2 * kk], w[2 * kk + 1], 0x5140);
-            b[kk] = __byte_perm(w[2 * kk], w[2 * kk + 1], 0x7362);
-          }
-          out[0] = make_uint4(bytes_to_h2(a[0], 0x4140, 0x64806480u), bytes_to_h2(a[1], 0x4140, 0x64806480u),
-                              bytes_to_h2(a[2], 0x4140, 0x64806480u), bytes_to_h2(a[3], 0x4140, 0x64806480u));
-          out[1] = make_uint4(bytes_to_h2(a[0], 0x4342, 0x64806480u), bytes_to_h2(a[1], 0x4342, 0x64806480u),
-                              bytes_to_h2(a[2], 0x4342, 0x64806480u), bytes_to_h2(a[3], 0x4342, 0x64806480u));
-          out[2] = make_uint4(bytes_to_h2(b[0], 0x4140, 0x64806480u), bytes_to_h2(b[1], 0x4140, 0x64806480u),
-                              bytes_to_h2(b[2], 0x4140, 0x64806480u), bytes_to_h2(b[3], 0x4140, 0x64806480u));
-          out[3] = make_uint4(bytes_to_h2(b[0], 0x4342, 0x64806480u), bytes_to_h2(b[1], 0x4342, 0x64806480u),
-                              bytes_to_h2(b[2], 0x4342, 0x64806480u), bytes_to_h2(b[3], 0x4342, 0x64806480u));
+        for (int kv = 0; kv < 2; ++kv) {
+          const uint8_t* src = raw + (kv ? kRV : kRK) + cc * 128 + hf * 64;
+          uint8_t* dst = op + (kv ? kOpV : kOpK) + hf * 8192;
 #pragma unroll
           for (int s4 = 0; s4 < 4; ++s4) {
-            const int jj = (s4 + (dq >> 1)) & 3;
-            const int d = 4 * dq + jj;
-            *reinterpret_cast<uint4*>(op + kOpV + sw128(d, oct)) = pick(out, jj);
+            const int i4 = (s4 + cc) & 3;
+            const uint4 v = *reinterpret_cast<const uint4*>(src + i4 * 16);
+            uint32_t hh[8];
+            s8x4_to_h2x2(v.x, hh[0], hh[1]);
+            s8x4_to_h2x2(v.y, hh[2], hh[3]);
+            s8x4_to_h2x2(v.z, hh[4], hh[5]);
+            s8x4_to_h2x2(v.w, hh[6], hh[7]);
+            *reinterpret_cast<uint4*>(dst + sw128(cc, 2 * i4)) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+            *reinterpret_cast<uint4*>(dst + sw128(cc, 2 * i4 + 1)) = make_uint4(hh[4], hh[5], hh[6], hh[7]);
           }
         }
       }
-      // K scales (as staged) and V scales times 2^k_ref; k_ref only decreases, tile by tile.
+      // Scales, group-major.  Every warp takes the max |vs| of the whole tile (cells below n_filled)
+      // itself, so the four agree on k without a barrier; k only decreases, tile by tile.
       {
         const float* ksr = reinterpret_cast<const float*>(raw + kRKs);
         const float* vsr = reinterpret_cast<const float*>(raw + kRVs);
-        float* ksa = reinterpret_cast<float*>(aux + kAuxKs);
-        float* vsa = reinterpret_cast<float*>(aux + kAuxVs);
-        ksa[ct] = ksr[ct];   // 128 floats = [64 cells][2]
+        const float4 v4 = reinterpret_cast<const float4*>(vsr)[lane];   // cells 2 lane, 2 lane + 1
         float mx = 0.f;
-        const bool v0 = cell0 + (ct >> 1) < pool.n_filled;
-        if (v0) mx = fabsf(vsr[ct]);
+        if (cell0 + 2 * lane < pool.n_filled) mx = fmaxf(fabsf(v4.x), fabsf(v4.y));
+        if (cell0 + 2 * lane + 1 < pool.n_filled) mx = fmaxf(mx, fmaxf(fabsf(v4.z), fabsf(v4.w)));
         mx = warp_max(mx);
-        // combine the 4 warps' maxima through the aux info words
-        volatile float* cm = reinterpret_cast<volatile float*>(aux + kAuxInfo + 8);
-        if (lane == 0) cm[ct >> 5] = mx;
-        tc::named_barrier(2, 128);
-        mx = fmaxf(fmaxf(cm[0], cm[1]), fmaxf(cm[2], cm[3]));
         int e = 0;
         if (mx > 0.f) frexpf(mx, &e);
         const int kt = mx > 0.f ? 4 - e : k_ref;   // max |vs| 2^k in [8, 16)
         int changed = 0;
         if (i == 0) k_ref = kt;
         else if (kt < k_ref) { k_ref = kt; changed = 1; }
-        const float up = pow2f(k_ref);
-        // vsa[g][cell] from vsr[cell][g]
-        vsa[(ct & 1) * 64 + (ct >> 1)] = v0 ? vsr[ct] * up : 0.f;
+        const int cl = 16 * cw + (lane >> 1), g = lane & 1;
+        float* ksa = reinterpret_cast<float*>(aux + kAuxKs);
+        float* vsa = reinterpret_cast<float*>(aux + kAuxVs);
+        ksa[g * 64 + cl] = ksr[2 * cl + g];
+        vsa[g * 64 + cl] = (cell0 + cl < pool.n_filled) ? vsr[2 * cl + g] * pow2f(k_ref) : 0.f;
         if (ct == 0) {
           reinterpret_cast<volatile int*>(aux + kAuxInfo)[0] = k_ref;
           reinterpret_cast<volatile int*>(aux + kAuxInfo)[1] = changed;
@@ -877,161 +885,145 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
   }
   // =========================================================== softmax
   else if (is_sm) {
-    const int st_id = tid - 256;   // 0..255
+    const int pair_bar = 1 + quarter;          // warps quarter + 8 and quarter + 12
+    const int partner = (warp - 8) ^ 4;
+    float* O = reinterpret_cast<float*>(smem + kO);
     float m_P = -INFINITY, m_O = -INFINITY, l = 0.f;
     int k_P = 0, k_O = 0;
-    bool o_empty = true;
-    bool alive = true;
-    for (int i = 0; i < n_tiles && alive; ++i) {
+    bool o_empty = true, alive = true;
+    const float zero16[16] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int i = 0; i < n_tiles; ++i) {
       const int sl = i & 1;
-      if (st_id == 0) {
-        bool ok = wait_b(c, OP_FULL + sl, (i >> 1) & 1, limit);
-        if (ok) ok = wait_b(c, S_FULL + sl, (i >> 1) & 1, limit);
-        c.w[C_GO_SM + (i & 1)] = ok && !c.w[C_ABORT];
-      }
-      tc::named_barrier(1, 256);
-      if (!c.w[C_GO_SM + (i & 1)]) { alive = false; break; }
-      if (st_id != 0) {
-        acquire(c, OP_FULL + sl, (i >> 1) & 1);
-        acquire(c, S_FULL + sl, (i >> 1) & 1);
-      }
-      tc::fence_after_sync();
-      const uint8_t* aux = smem + kAux0 + sl * kAuxBytes;
-      const float2* ks = reinterpret_cast<const float2*>(aux + kAuxKs);
-      const float* vsa = reinterpret_cast<const float*>(aux + kAuxVs);
-      const int k_tile = reinterpret_cast<const volatile int*>(aux + kAuxInfo)[0];
-      const int k_changed = reinterpret_cast<const volatile int*>(aux + kAuxInfo)[1];
+      bool ok = wait_b(c, OP_FULL + i % kOpStages, (i / kOpStages) & 1, limit);
+      if (ok) ok = wait_b(c, S_FULL + sl, (i >> 1) & 1, limit);
+      ok = __all_sync(0xffffffffu, ok && !c.w[C_ABORT]);
+      const uint8_t* aux = smem + kAux0 + (i % kOpStages) * kAuxBytes;
       const int cell0 = i * kN;
-      // logits (scaled by f) of this half's 32 cells
       float X[32];
-      {
-        const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + sl * 128 + 32 * half;
+      float xmax = -INFINITY;
+      if (ok) {
+        tc::fence_after_sync();
+        const float* ksa = reinterpret_cast<const float*>(aux + kAuxKs);
 #pragma unroll
         for (int q2 = 0; q2 < 2; ++q2) {
           float s0[16], s1[16];
-          tc::tmem_ld16(trow + 16 * q2, s0);
-          tc::tmem_ld16(trow + kN + 16 * q2, s1);
+          tc::tmem_ld16(tl + kTS + 128 * sl + 32 * half + 16 * q2, s0);
+          tc::tmem_ld16(tl + kTS + 128 * sl + 64 + 32 * half + 16 * q2, s1);
           tc::tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float2 kk = ks[32 * half + 16 * q2 + j];
-            X[16 * q2 + j] = fmaf(s1[j], kk.y, s0[j] * kk.x);
+          for (int j4 = 0; j4 < 4; ++j4) {
+            const float4 k0 = reinterpret_cast<const float4*>(ksa + 32 * half + 16 * q2)[j4];
+            const float4 k1 = reinterpret_cast<const float4*>(ksa + 64 + 32 * half + 16 * q2)[j4];
+            const int j = 4 * j4;
+            const float2 xa = upk(ffma2(pk(s1[j], s1[j + 1]), pk(k1.x, k1.y), fmul2(pk(s0[j], s0[j + 1]), pk(k0.x, k0.y))));
+            const float2 xb = upk(ffma2(pk(s1[j + 2], s1[j + 3]), pk(k1.z, k1.w),
+                                        fmul2(pk(s0[j + 2], s0[j + 3]), pk(k0.z, k0.w))));
+            X[16 * q2 + j] = xa.x;
+            X[16 * q2 + j + 1] = xa.y;
+            X[16 * q2 + j + 2] = xb.x;
+            X[16 * q2 + j + 3] = xb.y;
           }
         }
-      }
-      const bool full = (cell0 + kN - 1 <= pos_first);
-      float xmax = -INFINITY;
+        if (cell0 + kN - 1 > pos_first) {   // tile reaches past some row's position: causal mask
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        if (!full && cell0 + 32 * half + j > pos) X[j] = -INFINITY;
-        xmax = fmaxf(xmax, X[j]);
+          for (int j = 0; j < 32; ++j)
+            if (cell0 + 32 * half + j > pos) X[j] = -INFINITY;
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) xmax = fmaxf(xmax, X[j]);
       }
-      // row maximum over both halves; fold decision for the CTA
-      red[half * 128 + r] = xmax;
-      if (st_id == 0) c.w[C_FOLD + ((i + 1) & 1)] = 0;
-      tc::named_barrier(1, 256);
-      xmax = fmaxf(xmax, red[(1 - half) * 128 + r]);
+      // Row maximum over the two halves; the pair also agrees on whether to go on.
+      red[kRedMax + (sl * 2 + half) * 128 + r] = xmax;
+      if (lane == 0) wflag[sl * 8 + (warp - 8)] = ok ? 1 : 0;
+      tc::named_barrier(pair_bar, 64);
+      if (!ok || !wflag[sl * 8 + partner]) { alive = false; break; }
+      xmax = fmaxf(xmax, red[kRedMax + (sl * 2 + (half ^ 1)) * 128 + r]);
+      const int k_tile = reinterpret_cast<const volatile int*>(aux + kAuxInfo)[0];
+      const int k_changed = reinterpret_cast<const volatile int*>(aux + kAuxInfo)[1];
       const float ymax = xmax * lambda;   // lambda > 0
       const float m_new = (ymax > m_P + 8.0f) ? ymax : m_P;
-      if (m_new != m_P || (st_id == 0 && (k_changed || (i > 0 && i % kFoldEvery == 0))))
-        c.w[C_FOLD + (i & 1)] = 1;
-      tc::named_barrier(1, 256);
-      const bool fold = c.w[C_FOLD + (i & 1)] != 0 && i > 0;
+      const bool fold = __any_sync(0xffffffffu, i > 0 && (m_new != m_P || k_changed || i % kFoldEvery == 0));
       if (fold) {
-        // P holds tiles since the last fold, referenced to (m_P, k_P): wait for P.V(i-1), then
-        // O = O * 2^(m_O - m_P) * 2^(k_P - k_O) + P.
-        if (st_id == 0) c.w[C_GO_FD + (i & 1)] = wait_b(c, PV_DONE, (i - 1) & 1, limit) && !c.w[C_ABORT];
-        tc::named_barrier(1, 256);
-        if (!c.w[C_GO_FD + (i & 1)]) { alive = false; break; }
-        if (st_id != 0) acquire(c, PV_DONE, (i - 1) & 1);
+        // P holds this warp's rows since their last fold, referenced to (m_P, k_P); after P.V(i-1):
+        // O = O * 2^(m_O - m_P) * 2^(k_P - k_O) + P, then P = 0.  (A wait that runs out only raises
+        // the abort: the pair stops at its next barrier.)
+        wait_b(c, S_EMPTY + ((i - 1) & 1), ((i - 1) >> 1) & 1, limit);
         tc::fence_after_sync();
-        const float fo = o_empty ? 0.f : exp2f(m_O - m_P) * pow2f(k_P - k_O);
-        const uint32_t tp = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 256 + 64 * half;
+        const float fo = o_empty ? 0.f : ex2(m_O - m_P) * pow2f(k_P - k_O);
 #pragma unroll 1
-        for (int h4 = 0; h4 < 4; ++h4) {
-          float pv[16], o[16];
-          tc::tmem_ld16(tp + 16 * h4, pv);
-          if (!o_empty) tc::tmem_ld16(tp + 128 + 16 * h4, o);
+        for (int c4 = 0; c4 < 4; ++c4) {
+          float pv[16];
+          tc::tmem_ld16(tl + kTP + 64 * half + 16 * c4, pv);
           tc::tmem_wait_ld();
-          if (o_empty) {
+          float* od = O + (64 * half + 16 * c4) * kM + r;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) o[j] = pv[j];
-          } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) o[j] = fmaf(o[j], fo, pv[j]);
-          }
-          tc::tmem_st16f(tp + 128 + 16 * h4, o);
+          for (int j = 0; j < 16; ++j) od[j * kM] = o_empty ? pv[j] : fmaf(od[j * kM], fo, pv[j]);
+          tc::tmem_st16f(tl + kTP + 64 * half + 16 * c4, zero16);
         }
-        tc::tmem_wait_st();
         o_empty = false;
         m_O = m_P;
         k_O = k_P;
       }
-      // new references for the tiles from i on
       if (m_new != m_P) {
-        if (m_P != -INFINITY) l *= exp2f(m_P - m_new);
+        if (m_P != -INFINITY) l *= ex2(m_P - m_new);
         m_P = m_new;
       }
       k_P = k_tile;
-      // p, this half's l, and W = p vscale 2^k as fp16 hi/lo, written over S(i)
-      float psum = 0.f;
+      // p = 2^(X lambda - m), this half's row sum, W = p vscale 2^k in fp16 hi/lo over S(i).
+      {
+        const uint64_t lam2 = pk(lambda, lambda), negm2 = pk(-m_P, -m_P);
+        float psum = 0.f;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float pj = (X[j] == -INFINITY) ? 0.f : exp2f(fmaf(X[j], lambda, -m_P));
-        X[j] = pj;
-        psum += pj;
+        for (int j = 0; j < 32; j += 2) {
+          const float2 y = upk(ffma2(pk(X[j], X[j + 1]), lam2, negm2));
+          X[j] = ex2(y.x);
+          X[j + 1] = ex2(y.y);
+          psum += X[j] + X[j + 1];
+        }
+        l += psum;
       }
-      l += psum;
-      const uint32_t tw = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + sl * 128;
+      const float* vsa = reinterpret_cast<const float*>(aux + kAuxVs);
 #pragma unroll
       for (int g = 0; g < 2; ++g) {
         uint32_t hi[16], lo[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int c0 = 32 * half + 2 * j;
-          split2(X[2 * j] * vsa[g * 64 + c0], X[2 * j + 1] * vsa[g * 64 + c0 + 1], hi[j], lo[j]);
+        for (int j4 = 0; j4 < 8; ++j4) {
+          const float4 v = reinterpret_cast<const float4*>(vsa + 64 * g + 32 * half)[j4];
+          split_pair(fmul2(pk(X[4 * j4], X[4 * j4 + 1]), pk(v.x, v.y)), hi[2 * j4], lo[2 * j4]);
+          split_pair(fmul2(pk(X[4 * j4 + 2], X[4 * j4 + 3]), pk(v.z, v.w)), hi[2 * j4 + 1], lo[2 * j4 + 1]);
         }
-        tc::tmem_st16(tw + (2 * g) * 32 + 16 * half, hi);
-        tc::tmem_st16(tw + (2 * g + 1) * 32 + 16 * half, lo);
+        tc::tmem_st16(tl + kTS + 128 * sl + 64 * g + 16 * half, hi);
+        tc::tmem_st16(tl + kTS + 128 * sl + 64 * g + 32 + 16 * half, lo);
       }
       tc::tmem_wait_st();
       tc::fence_before_sync();
-      // One thread takes every phase of PV_DONE in order (P.V(i-1) here, unless the fold took it),
-      // so that each parity wait on it is unambiguous.  A wait that runs out raises the abort.
-      if (st_id == 0 && i > 0 && !fold) wait_b(c, PV_DONE, (i - 1) & 1, limit);
-      if (st_id == 0) c.w[C_PVACC + sl] = fold ? 0 : (i == 0 ? 0 : 1);
       __syncwarp();
       if (lane == 0) arrive(c, W_FULL + sl);
     }
-    // ---- epilogue: last P.V, final fold, normalise, write.
+    // ---- epilogue: after the last P.V, out = (O * factor + P) 2^-k / l, lse = (m + log2 l) ln 2.
     if (alive) {
-      if (st_id == 0) c.w[C_GO_EP] = wait_b(c, PV_DONE, (n_tiles - 1) & 1, limit) && !c.w[C_ABORT];
-      tc::named_barrier(1, 256);
-      alive = c.w[C_GO_EP] != 0;
-    }
-    if (alive) {
-      if (st_id != 0) acquire(c, PV_DONE, (n_tiles - 1) & 1);
+      wait_b(c, S_EMPTY + ((n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1, limit);
       tc::fence_after_sync();
-      red[1024 / 4 + half * 128 + r] = l;   // l area: [2][128] after the maxima
-      tc::named_barrier(1, 256);
-      const float lt = red[256 + r] + red[256 + 128 + r];
-      const float fo = o_empty ? 0.f : exp2f(m_O - m_P) * pow2f(k_P - k_O);
+      red[kRedSum + half * 128 + r] = l;
+      tc::named_barrier(pair_bar, 64);
+      const float lt = red[kRedSum + r] + red[kRedSum + 128 + r];
+      const float fo = o_empty ? 0.f : ex2(m_O - m_P) * pow2f(k_P - k_O);
       const float scale = pow2f(-k_P) / lt;
-      const uint32_t tp = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 256 + 64 * half;
       float* orow = p.out + ((size_t)qi * p.n_q_heads + head) * kD + 64 * half;
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        float pv[32], o[32];
-        tc::tmem_ld32(tp + 32 * h2, pv);
-        tc::tmem_ld32(tp + 128 + 32 * h2, o);
+#pragma unroll 1
+      for (int c4 = 0; c4 < 4; ++c4) {
+        float pv[16];
+        tc::tmem_ld16(tl + kTP + 64 * half + 16 * c4, pv);
         tc::tmem_wait_ld();
+        const float* od = O + (64 * half + 16 * c4) * kM + r;
         if (row_valid) {
 #pragma unroll
-          for (int j = 0; j < 32; j += 4) {
+          for (int j = 0; j < 16; j += 4) {
             float v[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) v[u] = (o_empty ? pv[j + u] : fmaf(o[j + u], fo, pv[j + u])) * scale;
-            *reinterpret_cast<float4*>(orow + 32 * h2 + j) = make_float4(v[0], v[1], v[2], v[3]);
+            for (int u = 0; u < 4; ++u)
+              v[u] = (o_empty ? pv[j + u] : fmaf(od[(j + u) * kM], fo, pv[j + u])) * scale;
+            *reinterpret_cast<float4*>(orow + 16 * c4 + j) = make_float4(v[0], v[1], v[2], v[3]);
           }
         }
       }
