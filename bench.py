@@ -347,15 +347,17 @@ def run_ours(args):
         pq = torch.from_numpy(pcase.q).to(dev)
         pout = torch.empty((call[1], pcase.n_q_heads, 128), device=dev)
         plse = torch.empty((call[1], pcase.n_q_heads), device=dev)
+        pscratch = torch.empty(max(1, qsa.prompt_scratch_bytes(ppool, call[1], call[2])), dtype=torch.uint8,
+                               device=dev)
         for _ in range(2):
-            qsa.prompt_attn(ppool, pq, call[2], pout, plse)
+            qsa.prompt_attn(ppool, pq, call[2], pout, plse, scratch=pscratch)
         torch.cuda.synchronize()
         P = max(3, min(20, args.steps // 10))
         pev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(P)]
         for k in range(P):
             flush_l2()
             pev[k][0].record(stream)
-            qsa.prompt_attn(ppool, pq, call[2], pout, plse)
+            qsa.prompt_attn(ppool, pq, call[2], pout, plse, scratch=pscratch)
             pev[k][1].record(stream)
         torch.cuda.synchronize()
         if qsa.get_device_error() != 0:

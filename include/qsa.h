@@ -194,15 +194,31 @@ qsa_status qsa_attn_merge(const void* partials, const int32_t* n_sel, int n_rows
  *   lse[i,g] = ln sum_c exp(...)
  *   pool       (host) one descriptor; page_cells multiple of 64
  *   q          (dev)  fp32 [n_q][n_q_heads][128], 16-byte aligned
+ *   scratch    (dev)  caller-owned work space of scratch_bytes >=
+ *                     qsa_prompt_scratch_bytes(pool, n_q, q_pos0), 256-byte
+ *                     aligned; may be NULL when that size is 0.  With int8 V
+ *                     the call first converts every 64-cell tile it reads,
+ *                     once per KV head, into the fp16 operand image the
+ *                     tensor cores load (the codes are exact in fp16).
  *   out        (dev)  fp32 [n_q][n_q_heads][128], 16-byte aligned
  *   lse        (dev)  fp32 [n_q][n_q_heads], may be NULL
  *   q_pos0 >= 0, q_pos0 + n_q <= pool->n_filled
- * Errors: QSA_ERR_ARG, QSA_ERR_UNSUPPORTED (n_q_heads / n_kv_heads > 128).
+ * Errors: QSA_ERR_ARG, QSA_ERR_UNSUPPORTED (n_q_heads / n_kv_heads > 128),
+ * QSA_ERR_SCRATCH (scratch missing, misaligned or too small).
  * A kernel whose internal wait runs out sets the device error word (see
  * qsa_get_device_error) and leaves its outputs incomplete.
  */
 qsa_status qsa_prompt_attn(const qsa_pool* pool, const float* q, int n_q, int q_pos0,
-                           int n_q_heads, float* out, float* lse, void* stream);
+                           int n_q_heads, void* scratch, size_t scratch_bytes, float* out,
+                           float* lse, void* stream);
+
+/*
+ * qsa_prompt_scratch_bytes -- device scratch bytes qsa_prompt_attn needs for
+ * a call of n_q queries from position q_pos0 over `pool`: a 256-byte header
+ * plus 33,792 bytes per 64-cell tile of cells 0 .. q_pos0 + n_q - 1 per KV
+ * head with int8 V; 0 with 4-bit V.  Returns 0 for invalid arguments.
+ */
+size_t qsa_prompt_scratch_bytes(const qsa_pool* pool, int n_q, int q_pos0);
 
 /* Size of the library-owned scratch of qsa_decode_attn_noalloc (8 MiB). */
 #define QSA_NOALLOC_SCRATCH_BYTES (8u << 20)

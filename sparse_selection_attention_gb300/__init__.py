@@ -24,7 +24,7 @@ MAX_DECODE_ROWS = 32
 
 EXPORTS = [
     "qsa_block_scores", "qsa_topk", "qsa_decode_partials_bytes", "qsa_decode_attn", "qsa_attn_merge",
-    "qsa_prompt_attn", "qsa_get_device_error", "qsa_set_wait_limit_ns", "qsa_status_str", "qsa_abi_version",
+    "qsa_prompt_attn", "qsa_prompt_scratch_bytes", "qsa_get_device_error", "qsa_set_wait_limit_ns", "qsa_status_str", "qsa_abi_version",
     "qsa_decode_attn_noalloc",
 ]
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -65,7 +65,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qsa_decode_partials_bytes.restype = sz
     lib.qsa_decode_attn.argtypes = [pool_p, i, i32p, p, p, p, p, i, i, i, i, i, p, sz, p]
     lib.qsa_attn_merge.argtypes = [p, p, i, i, i, i, p, p, p]
-    lib.qsa_prompt_attn.argtypes = [pool_p, p, i, i, i, p, p, p]
+    lib.qsa_prompt_attn.argtypes = [pool_p, p, i, i, i, p, sz, p, p, p]
+    lib.qsa_prompt_scratch_bytes.argtypes = [pool_p, i, i]
+    lib.qsa_prompt_scratch_bytes.restype = sz
     lib.qsa_decode_attn_noalloc.argtypes = [pool_p, i, i32p, p, p, p, p, i, i, i, i, p, p, p]
     lib.qsa_get_device_error.argtypes = [i32p, p]
     lib.qsa_set_wait_limit_ns.argtypes = [u64]
@@ -170,12 +172,22 @@ def attn_merge(partials: torch.Tensor, n_sel: torch.Tensor, n_rows: int, n_q_hea
                                  _ptr(lse), _stream(stream)), "qsa_attn_merge")
 
 
+def prompt_scratch_bytes(pool: DevicePool, n_q: int, q_pos0: int) -> int:
+    pc = pool.c()
+    return int(load().qsa_prompt_scratch_bytes(ctypes.byref(pc), n_q, q_pos0))
+
+
 def prompt_attn(pool: DevicePool, q: torch.Tensor, q_pos0: int, out: torch.Tensor,
-                lse: Optional[torch.Tensor] = None, stream=None) -> None:
+                lse: Optional[torch.Tensor] = None, scratch: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Causal prompt attention.  `scratch` (uint8, device) must hold prompt_scratch_bytes(); when it is
+    None a buffer of that size is allocated for this call."""
     n_q, Hq, _ = q.shape
     pc = pool.c()
-    _check(load().qsa_prompt_attn(ctypes.byref(pc), _ptr(q), n_q, q_pos0, Hq, _ptr(out), _ptr(lse),
-                                  _stream(stream)), "qsa_prompt_attn")
+    if scratch is None:
+        need = prompt_scratch_bytes(pool, n_q, q_pos0)
+        scratch = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _check(load().qsa_prompt_attn(ctypes.byref(pc), _ptr(q), n_q, q_pos0, Hq, _ptr(scratch), scratch.numel(),
+                                  _ptr(out), _ptr(lse), _stream(stream)), "qsa_prompt_attn")
 
 
 def decode_attn_noalloc(pools: Sequence[DevicePool], row_pool: Sequence[int], q: torch.Tensor,

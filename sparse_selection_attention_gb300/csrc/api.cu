@@ -232,8 +232,13 @@ qsa_status qsa_attn_merge(const void* partials, const int32_t* n_sel, int n_rows
   return from_cuda(launch_attn_merge(p, static_cast<cudaStream_t>(stream)));
 }
 
-qsa_status qsa_prompt_attn(const qsa_pool* pool, const float* q, int n_q, int q_pos0, int n_q_heads, float* out,
-                           float* lse, void* stream) {
+size_t qsa_prompt_scratch_bytes(const qsa_pool* pool, int n_q, int q_pos0) {
+  if (!pool || n_q < 0 || q_pos0 < 0 || pool->n_kv_heads < 1) return 0;
+  return prompt_scratch_bytes(pool->v_bits, pool->n_kv_heads, q_pos0 + n_q);
+}
+
+qsa_status qsa_prompt_attn(const qsa_pool* pool, const float* q, int n_q, int q_pos0, int n_q_heads, void* scratch,
+                           size_t scratch_bytes, float* out, float* lse, void* stream) {
   if (!pool || !q || !out || !aligned16(q) || !aligned16(out)) return QSA_ERR_ARG;
   qsa_status s = check_pool(*pool, true);
   if (s != QSA_OK) return s;
@@ -241,7 +246,12 @@ qsa_status qsa_prompt_attn(const qsa_pool* pool, const float* q, int n_q, int q_
   if (n_q_heads < 1 || n_q_heads % pool->n_kv_heads != 0) return QSA_ERR_ARG;
   if (n_q_heads / pool->n_kv_heads > 128) return QSA_ERR_UNSUPPORTED;
   if (n_q == 0) return QSA_OK;
+  const size_t need = prompt_scratch_bytes(pool->v_bits, pool->n_kv_heads, q_pos0 + n_q);
+  if (need > 0 && (!scratch || (reinterpret_cast<uintptr_t>(scratch) & 255u) != 0 || scratch_bytes < need))
+    return QSA_ERR_SCRATCH;
   PromptParams p{};
+  p.scratch = static_cast<uint8_t*>(scratch);
+  p.n_tiles = (q_pos0 + n_q - 1) / 64 + 1;
   p.pool = to_dev(*pool);
   p.n_kv_heads = pool->n_kv_heads;
   p.n_q_heads = n_q_heads;
@@ -275,6 +285,6 @@ const char* qsa_status_str(qsa_status s) {
   return "unknown status";
 }
 
-int qsa_abi_version(void) { return 100; }
+int qsa_abi_version(void) { return 101; }
 
 }  // extern "C"

@@ -52,9 +52,12 @@ struct PromptParams {
   const float* q;
   float* out;
   float* lse;
+  uint8_t* scratch;   // tile images of the int8-V path (prompt_scratch_bytes)
+  int n_tiles;        // 64-cell tiles the call reads: (q_pos0 + n_q - 1) / 64 + 1
   unsigned long long wait_limit_ns;
 };
 
+size_t prompt_scratch_bytes(int v_bits, int n_kv_heads, int q_end_pos);
 size_t block_scores_smem_bytes(int n_rows, int n_q_heads, int n_kv_heads, int block_cells);
 bool block_scores_supported(int n_kv_heads, int block_cells);
 int block_scores_q_rows_per_batch(int n_rows, int n_q_heads, int n_kv_heads, int block_cells);

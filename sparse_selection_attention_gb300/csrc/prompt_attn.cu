@@ -517,50 +517,56 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const PromptPa
 
 namespace ws {
 
-// Warp-specialised prompt attention for int8 V.  Roles of the 16 warps:
-//   warp 0      one thread issues the bulk copies of each 64-cell K/V tile (codes and scales) into a
-//               3-stage ring of raw staging buffers;
-//   warp 1      issues every tcgen05.mma (one thread): S(i) = Q K(i)^T, with Q (hi and lo) held in
-//               tensor memory, into one of two S slots; then P += W(i-1) V(i-1), W read from the S
-//               slot it was written over;
-//   warps 4-7   convert raw tiles into fp16 operands in a 3-stage ring: K and V keep their stored
-//               [cell][dim] order (K is the K-major B operand of S = Q K^T, V the MN-major B operand
-//               of P = W V), plus the tile's K scales and V scales times a power of two 2^k;
-//   warps 8-15  softmax, two threads per row (warps w and w+4 share rows, 32 cells and 64 output
-//               dims each): logits, running max (rescaled lazily, past 2^8), p, and
-//               W = p * vscale * 2^k split into fp16 hi + lo, stored over S(i).
-// S(i+1) overlaps the softmax of tile i and P.V of tile i-1.  P holds at most kFoldEvery tiles in
-// tensor memory: a warp folds its rows' P into the fp32 output O in shared memory (O = O * factor + P)
-// and zeroes P whenever one of its rows changes its running max, when the V-scale exponent changes,
-// and every kFoldEvery tiles, so that P only ever holds tiles of one reference per row.  The only
-// thread barrier in the loop joins the two warps of a row pair; every other hand-off is an mbarrier
-// with a bounded wait.  A wait that runs out sets the device error word; every role then stops at
-// its next wait and the CTA drains its copies and MMAs before it exits.
-constexpr int kThreads = 512;
+// Warp-specialised prompt attention for int8 V, in two launches.
+//
+// 1. prompt_stage_kernel converts each 64-cell tile of the context once per KV head into the
+//    exact shared-memory image the tensor cores read: K and V codes as fp16 (exact) in their
+//    stored [cell][dim] order, two 64-dim blocks each in the 128-byte swizzle, then the tile's K
+//    and V scales group-major ([group][cell], 0 past n_filled).  It also takes the head's
+//    largest |V scale| (atomic max on its bits).
+// 2. prompt_attn_ws_kernel, one CTA per (128 rows, KV head), 12 warps in three warpgroups; the
+//    first gives registers to the other two (setmaxnreg):
+//      warp 0      one thread copies each tile image (one bulk copy) into a 6-stage ring;
+//      warp 1      issues every tcgen05.mma from one elected lane: S(i) = Q K(i)^T with Q (hi and
+//                  lo) held in tensor memory, into one of two S slots; then P += W(i-1) V(i-1)
+//                  with W read from the S slot it was written over (V the MN-major B operand);
+//      warps 4-11  softmax, two threads per row (warps w and w+4 share TMEM lanes 32 (w % 4)..,
+//                  rows; 32 cells and 64 output dims each): logits, running max (lazy, past 2^8),
+//                  p = 2^(y - m + k) with k the head's V-scale exponent (max |vs| 2^k in
+//                  [8, 16)), W = p vscale split into fp16 hi + lo, stored over S(i).
+//    S(i+1) overlaps the softmax of tile i and P.V of tile i-1.  P holds at most kFoldEvery tiles
+//    in tensor memory: a warp folds its rows' P into the output O, kept in registers
+//    (O = O * factor + P), and zeroes P when one of its rows changes its running max and every
+//    kFoldEvery tiles.  The only thread barrier in the loop joins the two warps of a row pair;
+//    every other hand-off is an mbarrier with a bounded wait.  A wait that runs out sets the
+//    device error word; every role then stops at its next wait and the CTA drains its copies and
+//    MMAs before it exits.
+constexpr int kThreads = 384;
+// Register split: launched at kLaunchRegs a thread (the compiler's count, checked on the host
+// before every launch), warpgroup 0 drops to kRegsLow and the softmax warpgroups rise to
+// kRegsHigh; 128 kRegsLow + 256 kRegsHigh = 384 kLaunchRegs.
+constexpr int kLaunchRegs = 168, kRegsLow = 56, kRegsHigh = 224;
+static_assert(128 * kRegsLow + 256 * kRegsHigh <= kThreads * kLaunchRegs, "register split exceeds the launch");
 constexpr int kM = 128;
 constexpr int kN = 64;
-constexpr int kRawStages = 3;
+constexpr int kStages = 6;
 constexpr int kFoldEvery = 8;
+// Tile image (global scratch and shared-memory stage alike).
+constexpr int kImgK = 0, kImgV = 16384, kImgKs = 32768, kImgVs = 33280, kImgBytes = 33792;
+constexpr int kScratchHeader = 256;   // uint32 max |V scale| bits per KV head
 // Tensor memory columns (512 allocated).
 constexpr uint32_t kTQ = 0;     // Q of dim group g: hi at 64g, lo at 64g + 32 (fp16 pairs)
 constexpr uint32_t kTS = 128;   // S slot s at 128 + 128s: S_g at +64g (fp32); W_g hi at +64g, lo at +64g+32
 constexpr uint32_t kTP = 384;   // P: output dim d at 384 + d (fp32)
 // Shared memory map (offsets from a 1024-byte aligned base).
-constexpr int kO = 0;                                   // O [128 dims][128 rows] fp32
-constexpr int kOpStages = 3;
-constexpr int kOp0 = 65536, kOpBytes = 32768;           // op stage: K, V as [dim group][64 cells][128 B]
-constexpr int kOpK = 0, kOpV = 16384;
-constexpr int kRaw0 = kOp0 + kOpStages * kOpBytes, kRawBytes = 17408;   // raw K 8 KB, V 8 KB, ks, vs 512 B
-constexpr int kRK = 0, kRV = 8192, kRKs = 16384, kRVs = 16896;
-constexpr int kAux0 = kRaw0 + kRawStages * kRawBytes, kAuxBytes = 1088;   // per op stage
-constexpr int kAuxKs = 0, kAuxVs = 512, kAuxInfo = 1024;                  // ks [2][64], vs [2][64], k, changed
-constexpr int kRed = kAux0 + kOpStages * kAuxBytes;             // row maxima [2][2][128], row sums [2][128], flags [2][8]
+constexpr int kStage0 = 0;
+constexpr int kRed = kStage0 + kStages * kImgBytes;     // row maxima [2][2][128], row sums [2][128], flags [2][8]
 constexpr int kRedMax = 0, kRedSum = 512, kRedFlag = 768;   // in 4-byte words
 constexpr int kCtl = kRed + 4096;
 constexpr int kSmemBytes = kCtl + 512 + 1024;           // + alignment slack
 
-constexpr int RAW_FULL = 0, RAW_EMPTY = 3, OP_FULL = 6, OP_EMPTY = 9, S_FULL = 12, S_EMPTY = 14, W_FULL = 16,
-              N_BARS = 18;
+constexpr int FULL = 0, EMPTY = kStages, S_FULL = 2 * kStages, S_EMPTY = S_FULL + 2, W_FULL = S_EMPTY + 2,
+              N_BARS = W_FULL + 2;
 constexpr int C_ABORT = 0, C_TMEM = 1, C_ISSUED = 2, C_LAST_BAR = 3, C_LAST_PAR = 4, N_CTL = 5;
 
 struct Ctl {
@@ -633,6 +639,44 @@ __device__ __forceinline__ void split_pair(uint64_t ab, uint32_t& hi, uint32_t& 
   lo = h2_bits(__floats2half2_rn(rem.x, rem.y));
 }
 
+// One CTA per (64-cell tile, KV head), 128 threads: thread (cell ct / 2, dim block ct % 2).
+__global__ void __launch_bounds__(128) prompt_stage_kernel(const PoolDev pool, int n_kv_heads, int n_tiles,
+                                                           uint8_t* scratch) {
+  const int t = blockIdx.x, h = blockIdx.y, ct = threadIdx.x, lane = ct & 31;
+  uint8_t* img = scratch + kScratchHeader + ((size_t)h * n_tiles + t) * kImgBytes;
+  const int cell0 = t * kN;
+  const int page = __ldg(pool.page_table + cell0 / pool.page_cells);
+  const long long slot0 = ((long long)page * n_kv_heads + h) * pool.page_cells + (cell0 % pool.page_cells);
+  const int cc = ct >> 1, hf = ct & 1;
+#pragma unroll
+  for (int kv = 0; kv < 2; ++kv) {
+    const uint4* src = reinterpret_cast<const uint4*>(
+        (kv ? pool.v_codes : reinterpret_cast<const uint8_t*>(pool.k_codes)) + (slot0 + cc) * kD + hf * 64);
+    uint8_t* dst = img + (kv ? kImgV : kImgK) + hf * 8192;
+    uint4 v[4];
+#pragma unroll
+    for (int s4 = 0; s4 < 4; ++s4) v[s4] = __ldg(src + s4);
+#pragma unroll
+    for (int s4 = 0; s4 < 4; ++s4) {
+      uint32_t hh[8];
+      s8x4_to_h2x2(v[s4].x, hh[0], hh[1]);
+      s8x4_to_h2x2(v[s4].y, hh[2], hh[3]);
+      s8x4_to_h2x2(v[s4].z, hh[4], hh[5]);
+      s8x4_to_h2x2(v[s4].w, hh[6], hh[7]);
+      *reinterpret_cast<uint4*>(dst + sw128(cc, 2 * s4)) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+      *reinterpret_cast<uint4*>(dst + sw128(cc, 2 * s4 + 1)) = make_uint4(hh[4], hh[5], hh[6], hh[7]);
+    }
+  }
+  const int g = ct & 1;
+  const bool valid = cell0 + cc < pool.n_filled;
+  const float ksv = valid ? __ldg(pool.k_scales + (slot0 + cc) * 2 + g) : 0.f;
+  const float vsv = valid ? __ldg(pool.v_scales + (slot0 + cc) * 2 + g) : 0.f;
+  reinterpret_cast<float*>(img + kImgKs)[g * 64 + cc] = ksv;
+  reinterpret_cast<float*>(img + kImgVs)[g * 64 + cc] = vsv;
+  const float mx = warp_max(fabsf(vsv));
+  if (lane == 0) atomicMax(reinterpret_cast<unsigned int*>(scratch) + h, __float_as_uint(mx));
+}
+
 __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const PromptParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -644,7 +688,6 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
   const int kvh = blockIdx.y;
   const int q_begin = blockIdx.x * QPC;
   const int q_end = min(p.n_q, q_begin + QPC);
-  const PoolDev& pool = p.pool;
   const int pos_first = p.q_pos0 + q_begin;
   const int pos_last = p.q_pos0 + q_end - 1;
   const int n_tiles = pos_last / kN + 1;
@@ -657,13 +700,9 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
   volatile int* wflag = reinterpret_cast<volatile int*>(red + kRedFlag);
 
   if (tid == 0) {
-    for (int s = 0; s < kRawStages; ++s) {
-      tc::mbar_init(c.bars + 8 * (RAW_FULL + s), 1);
-      tc::mbar_init(c.bars + 8 * (RAW_EMPTY + s), 4);
-    }
-    for (int s = 0; s < kOpStages; ++s) {
-      tc::mbar_init(c.bars + 8 * (OP_FULL + s), 4);
-      tc::mbar_init(c.bars + 8 * (OP_EMPTY + s), 1);
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(c.bars + 8 * (FULL + s), 1);
+      tc::mbar_init(c.bars + 8 * (EMPTY + s), 1);
     }
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(c.bars + 8 * (S_FULL + s), 1);
@@ -680,10 +719,10 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
   const uint32_t tmem = static_cast<uint32_t>(c.w[C_TMEM]);
 
   // Softmax threads: row r of the CTA (TMEM lane r), half h (cells 32h.., output dims 64h..).
-  const bool is_sm = warp >= 8;
+  const bool is_sm = warp >= 4;
   const int quarter = warp & 3;
   const int r = 32 * quarter + lane;
-  const int half = (warp - 8) >> 2;
+  const int half = (warp - 4) >> 2;
   const int qi = q_begin + r / G;
   const bool row_valid = (r < QPC * G) && (qi < q_end);
   const int head = kvh * G + (r % G);
@@ -724,186 +763,146 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
   // =========================================================== producer
-  if (warp == 0) {
-    if (lane == 0) {
-      int issued = 0;
-      for (int i = 0; i < n_tiles; ++i) {
-        const int st = i % kRawStages;
-        if (i >= kRawStages && !wait_b(c, RAW_EMPTY + st, ((i / kRawStages) - 1) & 1, limit)) break;
-        const int cell0 = i * kN;
-        const int page = __ldg(pool.page_table + cell0 / pool.page_cells);
-        const long long slot0 = ((long long)page * Hkv + kvh) * pool.page_cells + (cell0 % pool.page_cells);
-        const uint32_t dst = sbase + kRaw0 + st * kRawBytes;
-        const uint32_t bar = c.bars + 8 * (RAW_FULL + st);
-        tc::mbar_expect_tx(bar, 8192 + 8192 + 512 + 512);
-        tc::bulk_g2s(dst + kRK, pool.k_codes + slot0 * kD, 8192, bar);
-        tc::bulk_g2s(dst + kRV, pool.v_codes + slot0 * kD, 8192, bar);
-        tc::bulk_g2s(dst + kRKs, pool.k_scales + slot0 * 2, 512, bar);
-        tc::bulk_g2s(dst + kRVs, pool.v_scales + slot0 * 2, 512, bar);
-        issued = i + 1;
-      }
-      c.w[C_ISSUED] = issued;
-    }
-  }
-  // =========================================================== MMA issuer
-  // The whole warp runs the loop and waits; one elected lane issues (converged issue keeps the
-  // operands in uniform registers).  Descriptors step by 32-bit adds on their low word.
-  else if (warp == 1) {
-    const uint32_t idesc = tc::idesc_f16_f32(kM, 64);
-    const uint32_t idesc_v = tc::idesc_f16_f32_bmn(kM, 64);
-    const uint32_t d_hi = tc::sw128_desc_hi();
-    const uint32_t k_lo0 = tc::sw128_desc_lo(sbase + kOp0 + kOpK, 16);
-    const uint32_t v_lo0 = tc::sw128_desc_lo(sbase + kOp0 + kOpV, 8192);
-    int last_bar = -1;
-    uint32_t last_par = 0;
-    for (int i = 0; i <= n_tiles; ++i) {
-      if (i < n_tiles) {
-        const int sl = i & 1, os = i % kOpStages;
-        bool ok = wait_b(c, OP_FULL + os, (i / kOpStages) & 1, limit);
-        if (ok && i >= 2) ok = wait_b(c, S_EMPTY + sl, ((i - 2) >> 1) & 1, limit);
-        if (!__all_sync(0xffffffffu, ok)) break;
-        tc::fence_after_sync();
-        if (tc::elect_one()) {
-          const uint32_t k_lo = k_lo0 + (uint32_t)(os * (kOpBytes >> 4));
-          const uint32_t d = tmem + kTS + 128 * sl;
-#pragma unroll
-          for (int g = 0; g < 2; ++g) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint32_t b_lo = k_lo + (uint32_t)((g * 8192 + kk * 32) >> 4);
-              tc::mma_f16_tmem_a_w(d + 64 * g, tmem + kTQ + 64 * g + 8 * kk, b_lo, d_hi, idesc, kk > 0 ? 1u : 0u);
-              tc::mma_f16_tmem_a_w(d + 64 * g, tmem + kTQ + 64 * g + 32 + 8 * kk, b_lo, d_hi, idesc, 1u);
-            }
-          }
-          tc::mma_commit(c.bars + 8 * (S_FULL + sl));
-        }
-        __syncwarp();
-        last_bar = S_FULL + sl;
-        last_par = (i >> 1) & 1;
-      }
-      if (i >= 1) {
-        const int j = i - 1, sj = j & 1, oj = j % kOpStages;
-        if (!__all_sync(0xffffffffu, wait_b(c, W_FULL + sj, (j >> 1) & 1, limit))) break;
-        tc::fence_after_sync();
-        if (tc::elect_one()) {
-          const uint32_t v_lo = v_lo0 + (uint32_t)(oj * (kOpBytes >> 4));
-          const uint32_t aw = tmem + kTS + 128 * sj;
-          const uint32_t acc0 = j > 0 ? 1u : 0u;
-#pragma unroll
-          for (int g = 0; g < 2; ++g) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint32_t b_lo = v_lo + (uint32_t)((g * 8192 + kk * 2048) >> 4);
-              tc::mma_f16_tmem_a_w(tmem + kTP + 64 * g, aw + 64 * g + 8 * kk, b_lo, d_hi, idesc_v, kk > 0 ? 1u : acc0);
-              tc::mma_f16_tmem_a_w(tmem + kTP + 64 * g, aw + 64 * g + 32 + 8 * kk, b_lo, d_hi, idesc_v, 1u);
-            }
-          }
-          tc::mma_commit(c.bars + 8 * (S_EMPTY + sj));
-          tc::mma_commit(c.bars + 8 * (OP_EMPTY + oj));
-        }
-        __syncwarp();
-        last_bar = OP_EMPTY + oj;
-        last_par = (j / kOpStages) & 1;
-      }
-    }
-    if (lane == 0) {
-      c.w[C_LAST_BAR] = last_bar;
-      c.w[C_LAST_PAR] = (int)last_par;
-    }
-  }
-  // =========================================================== converters
-  else if (warp >= 4 && warp < 8) {
-    const int cw = warp - 4;
-    const int ct = tid - 128;   // 0..127
-    int k_ref = 0;              // V-scale exponent reference (the same in the 4 warps)
-    for (int i = 0; i < n_tiles; ++i) {
-      const int rs = i % kRawStages, os = i % kOpStages;
-      bool ok = wait_b(c, RAW_FULL + rs, (i / kRawStages) & 1, limit);
-      if (ok && i >= kOpStages) ok = wait_b(c, OP_EMPTY + os, ((i / kOpStages) - 1) & 1, limit);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      const uint8_t* raw = smem + kRaw0 + rs * kRawBytes;
-      uint8_t* op = smem + kOp0 + os * kOpBytes;
-      uint8_t* aux = smem + kAux0 + os * kAuxBytes;
-      const int cell0 = i * kN;
-      // K and V codes -> fp16 in their stored order: [dim group][cell][64 dims, 128 B], 128-byte
-      // swizzle (cells 16cw..16cw+15; thread: one cell, one dim group, of K and of V).
-      {
-        const int cc = ct >> 1, hf = ct & 1;
-#pragma unroll
-        for (int kv = 0; kv < 2; ++kv) {
-          const uint8_t* src = raw + (kv ? kRV : kRK) + cc * 128 + hf * 64;
-          uint8_t* dst = op + (kv ? kOpV : kOpK) + hf * 8192;
-#pragma unroll
-          for (int s4 = 0; s4 < 4; ++s4) {
-            const int i4 = (s4 + cc) & 3;
-            const uint4 v = *reinterpret_cast<const uint4*>(src + i4 * 16);
-            uint32_t hh[8];
-            s8x4_to_h2x2(v.x, hh[0], hh[1]);
-            s8x4_to_h2x2(v.y, hh[2], hh[3]);
-            s8x4_to_h2x2(v.z, hh[4], hh[5]);
-            s8x4_to_h2x2(v.w, hh[6], hh[7]);
-            *reinterpret_cast<uint4*>(dst + sw128(cc, 2 * i4)) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
-            *reinterpret_cast<uint4*>(dst + sw128(cc, 2 * i4 + 1)) = make_uint4(hh[4], hh[5], hh[6], hh[7]);
-          }
-        }
-      }
-      // Scales, group-major.  Every warp takes the max |vs| of the whole tile (cells below n_filled)
-      // itself, so the four agree on k without a barrier; k only decreases, tile by tile.
-      {
-        const float* ksr = reinterpret_cast<const float*>(raw + kRKs);
-        const float* vsr = reinterpret_cast<const float*>(raw + kRVs);
-        const float4 v4 = reinterpret_cast<const float4*>(vsr)[lane];   // cells 2 lane, 2 lane + 1
-        float mx = 0.f;
-        if (cell0 + 2 * lane < pool.n_filled) mx = fmaxf(fabsf(v4.x), fabsf(v4.y));
-        if (cell0 + 2 * lane + 1 < pool.n_filled) mx = fmaxf(mx, fmaxf(fabsf(v4.z), fabsf(v4.w)));
-        mx = warp_max(mx);
-        int e = 0;
-        if (mx > 0.f) frexpf(mx, &e);
-        const int kt = mx > 0.f ? 4 - e : k_ref;   // max |vs| 2^k in [8, 16)
-        int changed = 0;
-        if (i == 0) k_ref = kt;
-        else if (kt < k_ref) { k_ref = kt; changed = 1; }
-        const int cl = 16 * cw + (lane >> 1), g = lane & 1;
-        float* ksa = reinterpret_cast<float*>(aux + kAuxKs);
-        float* vsa = reinterpret_cast<float*>(aux + kAuxVs);
-        ksa[g * 64 + cl] = ksr[2 * cl + g];
-        vsa[g * 64 + cl] = (cell0 + cl < pool.n_filled) ? vsr[2 * cl + g] * pow2f(k_ref) : 0.f;
-        if (ct == 0) {
-          reinterpret_cast<volatile int*>(aux + kAuxInfo)[0] = k_ref;
-          reinterpret_cast<volatile int*>(aux + kAuxInfo)[1] = changed;
-        }
-      }
-      tc::fence_proxy_async_smem();
-      __syncwarp();
+    if (warp == 0) {
       if (lane == 0) {
-        arrive(c, RAW_EMPTY + rs);
-        arrive(c, OP_FULL + os);
+        const uint8_t* img0 = p.scratch + kScratchHeader + (size_t)kvh * p.n_tiles * kImgBytes;
+        int issued = 0;
+        for (int i = 0; i < n_tiles; ++i) {
+          const int st = i % kStages;
+          if (i >= kStages && !wait_b(c, EMPTY + st, ((i / kStages) - 1) & 1, limit)) break;
+          const uint32_t bar = c.bars + 8 * (FULL + st);
+          tc::mbar_expect_tx(bar, kImgBytes);
+          tc::bulk_g2s(sbase + kStage0 + st * kImgBytes, img0 + (size_t)i * kImgBytes, kImgBytes, bar);
+          issued = i + 1;
+        }
+        c.w[C_ISSUED] = issued;
       }
     }
+  // =========================================================== MMA issuer
+    // The whole warp runs the loop and waits; one elected lane issues (converged issue keeps the
+    // operands in uniform registers).  Descriptors step by 32-bit adds on their low word.
+    else if (warp == 1) {
+      const uint32_t idesc = tc::idesc_f16_f32(kM, 64);
+      const uint32_t idesc_v = tc::idesc_f16_f32_bmn(kM, 64);
+      const uint32_t d_hi = tc::sw128_desc_hi();
+      const uint32_t k_lo0 = tc::sw128_desc_lo(sbase + kStage0 + kImgK, 16);
+      const uint32_t v_lo0 = tc::sw128_desc_lo(sbase + kStage0 + kImgV, 8192);
+      int last_bar = -1;
+      uint32_t last_par = 0;
+      for (int i = 0; i <= n_tiles; ++i) {
+        if (i < n_tiles) {
+          const int sl = i & 1, st = i % kStages;
+          bool ok = wait_b(c, FULL + st, (i / kStages) & 1, limit);
+          if (ok && i >= 2) ok = wait_b(c, S_EMPTY + sl, ((i - 2) >> 1) & 1, limit);
+          if (!__all_sync(0xffffffffu, ok)) break;
+          tc::fence_after_sync();
+          if (tc::elect_one()) {
+            const uint32_t k_lo = k_lo0 + (uint32_t)(st * (kImgBytes >> 4));
+            const uint32_t d = tmem + kTS + 128 * sl;
+  #pragma unroll
+            for (int g = 0; g < 2; ++g) {
+  #pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint32_t b_lo = k_lo + (uint32_t)((g * 8192 + kk * 32) >> 4);
+                tc::mma_f16_tmem_a_w(d + 64 * g, tmem + kTQ + 64 * g + 8 * kk, b_lo, d_hi, idesc, kk > 0 ? 1u : 0u);
+                tc::mma_f16_tmem_a_w(d + 64 * g, tmem + kTQ + 64 * g + 32 + 8 * kk, b_lo, d_hi, idesc, 1u);
+              }
+            }
+            tc::mma_commit(c.bars + 8 * (S_FULL + sl));
+          }
+          __syncwarp();
+          last_bar = S_FULL + sl;
+          last_par = (i >> 1) & 1;
+        }
+        if (i >= 1) {
+          const int j = i - 1, sj = j & 1, sv = j % kStages;
+          if (!__all_sync(0xffffffffu, wait_b(c, W_FULL + sj, (j >> 1) & 1, limit))) break;
+          tc::fence_after_sync();
+          if (tc::elect_one()) {
+            const uint32_t v_lo = v_lo0 + (uint32_t)(sv * (kImgBytes >> 4));
+            const uint32_t aw = tmem + kTS + 128 * sj;
+            const uint32_t acc0 = j > 0 ? 1u : 0u;
+  #pragma unroll
+            for (int g = 0; g < 2; ++g) {
+  #pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint32_t b_lo = v_lo + (uint32_t)((g * 8192 + kk * 2048) >> 4);
+                tc::mma_f16_tmem_a_w(tmem + kTP + 64 * g, aw + 64 * g + 8 * kk, b_lo, d_hi, idesc_v, kk > 0 ? 1u : acc0);
+                tc::mma_f16_tmem_a_w(tmem + kTP + 64 * g, aw + 64 * g + 32 + 8 * kk, b_lo, d_hi, idesc_v, 1u);
+              }
+            }
+            tc::mma_commit(c.bars + 8 * (S_EMPTY + sj));
+            tc::mma_commit(c.bars + 8 * (EMPTY + sv));
+          }
+          __syncwarp();
+          last_bar = EMPTY + sv;
+          last_par = (j / kStages) & 1;
+        }
+      }
+      if (lane == 0) {
+        c.w[C_LAST_BAR] = last_bar;
+        c.w[C_LAST_PAR] = (int)last_par;
+      }
+    }
+    // After an abort (seen by every role at the first barrier), nothing may still write this
+    // CTA's shared or tensor memory when it exits: wait for the latest fill of every stage and the
+    // last MMA commit.  (The softmax warpgroups meet these two barriers at the end of their branch.)
+    __syncthreads();
+    if (c.w[C_ABORT] && lane == 0) {
+      const int issued = c.w[C_ISSUED], last_bar = c.w[C_LAST_BAR];
+      if (warp == 0) {
+        for (int st = 0; st < kStages && st < issued; ++st) {
+          const int last = st + kStages * ((issued - 1 - st) / kStages);
+          tc::mbar_wait(c.bars + 8 * (FULL + st), (last / kStages) & 1, 2000000000ull);
+        }
+      } else if (warp == 1 && last_bar >= 0) {
+        tc::mbar_wait(c.bars + 8 * last_bar, (uint32_t)c.w[C_LAST_PAR], 2000000000ull);
+      }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+      tc::fence_after_sync();
+      tc::tmem_dealloc(tmem, 512);
+    }
+    return;
   }
+
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
   // =========================================================== softmax
-  else if (is_sm) {
-    const int pair_bar = 1 + quarter;          // warps quarter + 8 and quarter + 12
-    const int partner = (warp - 8) ^ 4;
-    float* O = reinterpret_cast<float*>(smem + kO);
+  {
+    const int pair_bar = 1 + quarter;          // the two warps on TMEM lanes 32 quarter ..
+    const int widx = warp - 4, partner = widx ^ 4;
+    // V-scale exponent of the head: max |vs| 2^k in [8, 16); p carries the factor 2^k, which
+    // cancels between the output and the row sum.
+    int kv_exp = 0;
+    {
+      const float vmax = __uint_as_float(reinterpret_cast<const unsigned int*>(p.scratch)[kvh]);
+      int e = 0;
+      if (vmax > 0.f) frexpf(vmax, &e);
+      kv_exp = vmax > 0.f ? 4 - e : 0;
+    }
+    float O[64];
+#pragma unroll
+    for (int j = 0; j < 64; ++j) O[j] = 0.f;
     float m_P = -INFINITY, m_O = -INFINITY, l = 0.f;
-    int k_P = 0, k_O = 0;
     bool o_empty = true, alive = true;
     const float zero16[16] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int i = 0; i < n_tiles; ++i) {
-      const int sl = i & 1;
-      bool ok = wait_b(c, OP_FULL + i % kOpStages, (i / kOpStages) & 1, limit);
+      const int sl = i & 1, st = i % kStages;
+      bool ok = wait_b(c, FULL + st, (i / kStages) & 1, limit);
       if (ok) ok = wait_b(c, S_FULL + sl, (i >> 1) & 1, limit);
       ok = __all_sync(0xffffffffu, ok && !c.w[C_ABORT]);
-      const uint8_t* aux = smem + kAux0 + (i % kOpStages) * kAuxBytes;
+      const uint8_t* img = smem + kStage0 + st * kImgBytes;
       const int cell0 = i * kN;
       float X[32];
       float xmax = -INFINITY;
       if (ok) {
         tc::fence_after_sync();
-        const float* ksa = reinterpret_cast<const float*>(aux + kAuxKs);
+        const float* ksa = reinterpret_cast<const float*>(img + kImgKs);
 #pragma unroll
         for (int q2 = 0; q2 < 2; ++q2) {
           float s0[16], s1[16];
@@ -934,55 +933,52 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
       }
       // Row maximum over the two halves; the pair also agrees on whether to go on.
       red[kRedMax + (sl * 2 + half) * 128 + r] = xmax;
-      if (lane == 0) wflag[sl * 8 + (warp - 8)] = ok ? 1 : 0;
+      if (lane == 0) wflag[sl * 8 + widx] = ok ? 1 : 0;
       tc::named_barrier(pair_bar, 64);
       if (!ok || !wflag[sl * 8 + partner]) { alive = false; break; }
       xmax = fmaxf(xmax, red[kRedMax + (sl * 2 + (half ^ 1)) * 128 + r]);
-      const int k_tile = reinterpret_cast<const volatile int*>(aux + kAuxInfo)[0];
-      const int k_changed = reinterpret_cast<const volatile int*>(aux + kAuxInfo)[1];
       const float ymax = xmax * lambda;   // lambda > 0
       const float m_new = (ymax > m_P + 8.0f) ? ymax : m_P;
-      const bool fold = __any_sync(0xffffffffu, i > 0 && (m_new != m_P || k_changed || i % kFoldEvery == 0));
+      const bool fold = __any_sync(0xffffffffu, i > 0 && (m_new != m_P || i % kFoldEvery == 0));
       if (fold) {
-        // P holds this warp's rows since their last fold, referenced to (m_P, k_P); after P.V(i-1):
-        // O = O * 2^(m_O - m_P) * 2^(k_P - k_O) + P, then P = 0.  (A wait that runs out only raises
-        // the abort: the pair stops at its next barrier.)
+        // P holds this warp's rows since their last fold, referenced to m_P; after P.V(i-1):
+        // O = O 2^(m_O - m_P) + P, then P = 0.  (A wait that runs out only raises the abort: the
+        // pair stops at its next barrier.)
         wait_b(c, S_EMPTY + ((i - 1) & 1), ((i - 1) >> 1) & 1, limit);
         tc::fence_after_sync();
-        const float fo = o_empty ? 0.f : ex2(m_O - m_P) * pow2f(k_P - k_O);
-#pragma unroll 1
+        const float fo = o_empty ? 0.f : ex2(m_O - m_P);
+#pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
           float pv[16];
           tc::tmem_ld16(tl + kTP + 64 * half + 16 * c4, pv);
           tc::tmem_wait_ld();
-          float* od = O + (64 * half + 16 * c4) * kM + r;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) od[j * kM] = o_empty ? pv[j] : fmaf(od[j * kM], fo, pv[j]);
+          for (int j = 0; j < 16; ++j) O[16 * c4 + j] = fmaf(O[16 * c4 + j], fo, pv[j]);
           tc::tmem_st16f(tl + kTP + 64 * half + 16 * c4, zero16);
         }
         o_empty = false;
         m_O = m_P;
-        k_O = k_P;
       }
       if (m_new != m_P) {
         if (m_P != -INFINITY) l *= ex2(m_P - m_new);
         m_P = m_new;
       }
-      k_P = k_tile;
-      // p = 2^(X lambda - m), this half's row sum, W = p vscale 2^k in fp16 hi/lo over S(i).
+      // p = 2^(X lambda - m + k), this half's row sum, W = p vscale in fp16 hi/lo over S(i).
       {
-        const uint64_t lam2 = pk(lambda, lambda), negm2 = pk(-m_P, -m_P);
+        const uint64_t lam2 = pk(lambda, lambda);
+        const float nm = (float)kv_exp - m_P;
+        const uint64_t nm2 = pk(nm, nm);
         float psum = 0.f;
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
-          const float2 y = upk(ffma2(pk(X[j], X[j + 1]), lam2, negm2));
+          const float2 y = upk(ffma2(pk(X[j], X[j + 1]), lam2, nm2));
           X[j] = ex2(y.x);
           X[j + 1] = ex2(y.y);
           psum += X[j] + X[j + 1];
         }
         l += psum;
       }
-      const float* vsa = reinterpret_cast<const float*>(aux + kAuxVs);
+      const float* vsa = reinterpret_cast<const float*>(img + kImgVs);
 #pragma unroll
       for (int g = 0; g < 2; ++g) {
         uint32_t hi[16], lo[16];
@@ -1000,67 +996,71 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
       __syncwarp();
       if (lane == 0) arrive(c, W_FULL + sl);
     }
-    // ---- epilogue: after the last P.V, out = (O * factor + P) 2^-k / l, lse = (m + log2 l) ln 2.
+    // ---- epilogue: after the last P.V, out = (O 2^(m_O - m) + P) / l, lse = (m - k + log2 l) ln 2.
     if (alive) {
       wait_b(c, S_EMPTY + ((n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1, limit);
       tc::fence_after_sync();
       red[kRedSum + half * 128 + r] = l;
       tc::named_barrier(pair_bar, 64);
       const float lt = red[kRedSum + r] + red[kRedSum + 128 + r];
-      const float fo = o_empty ? 0.f : ex2(m_O - m_P) * pow2f(k_P - k_O);
-      const float scale = pow2f(-k_P) / lt;
+      const float fo = o_empty ? 0.f : ex2(m_O - m_P);
+      const float scale = 1.f / lt;
       float* orow = p.out + ((size_t)qi * p.n_q_heads + head) * kD + 64 * half;
-#pragma unroll 1
+#pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {
         float pv[16];
         tc::tmem_ld16(tl + kTP + 64 * half + 16 * c4, pv);
         tc::tmem_wait_ld();
-        const float* od = O + (64 * half + 16 * c4) * kM + r;
         if (row_valid) {
 #pragma unroll
           for (int j = 0; j < 16; j += 4) {
             float v[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-              v[u] = (o_empty ? pv[j + u] : fmaf(od[(j + u) * kM], fo, pv[j + u])) * scale;
+            for (int u = 0; u < 4; ++u) v[u] = fmaf(O[16 * c4 + j + u], fo, pv[j + u]) * scale;
             *reinterpret_cast<float4*>(orow + 16 * c4 + j) = make_float4(v[0], v[1], v[2], v[3]);
           }
         }
       }
-      if (row_valid && half == 0 && p.lse) p.lse[(size_t)qi * p.n_q_heads + head] = (m_P + log2f(lt)) * kLn2;
-    }
-  }
-
-  // After an abort (seen here by every role), nothing may still write this CTA's shared or tensor
-  // memory when it exits: wait for the latest fill of every raw stage and the last MMA commit.
-  __syncthreads();
-  if (c.w[C_ABORT] && lane == 0) {
-    const int issued = c.w[C_ISSUED], last_bar = c.w[C_LAST_BAR];
-    if (warp == 0) {
-      for (int st = 0; st < kRawStages && st < issued; ++st) {
-        const int last = st + kRawStages * ((issued - 1 - st) / kRawStages);
-        tc::mbar_wait(c.bars + 8 * (RAW_FULL + st), (last / kRawStages) & 1, 2000000000ull);
-      }
-    } else if (warp == 1 && last_bar >= 0) {
-      tc::mbar_wait(c.bars + 8 * last_bar, (uint32_t)c.w[C_LAST_PAR], 2000000000ull);
+      if (row_valid && half == 0 && p.lse)
+        p.lse[(size_t)qi * p.n_q_heads + head] = (m_P - (float)kv_exp + log2f(lt)) * kLn2;
     }
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 1) {
-    tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, 512);
-  }
+  __syncthreads();
 }
 
 }  // namespace ws
+
+size_t prompt_scratch_bytes(int v_bits, int n_kv_heads, int q_end_pos) {
+  if (v_bits != 8 || q_end_pos <= 0) return 0;
+  const int n_tiles = (q_end_pos - 1) / ws::kN + 1;
+  return (size_t)ws::kScratchHeader + (size_t)n_kv_heads * n_tiles * ws::kImgBytes;
+}
+
 
 cudaError_t launch_prompt_attn(const PromptParams& p, cudaStream_t stream) {
   const int G = p.n_q_heads / p.n_kv_heads;
   const int qpc = kM / G;
   dim3 grid((p.n_q + qpc - 1) / qpc, p.n_kv_heads);
   if (p.pool.v_bits == 8) {
+    // The register split inside the kernel assumes the compiled per-thread count: refuse to launch
+    // a build that differs (its setmaxnreg.inc could otherwise never be satisfied).
+    static int regs_checked = -1;
+    if (regs_checked < 0) {
+      cudaFuncAttributes fa{};
+      cudaError_t e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void*>(ws::prompt_attn_ws_kernel));
+      if (e != cudaSuccess) return e;
+      regs_checked = fa.numRegs;
+    }
+    if (regs_checked != ws::kLaunchRegs) return cudaErrorInvalidConfiguration;
     cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(ws::prompt_attn_ws_kernel), (size_t)ws::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaMemsetAsync(p.scratch, 0, ws::kScratchHeader, stream);
+    if (e != cudaSuccess) return e;
+    ws::prompt_stage_kernel<<<dim3(p.n_tiles, p.n_kv_heads), 128, 0, stream>>>(p.pool, p.n_kv_heads, p.n_tiles,
+                                                                                p.scratch);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     ws::prompt_attn_ws_kernel<<<grid, ws::kThreads, ws::kSmemBytes, stream>>>(p);
     return cudaGetLastError();

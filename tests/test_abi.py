@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_pure_host_calls(lib):
-    assert qsa.abi_version() == 100
+    assert qsa.abi_version() == 101
     assert qsa.status_str(qsa.QSA_ERR_SCRATCH) == "scratch buffer too small"
     assert qsa.decode_partials_bytes(5, 24, 64) == 4 * 5 * 24 * 64 * 130
     assert qsa.decode_partials_bytes(0, 24, 64) == 0
@@ -98,9 +98,19 @@ def test_decode_attn_validation(lib):
 
 def test_prompt_validation(lib):
     pool = _pool(n_filled=1000, capacity=1024)
-    assert lib.qsa_prompt_attn(ctypes.byref(pool), 16, 100, 950, 24, 32, None, None) == qsa.QSA_ERR_ARG
-    assert lib.qsa_prompt_attn(ctypes.byref(pool), 16, 100, -1, 24, 32, None, None) == qsa.QSA_ERR_ARG
-    assert lib.qsa_prompt_attn(ctypes.byref(pool), 16, 100, 0, 26, 32, None, None) == qsa.QSA_ERR_ARG
-    bad = _pool(page_cells=96)
-    assert lib.qsa_prompt_attn(ctypes.byref(bad), 16, 10, 0, 24, 32, None, None) == qsa.QSA_ERR_ARG
-    assert lib.qsa_prompt_attn(ctypes.byref(pool), 16, 0, 0, 24, 32, None, None) == qsa.QSA_OK   # nothing to do
+    need = lib.qsa_prompt_scratch_bytes(ctypes.byref(pool), 100, 900)
+    assert need == 256 + 4 * (999 // 64 + 1) * 33792                # int8 V: one tile image per tile and head
+    assert lib.qsa_prompt_scratch_bytes(ctypes.byref(_pool(v_bits=4, n_filled=1000, capacity=1024)), 100, 900) == 0
+    ok = dict(scratch=1 << 20, nbytes=need)
+
+    def call(pl, q_pos0, n_q, Hq=24, scratch=None, nbytes=None):
+        a = dict(ok, **({} if scratch is None else {"scratch": scratch}), **({} if nbytes is None else {"nbytes": nbytes}))
+        return lib.qsa_prompt_attn(ctypes.byref(pl), 16, n_q, q_pos0, Hq, a["scratch"], a["nbytes"], 32, None, None)
+    assert call(pool, 950, 100) == qsa.QSA_ERR_ARG                   # past n_filled
+    assert call(pool, -1, 100) == qsa.QSA_ERR_ARG
+    assert call(pool, 0, 100, Hq=26) == qsa.QSA_ERR_ARG               # not a multiple of the KV heads
+    assert call(_pool(page_cells=96), 0, 10) == qsa.QSA_ERR_ARG       # pages of a multiple of 64 cells only
+    assert call(pool, 0, 0) == qsa.QSA_OK                             # nothing to do
+    assert call(pool, 900, 100, nbytes=need - 1) == qsa.QSA_ERR_SCRATCH
+    assert call(pool, 900, 100, scratch=(1 << 20) + 16) == qsa.QSA_ERR_SCRATCH   # not 256-byte aligned
+    assert lib.qsa_prompt_attn(ctypes.byref(pool), 16, 100, 900, 24, None, need, 32, None, None) == qsa.QSA_ERR_SCRATCH

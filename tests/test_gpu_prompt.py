@@ -44,6 +44,21 @@ def test_small_prompt_full(n_ctx, n_q, Hq, Hkv, v_bits, page_cells):
     assert_close(lse, ref_lse, "lse")
 
 
+def test_prompt_heads_with_far_apart_v_scales():
+    """KV heads whose V scales differ by 2^10 in either direction, and one tile of near-zero V scales:
+    the V-scale exponent is taken per head and only shifts the reference of p."""
+    case = W.prompt_case(name="vs", seed=31, n_ctx=1100, n_q=70, n_q_heads=12, n_kv_heads=3, page_cells=128,
+                         capacity=1280)
+    case.pool.v_scales[:, 1] *= 1024.0
+    case.pool.v_scales[:, 2] /= 1024.0
+    phys0 = int(case.pool.page_table[3])
+    case.pool.v_scales[phys0, 0, :64] *= 1e-6
+    out, lse = run_prompt(case, case.calls[0])
+    ref_out, ref_lse = O.prompt_attention(case.pool, case.q, case.calls[0][2])
+    assert_close(out, ref_out, "out")
+    assert_close(lse, ref_lse, "lse")
+
+
 def _sample_rows(n_q, k, seed):
     rng = np.random.default_rng(seed)
     rows = set(rng.choice(n_q, size=k, replace=False).tolist()) | {0, 1, n_q - 1}
