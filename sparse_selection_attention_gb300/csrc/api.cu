@@ -144,6 +144,9 @@ qsa_status qsa_block_scores(const qsa_pool* pools, int n_pools, const int32_t* r
   p.max_blocks = max_blocks;
   p.q = q;
   p.scores = scores;
+  p.err = device_error_word();
+  p.wait_limit_ns = wait_limit_ns();
+  if (!p.err) return QSA_ERR_CUDA;
   if (!block_scores_supported(p.n_kv_heads, block_cells)) return QSA_ERR_UNSUPPORTED;
   p.q_rows_per_batch = block_scores_q_rows_per_batch(n_rows, n_q_heads, p.n_kv_heads, block_cells);
   if (block_scores_smem_bytes(n_rows, n_q_heads, p.n_kv_heads, block_cells) > (size_t)device_max_smem_optin())

@@ -268,6 +268,316 @@ size_t q_stage_floats(int n_rows, int n_q_heads) {
   return all < 16384 ? all : (row > 16384 ? row : 16384);
 }
 
+// ---------------------------------------------------------------------------------------------
+// Staged variant (used when a whole unit's K fits a shared-memory stage): the same per-task
+// arithmetic, fed by bulk copies.  A persistent CTA owns a contiguous range of units; its
+// producer warp looks up the units' pages in parallel (one lane per unit) and issues every copy of
+// the range up front into a ring of up to kMaxStages unit stages, so the whole range's K reads are
+// in flight together instead of one unit at a time.  Stage layout: K codes [head][B][128 B], then
+// K scales [head][B][2] floats.  Sixteen compute warps take the units' (head, m-tile) tasks as the
+// stages arrive, keeping each task's sum in shared memory; one barrier at the end precedes the
+// fixed-order reduction of every unit's task sums.  Waits are bounded: a
+// wait that runs out sets the device error word and the CTA runs to its end without further copies
+// (its scores are then not valid); before exiting it waits for every copy it issued.
+namespace staged {
+
+constexpr int kComputeWarps = 16;
+constexpr int kMaxUnitsPerCta = 64;   // task sums kept for the whole range
+constexpr int kThreads = 32 * (kComputeWarps + 1);
+constexpr int kMaxStages = 6;
+
+__host__ __device__ inline int stage_bytes(int n_kv_heads, int B) { return n_kv_heads * B * (kD + 8); }
+
+struct Layout {
+  int bfrag, inv_f, part, stage0, bars, ctl, total;
+};
+// upc: units per CTA (task sums are kept for all of them).
+__host__ __device__ inline Layout layout(int R, int Hkv, int B, int n_stages, int upc) {
+  const int NT = (R + 7) / 8, tpu = Hkv * (B / 16);
+  Layout L;
+  L.bfrag = 0;
+  L.inv_f = L.bfrag + 16 * Hkv * NT * 8 * 32;
+  L.part = L.inv_f + 4 * round4(R * Hkv);
+  L.stage0 = (L.part + 4 * upc * tpu * NT * 8 + 127) & ~127;
+  L.bars = L.stage0 + n_stages * stage_bytes(Hkv, B);
+  L.ctl = L.bars + 16 * kMaxStages;
+  L.total = L.ctl + 16;
+  return L;
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t gtimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait; false (and the abort flag set) when it runs out or the CTA has aborted.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* err,
+                                           uint64_t limit_ns) {
+  if (mbar_try(bar, parity)) return true;
+  if (limit_ns == 0 || *abort_flag) {
+    *abort_flag = 1;
+    atomicCAS(err, 0, 2);
+    return false;
+  }
+  const uint64_t t0 = gtimer();
+  while (!mbar_try(bar, parity)) {
+    if (*abort_flag || gtimer() - t0 > limit_ns) {
+      *abort_flag = 1;
+      atomicCAS(err, 0, 2);
+      return false;
+    }
+  }
+  return true;
+}
+
+template <int kMaxNt>
+__global__ void __launch_bounds__(kThreads, 1) block_scores_staged_kernel(const ScoresParams p, int n_stages, int upc) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int Hkv = p.n_kv_heads, G = p.n_q_heads / Hkv, B = p.block_cells;
+  const int R = p.n_rows, NT = (R + 7) / 8;
+  const int tpu = Hkv * (B / 16);
+  const Layout L = layout(R, Hkv, B, n_stages, upc);
+  uint4* bfrag = reinterpret_cast<uint4*>(smem + L.bfrag);
+  float* inv_f = reinterpret_cast<float*>(smem + L.inv_f);
+  float* part = reinterpret_cast<float*>(smem + L.part);
+  const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  const uint32_t full0 = sbase + L.bars, empty0 = full0 + 8 * kMaxStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.ctl);
+  volatile int* issued_w = abort_flag + 1;
+  const int SB = stage_bytes(Hkv, B);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, tq = lane & 3;
+  // Contiguous unit range of this CTA.
+  const int per = p.total_units / gridDim.x, extra = p.total_units % gridDim.x;
+  const int u0 = blockIdx.x * per + min((int)blockIdx.x, extra);
+  const int n_units = per + ((int)blockIdx.x < extra ? 1 : 0);
+
+  if (tid == 0) {
+    for (int s = 0; s < n_stages; ++s) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(full0 + 8 * s) : "memory");
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(empty0 + 8 * s), "r"(kComputeWarps) : "memory");
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    *abort_flag = 0;
+    *issued_w = 0;
+  }
+  __syncthreads();
+
+  if (warp == kComputeWarps) {
+    // ================================================= producer
+    int issued = 0;
+    for (int base = 0; base < n_units; base += 32) {
+      const int n = min(32, n_units - base);
+      int pg = 0;
+      if (lane < n) {
+        const int unit = u0 + base + lane;
+        const int pi = pool_of(p, unit);
+        const int b = unit - p.unit_begin[pi];
+        pg = __ldg(p.pools[pi].page_table + (b * B) / p.pools[pi].page_cells);
+      }
+      for (int k = 0; k < n; ++k) {
+        const int page = __shfl_sync(0xffffffffu, pg, k);
+        if (lane == 0 && !*abort_flag) {
+          const int i = base + k, st = i % n_stages;
+          bool ok = true;
+          if (i >= n_stages) ok = wait_phase(empty0 + 8 * st, ((i / n_stages) - 1) & 1, abort_flag, p.err, p.wait_limit_ns);
+          if (ok) {
+            const int unit = u0 + i;
+            const int pi = pool_of(p, unit);
+            const PoolDev& pool = p.pools[pi];
+            const int cell0 = (unit - p.unit_begin[pi]) * B;
+            const uint32_t dst = sbase + L.stage0 + st * SB, bar = full0 + 8 * st;
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(SB) : "memory");
+            for (int h = 0; h < Hkv; ++h) {
+              const long long slot0 = ((long long)page * Hkv + h) * pool.page_cells + cell0 % pool.page_cells;
+              asm volatile(
+                  "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                      dst + h * B * kD),
+                  "l"(pool.k_codes + slot0 * kD), "r"(B * kD), "r"(bar)
+                  : "memory");
+              asm volatile(
+                  "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                      dst + Hkv * B * kD + h * B * 8),
+                  "l"(pool.k_scales + slot0 * 2), "r"(B * 8), "r"(bar)
+                  : "memory");
+            }
+            issued = i + 1;
+          }
+        }
+        __syncwarp();
+      }
+    }
+    if (lane == 0) *issued_w = issued;
+  } else {
+    // ================================================= compute warps
+    // qbar 2^f per (row, head) from q in global memory, split fp16 hi/lo, as B fragments.
+    for (int rh = warp; rh < R * Hkv; rh += kComputeWarps) {
+      const int t = rh / Hkv, h = rh % Hkv;
+      const float* qg = p.q + ((size_t)t * p.n_q_heads + h * G) * kD + 4 * lane;
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+      for (int gg = 0; gg < G; ++gg) {
+        const float4 x = __ldg(reinterpret_cast<const float4*>(qg + gg * kD));
+        v[0] += x.x; v[1] += x.y; v[2] += x.z; v[3] += x.w;
+      }
+      float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+      amax = warp_max(amax);
+      int e = 0;
+      if (amax > 0.f) frexpf(amax, &e);
+      const int fe = amax > 0.f ? max(-126, min(127, 7 - e)) : 0;
+      const float f = pow2i(fe);
+      if (lane == 0) inv_f[t * Hkv + h] = pow2i(-fe);
+      const int d0 = 4 * lane, grp = d0 >> 6, tqp = (d0 >> 4) & 3, sp = (d0 >> 2) & 3;
+      const int s = 4 * grp + sp, nt = t >> 3, gp = t & 7;
+      const __half2 h01 = __floats2half2_rn(v[0] * f, v[1] * f), h23 = __floats2half2_rn(v[2] * f, v[3] * f);
+      const float2 b01 = __half22float2(h01), b23 = __half22float2(h23);
+      const __half2 l01 = __floats2half2_rn(v[0] * f - b01.x, v[1] * f - b01.y);
+      const __half2 l23 = __floats2half2_rn(v[2] * f - b23.x, v[3] * f - b23.y);
+      bfrag[((h * NT + nt) * 8 + s) * 32 + gp * 4 + tqp] = make_uint4(h2u(h01), h2u(h23), h2u(l01), h2u(l23));
+    }
+    for (int k = tid; k < Hkv * 8 * 32; k += 32 * kComputeWarps) {   // rows R .. NT*8-1: zero fragments
+      const int h = k / 256, s = (k / 32) % 8, ln = k % 32, row = (NT - 1) * 8 + (ln >> 2);
+      if (row >= R) bfrag[((h * NT + NT - 1) * 8 + s) * 32 + ln] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * kComputeWarps) : "memory");
+
+    for (int i = 0; i < n_units; ++i) {
+      const int st = i % n_stages;
+      wait_phase(full0 + 8 * st, (i / n_stages) & 1, abort_flag, p.err, p.wait_limit_ns);
+      const int unit = u0 + i;
+      const int pi = pool_of(p, unit);
+      const int b = unit - p.unit_begin[pi];
+      const int n_b = min(B, p.pools[pi].n_filled - b * B);
+      const uint8_t* stg = smem + L.stage0 + st * SB;
+      float* pu = part + i * tpu * NT * 8;
+      for (int task = warp; task < tpu; task += kComputeWarps) {   // warp-uniform
+        const int h = task / (B / 16), mt = task % (B / 16);
+        const uint8_t* codes = stg + h * B * kD;
+        const float* kscale = reinterpret_cast<const float*>(stg + Hkv * B * kD + h * B * 8);
+        uint4 c[2][2];
+        float2 ks[2];
+#pragma unroll
+        for (int ab = 0; ab < 2; ++ab) {
+          const int cell = 16 * mt + g + 8 * ab;
+          if (cell < n_b) {
+            c[ab][0] = *reinterpret_cast<const uint4*>(codes + cell * kD + 16 * tq);
+            c[ab][1] = *reinterpret_cast<const uint4*>(codes + cell * kD + 64 + 16 * tq);
+            ks[ab] = *reinterpret_cast<const float2*>(kscale + 2 * cell);
+          } else {
+            c[ab][0] = c[ab][1] = make_uint4(0u, 0u, 0u, 0u);
+            ks[ab] = make_float2(0.f, 0.f);
+          }
+        }
+        // hi and lo parts of q accumulate in separate chains (half the dependent MMA chain), summed after
+        float d[kMaxNt][2][4], dl[kMaxNt][2][4];
+#pragma unroll
+        for (int nt = 0; nt < kMaxNt; ++nt)
+#pragma unroll
+          for (int gr = 0; gr < 2; ++gr)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) d[nt][gr][q] = dl[nt][gr][q] = 0.f;
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+          const int gr = s >> 2, w = s & 3;
+          const uint32_t wa = word_of(c[0][gr], w) ^ 0x80808080u;
+          const uint32_t wb = word_of(c[1][gr], w) ^ 0x80808080u;
+          uint32_t a[4];
+          a[0] = byte_pair_h2(wa, 0x4140);
+          a[2] = byte_pair_h2(wa, 0x4342);
+          a[1] = byte_pair_h2(wb, 0x4140);
+          a[3] = byte_pair_h2(wb, 0x4342);
+#pragma unroll
+          for (int nt = 0; nt < kMaxNt; ++nt) {
+            if (nt < NT) {
+              const uint4 bf = bfrag[((h * NT + nt) * 8 + s) * 32 + lane];
+              mma16816(d[nt][gr], a, bf.x, bf.y);
+              mma16816(dl[nt][gr], a, bf.z, bf.w);
+            }
+          }
+        }
+#pragma unroll
+        for (int nt = 0; nt < kMaxNt; ++nt)
+#pragma unroll
+          for (int gr = 0; gr < 2; ++gr)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) d[nt][gr][q] += dl[nt][gr][q];
+#pragma unroll
+        for (int nt = 0; nt < kMaxNt; ++nt) {
+          if (nt < NT) {
+            float e0 = fmaf(ks[0].y, d[nt][1][0], ks[0].x * d[nt][0][0]);
+            e0 += fmaf(ks[1].y, d[nt][1][2], ks[1].x * d[nt][0][2]);
+            float e1 = fmaf(ks[0].y, d[nt][1][1], ks[0].x * d[nt][0][1]);
+            e1 += fmaf(ks[1].y, d[nt][1][3], ks[1].x * d[nt][0][3]);
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+              e0 += __shfl_xor_sync(0xffffffffu, e0, o);
+              e1 += __shfl_xor_sync(0xffffffffu, e1, o);
+            }
+            if (g == 0) {
+              const int row = nt * 8 + 2 * tq;
+              pu[task * NT * 8 + row] = row < R ? e0 * inv_f[row * Hkv + h] : 0.f;
+              pu[task * NT * 8 + row + 1] = row + 1 < R ? e1 * inv_f[(row + 1) * Hkv + h] : 0.f;
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(empty0 + 8 * st) : "memory");
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * kComputeWarps) : "memory");
+    // S[t, b]: one warp per (unit, row); lane l holds task l (<= 32 tasks), then a fixed butterfly.
+    for (int ut = warp; ut < n_units * R; ut += kComputeWarps) {
+      const int i = ut / R, t = ut % R;
+      const int unit = u0 + i;
+      const int pi = pool_of(p, unit);
+      if (p.row_pool[t] != pi) continue;
+      const int b = unit - p.unit_begin[pi];
+      const int n_b = min(B, p.pools[pi].n_filled - b * B);
+      float s = lane < tpu ? part[(i * tpu + lane) * NT * 8 + t] : 0.f;
+      s = warp_sum(s);
+      if (lane == 0) p.scores[(size_t)t * p.max_blocks + b] = s * (kInvSqrtD / (float)n_b);
+    }
+  }
+
+  // Nothing may still write this CTA's shared memory when it exits: after an abort, wait for the
+  // latest fill of every stage that was issued.
+  __syncthreads();
+  if (*abort_flag && tid == 0) {
+    const int issued = *issued_w;
+    for (int st = 0; st < n_stages && st < issued; ++st) {
+      const int last = st + n_stages * ((issued - 1 - st) / n_stages);
+      const uint64_t t0 = gtimer();
+      while (!mbar_try(full0 + 8 * st, (last / n_stages) & 1) && gtimer() - t0 < 2000000000ull) {
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// Stages that fit next to the fragment table (0: the staged kernel does not apply).
+int n_stages_for(int R, int Hkv, int B, int total_units, int grid, int smem_max) {
+  const int units_per_cta = (total_units + grid - 1) / grid;
+  if (units_per_cta > kMaxUnitsPerCta || R > 16) return 0;
+  const int SB = stage_bytes(Hkv, B);
+  if (SB > 72 * 1024) return 0;
+  int s = min(kMaxStages, units_per_cta);
+  while (s >= 2 && layout(R, Hkv, B, s, units_per_cta).total + 128 > smem_max) --s;
+  if (s < 2 && units_per_cta >= 2) return 0;
+  if (s < 1 || layout(R, Hkv, B, s, units_per_cta).total + 128 > smem_max) return 0;
+  return s;
+}
+
+}  // namespace staged
+
 }  // namespace
 
 int block_scores_q_rows_per_batch(int n_rows, int n_q_heads, int n_kv_heads, int block_cells) {
@@ -299,10 +609,30 @@ static cudaError_t launch_variant(const ScoresParams& p, size_t smem, int grid, 
   return cudaGetLastError();
 }
 
+template <int NT>
+static cudaError_t launch_staged(const ScoresParams& p, int grid, int n_stages, cudaStream_t stream) {
+  const int upc = (p.total_units + grid - 1) / grid;
+  const size_t smem = staged::layout(p.n_rows, p.n_kv_heads, p.block_cells, n_stages, upc).total + 128;
+  const void* k = reinterpret_cast<const void*>(staged::block_scores_staged_kernel<NT>);
+  cudaError_t e = ensure_dynamic_smem(k, smem);
+  if (e != cudaSuccess) return e;
+  staged::block_scores_staged_kernel<NT><<<grid, staged::kThreads, smem, stream>>>(p, n_stages, upc);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_block_scores(const ScoresParams& p, cudaStream_t stream) {
   if (p.total_units == 0) return cudaSuccess;
   const int nt = (p.n_rows + 7) / 8;
   if (nt > kNtMax) return cudaErrorInvalidValue;
+  {
+    const int grid = min(p.total_units, device_sm_count());
+    const int ns = staged::n_stages_for(p.n_rows, p.n_kv_heads, p.block_cells, p.total_units, grid,
+                                        device_max_smem_optin());
+    if (ns > 0 && p.n_kv_heads * (p.block_cells / 16) <= 32) {
+      if (nt == 1) return launch_staged<1>(p, grid, ns, stream);
+      return launch_staged<2>(p, grid, ns, stream);
+    }
+  }
   const size_t smem = block_scores_smem_bytes(p.n_rows, p.n_q_heads, p.n_kv_heads, p.block_cells);
   const int tpu = p.n_kv_heads * (p.block_cells / 16);
   const int upi = max(1, kWarps / tpu);

@@ -14,6 +14,8 @@ struct ScoresParams {
   int q_rows_per_batch;   // rows of q staged in shared memory at a time
   const float* q;
   float* scores;
+  int* err;               // device error word (bounded waits of the staged kernel)
+  unsigned long long wait_limit_ns;
 };
 
 struct TopkParams {
@@ -68,5 +70,8 @@ cudaError_t launch_decode_attn(const AttnParams& p, cudaStream_t stream);
 cudaError_t launch_attn_merge(const MergeParams& p, cudaStream_t stream);
 cudaError_t launch_prompt_attn(const PromptParams& p, cudaStream_t stream);
 cudaError_t read_and_clear_device_error(int32_t* code, cudaStream_t stream);
+// Device address of the library's error word on the current device (for kernels of other
+// translation units), or nullptr.
+int* device_error_word();
 
 }  // namespace qsa

@@ -1071,6 +1071,18 @@ cudaError_t launch_prompt_attn(const PromptParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+int* device_error_word() {
+  static int* ptr[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    ptr[dev] = static_cast<int*>(p);
+  }
+  return ptr[dev];
+}
+
 cudaError_t read_and_clear_device_error(int32_t* code, cudaStream_t stream) {
   static const int zero = 0;
   cudaError_t e = cudaMemcpyFromSymbolAsync(code, g_device_error, sizeof(int), 0, cudaMemcpyDeviceToHost, stream);

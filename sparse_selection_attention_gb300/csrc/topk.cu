@@ -8,16 +8,14 @@
 // digit with a work-group scan over the bins; integers only, so the same ids).
 //
 // One CTA per row; thread i holds the keys of blocks [i*K, (i+1)*K) in
-// registers.  Four radix passes of 8 bits (most significant first) find the
-// threshold key T.  A pass histograms the digit of the keys still matching
-// the prefix into per-warp bins (shared atomics, aggregated over lanes with
-// equal digits; integer counts do not depend on their order), then 256
-// threads each sum one digit over the warps and scan the bins from the
-// highest digit down to find the digit holding the k-th key.  Blocks with
-// key > T are taken, then the lowest-id blocks with key == T.  Two CTA prefix
-// sums in block-id order give each chosen block its rank j; every block but
-// the row's last holds exactly B cells, so chosen block j fills ids[j*B ..],
-// written coalesced by the whole CTA.
+// registers.  The threshold T (the kb-th largest key) is found one bit at a
+// time from the most significant: T | bit is kept when at least kb keys are
+// >= it.  Each step is one CTA-wide count: __syncthreads_count when a thread
+// holds one key, else a warp reduction and one barrier.  Blocks with key > T
+// are taken, then the lowest-id blocks with key == T.  Two CTA prefix sums in
+// block-id order give each chosen block its rank j; every block but the row's
+// last holds exactly B cells, so chosen block j fills ids[j*B ..], written
+// coalesced by the whole CTA.
 #include "kernels.h"
 
 namespace qsa {
@@ -34,7 +32,8 @@ __device__ __forceinline__ uint32_t score_key(float x) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Exclusive CTA-wide prefix sum of one int per thread; `tot` receives the total.
+// Exclusive CTA-wide prefix sum of one int per thread; `tot` receives the total.  The warp totals
+// are scanned lane-parallel by every warp (no serial loop over warps).
 __device__ __forceinline__ int cta_exclusive_scan(int v, int* warp_tot, int& tot) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, n_warps = blockDim.x >> 5;
   int inc = v;
@@ -45,24 +44,40 @@ __device__ __forceinline__ int cta_exclusive_scan(int v, int* warp_tot, int& tot
   }
   if (lane == 31) warp_tot[warp] = inc;
   __syncthreads();
-  int base = 0, total = 0;
-  for (int w = 0; w < n_warps; ++w) {   // every thread reads the (few) warp totals
-    const int x = warp_tot[w];
-    base += (w < warp) ? x : 0;
-    total += x;
+  int wt = lane < n_warps ? warp_tot[lane] : 0;
+  int winc = wt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, winc, o);
+    if (lane >= o) winc += n;
   }
+  const int base = __shfl_sync(0xffffffffu, winc - wt, warp);
+  tot = __shfl_sync(0xffffffffu, winc, 31);
   __syncthreads();
-  tot = total;
   return base + inc - v;
 }
 
+// Number of this CTA's keys >= cand (every thread gets the total).
+__device__ __forceinline__ int cta_count_ge(const uint32_t (&key)[kMaxKeys], int K, int b0, int nb, uint32_t cand,
+                                            int* wsum, int parity) {
+  if (K == 1) return __syncthreads_count(b0 < nb && key[0] >= cand);
+  int c = 0;
+#pragma unroll
+  for (int i = 0; i < kMaxKeys; ++i) c += (i < K && b0 + i < nb && key[i] >= cand) ? 1 : 0;
+  c = __reduce_add_sync(0xffffffffu, c);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, n_warps = blockDim.x >> 5;
+  if (lane == 0) wsum[parity * 32 + warp] = c;
+  __syncthreads();
+  // wsum[parity] is rewritten two steps later, after the next barrier
+  return __reduce_add_sync(0xffffffffu, lane < n_warps ? wsum[parity * 32 + lane] : 0);
+}
+
 __global__ void __launch_bounds__(kMaxThreads) topk_kernel(const TopkParams p) {
-  extern __shared__ int smem[];          // per-warp histograms [n_warps][256], then chosen list [kb]
+  extern __shared__ int smem[];          // chosen list [kb]
   __shared__ int warp_tot[32];
-  __shared__ int bin_tot[8];
-  __shared__ int s_digit, s_gt;
-  const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int n_threads = blockDim.x, n_warps = n_threads >> 5;
+  __shared__ int wsum[64];
+  const int t = blockIdx.x, tid = threadIdx.x;
+  const int n_threads = blockDim.x;
   const int B = p.block_cells;
   const int n_filled = p.n_filled[t];
   const int nb = (n_filled + B - 1) / B;
@@ -72,8 +87,7 @@ __global__ void __launch_bounds__(kMaxThreads) topk_kernel(const TopkParams p) {
     if (tid == 0) p.n_sel[t] = 0;
     return;
   }
-  int* whist = smem;
-  int* sel = smem + n_warps * 256;
+  int* sel = smem;
   const int K = (nb + n_threads - 1) / n_threads;   // <= kMaxKeys
   const int b0 = tid * K;
   const float* sc = p.scores + (size_t)t * p.max_blocks;
@@ -81,58 +95,16 @@ __global__ void __launch_bounds__(kMaxThreads) topk_kernel(const TopkParams p) {
 #pragma unroll
   for (int i = 0; i < kMaxKeys; ++i) key[i] = (i < K && b0 + i < nb) ? score_key(__ldg(sc + b0 + i)) : 0u;
 
+  const bool take_all = (kb == nb);
   uint32_t T = 0;
   int need = 0;
-  const bool take_all = (kb == nb);
   if (!take_all) {
-    uint32_t prefix = 0, mask = 0;
-    int rem = kb;
-    for (int pass = 0; pass < 4; ++pass) {
-      const int shift = 24 - 8 * pass;
-      int* wh = whist + warp * 256;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) wh[lane * 8 + i] = 0;
-      __syncwarp();
-#pragma unroll
-      for (int i = 0; i < kMaxKeys; ++i) {
-        if (i < K) {   // uniform
-          const bool live = b0 + i < nb && (key[i] & mask) == prefix;
-          const int digit = live ? (int)((key[i] >> shift) & 0xFF) : -1;
-          const unsigned peers = __match_any_sync(0xffffffffu, digit);
-          if (live && (__ffs(peers) - 1) == lane) atomicAdd(&wh[digit], __popc(peers));
-        }
-      }
-      __syncthreads();
-      // Threads 0..255: digit d = 255 - tid; count over warps, then a descending scan.
-      if (tid < 256) {
-        const int d = 255 - tid;
-        int c = 0;
-        for (int w = 0; w < n_warps; ++w) c += whist[w * 256 + d];
-        int inc = c;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int n = __shfl_up_sync(0xffffffffu, inc, o);
-          if (lane >= o) inc += n;
-        }
-        if (lane == 31) bin_tot[warp] = inc;
-        __syncwarp();
-        asm volatile("bar.sync 1, 256;" ::: "memory");
-        int before = 0;
-        for (int w = 0; w < warp; ++w) before += bin_tot[w];
-        const int lo = before + inc - c, hi = before + inc;   // keys above d, and up to d
-        if (lo < rem && rem <= hi) {
-          s_digit = d;
-          s_gt = lo;
-        }
-      }
-      __syncthreads();
-      rem -= s_gt;
-      prefix |= (uint32_t)s_digit << shift;
-      mask |= 0xFFu << shift;
-      __syncthreads();
+    for (int bit = 31; bit >= 0; --bit) {
+      const uint32_t cand = T | (1u << bit);
+      if (cta_count_ge(key, K, b0, nb, cand, wsum, bit & 1) >= kb) T = cand;
     }
-    T = prefix;
-    need = rem;   // keys equal to T to take, lowest ids first
+    // keys > T (T + 1 does not wrap: the largest key, +inf's, is 0xFF800000); parity 1 follows bit 0's 0
+    need = kb - cta_count_ge(key, K, b0, nb, T + 1u, wsum, 1);
   }
 
   int tot = 0;
@@ -157,9 +129,25 @@ __global__ void __launch_bounds__(kMaxThreads) topk_kernel(const TopkParams p) {
   for (int i = 0; i < kMaxKeys; ++i)
     if (chosen_bits & (1u << i)) sel[j++] = b0 + i;
   __syncthreads();
-  for (int idx = tid; idx < kb * B; idx += n_threads) {
-    const int cell = sel[idx / B] * B + idx % B;
-    if (cell < n_filled) ids[idx] = cell;
+  // ids[j*B + i] = sel[j]*B + i, four at a time when the row's ids start 16-byte aligned (ids aligned,
+  // k_cells and B multiples of 4); cells past n_filled (the row's last block) are not written.
+  if ((B & 3) == 0 && (p.k_cells & 3) == 0 && (reinterpret_cast<uintptr_t>(p.ids) & 15) == 0) {
+    for (int i4 = tid; i4 < kb * B / 4; i4 += n_threads) {
+      const int idx = 4 * i4;
+      const int cell = sel[idx / B] * B + idx % B;
+      if (cell + 3 < n_filled) {
+        *reinterpret_cast<int4*>(ids + idx) = make_int4(cell, cell + 1, cell + 2, cell + 3);
+      } else {
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (cell + u < n_filled) ids[idx + u] = cell + u;
+      }
+    }
+  } else {
+    for (int idx = tid; idx < kb * B; idx += n_threads) {
+      const int cell = sel[idx / B] * B + idx % B;
+      if (cell < n_filled) ids[idx] = cell;
+    }
   }
   if (tid == 0) {
     const int n_last = n_filled - (nb - 1) * B;
@@ -168,18 +156,16 @@ __global__ void __launch_bounds__(kMaxThreads) topk_kernel(const TopkParams p) {
 }
 
 int topk_threads(int max_nb) {
-  // about four keys per thread, 256..1024 threads (256 threads scan the bins)
-  int th = ((max_nb + 3) / 4 + 31) / 32 * 32;
-  th = th < 256 ? 256 : (th > kMaxThreads ? kMaxThreads : th);
+  // one key per thread up to 1,024 blocks (the count is then one __syncthreads_count), else 1,024
+  // threads with up to kMaxKeys keys each
+  int th = (max_nb + 31) / 32 * 32;
+  th = th < 128 ? 128 : (th > kMaxThreads ? kMaxThreads : th);
   return th;
 }
 
 }  // namespace
 
-size_t topk_smem_bytes(int max_nb) {
-  const int th = topk_threads(max_nb);
-  return sizeof(int) * ((size_t)(th / 32) * 256 + (size_t)max_nb);
-}
+size_t topk_smem_bytes(int max_nb) { return sizeof(int) * (size_t)max_nb; }
 
 cudaError_t launch_topk(const TopkParams& p, int max_nb, cudaStream_t stream) {
   const int th = topk_threads(max_nb);
