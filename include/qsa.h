@@ -185,6 +185,41 @@ qsa_status qsa_attn_merge(const void* partials, const int32_t* n_sel, int n_rows
                           int chunk_cells, int n_chunks, float* out, float* lse, void* stream);
 
 /*
+ * qsa_decode_window -- one whole decode window in one call: block scores ->
+ * top-k -> split-KV attention -> log-sum-exp merge (the four steps above),
+ * enqueued as four chained launches on `stream` ("#2806 sycl: decode QSA
+ * selection and attention in fewer, shorter launches", Summary: selection
+ * and attention of a window in fewer, shorter launches).  scores, ids and
+ * n_sel are written exactly as qsa_block_scores and qsa_topk write them.
+ * The attention splits each (row, KV head)'s selection into splits of a
+ * multiple of 64 cells chosen by the library for this GPU, and the merge
+ * folds the splits in split order, skipping empty ones; out and lse follow
+ * the qsa_attn_merge definition (equal to the chunked result up to
+ * rounding; bitwise reproducible run to run on the same GPU).
+ *   pools, row_pool, q, n_rows, n_q_heads, block_cells, max_blocks
+ *              as qsa_block_scores
+ *   row_pos    (dev)  int32 [n_rows], as qsa_decode_attn
+ *   k_cells    multiple of block_cells, >= 0
+ *   scores     (dev)  fp32 [n_rows][max_blocks]   (output)
+ *   ids        (dev)  int32 [n_rows][max(k_cells, 1)] (output)
+ *   n_sel      (dev)  int32 [n_rows]              (output)
+ *   out        (dev)  fp32 [n_rows][n_q_heads][128] (output)
+ *   lse        (dev)  fp32 [n_rows][n_q_heads], may be NULL (output)
+ *   workspace  (dev)  caller-owned, 256-byte aligned, workspace_bytes >=
+ *              qsa_decode_window_workspace_bytes(); needs no initialisation.
+ * Calls on one stream may reuse one workspace; calls that run concurrently
+ * need their own.
+ * Errors: as qsa_block_scores / qsa_topk / qsa_decode_attn, and
+ * QSA_ERR_SCRATCH when the workspace is too small.
+ */
+size_t qsa_decode_window_workspace_bytes(int n_rows, int n_q_heads, int n_kv_heads, int k_cells);
+qsa_status qsa_decode_window(const qsa_pool* pools, int n_pools, const int32_t* row_pool,
+                             const float* q, const int32_t* row_pos, int n_rows, int n_q_heads,
+                             int block_cells, int k_cells, float* scores, int max_blocks,
+                             int32_t* ids, int32_t* n_sel, float* out, float* lse,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * qsa_prompt_attn -- causal attention of a chunk of n_q queries over the
  * cached context, on the tensor cores (#1367 What it does: both products on
  * the tensor cores with an exact split of the non-code operand; #600

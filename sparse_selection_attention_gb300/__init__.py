@@ -25,7 +25,7 @@ MAX_DECODE_ROWS = 32
 EXPORTS = [
     "qsa_block_scores", "qsa_topk", "qsa_decode_partials_bytes", "qsa_decode_attn", "qsa_attn_merge",
     "qsa_prompt_attn", "qsa_prompt_scratch_bytes", "qsa_get_device_error", "qsa_set_wait_limit_ns", "qsa_status_str", "qsa_abi_version",
-    "qsa_decode_attn_noalloc",
+    "qsa_decode_attn_noalloc", "qsa_decode_window", "qsa_decode_window_workspace_bytes",
 ]
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -69,6 +69,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qsa_prompt_scratch_bytes.argtypes = [pool_p, i, i]
     lib.qsa_prompt_scratch_bytes.restype = sz
     lib.qsa_decode_attn_noalloc.argtypes = [pool_p, i, i32p, p, p, p, p, i, i, i, i, p, p, p]
+    lib.qsa_decode_window.argtypes = [pool_p, i, i32p, p, p, i, i, i, i, p, i, p, p, p, p, p, sz, p]
+    lib.qsa_decode_window_workspace_bytes.argtypes = [i, i, i, i]
+    lib.qsa_decode_window_workspace_bytes.restype = sz
     lib.qsa_get_device_error.argtypes = [i32p, p]
     lib.qsa_set_wait_limit_ns.argtypes = [u64]
     lib.qsa_set_wait_limit_ns.restype = None
@@ -76,7 +79,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qsa_status_str.restype = ctypes.c_char_p
     lib.qsa_abi_version.argtypes = []
     for name in ("qsa_block_scores", "qsa_topk", "qsa_decode_attn", "qsa_attn_merge", "qsa_prompt_attn",
-                 "qsa_get_device_error", "qsa_abi_version", "qsa_decode_attn_noalloc"):
+                 "qsa_get_device_error", "qsa_abi_version", "qsa_decode_attn_noalloc", "qsa_decode_window"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -248,6 +251,7 @@ class DecodeWindow:
         self._c_row_pool = _i32_array(self.row_pool)
         self._c_n_filled = _i32_array(self.n_filled)
         self._nbytes = nbytes
+        self._ws = None
 
     def scores_step(self, q: torch.Tensor, stream=None) -> None:
         _check(load().qsa_block_scores(self._c_pools, len(self.pools), self._c_row_pool, _ptr(q), self.n_rows,
@@ -269,6 +273,18 @@ class DecodeWindow:
         _check(load().qsa_attn_merge(self.partials.data_ptr(), self.n_sel.data_ptr(), self.n_rows, self.n_q_heads,
                                      self.chunk_cells, self.n_chunks, self.out.data_ptr(), self.lse.data_ptr(),
                                      _stream(stream)), "qsa_attn_merge")
+
+    def run_window(self, q: torch.Tensor, row_pos: torch.Tensor, stream=None) -> None:
+        """The whole window in one call (qsa_decode_window): scores, ids, n_sel, out and lse."""
+        if self._ws is None:
+            nbytes = int(load().qsa_decode_window_workspace_bytes(self.n_rows, self.n_q_heads,
+                                                                  self.pools[0].n_kv_heads, self.k_cells))
+            self._ws = torch.empty((max(nbytes, 256),), dtype=torch.uint8, device=self.out.device)
+        _check(load().qsa_decode_window(self._c_pools, len(self.pools), self._c_row_pool, _ptr(q), _ptr(row_pos),
+                                        self.n_rows, self.n_q_heads, self.block_cells, self.k_cells,
+                                        self.scores.data_ptr(), self.max_blocks, self.ids.data_ptr(),
+                                        self.n_sel.data_ptr(), self.out.data_ptr(), self.lse.data_ptr(),
+                                        self._ws.data_ptr(), self._ws.numel(), _stream(stream)), "qsa_decode_window")
 
     def run(self, q: torch.Tensor, row_pos: torch.Tensor, stream=None) -> None:
         """block scores -> top-k -> chunk attention -> merge, enqueued on one stream."""

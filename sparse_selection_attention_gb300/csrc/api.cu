@@ -235,6 +235,88 @@ qsa_status qsa_attn_merge(const void* partials, const int32_t* n_sel, int n_rows
   return from_cuda(launch_attn_merge(p, static_cast<cudaStream_t>(stream)));
 }
 
+size_t qsa_decode_window_workspace_bytes(int n_rows, int n_q_heads, int n_kv_heads, int k_cells) {
+  if (n_rows < 1 || n_rows > QSA_MAX_DECODE_ROWS || n_kv_heads < 1 || n_q_heads < 1 || n_q_heads % n_kv_heads != 0 ||
+      k_cells < 0)
+    return 0;
+  return window_layout(n_rows, n_q_heads, n_kv_heads, k_cells, device_sm_count()).total;
+}
+
+qsa_status qsa_decode_window(const qsa_pool* pools, int n_pools, const int32_t* row_pool, const float* q,
+                             const int32_t* row_pos, int n_rows, int n_q_heads, int block_cells, int k_cells,
+                             float* scores, int max_blocks, int32_t* ids, int32_t* n_sel, float* out, float* lse,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  qsa_status s = check_window(pools, n_pools, row_pool, n_rows, n_q_heads, true);
+  if (s != QSA_OK) return s;
+  if (!q || !row_pos || !scores || !ids || !n_sel || !out || !workspace) return QSA_ERR_ARG;
+  if (!aligned16(q) || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return QSA_ERR_ARG;
+  if (block_cells != 32 && block_cells != 64 && block_cells != 128 && block_cells != 256) return QSA_ERR_ARG;
+  if (k_cells < 0 || k_cells % block_cells != 0) return QSA_ERR_ARG;
+  const int Hkv = pools[0].n_kv_heads;
+  WindowArgs a{};
+  // block scores
+  ScoresParams& sp = a.scores;
+  sp.n_pools = n_pools;
+  sp.unit_begin[0] = 0;
+  for (int i = 0; i < n_pools; ++i) {
+    if (pools[i].page_cells % block_cells != 0) return QSA_ERR_ARG;
+    const int nb = (pools[i].n_filled + block_cells - 1) / block_cells;
+    if (nb > max_blocks) return QSA_ERR_ARG;
+    if (nb > QSA_MAX_TOPK_BLOCKS) return QSA_ERR_UNSUPPORTED;
+    sp.pools[i] = to_dev(pools[i]);
+    sp.unit_begin[i + 1] = sp.unit_begin[i] + nb;
+  }
+  sp.total_units = sp.unit_begin[n_pools];
+  for (int t = 0; t < n_rows; ++t) sp.row_pool[t] = row_pool[t];
+  sp.n_rows = n_rows;
+  sp.n_q_heads = n_q_heads;
+  sp.n_kv_heads = Hkv;
+  sp.block_cells = block_cells;
+  sp.max_blocks = max_blocks;
+  sp.q = q;
+  sp.scores = scores;
+  sp.err = device_error_word();
+  sp.wait_limit_ns = wait_limit_ns();
+  if (!sp.err) return QSA_ERR_CUDA;
+  if (!window_scores_supported(n_rows, Hkv, block_cells)) return QSA_ERR_UNSUPPORTED;
+  // top-k
+  TopkParams& tp = a.topk;
+  int max_nb = 1;
+  for (int t = 0; t < n_rows; ++t) {
+    const int nf = pools[row_pool[t]].n_filled;
+    const int nb = (nf + block_cells - 1) / block_cells;
+    max_nb = nb > max_nb ? nb : max_nb;
+    tp.n_filled[t] = nf;
+  }
+  tp.scores = scores;
+  tp.max_blocks = max_blocks;
+  tp.n_rows = n_rows;
+  tp.block_cells = block_cells;
+  tp.k_cells = k_cells;
+  tp.ids = ids;
+  tp.n_sel = n_sel;
+  a.max_nb = max_nb;
+  if (topk_smem_bytes(max_nb) > (size_t)device_max_smem_optin()) return QSA_ERR_UNSUPPORTED;
+  // attention + merge
+  a.layout = window_layout(n_rows, n_q_heads, Hkv, k_cells, device_sm_count());
+  if (workspace_bytes < a.layout.total) return QSA_ERR_SCRATCH;
+  WinAttnParams& ap = a.attn;
+  for (int i = 0; i < n_pools; ++i) ap.pools[i] = to_dev(pools[i]);
+  for (int t = 0; t < n_rows; ++t) ap.row_pool[t] = row_pool[t];
+  ap.q = q;
+  ap.row_pos = row_pos;
+  ap.ids = ids;
+  ap.n_sel = n_sel;
+  ap.n_rows = n_rows;
+  ap.n_q_heads = n_q_heads;
+  ap.n_kv_heads = Hkv;
+  ap.k_cells = k_cells;
+  ap.out = out;
+  ap.lse = lse;
+  a.workspace = workspace;
+  return from_cuda(launch_decode_window(a, static_cast<cudaStream_t>(stream)));
+}
+
 size_t qsa_prompt_scratch_bytes(const qsa_pool* pool, int n_q, int q_pos0) {
   if (!pool || n_q < 0 || q_pos0 < 0 || pool->n_kv_heads < 1) return 0;
   return prompt_scratch_bytes(pool->v_bits, pool->n_kv_heads, q_pos0 + n_q);
@@ -288,6 +370,6 @@ const char* qsa_status_str(qsa_status s) {
   return "unknown status";
 }
 
-int qsa_abi_version(void) { return 101; }
+int qsa_abi_version(void) { return 102; }
 
 }  // extern "C"

@@ -1,0 +1,626 @@
+// One decode window in one call (qsa_decode_window): block scores -> top-k ->
+// split-KV attention with the log-sum-exp merge fused in, as four launches
+// chained on one stream with programmatic dependent launch, so that each
+// launch's start-up and prologue overlap the tail of the one before
+// ("#2806 sycl: decode QSA selection and attention in fewer, shorter
+// launches", Summary and What changed: selection and attention of a window in
+// fewer launches; "#1888 QSA decode attention: split each query's cells
+// across blocks", Summary: each query's cells split among blocks and merged by
+// the log-sum-exp rescale in split order).
+//
+//  1. win_qprep_kernel: per (row, KV head) qbar = sum of the group's q heads,
+//     scaled by a power of two and split into fp16 hi + lo, laid out as the
+//     block-score kernel's mma B fragments (computed once per window instead
+//     of once per CTA).  It also clears the merge tickets.
+//  2. win_scores_kernel: one CTA per (pool, block), one warp per (KV head,
+//     16-cell m-tile); each lane's K codes and scales are loaded into
+//     registers before the kernel waits for step 1.  S^T = Kcode . qbar on
+//     mma.sync; cell weights by K scale, fixed butterflies over cells, then
+//     over heads and m-tiles.  The result is the qsa_block_scores definition.
+//  3. topk_kernel (topk.cu), unchanged arithmetic.
+//  4. win_attn_kernel: one CTA per (row, KV head, split of the selection);
+//     the split's partial (m, l, o) of each q head is written to the
+//     workspace; the CTA that takes the last ticket of its (row, KV head)
+//     merges every split in split order (the ticket decides who merges, never
+//     the order), so the result is bitwise reproducible.
+#include "kernels.h"
+#include "mma_sync.cuh"
+
+namespace qsa {
+
+namespace {
+
+using namespace ms;
+
+constexpr int kAttnThreads = 128;
+constexpr int kSub = 64;   // cells per sub-tile of the attention
+constexpr int kMaxSplits = 256;
+
+__device__ __forceinline__ int pool_index(const int* unit_begin, int n_pools, int unit) {
+  int pi = 0;
+  while (pi + 1 < n_pools && unit >= unit_begin[pi + 1]) ++pi;
+  return pi;
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int w) {
+  return w == 0 ? v.x : (w == 1 ? v.y : (w == 2 ? v.z : v.w));
+}
+
+// ------------------------------------------------------------------------------------------ 1
+// Fragment layout (uint4 per lane): frag[((h * NT + nt) * 8 + s) * 32 + lane] holds, for row
+// 8 nt + lane / 4, the dims 64 grp + 16 (lane % 4) + 4 sp .. + 3 of k-step s = 4 grp + sp as
+// {hi(d0, d0+1), hi(d0+2, d0+3), lo(d0, d0+1), lo(d0+2, d0+3)}: the B operand of
+// mma.m16n8k16 for the same permutation of dims that the A fragments of the codes use.
+__global__ void __launch_bounds__(32) win_qprep_kernel(const float* __restrict__ q, int n_rows, int n_q_heads,
+                                                       int n_kv_heads, int NT, uint4* frag, float* inv_f,
+                                                       unsigned* tickets, int n_tickets) {
+  const int t = blockIdx.x, h = blockIdx.y, lane = threadIdx.x;
+  const int G = n_q_heads / n_kv_heads;
+  if (t == 0 && h == 0)
+    for (int i = lane; i < n_tickets; i += 32) tickets[i] = 0u;
+  pdl_trigger();
+  float v[4] = {0.f, 0.f, 0.f, 0.f};
+  if (t < n_rows) {
+    const float* qg = q + ((size_t)t * n_q_heads + (size_t)h * G) * kD + 4 * lane;
+    for (int gg = 0; gg < G; ++gg) {
+      const float4 x = __ldg(reinterpret_cast<const float4*>(qg + (size_t)gg * kD));
+      v[0] += x.x;
+      v[1] += x.y;
+      v[2] += x.z;
+      v[3] += x.w;
+    }
+  }
+  const float amax = warp_max(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))));
+  const int fe = scale_exp_128(amax);
+  const float f = pow2i(fe);
+  if (lane == 0 && t < n_rows) inv_f[t * n_kv_heads + h] = pow2i(-fe);
+  const int d0 = 4 * lane, grp = d0 >> 6, tqp = (d0 >> 4) & 3, sp = (d0 >> 2) & 3;
+  const int s = 4 * grp + sp, nt = t >> 3, gp = t & 7;
+  uint32_t h01, l01, h23, l23;
+  split_pair(v[0] * f, v[1] * f, h01, l01);
+  split_pair(v[2] * f, v[3] * f, h23, l23);
+  frag[((h * NT + nt) * 8 + s) * 32 + gp * 4 + tqp] = make_uint4(h01, h23, l01, l23);
+}
+
+// ------------------------------------------------------------------------------------------ 2
+template <int NT>
+__global__ void __launch_bounds__(1024) win_scores_kernel(const ScoresParams p, const uint4* __restrict__ frag,
+                                                          const float* __restrict__ inv_f) {
+  extern __shared__ float part[];   // [tasks][NT * 8]
+  const int B = p.block_cells, Hkv = p.n_kv_heads, R = p.n_rows;
+  const int mts = B / 16, tpu = Hkv * mts;
+  const int unit = blockIdx.x;
+  const int pi = pool_index(p.unit_begin, p.n_pools, unit);
+  const PoolDev& pool = p.pools[pi];
+  const int b = unit - p.unit_begin[pi];
+  const int cell0 = b * B;
+  const int n_b = min(B, pool.n_filled - cell0);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, tq = lane & 3;
+  const int h = warp / mts, mt = warp % mts;
+
+  // ---- this lane's codes (cells 16 mt + g and + 8, dims 16 tq .. and 64 + 16 tq ..) and scales
+  uint4 c[2][2];
+  float2 ks[2];
+  {
+    const int page = __ldg(pool.page_table + cell0 / pool.page_cells);
+    const long long slot0 = ((long long)page * Hkv + h) * pool.page_cells + cell0 % pool.page_cells;
+#pragma unroll
+    for (int ab = 0; ab < 2; ++ab) {
+      const int cc = 16 * mt + g + 8 * ab;
+      if (cc < n_b) {
+        const uint4* src = reinterpret_cast<const uint4*>(pool.k_codes + (slot0 + cc) * kD);
+        c[ab][0] = __ldg(src + tq);
+        c[ab][1] = __ldg(src + 4 + tq);
+        ks[ab] = __ldg(reinterpret_cast<const float2*>(pool.k_scales) + slot0 + cc);
+      } else {
+        c[ab][0] = c[ab][1] = make_uint4(0u, 0u, 0u, 0u);
+        ks[ab] = make_float2(0.f, 0.f);
+      }
+    }
+  }
+  pdl_trigger();
+  pdl_wait();   // q fragments of the preceding launch
+
+  float d[NT][2][4];   // [n-tile][K-scale group]: hi and lo parts of qbar accumulate together
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int gr = 0; gr < 2; ++gr)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) d[nt][gr][i] = 0.f;
+  const uint4* fr = frag + (size_t)h * NT * 8 * 32 + lane;
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    const int gr = s >> 2, w = s & 3;
+    const uint32_t wa = word_of(c[0][gr], w) ^ 0x80808080u;
+    const uint32_t wb = word_of(c[1][gr], w) ^ 0x80808080u;
+    uint32_t a[4];
+    a[0] = byte_pair_h2(wa, 0x4140, kBiasS8);
+    a[2] = byte_pair_h2(wa, 0x4342, kBiasS8);
+    a[1] = byte_pair_h2(wb, 0x4140, kBiasS8);
+    a[3] = byte_pair_h2(wb, 0x4342, kBiasS8);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const uint4 bf = __ldg(fr + (nt * 8 + s) * 32);
+      mma16816(d[nt][gr], a, bf.x, bf.y);
+      mma16816(d[nt][gr], a, bf.z, bf.w);
+    }
+  }
+  // cell weights by K scale, the two cells of the lane summed, then a butterfly over the 8 cell pairs
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const float(&x)[2][4] = d[nt];
+    float e0 = fmaf(ks[0].y, x[1][0], ks[0].x * x[0][0]);
+    e0 += fmaf(ks[1].y, x[1][2], ks[1].x * x[0][2]);
+    float e1 = fmaf(ks[0].y, x[1][1], ks[0].x * x[0][1]);
+    e1 += fmaf(ks[1].y, x[1][3], ks[1].x * x[0][3]);
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      e0 += __shfl_xor_sync(0xffffffffu, e0, o);
+      e1 += __shfl_xor_sync(0xffffffffu, e1, o);
+    }
+    if (g == 0) {
+      const int row = nt * 8 + 2 * tq;
+      part[warp * NT * 8 + row] = row < R ? e0 * __ldg(inv_f + row * Hkv + h) : 0.f;
+      part[warp * NT * 8 + row + 1] = row + 1 < R ? e1 * __ldg(inv_f + (row + 1) * Hkv + h) : 0.f;
+    }
+  }
+  __syncthreads();
+  // S[t, b] for the rows of this pool: lane l holds task l (head-major), then a fixed butterfly.
+  const int n_warps = blockDim.x >> 5;
+  for (int t = warp; t < R; t += n_warps) {
+    if (p.row_pool[t] != pi) continue;
+    float sum = lane < tpu ? part[lane * NT * 8 + t] : 0.f;
+    sum = warp_sum(sum);
+    if (lane == 0) p.scores[(size_t)t * p.max_blocks + b] = sum * (kInvSqrtD / (float)n_b);
+  }
+}
+
+// ------------------------------------------------------------------------------------------ 4
+struct Stage {
+  int8_t k[kSub * kD];
+  uint8_t v[kSub * kD];
+  float ks[kSub * 2];
+  float vs[kSub * 4];
+  int valid[kSub];
+};
+
+// Copies of sub-tile `st` of the split into `sg`: thread (cell c = tid / 2, half) copies half of
+// the cell's K and V pieces and one of its scale rows; invisible cells copy nothing.
+__device__ __forceinline__ void prefetch_sub(const WinAttnParams& p, const PoolDev& pool, Stage& sg, int base, int n_cells,
+                                             int st, int t, int h, int pos, bool v4) {
+  const int c = threadIdx.x >> 1, half = threadIdx.x & 1;
+  const int idx = st * kSub + c;
+  bool valid = false;
+  long long slot = 0;
+  if (idx < n_cells) {
+    const int cell = __ldg(p.ids + (size_t)t * p.k_cells + base + idx);
+    valid = cell <= pos && cell >= 0 && cell < pool.n_filled;
+    if (valid) slot = cell_slot(pool, p.n_kv_heads, h, cell);
+  }
+  if (valid) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int pc = 4 * half + k;
+      cp_async16(sg.k + c * kD + pc * 16, pool.k_codes + slot * kD + pc * 16);
+    }
+    if (!v4) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int pc = 4 * half + k;
+        cp_async16(sg.v + c * kD + pc * 16, pool.v_codes + slot * kD + pc * 16);
+      }
+      if (half) cp_async8(sg.vs + 2 * c, pool.v_scales + slot * 2);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int pc = 2 * half + k;
+        cp_async16(sg.v + c * 64 + pc * 16, pool.v_codes + slot * 64 + pc * 16);
+      }
+      if (half) cp_async16(sg.vs + 4 * c, pool.v_scales + slot * 4);
+    }
+    if (!half) cp_async8(sg.ks + 2 * c, pool.k_scales + slot * 2);
+  }
+  if (!half) sg.valid[c] = valid;
+  cp_async_commit();
+}
+
+// Writes the empty result (out = 0, lse = -inf) of the G q heads of (t, KV head h).
+__device__ __forceinline__ void write_empty(const WinAttnParams& p, int t, int h, int G) {
+  for (int i = threadIdx.x; i < G * kD; i += blockDim.x)
+    p.out[((size_t)t * p.n_q_heads + h * G) * kD + i] = 0.f;
+  if (p.lse && threadIdx.x < G) p.lse[(size_t)t * p.n_q_heads + h * G + threadIdx.x] = -INFINITY;
+}
+
+__global__ void __launch_bounds__(kAttnThreads, 5) win_attn_kernel(const WinAttnParams p) {
+  const int R = p.n_rows, Hkv = p.n_kv_heads;
+  const int n_pairs = R * Hkv;
+  const int pair = blockIdx.x % n_pairs, split = blockIdx.x / n_pairs;
+  const int t = pair % R, h = pair / R;
+  const int G = p.n_q_heads / Hkv;
+  const int pos = __ldg(p.row_pos + t);
+  const PoolDev& pool = p.pools[p.row_pool[t]];
+  const bool v4 = pool.v_bits == 4;
+  const int n_vg = v4 ? 4 : 2;
+
+  __shared__ __align__(16) Stage stages[2];
+  __shared__ __align__(16) float p_s[8][kSub];
+  __shared__ float red_s[2][4][8];
+  __shared__ int s_last;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, tq = lane & 3;
+
+  // ---- q of head g (this thread's B columns): dims 16s + 4tq .. +3, s = 0..7, scaled by 2^fe
+  // (max |q 2^fe| in [64, 128)) and split into fp16 hi + lo.  q is an input of the window, so this
+  // runs before the wait for the selection.
+  uint32_t qh[8][2], ql[8][2];
+  float lam_lo, lam_hi;   // logit scale of heads 2tq and 2tq+1
+  {
+    float qv[8][4];
+    float amax = 0.f;
+    const float* qrow = p.q + ((size_t)t * p.n_q_heads + h * G + min(g, G - 1)) * kD + 4 * tq;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (g < G) v = __ldg(reinterpret_cast<const float4*>(qrow + 16 * s));
+      qv[s][0] = v.x; qv[s][1] = v.y; qv[s][2] = v.z; qv[s][3] = v.w;
+      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const int fe = scale_exp_128(amax);
+    const float f = pow2i(fe);
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      split_pair(qv[s][0] * f, qv[s][1] * f, qh[s][0], ql[s][0]);
+      split_pair(qv[s][2] * f, qv[s][3] * f, qh[s][1], ql[s][1]);
+    }
+    const float lam = kInvSqrtD * pow2i(-fe);
+    lam_lo = __shfl_sync(0xffffffffu, lam, 4 * (2 * tq));
+    lam_hi = __shfl_sync(0xffffffffu, lam, 4 * (2 * tq + 1));
+  }
+
+  pdl_wait();   // ids and n_sel of the preceding launch
+  const int n_sel = min(__ldg(p.n_sel + t), p.k_cells);
+  const int n_act = (n_sel + p.split_cells - 1) / p.split_cells;
+  if (split >= n_act) {
+    if (split == 0) write_empty(p, t, h, G);   // no selected cell: out = 0, lse = -inf
+    return;
+  }
+  const int base = split * p.split_cells;
+  const int n_cells = min(p.split_cells, n_sel - base);
+  const int n_sub = (n_cells + kSub - 1) / kSub;
+  prefetch_sub(p, pool, stages[0], base, n_cells, 0, t, h, pos, v4);
+
+  const int vgrp = v4 ? warp : (warp >> 1);   // V-scale group of this warp's 32 dims
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+  float o_acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  for (int st = 0; st < n_sub; ++st) {
+    Stage& S = stages[st & 1];
+    if (st + 1 < n_sub) {
+      prefetch_sub(p, pool, stages[(st + 1) & 1], base, n_cells, st + 1, t, h, pos, v4);
+      cp_async_wait_group1();
+    } else {
+      cp_async_wait_all();
+    }
+    __syncthreads();
+
+    // ---- S^T = Kcode . (q f)^T on this warp's 16 cells, per K-scale group.
+    const int cb = 16 * warp;
+    float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      const uint32_t w0 = *reinterpret_cast<const uint32_t*>(S.k + (cb + g) * kD + 16 * s + 4 * tq) ^ 0x80808080u;
+      const uint32_t w1 = *reinterpret_cast<const uint32_t*>(S.k + (cb + g + 8) * kD + 16 * s + 4 * tq) ^ 0x80808080u;
+      uint32_t a[4];
+      a[0] = byte_pair_h2(w0, 0x4140, kBiasS8);
+      a[2] = byte_pair_h2(w0, 0x4342, kBiasS8);
+      a[1] = byte_pair_h2(w1, 0x4140, kBiasS8);
+      a[3] = byte_pair_h2(w1, 0x4342, kBiasS8);
+      if (s < 4) {
+        mma16816(d0, a, qh[s][0], qh[s][1]);
+        mma16816(d0, a, ql[s][0], ql[s][1]);
+      } else {
+        mma16816(d1, a, qh[s][0], qh[s][1]);
+        mma16816(d1, a, ql[s][0], ql[s][1]);
+      }
+    }
+    // ---- logits of cells cb+g, cb+g+8 for heads 2tq, 2tq+1; masked cells -> -inf.
+    float z[4];
+    {
+      const bool va = S.valid[cb + g], vb = S.valid[cb + g + 8];
+      const float2 ka = *reinterpret_cast<const float2*>(S.ks + 2 * (cb + g));
+      const float2 kb = *reinterpret_cast<const float2*>(S.ks + 2 * (cb + g + 8));
+      z[0] = va ? fmaf(d1[0], ka.y, d0[0] * ka.x) * lam_lo : -INFINITY;
+      z[1] = va ? fmaf(d1[1], ka.y, d0[1] * ka.x) * lam_hi : -INFINITY;
+      z[2] = vb ? fmaf(d1[2], kb.y, d0[2] * kb.x) * lam_lo : -INFINITY;
+      z[3] = vb ? fmaf(d1[3], kb.y, d0[3] * kb.x) * lam_hi : -INFINITY;
+    }
+    float mx0 = fmaxf(z[0], z[2]), mx1 = fmaxf(z[1], z[3]);
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
+    if (g == 0) {
+      red_s[0][warp][2 * tq] = mx0;
+      red_s[0][warp][2 * tq + 1] = mx1;
+    }
+    __syncthreads();
+    float mt0 = red_s[0][0][2 * tq], mt1 = red_s[0][0][2 * tq + 1];
+#pragma unroll
+    for (int w = 1; w < 4; ++w) {
+      mt0 = fmaxf(mt0, red_s[0][w][2 * tq]);
+      mt1 = fmaxf(mt1, red_s[0][w][2 * tq + 1]);
+    }
+    const float mn0 = fmaxf(m_run[0], mt0), mn1 = fmaxf(m_run[1], mt1);
+    const float al0 = (mn0 == -INFINITY) ? 1.f : expf(m_run[0] - mn0);
+    const float al1 = (mn1 == -INFINITY) ? 1.f : expf(m_run[1] - mn1);
+    float pr[4];
+    pr[0] = (z[0] == -INFINITY) ? 0.f : expf(z[0] - mn0);
+    pr[1] = (z[1] == -INFINITY) ? 0.f : expf(z[1] - mn1);
+    pr[2] = (z[2] == -INFINITY) ? 0.f : expf(z[2] - mn0);
+    pr[3] = (z[3] == -INFINITY) ? 0.f : expf(z[3] - mn1);
+    float ls0 = pr[0] + pr[2], ls1 = pr[1] + pr[3];
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      ls0 += __shfl_xor_sync(0xffffffffu, ls0, o);
+      ls1 += __shfl_xor_sync(0xffffffffu, ls1, o);
+    }
+    if (g == 0) {
+      red_s[1][warp][2 * tq] = ls0;
+      red_s[1][warp][2 * tq + 1] = ls1;
+    }
+    p_s[2 * tq][cb + g] = pr[0];
+    p_s[2 * tq + 1][cb + g] = pr[1];
+    p_s[2 * tq][cb + g + 8] = pr[2];
+    p_s[2 * tq + 1][cb + g + 8] = pr[3];
+    __syncthreads();
+    float lt0 = red_s[1][0][2 * tq], lt1 = red_s[1][0][2 * tq + 1];
+#pragma unroll
+    for (int w = 1; w < 4; ++w) {
+      lt0 += red_s[1][w][2 * tq];
+      lt1 += red_s[1][w][2 * tq + 1];
+    }
+    l_run[0] = fmaf(l_run[0], al0, lt0);
+    l_run[1] = fmaf(l_run[1], al1, lt1);
+    m_run[0] = mn0;
+    m_run[1] = mn1;
+
+    // ---- power of two 2^k for this warp's V-scale group: max |vs| 2^k in [8, 16).
+    float vmax = 0.f;
+#pragma unroll
+    for (int q2 = 0; q2 < 2; ++q2) {
+      const int c = lane + 32 * q2;
+      if (S.valid[c]) vmax = fmaxf(vmax, fabsf(S.vs[c * n_vg + vgrp]));
+    }
+    vmax = warp_max(vmax);
+    int ve = 0;
+    if (vmax > 0.f) frexpf(vmax, &ve);
+    const int vk = vmax > 0.f ? max(-126, min(127, 4 - ve)) : 0;
+    const float vup = pow2i(vk), vdown = pow2i(-vk);
+
+    // ---- O^T[32 dims of this warp x heads] = Vcode^T . W over the sub-tile's 64 cells.
+    float pv[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      const int c0 = 16 * s + 4 * tq;
+      const float4 pp = *reinterpret_cast<const float4*>(&p_s[g][c0]);
+      float w[4] = {pp.x, pp.y, pp.z, pp.w};
+#pragma unroll
+      for (int q2 = 0; q2 < 4; ++q2) w[q2] = S.valid[c0 + q2] ? w[q2] * (S.vs[(c0 + q2) * n_vg + vgrp] * vup) : 0.f;
+      uint32_t bh0, bl0, bh1, bl1;
+      split_pair(w[0], w[1], bh0, bl0);
+      split_pair(w[2], w[3], bh1, bl1);
+      uint32_t x[4];
+      uint32_t bias;
+      if (!v4) {
+#pragma unroll
+        for (int q2 = 0; q2 < 4; ++q2)
+          x[q2] = *reinterpret_cast<const uint32_t*>(S.v + (c0 + q2) * kD + 32 * warp + 4 * g) ^ 0x80808080u;
+        bias = kBiasS8;
+      } else {
+#pragma unroll
+        for (int q2 = 0; q2 < 4; ++q2) {
+          const uint32_t bb = *reinterpret_cast<const uint16_t*>(S.v + (c0 + q2) * 64 + 16 * warp + 2 * g);
+          x[q2] = __byte_perm(bb & 0x0F0Fu, (bb >> 4) & 0x0F0Fu, 0x5140);   // nibbles -> bytes, dim order
+        }
+        bias = kBiasNibble;
+      }
+      // m-tile 0: dims 32w + 4g + {0, 1}; m-tile 1: dims 32w + 4g + {2, 3}
+      const uint32_t y01l = __byte_perm(x[0], x[1], 0x5140), y01h = __byte_perm(x[0], x[1], 0x7362);
+      const uint32_t y23l = __byte_perm(x[2], x[3], 0x5140), y23h = __byte_perm(x[2], x[3], 0x7362);
+      uint32_t a0[4], a1[4];
+      a0[0] = byte_pair_h2(y01l, 0x4140, bias);
+      a0[1] = byte_pair_h2(y01l, 0x4342, bias);
+      a0[2] = byte_pair_h2(y23l, 0x4140, bias);
+      a0[3] = byte_pair_h2(y23l, 0x4342, bias);
+      a1[0] = byte_pair_h2(y01h, 0x4140, bias);
+      a1[1] = byte_pair_h2(y01h, 0x4342, bias);
+      a1[2] = byte_pair_h2(y23h, 0x4140, bias);
+      a1[3] = byte_pair_h2(y23h, 0x4342, bias);
+      mma16816(pv[0], a0, bh0, bh1);
+      mma16816(pv[0], a0, bl0, bl1);
+      mma16816(pv[1], a1, bh0, bh1);
+      mma16816(pv[1], a1, bl0, bl1);
+    }
+    // ---- fold: O = O * alpha + PV / 2^k (columns: heads 2tq, 2tq+1)
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      o_acc[i][0] = fmaf(o_acc[i][0], al0, pv[i][0] * vdown);
+      o_acc[i][1] = fmaf(o_acc[i][1], al1, pv[i][1] * vdown);
+      o_acc[i][2] = fmaf(o_acc[i][2], al0, pv[i][2] * vdown);
+      o_acc[i][3] = fmaf(o_acc[i][3], al1, pv[i][3] * vdown);
+    }
+    __syncthreads();   // the stage and p_s are rewritten by the sub-tile after next
+  }
+
+  // ---- this split's partial: heads 2tq, 2tq+1 < G, dims 32w + 4g ..
+  const size_t sbase = ((size_t)pair * p.n_splits + split) * G;
+  if (2 * tq < G) {
+    *reinterpret_cast<float4*>(p.part_o + (sbase + 2 * tq) * kD + 32 * warp + 4 * g) =
+        make_float4(o_acc[0][0], o_acc[0][2], o_acc[1][0], o_acc[1][2]);
+    if (warp == 0 && g == 0)
+      *reinterpret_cast<float2*>(p.part_ml + (sbase + 2 * tq) * 2) = make_float2(m_run[0], l_run[0]);
+  }
+  if (2 * tq + 1 < G) {
+    *reinterpret_cast<float4*>(p.part_o + (sbase + 2 * tq + 1) * kD + 32 * warp + 4 * g) =
+        make_float4(o_acc[0][1], o_acc[0][3], o_acc[1][1], o_acc[1][3]);
+    if (warp == 0 && g == 0)
+      *reinterpret_cast<float2*>(p.part_ml + (sbase + 2 * tq + 1) * 2) = make_float2(m_run[1], l_run[1]);
+  }
+
+  // ---- ticket: the CTA that completes the (row, KV head)'s last split merges all of them.
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = (atomicAdd(p.tickets + pair, 1u) == (unsigned)(n_act - 1));
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  // Weights exp(m_j - M) of every split and head, staged in the (now unused) stage memory.
+  float* mw = reinterpret_cast<float*>(&stages[0]);        // [n_act][G]: m, then the weight
+  float* lw = mw + kMaxSplits * 8;                          // [n_act][G]: l
+  float* ML = lw + kMaxSplits * 8;                          // [G][2]: M, L
+  const size_t pbase = (size_t)pair * p.n_splits * G;
+  for (int i = tid; i < n_act * G; i += kAttnThreads) {
+    const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + pbase + i);
+    mw[i] = ml.x;
+    lw[i] = ml.y;
+  }
+  __syncthreads();
+  if (tid < G) {
+    float M = -INFINITY;
+    for (int j = 0; j < n_act; ++j) M = fmaxf(M, mw[j * G + tid]);
+    float L = 0.f;
+    for (int j = 0; j < n_act; ++j) {
+      const float mj = mw[j * G + tid];
+      const float w = (mj == -INFINITY) ? 0.f : expf(mj - M);
+      mw[j * G + tid] = w;
+      L = fmaf(lw[j * G + tid], w, L);
+    }
+    ML[2 * tid] = M;
+    ML[2 * tid + 1] = L;
+  }
+  __syncthreads();
+  for (int gg = 0; gg < G; ++gg) {
+    const float M = ML[2 * gg], L = ML[2 * gg + 1];
+    float* orow = p.out + ((size_t)t * p.n_q_heads + h * G + gg) * kD;
+    if (M == -INFINITY) {   // every visible cell of the selection masked: empty
+      orow[tid] = 0.f;
+      if (p.lse && tid == 0) p.lse[(size_t)t * p.n_q_heads + h * G + gg] = -INFINITY;
+      continue;
+    }
+    const float* po = p.part_o + (pbase + gg) * kD + tid;
+    float acc = 0.f;
+#pragma unroll 8
+    for (int j = 0; j < n_act; ++j) acc = fmaf(__ldcg(po + (size_t)j * G * kD), mw[j * G + gg], acc);
+    orow[tid] = acc / L;
+    if (p.lse && tid == 0) p.lse[(size_t)t * p.n_q_heads + h * G + gg] = M + logf(L);
+  }
+  if (tid == 0) p.tickets[pair] = 0u;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------------------------
+// Host side
+
+int window_split_cells(int n_rows, int n_kv_heads, int k_cells, int n_sm) {
+  // about five 128-thread CTAs per SM in one wave, splits a multiple of the 64-cell sub-tile, at
+  // most kMaxSplits splits per (row, KV head)
+  const long long total = (long long)n_rows * n_kv_heads * (k_cells > 0 ? k_cells : 1);
+  const long long target = 5LL * (n_sm > 0 ? n_sm : 1);
+  long long sc = kSub * ((total + kSub * target - 1) / (kSub * target));
+  const long long min_sc = kSub * (((long long)k_cells + (long long)kSub * kMaxSplits - 1) / ((long long)kSub * kMaxSplits));
+  if (sc < min_sc) sc = min_sc;
+  if (sc < kSub) sc = kSub;
+  return (int)sc;
+}
+
+WindowLayout window_layout(int n_rows, int n_q_heads, int n_kv_heads, int k_cells, int n_sm) {
+  WindowLayout L{};
+  const int NT = (n_rows + 7) / 8;
+  const int G = n_q_heads / n_kv_heads;
+  const int n_pairs = n_rows * n_kv_heads;
+  L.split_cells = window_split_cells(n_rows, n_kv_heads, k_cells, n_sm);
+  L.n_splits = (k_cells + L.split_cells - 1) / L.split_cells;
+  if (L.n_splits < 1) L.n_splits = 1;
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  size_t off = 0;
+  L.frag = off;
+  off = up(off + (size_t)16 * n_kv_heads * NT * 8 * 32);
+  L.inv_f = off;
+  off = up(off + sizeof(float) * (size_t)n_rows * n_kv_heads);
+  L.tickets = off;
+  off = up(off + sizeof(unsigned) * (size_t)n_pairs);
+  L.part_ml = off;
+  off = up(off + sizeof(float) * 2 * (size_t)n_pairs * L.n_splits * G);
+  L.part_o = off;
+  off = up(off + sizeof(float) * kD * (size_t)n_pairs * L.n_splits * G);
+  L.total = off;
+  return L;
+}
+
+bool window_scores_supported(int n_rows, int n_kv_heads, int block_cells) {
+  return n_rows <= 32 && block_cells % 16 == 0 && n_kv_heads * (block_cells / 16) <= 32;
+}
+
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+cudaError_t launch_decode_window(const WindowArgs& a, cudaStream_t stream) {
+  const ScoresParams& sp = a.scores;
+  const int R = sp.n_rows, Hkv = sp.n_kv_heads, NT = (R + 7) / 8;
+  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+  uint4* frag = reinterpret_cast<uint4*>(ws + a.layout.frag);
+  float* inv_f = reinterpret_cast<float*>(ws + a.layout.inv_f);
+  WinAttnParams ap = a.attn;
+  ap.tickets = reinterpret_cast<unsigned*>(ws + a.layout.tickets);
+  ap.part_ml = reinterpret_cast<float*>(ws + a.layout.part_ml);
+  ap.part_o = reinterpret_cast<float*>(ws + a.layout.part_o);
+  ap.split_cells = a.layout.split_cells;
+  ap.n_splits = a.layout.n_splits;
+  const int n_pairs = R * Hkv;
+
+  // 1. q fragments + ticket reset: an ordinary launch, ordered after everything before it on the
+  //    stream (the previous window's merge may still hold the tickets).
+  cudaError_t e = launch_ex(win_qprep_kernel, dim3(NT * 8, Hkv), dim3(32), 0, stream, false, sp.q, R, sp.n_q_heads,
+                            Hkv, NT, frag, inv_f, ap.tickets, n_pairs);
+  if (e != cudaSuccess) return e;
+  // 2. block scores
+  if (sp.total_units > 0) {
+    const int tpu = Hkv * (sp.block_cells / 16);
+    const size_t smem = sizeof(float) * (size_t)tpu * NT * 8;
+    const dim3 grid(sp.total_units), block(32 * tpu);
+    switch (NT) {
+      case 1: e = launch_ex(win_scores_kernel<1>, grid, block, smem, stream, true, sp, (const uint4*)frag, (const float*)inv_f); break;
+      case 2: e = launch_ex(win_scores_kernel<2>, grid, block, smem, stream, true, sp, (const uint4*)frag, (const float*)inv_f); break;
+      case 3: e = launch_ex(win_scores_kernel<3>, grid, block, smem, stream, true, sp, (const uint4*)frag, (const float*)inv_f); break;
+      default: e = launch_ex(win_scores_kernel<4>, grid, block, smem, stream, true, sp, (const uint4*)frag, (const float*)inv_f); break;
+    }
+    if (e != cudaSuccess) return e;
+  }
+  // 3. top-k
+  e = launch_topk_ex(a.topk, a.max_nb, stream, true);
+  if (e != cudaSuccess) return e;
+  // 4. attention + merge
+  return launch_ex(win_attn_kernel, dim3(n_pairs * ap.n_splits), dim3(kAttnThreads), 0, stream, true, ap);
+}
+
+}  // namespace qsa

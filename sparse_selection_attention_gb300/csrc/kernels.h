@@ -59,6 +59,45 @@ struct PromptParams {
   unsigned long long wait_limit_ns;
 };
 
+// Split attention + fused merge of a decode window (qsa_decode_window).
+struct WinAttnParams {
+  PoolDev pools[QSA_MAX_POOLS];
+  int row_pool[QSA_MAX_DECODE_ROWS];
+  const float* q;
+  const int32_t* row_pos;
+  const int32_t* ids;
+  const int32_t* n_sel;
+  int n_rows, n_q_heads, n_kv_heads, k_cells;
+  int split_cells;   // cells of one split (multiple of 64)
+  int n_splits;      // splits per (row, KV head) in the workspace
+  float* part_ml;    // [n_rows * n_kv_heads][n_splits][G][2]
+  float* part_o;     // [n_rows * n_kv_heads][n_splits][G][128]
+  unsigned* tickets; // [n_rows * n_kv_heads]
+  float* out;        // [n_rows][n_q_heads][128]
+  float* lse;        // [n_rows][n_q_heads] or nullptr
+};
+
+// Byte offsets of the parts of a decode-window workspace.
+struct WindowLayout {
+  size_t frag, inv_f, tickets, part_ml, part_o, total;
+  int split_cells, n_splits;
+};
+
+struct WindowArgs {
+  ScoresParams scores;
+  TopkParams topk;
+  int max_nb;
+  WinAttnParams attn;
+  WindowLayout layout;
+  void* workspace;
+};
+
+WindowLayout window_layout(int n_rows, int n_q_heads, int n_kv_heads, int k_cells, int n_sm);
+bool window_scores_supported(int n_rows, int n_kv_heads, int block_cells);
+cudaError_t launch_decode_window(const WindowArgs& a, cudaStream_t stream);
+// Top-k launch; with pdl the launch may start before the preceding kernel of the stream ends.
+cudaError_t launch_topk_ex(const TopkParams& p, int max_nb, cudaStream_t stream, bool pdl);
+
 size_t prompt_scratch_bytes(int v_bits, int n_kv_heads, int q_end_pos);
 size_t block_scores_smem_bytes(int n_rows, int n_q_heads, int n_kv_heads, int block_cells);
 bool block_scores_supported(int n_kv_heads, int block_cells);

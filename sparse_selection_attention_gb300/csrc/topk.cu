@@ -8,15 +8,17 @@
 // digit with a work-group scan over the bins; integers only, so the same ids).
 //
 // One CTA per row; thread i holds the keys of blocks [i*K, (i+1)*K) in
-// registers.  The threshold T (the kb-th largest key) is found one bit at a
-// time from the most significant: T | bit is kept when at least kb keys are
-// >= it.  Each step is one CTA-wide count: __syncthreads_count when a thread
-// holds one key, else a warp reduction and one barrier.  Blocks with key > T
+// registers.  The threshold T (the kb-th largest key) is found one 8-bit digit
+// at a time from the most significant: for the keys that share the digits
+// found so far, a 256-bin histogram of the next digit (warp-aggregated shared
+// memory counts) is scanned from the top by one warp, which picks the digit
+// where the running count reaches the number still needed.  Blocks with key > T
 // are taken, then the lowest-id blocks with key == T.  Two CTA prefix sums in
 // block-id order give each chosen block its rank j; every block but the row's
 // last holds exactly B cells, so chosen block j fills ids[j*B ..], written
 // coalesced by the whole CTA.
 #include "kernels.h"
+#include "mma_sync.cuh"
 
 namespace qsa {
 
@@ -57,26 +59,66 @@ __device__ __forceinline__ int cta_exclusive_scan(int v, int* warp_tot, int& tot
   return base + inc - v;
 }
 
-// Number of this CTA's keys >= cand (every thread gets the total).
-__device__ __forceinline__ int cta_count_ge(const uint32_t (&key)[kMaxKeys], int K, int b0, int nb, uint32_t cand,
-                                            int* wsum, int parity) {
-  if (K == 1) return __syncthreads_count(b0 < nb && key[0] >= cand);
-  int c = 0;
+// Adds, for every key of this thread whose bits under `mask` equal `prefix`, one count to the
+// bin of its digit (key >> shift) & 255; lanes with the same digit add once, together.
+__device__ __forceinline__ void add_digits(const uint32_t (&key)[kMaxKeys], int K, int b0, int nb, uint32_t mask,
+                                           uint32_t prefix, int shift, unsigned* hist) {
+  const int lane = threadIdx.x & 31;
 #pragma unroll
-  for (int i = 0; i < kMaxKeys; ++i) c += (i < K && b0 + i < nb && key[i] >= cand) ? 1 : 0;
-  c = __reduce_add_sync(0xffffffffu, c);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, n_warps = blockDim.x >> 5;
-  if (lane == 0) wsum[parity * 32 + warp] = c;
-  __syncthreads();
-  // wsum[parity] is rewritten two steps later, after the next barrier
-  return __reduce_add_sync(0xffffffffu, lane < n_warps ? wsum[parity * 32 + lane] : 0);
+  for (int i = 0; i < kMaxKeys; ++i) {
+    if (i < K) {   // uniform across the CTA
+      const bool live = b0 + i < nb && (key[i] & mask) == prefix;
+      const uint32_t digit = (key[i] >> shift) & 255u;
+      const unsigned peers = __match_any_sync(0xffffffffu, live ? digit : 256u + lane);
+      if (live && lane == __ffs(peers) - 1) atomicAdd(hist + digit, (unsigned)__popc(peers));
+    }
+  }
+}
+
+// Warp 0: the largest digit d whose count of keys with digit >= d reaches `need`; returns (d, need
+// minus the keys with digit > d) through s_out.  Lane l scans bins 8l .. 8l+7.
+__device__ __forceinline__ void pick_digit(const unsigned* hist, int need, int* s_out) {
+  const int lane = threadIdx.x & 31;
+  unsigned c[8], own = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    c[j] = hist[8 * lane + j];
+    own += c[j];
+  }
+  unsigned incl = own;   // keys in bins of lanes >= this lane
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned n = __shfl_down_sync(0xffffffffu, incl, o);
+    if (lane + o < 32) incl += n;
+  }
+  const unsigned above = incl - own;
+  if (above < (unsigned)need && (unsigned)need <= incl) {   // exactly one lane
+    unsigned cum = above;
+    int d = 8 * lane;
+#pragma unroll
+    for (int j = 7; j >= 0; --j) {
+      if (cum + c[j] >= (unsigned)need) {
+        d = 8 * lane + j;
+        break;
+      }
+      cum += c[j];
+    }
+    s_out[0] = d;
+    s_out[1] = need - (int)cum;
+  }
 }
 
 __global__ void __launch_bounds__(kMaxThreads) topk_kernel(const TopkParams p) {
   extern __shared__ int smem[];          // chosen list [kb]
   __shared__ int warp_tot[32];
-  __shared__ int wsum[64];
+  __shared__ unsigned hist[4][256];
+  __shared__ int s_pick[2];
   const int t = blockIdx.x, tid = threadIdx.x;
+  for (int i = tid; i < 4 * 256; i += blockDim.x) (&hist[0][0])[i] = 0u;
+  // Scores come from the preceding launch of the stream (a no-op without that dependency); the next
+  // launch may start its CTAs now (they wait for this grid before reading ids).
+  ms::pdl_trigger();
+  ms::pdl_wait();
   const int n_threads = blockDim.x;
   const int B = p.block_cells;
   const int n_filled = p.n_filled[t];
@@ -94,17 +136,26 @@ __global__ void __launch_bounds__(kMaxThreads) topk_kernel(const TopkParams p) {
   uint32_t key[kMaxKeys];
 #pragma unroll
   for (int i = 0; i < kMaxKeys; ++i) key[i] = (i < K && b0 + i < nb) ? score_key(__ldg(sc + b0 + i)) : 0u;
+  __syncthreads();   // histograms zeroed
 
   const bool take_all = (kb == nb);
   uint32_t T = 0;
   int need = 0;
   if (!take_all) {
-    for (int bit = 31; bit >= 0; --bit) {
-      const uint32_t cand = T | (1u << bit);
-      if (cta_count_ge(key, K, b0, nb, cand, wsum, bit & 1) >= kb) T = cand;
+    need = kb;
+    uint32_t mask = 0;
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+      add_digits(key, K, b0, nb, mask, T, shift, hist[pass]);
+      __syncthreads();
+      if (tid < 32) pick_digit(hist[pass], need, s_pick);
+      __syncthreads();
+      T |= (uint32_t)s_pick[0] << shift;
+      need = s_pick[1];
+      mask |= 255u << shift;
+      // s_pick is rewritten in the next pass only after its histogram barrier
     }
-    // keys > T (T + 1 does not wrap: the largest key, +inf's, is 0xFF800000); parity 1 follows bit 0's 0
-    need = kb - cta_count_ge(key, K, b0, nb, T + 1u, wsum, 1);
+    // need = the keys equal to T that are taken (lowest block ids first)
   }
 
   int tot = 0;
@@ -167,14 +218,27 @@ int topk_threads(int max_nb) {
 
 size_t topk_smem_bytes(int max_nb) { return sizeof(int) * (size_t)max_nb; }
 
-cudaError_t launch_topk(const TopkParams& p, int max_nb, cudaStream_t stream) {
+cudaError_t launch_topk_ex(const TopkParams& p, int max_nb, cudaStream_t stream, bool pdl) {
   const int th = topk_threads(max_nb);
   if ((max_nb + th - 1) / th > kMaxKeys) return cudaErrorInvalidValue;
   const size_t smem = topk_smem_bytes(max_nb);
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(topk_kernel), smem);
   if (e != cudaSuccess) return e;
-  topk_kernel<<<p.n_rows, th, smem, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.n_rows);
+  cfg.blockDim = dim3(th);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, topk_kernel, p);
+}
+
+cudaError_t launch_topk(const TopkParams& p, int max_nb, cudaStream_t stream) {
+  return launch_topk_ex(p, max_nb, stream, false);
 }
 
 }  // namespace qsa

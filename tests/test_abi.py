@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_pure_host_calls(lib):
-    assert qsa.abi_version() == 101
+    assert qsa.abi_version() == 102
     assert qsa.status_str(qsa.QSA_ERR_SCRATCH) == "scratch buffer too small"
     assert qsa.decode_partials_bytes(5, 24, 64) == 4 * 5 * 24 * 64 * 130
     assert qsa.decode_partials_bytes(0, 24, 64) == 0

@@ -1,0 +1,124 @@
+"""GPU parity of the one-call decode window (qsa_decode_window: block scores ->
+top-k -> split attention with the merge fused in) against the FP64 oracle,
+through the C ABI.
+
+Gates as for the four separate calls: ids bit-exact given the GPU's own fp32
+scores; scores, out and lse within max |gpu - oracle| / max |oracle| <= 1e-5;
+bitwise run-to-run determinism."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import sparse_selection_attention_gb300 as qsa
+import workloads as W
+from _parity import assert_close, gpu_ids, upload_case
+
+pytestmark = pytest.mark.gpu
+
+
+def run_window_and_check(case):
+    win, q, row_pos = upload_case(case)
+    win.out.fill_(float("nan"))
+    win.lse.fill_(float("nan"))
+    win.run_window(q, row_pos)
+    torch.cuda.synchronize()
+    R = case.n_rows
+    scores_gpu = win.scores.cpu().numpy()
+    ref = O.decode_window(case, scores_f32=scores_gpu)
+    for t in range(R):
+        nb = len(ref["scores"][t])
+        assert_close(scores_gpu[t, :nb], ref["scores"][t], f"scores row {t}")
+    ids, n_sel = gpu_ids(win)
+    for t in range(R):
+        assert n_sel[t] == ref["n_sel"][t], f"n_sel row {t}"
+        assert np.array_equal(ids[t], ref["ids"][t]), f"ids row {t}"
+    assert_close(win.out.cpu().numpy(), ref["out"], "out")
+    assert_close(win.lse.cpu().numpy(), ref["lse"], "lse")
+    return win, q, row_pos
+
+
+def test_window_tiny_dense_decode():
+    run_window_and_check(W.tiny_dense_decode())
+
+
+def test_window_verify_window_full_size():
+    run_window_and_check(W.verify_window())
+
+
+def test_window_batched_long_context_full_size():
+    run_window_and_check(W.batched_long_context())
+
+
+@pytest.mark.parametrize("fill,page_cells,Hq,Hkv,k,v_bits,B", [
+    (1000, 128, 6, 2, 256, 8, 64),      # ragged last block
+    (1000, 256, 8, 1, 2048, 8, 64),     # k above all cells: take all
+    (777, 64, 4, 4, 320, 4, 64),        # 4-bit V
+    (300, 64, 24, 4, 64, 8, 64),        # one block
+    (2000, 256, 32, 4, 512, 8, 128),    # 128-cell blocks, 8 q heads per KV head
+    (2000, 256, 16, 8, 256, 8, 32),     # 32-cell blocks, 8 KV heads
+    (3000, 256, 16, 16, 1024, 8, 32),   # 16 KV heads x 2 m-tiles: 32 warps per block
+])
+def test_window_small_ragged(fill, page_cells, Hq, Hkv, k, v_bits, B):
+    case = W.decode_case(name="wragged", seed=fill + k + B, fills=[fill], capacity=fill + 100, rows_per_slot=3,
+                         n_q_heads=Hq, n_kv_heads=Hkv, k_cells=k, chunk_cells=64, page_cells=page_cells,
+                         v_bits=v_bits, block_cells=B, bias_prob=0.05)
+    run_window_and_check(case)
+
+
+def test_window_many_rows_two_pools():
+    """20 rows (three 8-row n-tiles) over two pools in one call."""
+    case = W.decode_case(name="wmany", seed=77, fills=[2000, 1500], capacity=2048, rows_per_slot=10,
+                         n_q_heads=16, n_kv_heads=8, k_cells=256, chunk_cells=64, page_cells=256,
+                         bias_prob=0.05)
+    run_window_and_check(case)
+
+
+def test_window_rows_with_masked_cells():
+    """Rows early in the context: selected cells past a row's position are masked; splits whose cells are
+    all masked are empty and carry no weight in the merge."""
+    case = W.decode_case(name="wmasked", seed=5, fills=[900, 1500], capacity=2048, rows_per_slot=2,
+                         n_q_heads=12, n_kv_heads=2, k_cells=512, chunk_cells=64, page_cells=128,
+                         row_pos=[100, 899, 0, 1499], bias_prob=0.05)
+    run_window_and_check(case)
+
+
+def test_window_empty_selection():
+    case = W.decode_case(name="wk0", seed=9, fills=[500], capacity=512, rows_per_slot=2, n_q_heads=4,
+                         n_kv_heads=1, k_cells=0, chunk_cells=64, page_cells=64, n_chunks=2)
+    win, q, row_pos = upload_case(case)
+    win.out.fill_(float("nan"))
+    win.run_window(q, row_pos)
+    torch.cuda.synchronize()
+    assert win.n_sel.cpu().tolist() == [0, 0]
+    assert torch.all(win.out == 0) and torch.all(torch.isinf(win.lse)) and torch.all(win.lse < 0)
+
+
+def test_window_deterministic_and_reusable_workspace():
+    """Three calls on one workspace give the same bits (the tickets are cleared by every call), and the
+    result matches the four separate calls within the gate."""
+    case = W.verify_window()
+    win, q, row_pos = upload_case(case)
+    outs = []
+    for _ in range(3):
+        win.run_window(q, row_pos)
+        torch.cuda.synchronize()
+        outs.append((win.scores.clone(), win.ids.clone(), win.n_sel.clone(), win.out.clone(), win.lse.clone()))
+    for other in outs[1:]:
+        for a, b in zip(outs[0], other):
+            assert torch.equal(a, b)
+    win.run(q, row_pos)
+    torch.cuda.synchronize()
+    assert_close(outs[0][3].cpu().numpy(), win.out.cpu().numpy(), "window vs separate calls")
+
+
+def test_window_refuses_small_workspace():
+    case = W.tiny_dense_decode()
+    win, q, row_pos = upload_case(case)
+    need = qsa.load().qsa_decode_window_workspace_bytes(case.n_rows, case.n_q_heads, case.pools[0].n_kv_heads,
+                                                        case.k_cells)
+    assert need > 0
+    win._ws = torch.empty((need - 256,), dtype=torch.uint8, device="cuda")
+    with pytest.raises(qsa.QsaError) as e:
+        win.run_window(q, row_pos)
+    assert e.value.status == qsa.QSA_ERR_SCRATCH
