@@ -27,6 +27,7 @@
 #include <cuda_fp16.h>
 
 #include "kernels.h"
+#include "mma_sync.cuh"
 
 namespace qsa {
 
@@ -404,6 +405,7 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const MergePa
   const int g = blockIdx.x, t = blockIdx.y, tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
   const int d = tid & (kD - 1), qtr = tid >> 7;
+  ms::pdl_wait();   // partials of the preceding launch (a no-op without that dependency)
   const int n_sel = __ldg(p.n_sel + t);
   const int n_act = min(p.n_chunks, (max(n_sel, 0) + p.chunk_cells - 1) / p.chunk_cells);
   const size_t base = ((size_t)t * p.n_q_heads + g) * p.n_chunks;
@@ -485,10 +487,20 @@ cudaError_t launch_decode_attn(const AttnParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_attn_merge(const MergeParams& p, cudaStream_t stream) {
-  dim3 grid(p.n_q_heads, p.n_rows);
-  attn_merge_kernel<<<grid, kMergeThreads, sizeof(float) * p.n_chunks, stream>>>(p);
-  return cudaGetLastError();
+cudaError_t launch_attn_merge_ex(const MergeParams& p, cudaStream_t stream, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.n_q_heads, p.n_rows);
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.dynamicSmemBytes = sizeof(float) * p.n_chunks;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, attn_merge_kernel, p);
 }
+
+cudaError_t launch_attn_merge(const MergeParams& p, cudaStream_t stream) { return launch_attn_merge_ex(p, stream, false); }
 
 }  // namespace qsa

@@ -11,7 +11,7 @@
 //  1. win_qprep_kernel: per (row, KV head) qbar = sum of the group's q heads,
 //     scaled by a power of two and split into fp16 hi + lo, laid out as the
 //     block-score kernel's mma B fragments (computed once per window instead
-//     of once per CTA).  It also clears the merge tickets.
+//     of once per CTA).
 //  2. win_scores_kernel: one CTA per (pool, block), one warp per (KV head,
 //     16-cell m-tile); each lane's K codes and scales are loaded into
 //     registers before the kernel waits for step 1.  S^T = Kcode . qbar on
@@ -19,10 +19,11 @@
 //     over heads and m-tiles.  The result is the qsa_block_scores definition.
 //  3. topk_kernel (topk.cu), unchanged arithmetic.
 //  4. win_attn_kernel: one CTA per (row, KV head, split of the selection);
-//     the split's partial (m, l, o) of each q head is written to the
-//     workspace; the CTA that takes the last ticket of its (row, KV head)
-//     merges every split in split order (the ticket decides who merges, never
-//     the order), so the result is bitwise reproducible.
+//     each split's partial (m, l, o) per q head goes to the workspace in the
+//     qsa_decode_attn partials layout (a split of the window is a chunk of
+//     that layout).  Splits past the selection launch no work.
+//  5. attn_merge_kernel (decode_attn.cu): the log-sum-exp merge in split
+//     order, skipping empty splits; bitwise reproducible.
 #include "kernels.h"
 #include "mma_sync.cuh"
 
@@ -34,7 +35,7 @@ using namespace ms;
 
 constexpr int kAttnThreads = 128;
 constexpr int kSub = 64;   // cells per sub-tile of the attention
-constexpr int kMaxSplits = 256;
+constexpr int kMaxSplits = 256;   // splits per (row, KV head)
 
 __device__ __forceinline__ int pool_index(const int* unit_begin, int n_pools, int unit) {
   int pi = 0;
@@ -52,12 +53,9 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int w) {
 // {hi(d0, d0+1), hi(d0+2, d0+3), lo(d0, d0+1), lo(d0+2, d0+3)}: the B operand of
 // mma.m16n8k16 for the same permutation of dims that the A fragments of the codes use.
 __global__ void __launch_bounds__(32) win_qprep_kernel(const float* __restrict__ q, int n_rows, int n_q_heads,
-                                                       int n_kv_heads, int NT, uint4* frag, float* inv_f,
-                                                       unsigned* tickets, int n_tickets) {
+                                                       int n_kv_heads, int NT, uint4* frag, float* inv_f) {
   const int t = blockIdx.x, h = blockIdx.y, lane = threadIdx.x;
   const int G = n_q_heads / n_kv_heads;
-  if (t == 0 && h == 0)
-    for (int i = lane; i < n_tickets; i += 32) tickets[i] = 0u;
   pdl_trigger();
   float v[4] = {0.f, 0.f, 0.f, 0.f};
   if (t < n_rows) {
@@ -226,13 +224,6 @@ __device__ __forceinline__ void prefetch_sub(const WinAttnParams& p, const PoolD
   cp_async_commit();
 }
 
-// Writes the empty result (out = 0, lse = -inf) of the G q heads of (t, KV head h).
-__device__ __forceinline__ void write_empty(const WinAttnParams& p, int t, int h, int G) {
-  for (int i = threadIdx.x; i < G * kD; i += blockDim.x)
-    p.out[((size_t)t * p.n_q_heads + h * G) * kD + i] = 0.f;
-  if (p.lse && threadIdx.x < G) p.lse[(size_t)t * p.n_q_heads + h * G + threadIdx.x] = -INFINITY;
-}
-
 __global__ void __launch_bounds__(kAttnThreads, 5) win_attn_kernel(const WinAttnParams p) {
   const int R = p.n_rows, Hkv = p.n_kv_heads;
   const int n_pairs = R * Hkv;
@@ -247,7 +238,6 @@ __global__ void __launch_bounds__(kAttnThreads, 5) win_attn_kernel(const WinAttn
   __shared__ __align__(16) Stage stages[2];
   __shared__ __align__(16) float p_s[8][kSub];
   __shared__ float red_s[2][4][8];
-  __shared__ int s_last;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, tq = lane & 3;
@@ -285,10 +275,7 @@ __global__ void __launch_bounds__(kAttnThreads, 5) win_attn_kernel(const WinAttn
   pdl_wait();   // ids and n_sel of the preceding launch
   const int n_sel = min(__ldg(p.n_sel + t), p.k_cells);
   const int n_act = (n_sel + p.split_cells - 1) / p.split_cells;
-  if (split >= n_act) {
-    if (split == 0) write_empty(p, t, h, G);   // no selected cell: out = 0, lse = -inf
-    return;
-  }
+  if (split >= n_act) return;   // past the selection: nothing to read, nothing the merge reads
   const int base = split * p.split_cells;
   const int n_cells = min(p.split_cells, n_sel - base);
   const int n_sub = (n_cells + kSub - 1) / kSub;
@@ -457,70 +444,21 @@ __global__ void __launch_bounds__(kAttnThreads, 5) win_attn_kernel(const WinAttn
     __syncthreads();   // the stage and p_s are rewritten by the sub-tile after next
   }
 
-  // ---- this split's partial: heads 2tq, 2tq+1 < G, dims 32w + 4g ..
-  const size_t sbase = ((size_t)pair * p.n_splits + split) * G;
+  // ---- this split's partial (qsa_decode_attn layout, split = chunk): heads 2tq, 2tq+1 < G,
+  // dims 32w + 4g ..
+  const size_t cbase = ((size_t)t * p.n_q_heads + h * G) * p.n_splits + split;
   if (2 * tq < G) {
-    *reinterpret_cast<float4*>(p.part_o + (sbase + 2 * tq) * kD + 32 * warp + 4 * g) =
+    const size_t ci = cbase + (size_t)(2 * tq) * p.n_splits;
+    *reinterpret_cast<float4*>(p.part_o + ci * kD + 32 * warp + 4 * g) =
         make_float4(o_acc[0][0], o_acc[0][2], o_acc[1][0], o_acc[1][2]);
-    if (warp == 0 && g == 0)
-      *reinterpret_cast<float2*>(p.part_ml + (sbase + 2 * tq) * 2) = make_float2(m_run[0], l_run[0]);
+    if (warp == 0 && g == 0) *reinterpret_cast<float2*>(p.part_ml + ci * 2) = make_float2(m_run[0], l_run[0]);
   }
   if (2 * tq + 1 < G) {
-    *reinterpret_cast<float4*>(p.part_o + (sbase + 2 * tq + 1) * kD + 32 * warp + 4 * g) =
+    const size_t ci = cbase + (size_t)(2 * tq + 1) * p.n_splits;
+    *reinterpret_cast<float4*>(p.part_o + ci * kD + 32 * warp + 4 * g) =
         make_float4(o_acc[0][1], o_acc[0][3], o_acc[1][1], o_acc[1][3]);
-    if (warp == 0 && g == 0)
-      *reinterpret_cast<float2*>(p.part_ml + (sbase + 2 * tq + 1) * 2) = make_float2(m_run[1], l_run[1]);
+    if (warp == 0 && g == 0) *reinterpret_cast<float2*>(p.part_ml + ci * 2) = make_float2(m_run[1], l_run[1]);
   }
-
-  // ---- ticket: the CTA that completes the (row, KV head)'s last split merges all of them.
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last = (atomicAdd(p.tickets + pair, 1u) == (unsigned)(n_act - 1));
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-
-  // Weights exp(m_j - M) of every split and head, staged in the (now unused) stage memory.
-  float* mw = reinterpret_cast<float*>(&stages[0]);        // [n_act][G]: m, then the weight
-  float* lw = mw + kMaxSplits * 8;                          // [n_act][G]: l
-  float* ML = lw + kMaxSplits * 8;                          // [G][2]: M, L
-  const size_t pbase = (size_t)pair * p.n_splits * G;
-  for (int i = tid; i < n_act * G; i += kAttnThreads) {
-    const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + pbase + i);
-    mw[i] = ml.x;
-    lw[i] = ml.y;
-  }
-  __syncthreads();
-  if (tid < G) {
-    float M = -INFINITY;
-    for (int j = 0; j < n_act; ++j) M = fmaxf(M, mw[j * G + tid]);
-    float L = 0.f;
-    for (int j = 0; j < n_act; ++j) {
-      const float mj = mw[j * G + tid];
-      const float w = (mj == -INFINITY) ? 0.f : expf(mj - M);
-      mw[j * G + tid] = w;
-      L = fmaf(lw[j * G + tid], w, L);
-    }
-    ML[2 * tid] = M;
-    ML[2 * tid + 1] = L;
-  }
-  __syncthreads();
-  for (int gg = 0; gg < G; ++gg) {
-    const float M = ML[2 * gg], L = ML[2 * gg + 1];
-    float* orow = p.out + ((size_t)t * p.n_q_heads + h * G + gg) * kD;
-    if (M == -INFINITY) {   // every visible cell of the selection masked: empty
-      orow[tid] = 0.f;
-      if (p.lse && tid == 0) p.lse[(size_t)t * p.n_q_heads + h * G + gg] = -INFINITY;
-      continue;
-    }
-    const float* po = p.part_o + (pbase + gg) * kD + tid;
-    float acc = 0.f;
-#pragma unroll 8
-    for (int j = 0; j < n_act; ++j) acc = fmaf(__ldcg(po + (size_t)j * G * kD), mw[j * G + gg], acc);
-    orow[tid] = acc / L;
-    if (p.lse && tid == 0) p.lse[(size_t)t * p.n_q_heads + h * G + gg] = M + logf(L);
-  }
-  if (tid == 0) p.tickets[pair] = 0u;
 }
 
 }  // namespace
@@ -543,8 +481,6 @@ int window_split_cells(int n_rows, int n_kv_heads, int k_cells, int n_sm) {
 WindowLayout window_layout(int n_rows, int n_q_heads, int n_kv_heads, int k_cells, int n_sm) {
   WindowLayout L{};
   const int NT = (n_rows + 7) / 8;
-  const int G = n_q_heads / n_kv_heads;
-  const int n_pairs = n_rows * n_kv_heads;
   L.split_cells = window_split_cells(n_rows, n_kv_heads, k_cells, n_sm);
   L.n_splits = (k_cells + L.split_cells - 1) / L.split_cells;
   if (L.n_splits < 1) L.n_splits = 1;
@@ -554,12 +490,10 @@ WindowLayout window_layout(int n_rows, int n_q_heads, int n_kv_heads, int k_cell
   off = up(off + (size_t)16 * n_kv_heads * NT * 8 * 32);
   L.inv_f = off;
   off = up(off + sizeof(float) * (size_t)n_rows * n_kv_heads);
-  L.tickets = off;
-  off = up(off + sizeof(unsigned) * (size_t)n_pairs);
-  L.part_ml = off;
-  off = up(off + sizeof(float) * 2 * (size_t)n_pairs * L.n_splits * G);
+  L.part_ml = off;   // the qsa_decode_attn partials layout: ml, then o, back to back
+  off += sizeof(float) * 2 * (size_t)n_rows * n_q_heads * L.n_splits;
   L.part_o = off;
-  off = up(off + sizeof(float) * kD * (size_t)n_pairs * L.n_splits * G);
+  off = up(off + sizeof(float) * kD * (size_t)n_rows * n_q_heads * L.n_splits);
   L.total = off;
   return L;
 }
@@ -591,17 +525,16 @@ cudaError_t launch_decode_window(const WindowArgs& a, cudaStream_t stream) {
   uint4* frag = reinterpret_cast<uint4*>(ws + a.layout.frag);
   float* inv_f = reinterpret_cast<float*>(ws + a.layout.inv_f);
   WinAttnParams ap = a.attn;
-  ap.tickets = reinterpret_cast<unsigned*>(ws + a.layout.tickets);
   ap.part_ml = reinterpret_cast<float*>(ws + a.layout.part_ml);
   ap.part_o = reinterpret_cast<float*>(ws + a.layout.part_o);
   ap.split_cells = a.layout.split_cells;
   ap.n_splits = a.layout.n_splits;
   const int n_pairs = R * Hkv;
 
-  // 1. q fragments + ticket reset: an ordinary launch, ordered after everything before it on the
-  //    stream (the previous window's merge may still hold the tickets).
+  // 1. q fragments: an ordinary launch, ordered after everything before it on the stream (the
+  //    previous window may still read the workspace).
   cudaError_t e = launch_ex(win_qprep_kernel, dim3(NT * 8, Hkv), dim3(32), 0, stream, false, sp.q, R, sp.n_q_heads,
-                            Hkv, NT, frag, inv_f, ap.tickets, n_pairs);
+                            Hkv, NT, frag, inv_f);
   if (e != cudaSuccess) return e;
   // 2. block scores
   if (sp.total_units > 0) {
@@ -619,8 +552,21 @@ cudaError_t launch_decode_window(const WindowArgs& a, cudaStream_t stream) {
   // 3. top-k
   e = launch_topk_ex(a.topk, a.max_nb, stream, true);
   if (e != cudaSuccess) return e;
-  // 4. attention + merge
-  return launch_ex(win_attn_kernel, dim3(n_pairs * ap.n_splits), dim3(kAttnThreads), 0, stream, true, ap);
+  // 4. split attention
+  e = launch_ex(win_attn_kernel, dim3(n_pairs * ap.n_splits), dim3(kAttnThreads), 0, stream, true, ap);
+  if (e != cudaSuccess) return e;
+  // 5. merge of the splits
+  MergeParams mp{};
+  mp.ml = ap.part_ml;
+  mp.o = ap.part_o;
+  mp.n_sel = ap.n_sel;
+  mp.n_rows = R;
+  mp.n_q_heads = sp.n_q_heads;
+  mp.chunk_cells = ap.split_cells;
+  mp.n_chunks = ap.n_splits;
+  mp.out = ap.out;
+  mp.lse = ap.lse;
+  return launch_attn_merge_ex(mp, stream, true);
 }
 
 }  // namespace qsa

@@ -69,17 +69,16 @@ struct WinAttnParams {
   const int32_t* n_sel;
   int n_rows, n_q_heads, n_kv_heads, k_cells;
   int split_cells;   // cells of one split (multiple of 64)
-  int n_splits;      // splits per (row, KV head) in the workspace
-  float* part_ml;    // [n_rows * n_kv_heads][n_splits][G][2]
-  float* part_o;     // [n_rows * n_kv_heads][n_splits][G][128]
-  unsigned* tickets; // [n_rows * n_kv_heads]
+  int n_splits;      // splits per (row, q head) in the workspace
+  float* part_ml;    // [n_rows][n_q_heads][n_splits][2]
+  float* part_o;     // [n_rows][n_q_heads][n_splits][128]
   float* out;        // [n_rows][n_q_heads][128]
   float* lse;        // [n_rows][n_q_heads] or nullptr
 };
 
 // Byte offsets of the parts of a decode-window workspace.
 struct WindowLayout {
-  size_t frag, inv_f, tickets, part_ml, part_o, total;
+  size_t frag, inv_f, part_ml, part_o, total;
   int split_cells, n_splits;
 };
 
@@ -107,6 +106,7 @@ cudaError_t launch_block_scores(const ScoresParams& p, cudaStream_t stream);
 cudaError_t launch_topk(const TopkParams& p, int max_nb, cudaStream_t stream);
 cudaError_t launch_decode_attn(const AttnParams& p, cudaStream_t stream);
 cudaError_t launch_attn_merge(const MergeParams& p, cudaStream_t stream);
+cudaError_t launch_attn_merge_ex(const MergeParams& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_prompt_attn(const PromptParams& p, cudaStream_t stream);
 cudaError_t read_and_clear_device_error(int32_t* code, cudaStream_t stream);
 // Device address of the library's error word on the current device (for kernels of other

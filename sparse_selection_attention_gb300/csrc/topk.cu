@@ -61,17 +61,16 @@ __device__ __forceinline__ int cta_exclusive_scan(int v, int* warp_tot, int& tot
 
 // Adds, for every key of this thread whose bits under `mask` equal `prefix`, one count to the
 // bin of its digit (key >> shift) & 255; lanes with the same digit add once, together.
-__device__ __forceinline__ void add_digits(const uint32_t (&key)[kMaxKeys], int K, int b0, int nb, uint32_t mask,
-                                           uint32_t prefix, int shift, unsigned* hist) {
+template <int KK>
+__device__ __forceinline__ void add_digits(const uint32_t (&key)[KK], int b0, int nb, uint32_t mask, uint32_t prefix,
+                                           int shift, unsigned* hist) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
-  for (int i = 0; i < kMaxKeys; ++i) {
-    if (i < K) {   // uniform across the CTA
-      const bool live = b0 + i < nb && (key[i] & mask) == prefix;
-      const uint32_t digit = (key[i] >> shift) & 255u;
-      const unsigned peers = __match_any_sync(0xffffffffu, live ? digit : 256u + lane);
-      if (live && lane == __ffs(peers) - 1) atomicAdd(hist + digit, (unsigned)__popc(peers));
-    }
+  for (int i = 0; i < KK; ++i) {
+    const bool live = b0 + i < nb && (key[i] & mask) == prefix;
+    const uint32_t digit = (key[i] >> shift) & 255u;
+    const unsigned peers = __match_any_sync(0xffffffffu, live ? digit : 256u + lane);
+    if (live && lane == __ffs(peers) - 1) atomicAdd(hist + digit, (unsigned)__popc(peers));
   }
 }
 
@@ -108,6 +107,8 @@ __device__ __forceinline__ void pick_digit(const unsigned* hist, int need, int* 
   }
 }
 
+// KK keys per thread: thread i holds blocks [i KK, (i + 1) KK).
+template <int KK>
 __global__ void __launch_bounds__(kMaxThreads) topk_kernel(const TopkParams p) {
   extern __shared__ int smem[];          // chosen list [kb]
   __shared__ int warp_tot[32];
@@ -119,7 +120,6 @@ __global__ void __launch_bounds__(kMaxThreads) topk_kernel(const TopkParams p) {
   // launch may start its CTAs now (they wait for this grid before reading ids).
   ms::pdl_trigger();
   ms::pdl_wait();
-  const int n_threads = blockDim.x;
   const int B = p.block_cells;
   const int n_filled = p.n_filled[t];
   const int nb = (n_filled + B - 1) / B;
@@ -130,12 +130,11 @@ __global__ void __launch_bounds__(kMaxThreads) topk_kernel(const TopkParams p) {
     return;
   }
   int* sel = smem;
-  const int K = (nb + n_threads - 1) / n_threads;   // <= kMaxKeys
-  const int b0 = tid * K;
+  const int b0 = tid * KK;
   const float* sc = p.scores + (size_t)t * p.max_blocks;
-  uint32_t key[kMaxKeys];
+  uint32_t key[KK];
 #pragma unroll
-  for (int i = 0; i < kMaxKeys; ++i) key[i] = (i < K && b0 + i < nb) ? score_key(__ldg(sc + b0 + i)) : 0u;
+  for (int i = 0; i < KK; ++i) key[i] = (b0 + i < nb) ? score_key(__ldg(sc + b0 + i)) : 0u;
   __syncthreads();   // histograms zeroed
 
   const bool take_all = (kb == nb);
@@ -146,7 +145,7 @@ __global__ void __launch_bounds__(kMaxThreads) topk_kernel(const TopkParams p) {
     uint32_t mask = 0;
     for (int pass = 0; pass < 4; ++pass) {
       const int shift = 24 - 8 * pass;
-      add_digits(key, K, b0, nb, mask, T, shift, hist[pass]);
+      add_digits<KK>(key, b0, nb, mask, T, shift, hist[pass]);
       __syncthreads();
       if (tid < 32) pick_digit(hist[pass], need, s_pick);
       __syncthreads();
@@ -162,14 +161,14 @@ __global__ void __launch_bounds__(kMaxThreads) topk_kernel(const TopkParams p) {
   int eq = 0;
   if (!take_all) {
 #pragma unroll
-    for (int i = 0; i < kMaxKeys; ++i) eq += (i < K && b0 + i < nb && key[i] == T);
+    for (int i = 0; i < KK; ++i) eq += (b0 + i < nb && key[i] == T);
   }
   int e = take_all ? 0 : cta_exclusive_scan(eq, warp_tot, tot);
   int chosen = 0;
   uint32_t chosen_bits = 0;
 #pragma unroll
-  for (int i = 0; i < kMaxKeys; ++i) {
-    if (i < K && b0 + i < nb) {
+  for (int i = 0; i < KK; ++i) {
+    if (b0 + i < nb) {
       bool c = take_all || key[i] > T;
       if (!take_all && key[i] == T) { c = e < need; ++e; }
       if (c) { ++chosen; chosen_bits |= 1u << i; }
@@ -177,13 +176,13 @@ __global__ void __launch_bounds__(kMaxThreads) topk_kernel(const TopkParams p) {
   }
   int j = cta_exclusive_scan(chosen, warp_tot, tot);
 #pragma unroll
-  for (int i = 0; i < kMaxKeys; ++i)
+  for (int i = 0; i < KK; ++i)
     if (chosen_bits & (1u << i)) sel[j++] = b0 + i;
   __syncthreads();
   // ids[j*B + i] = sel[j]*B + i, four at a time when the row's ids start 16-byte aligned (ids aligned,
   // k_cells and B multiples of 4); cells past n_filled (the row's last block) are not written.
   if ((B & 3) == 0 && (p.k_cells & 3) == 0 && (reinterpret_cast<uintptr_t>(p.ids) & 15) == 0) {
-    for (int i4 = tid; i4 < kb * B / 4; i4 += n_threads) {
+    for (int i4 = tid; i4 < kb * B / 4; i4 += blockDim.x) {
       const int idx = 4 * i4;
       const int cell = sel[idx / B] * B + idx % B;
       if (cell + 3 < n_filled) {
@@ -195,7 +194,7 @@ __global__ void __launch_bounds__(kMaxThreads) topk_kernel(const TopkParams p) {
       }
     }
   } else {
-    for (int idx = tid; idx < kb * B; idx += n_threads) {
+    for (int idx = tid; idx < kb * B; idx += blockDim.x) {
       const int cell = sel[idx / B] * B + idx % B;
       if (cell < n_filled) ids[idx] = cell;
     }
@@ -220,9 +219,13 @@ size_t topk_smem_bytes(int max_nb) { return sizeof(int) * (size_t)max_nb; }
 
 cudaError_t launch_topk_ex(const TopkParams& p, int max_nb, cudaStream_t stream, bool pdl) {
   const int th = topk_threads(max_nb);
-  if ((max_nb + th - 1) / th > kMaxKeys) return cudaErrorInvalidValue;
+  const int need = (max_nb + th - 1) / th;
+  if (need > kMaxKeys) return cudaErrorInvalidValue;
+  const int kk = need <= 1 ? 1 : need <= 2 ? 2 : need <= 4 ? 4 : need <= 8 ? 8 : 16;
   const size_t smem = topk_smem_bytes(max_nb);
-  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(topk_kernel), smem);
+  void (*kern)(TopkParams) = kk == 1 ? topk_kernel<1> : kk == 2 ? topk_kernel<2> : kk == 4 ? topk_kernel<4>
+                                : kk == 8 ? topk_kernel<8> : topk_kernel<16>;
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.n_rows);
@@ -234,7 +237,7 @@ cudaError_t launch_topk_ex(const TopkParams& p, int max_nb, cudaStream_t stream,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, topk_kernel, p);
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 cudaError_t launch_topk(const TopkParams& p, int max_nb, cudaStream_t stream) {

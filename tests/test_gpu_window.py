@@ -95,7 +95,7 @@ def test_window_empty_selection():
 
 
 def test_window_deterministic_and_reusable_workspace():
-    """Three calls on one workspace give the same bits (the tickets are cleared by every call), and the
+    """Three calls on one workspace give the same bits, and the
     result matches the four separate calls within the gate."""
     case = W.verify_window()
     win, q, row_pos = upload_case(case)
