@@ -12,11 +12,12 @@
 //     scaled by a power of two and split into fp16 hi + lo, laid out as the
 //     block-score kernel's mma B fragments (computed once per window instead
 //     of once per CTA).
-//  2. win_scores_kernel: one CTA per (pool, block), one warp per (KV head,
-//     16-cell m-tile); each lane's K codes and scales are loaded into
-//     registers before the kernel waits for step 1.  S^T = Kcode . qbar on
-//     mma.sync; cell weights by K scale, fixed butterflies over cells, then
-//     over heads and m-tiles.  The result is the qsa_block_scores definition.
+//  2. win_scores_kernel: one CTA per (pool, block); all of the block's K
+//     codes and scales are copied into shared memory (cp.async) before the
+//     kernel waits for step 1; one warp task per (KV head, 16-cell m-tile).  S^T = Kcode .
+//     qbar on mma.sync; cell weights by K scale, fixed butterflies over cells,
+//     then over heads and m-tiles.  The result is the qsa_block_scores
+//     definition.
 //  3. topk_kernel (topk.cu), unchanged arithmetic.
 //  4. win_attn_kernel: one CTA per (row, KV head, split of the selection);
 //     each split's partial (m, l, o) per q head goes to the workspace in the
@@ -81,12 +82,23 @@ __global__ void __launch_bounds__(32) win_qprep_kernel(const float* __restrict__
 }
 
 // ------------------------------------------------------------------------------------------ 2
+// One 256-thread CTA per unit (pool, block).  Thread i copies 64 bytes of one cell's K codes (and
+// half 0 its two K scales) into shared memory with cp.async before the kernel waits for step 1, so
+// every read of the CTA is in flight at once and no register is held across the wait; warp tasks
+// (KV head, 16-cell m-tile) then take their operands from shared memory.
+constexpr int kScoreThreads = 256;
+
 template <int NT>
-__global__ void __launch_bounds__(1024) win_scores_kernel(const ScoresParams p, const uint4* __restrict__ frag,
-                                                          const float* __restrict__ inv_f) {
-  extern __shared__ float part[];   // [tasks][NT * 8]
+__global__ void __launch_bounds__(kScoreThreads, 4) win_scores_kernel(const ScoresParams p,
+                                                                       const uint4* __restrict__ frag,
+                                                                       const float* __restrict__ inv_f) {
+  extern __shared__ __align__(16) uint8_t sm[];
   const int B = p.block_cells, Hkv = p.n_kv_heads, R = p.n_rows;
-  const int mts = B / 16, tpu = Hkv * mts;
+  const int lgB = 31 - __clz(B);   // B is a power of two
+  const int mts = B >> 4, tpu = Hkv * mts;
+  uint8_t* codes = sm;                                                    // [Hkv][B][128]
+  float* kscale = reinterpret_cast<float*>(sm + (size_t)Hkv * B * kD);    // [Hkv][B][2]
+  float* part = kscale + (size_t)Hkv * B * 2;                             // [tpu][NT * 8]
   const int unit = blockIdx.x;
   const int pi = pool_index(p.unit_begin, p.n_pools, unit);
   const PoolDev& pool = p.pools[pi];
@@ -95,79 +107,90 @@ __global__ void __launch_bounds__(1024) win_scores_kernel(const ScoresParams p, 
   const int n_b = min(B, pool.n_filled - cell0);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, tq = lane & 3;
-  const int h = warp / mts, mt = warp % mts;
-
-  // ---- this lane's codes (cells 16 mt + g and + 8, dims 16 tq .. and 64 + 16 tq ..) and scales
-  uint4 c[2][2];
-  float2 ks[2];
   {
     const int page = __ldg(pool.page_table + cell0 / pool.page_cells);
-    const long long slot0 = ((long long)page * Hkv + h) * pool.page_cells + cell0 % pool.page_cells;
+    const long long slot00 = (long long)page * Hkv * pool.page_cells + cell0 % pool.page_cells;
+    for (int item = tid; item < 2 * Hkv * B; item += kScoreThreads) {
+      const int half = item & 1, hc = item >> 1, h = hc >> lgB, c = hc & (B - 1);
+      if (c < n_b) {
+        const long long slot = slot00 + (long long)h * pool.page_cells + c;
+        const int8_t* src = pool.k_codes + slot * kD + 64 * half;
+        uint8_t* dst = codes + (size_t)hc * kD + 64 * half;
 #pragma unroll
-    for (int ab = 0; ab < 2; ++ab) {
-      const int cc = 16 * mt + g + 8 * ab;
-      if (cc < n_b) {
-        const uint4* src = reinterpret_cast<const uint4*>(pool.k_codes + (slot0 + cc) * kD);
-        c[ab][0] = __ldg(src + tq);
-        c[ab][1] = __ldg(src + 4 + tq);
-        ks[ab] = __ldg(reinterpret_cast<const float2*>(pool.k_scales) + slot0 + cc);
-      } else {
-        c[ab][0] = c[ab][1] = make_uint4(0u, 0u, 0u, 0u);
-        ks[ab] = make_float2(0.f, 0.f);
+        for (int k = 0; k < 4; ++k) cp_async16(dst + 16 * k, src + 16 * k);
+        if (!half) cp_async8(kscale + 2 * hc, pool.k_scales + slot * 2);
+      } else if (!half) {
+        kscale[2 * hc] = 0.f;   // cells past the fill weigh nothing
+        kscale[2 * hc + 1] = 0.f;
       }
     }
+    cp_async_commit();
   }
   pdl_trigger();
   pdl_wait();   // q fragments of the preceding launch
+  cp_async_wait_all();
+  __syncthreads();
 
-  float d[NT][2][4];   // [n-tile][K-scale group]: hi and lo parts of qbar accumulate together
+  for (int task = warp; task < tpu; task += kScoreThreads / 32) {
+    const int h = task / mts, mt = task % mts;
+    const int row0 = h * B + 16 * mt + g;   // (head, cell) row of the lane's first cell
+    uint4 c[2][2];
+    float2 ks[2];
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
+    for (int ab = 0; ab < 2; ++ab) {
+      const uint8_t* src = codes + (size_t)(row0 + 8 * ab) * kD;
+      c[ab][0] = *reinterpret_cast<const uint4*>(src + 16 * tq);
+      c[ab][1] = *reinterpret_cast<const uint4*>(src + 64 + 16 * tq);
+      ks[ab] = *reinterpret_cast<const float2*>(kscale + 2 * (row0 + 8 * ab));
+    }
+    float d[NT][2][4];   // [n-tile][K-scale group]: hi and lo parts of qbar accumulate together
 #pragma unroll
-    for (int gr = 0; gr < 2; ++gr)
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) d[nt][gr][i] = 0.f;
-  const uint4* fr = frag + (size_t)h * NT * 8 * 32 + lane;
+      for (int gr = 0; gr < 2; ++gr)
 #pragma unroll
-  for (int s = 0; s < 8; ++s) {
-    const int gr = s >> 2, w = s & 3;
-    const uint32_t wa = word_of(c[0][gr], w) ^ 0x80808080u;
-    const uint32_t wb = word_of(c[1][gr], w) ^ 0x80808080u;
-    uint32_t a[4];
-    a[0] = byte_pair_h2(wa, 0x4140, kBiasS8);
-    a[2] = byte_pair_h2(wa, 0x4342, kBiasS8);
-    a[1] = byte_pair_h2(wb, 0x4140, kBiasS8);
-    a[3] = byte_pair_h2(wb, 0x4342, kBiasS8);
+        for (int i = 0; i < 4; ++i) d[nt][gr][i] = 0.f;
+    const uint4* fr = frag + (size_t)h * NT * 8 * 32 + lane;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      const int gr = s >> 2, w = s & 3;
+      const uint32_t wa = word_of(c[0][gr], w) ^ 0x80808080u;
+      const uint32_t wb = word_of(c[1][gr], w) ^ 0x80808080u;
+      uint32_t a[4];
+      a[0] = byte_pair_h2(wa, 0x4140, kBiasS8);
+      a[2] = byte_pair_h2(wa, 0x4342, kBiasS8);
+      a[1] = byte_pair_h2(wb, 0x4140, kBiasS8);
+      a[3] = byte_pair_h2(wb, 0x4342, kBiasS8);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const uint4 bf = __ldg(fr + (nt * 8 + s) * 32);
+        mma16816(d[nt][gr], a, bf.x, bf.y);
+        mma16816(d[nt][gr], a, bf.z, bf.w);
+      }
+    }
+    // cell weights by K scale, the lane's two cells summed, then a butterfly over the 8 cell pairs
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const uint4 bf = __ldg(fr + (nt * 8 + s) * 32);
-      mma16816(d[nt][gr], a, bf.x, bf.y);
-      mma16816(d[nt][gr], a, bf.z, bf.w);
-    }
-  }
-  // cell weights by K scale, the two cells of the lane summed, then a butterfly over the 8 cell pairs
+      const float(&x)[2][4] = d[nt];
+      float e0 = fmaf(ks[0].y, x[1][0], ks[0].x * x[0][0]);
+      e0 += fmaf(ks[1].y, x[1][2], ks[1].x * x[0][2]);
+      float e1 = fmaf(ks[0].y, x[1][1], ks[0].x * x[0][1]);
+      e1 += fmaf(ks[1].y, x[1][3], ks[1].x * x[0][3]);
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const float(&x)[2][4] = d[nt];
-    float e0 = fmaf(ks[0].y, x[1][0], ks[0].x * x[0][0]);
-    e0 += fmaf(ks[1].y, x[1][2], ks[1].x * x[0][2]);
-    float e1 = fmaf(ks[0].y, x[1][1], ks[0].x * x[0][1]);
-    e1 += fmaf(ks[1].y, x[1][3], ks[1].x * x[0][3]);
-#pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      e0 += __shfl_xor_sync(0xffffffffu, e0, o);
-      e1 += __shfl_xor_sync(0xffffffffu, e1, o);
-    }
-    if (g == 0) {
-      const int row = nt * 8 + 2 * tq;
-      part[warp * NT * 8 + row] = row < R ? e0 * __ldg(inv_f + row * Hkv + h) : 0.f;
-      part[warp * NT * 8 + row + 1] = row + 1 < R ? e1 * __ldg(inv_f + (row + 1) * Hkv + h) : 0.f;
+      for (int o = 4; o < 32; o <<= 1) {
+        e0 += __shfl_xor_sync(0xffffffffu, e0, o);
+        e1 += __shfl_xor_sync(0xffffffffu, e1, o);
+      }
+      if (g == 0) {
+        const int row = nt * 8 + 2 * tq;
+        part[task * NT * 8 + row] = row < R ? e0 * __ldg(inv_f + row * Hkv + h) : 0.f;
+        part[task * NT * 8 + row + 1] = row + 1 < R ? e1 * __ldg(inv_f + (row + 1) * Hkv + h) : 0.f;
+      }
     }
   }
   __syncthreads();
   // S[t, b] for the rows of this pool: lane l holds task l (head-major), then a fixed butterfly.
-  const int n_warps = blockDim.x >> 5;
-  for (int t = warp; t < R; t += n_warps) {
+  for (int t = warp; t < R; t += kScoreThreads / 32) {
     if (p.row_pool[t] != pi) continue;
     float sum = lane < tpu ? part[lane * NT * 8 + t] : 0.f;
     sum = warp_sum(sum);
@@ -539,14 +562,14 @@ cudaError_t launch_decode_window(const WindowArgs& a, cudaStream_t stream) {
   // 2. block scores
   if (sp.total_units > 0) {
     const int tpu = Hkv * (sp.block_cells / 16);
-    const size_t smem = sizeof(float) * (size_t)tpu * NT * 8;
-    const dim3 grid(sp.total_units), block(32 * tpu);
-    switch (NT) {
-      case 1: e = launch_ex(win_scores_kernel<1>, grid, block, smem, stream, true, sp, (const uint4*)frag, (const float*)inv_f); break;
-      case 2: e = launch_ex(win_scores_kernel<2>, grid, block, smem, stream, true, sp, (const uint4*)frag, (const float*)inv_f); break;
-      case 3: e = launch_ex(win_scores_kernel<3>, grid, block, smem, stream, true, sp, (const uint4*)frag, (const float*)inv_f); break;
-      default: e = launch_ex(win_scores_kernel<4>, grid, block, smem, stream, true, sp, (const uint4*)frag, (const float*)inv_f); break;
-    }
+    const size_t smem = (size_t)Hkv * sp.block_cells * (kD + 8) + sizeof(float) * (size_t)tpu * NT * 8;
+    void (*kern)(ScoresParams, const uint4*, const float*) =
+        NT == 1 ? win_scores_kernel<1> : NT == 2 ? win_scores_kernel<2> : NT == 3 ? win_scores_kernel<3>
+                                                                         : win_scores_kernel<4>;
+    e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
+    if (e != cudaSuccess) return e;
+    e = launch_ex(kern, dim3(sp.total_units), dim3(kScoreThreads), smem, stream, true, sp, (const uint4*)frag,
+                  (const float*)inv_f);
     if (e != cudaSuccess) return e;
   }
   // 3. top-k
