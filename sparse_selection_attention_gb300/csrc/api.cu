@@ -61,6 +61,7 @@ PoolDev to_dev(const qsa_pool& p) {
   d.page_table = p.page_table;
   d.n_filled = p.n_filled;
   d.page_cells = p.page_cells;
+  d.page_shift = (p.page_cells & (p.page_cells - 1)) == 0 ? __builtin_ctz((unsigned)p.page_cells) : -1;
   d.v_bits = p.v_bits;
   return d;
 }

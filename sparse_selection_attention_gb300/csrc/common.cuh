@@ -21,13 +21,21 @@ struct PoolDev {
   const int32_t* page_table;
   int n_filled;
   int page_cells;
+  int page_shift;   // log2(page_cells) when page_cells is a power of two, else -1
   int v_bits;
 };
 
 // Linear (page, head, cell) slot of logical cell c of KV head h.
 __device__ __forceinline__ long long cell_slot(const PoolDev& p, int n_kv_heads, int h, int c) {
-  const int page = __ldg(p.page_table + c / p.page_cells);
-  const int off = c - (c / p.page_cells) * p.page_cells;
+  int pg, off;
+  if (p.page_shift >= 0) {
+    pg = c >> p.page_shift;
+    off = c & (p.page_cells - 1);
+  } else {
+    pg = c / p.page_cells;
+    off = c - pg * p.page_cells;
+  }
+  const int page = __ldg(p.page_table + pg);
   return ((long long)page * n_kv_heads + h) * p.page_cells + off;
 }
 

@@ -484,20 +484,378 @@ __global__ void __launch_bounds__(kAttnThreads, 5) win_attn_kernel(const WinAttn
   }
 }
 
+// ------------------------------------------------------------------------------------------ 4'
+// int8 V: the four warps of a CTA own their cells.  Warp w walks the 16-cell slices w, w + 4, ...
+// of the split through its own two-stage cp.async ring and keeps its own online softmax (base-2
+// logits) and O^T accumulators, so no CTA barrier sits in the loop; the W = p * vscale operand is
+// formed once per (cell, head, V group).  The warps' states are combined in warp order at the end
+// of the split.
+//   QK^T: A = K codes of the slice (16 cells x 16 dims per k-step, converted exactly to fp16),
+//         B = q of the 8 heads scaled by 2^fe and split into fp16 hi + lo; one accumulator per
+//         64-dim K-scale group.
+//   PV:   A = V^T (16 dims x 16 cells), B = W of the slice in fp16 hi + lo per 64-dim V-scale
+//         group, accumulated in O^T (dims x heads).  m-tile mt holds the dims 64 (mt / 4) + 8 r +
+//         2 (mt % 4) (row r) and + 1 (row r + 8), so every m-tile lies in one V-scale group.
+//   W is scaled by 2^kv[group] (max |vscale| 2^kv in [8, 16) over the slices seen so far; kv only
+//   decreases, and O's rows of that group are rescaled when it does).
+constexpr int kSlice = 16;
+
+struct WarpStage {
+  int8_t k[kSlice * kD];
+  int8_t v[kSlice * kD];
+  float ks[kSlice * 2];
+  float vs[kSlice * 2];
+};
+
+// Copies slice entries [first, first + 16) of the split into `sg` (lane: cell lane / 2, half
+// lane % 2); returns the warp's ballot of visible cells (bit 2c + half for cell c).
+__device__ __forceinline__ uint32_t prefetch_slice(const WinAttnParams& p, const PoolDev& pool, WarpStage& sg,
+                                                   const int32_t* row_ids, int first, int n_cells, int h, int pos) {
+  const int lane = threadIdx.x & 31, c = lane >> 1, half = lane & 1;
+  const int idx = first + c;
+  bool valid = false;
+  long long slot = 0;
+  if (idx < n_cells) {
+    const int cell = __ldg(row_ids + idx);
+    valid = cell <= pos && cell >= 0 && cell < pool.n_filled;
+    if (valid) slot = cell_slot(pool, p.n_kv_heads, h, cell);
+  }
+  if (valid) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int pc = 4 * half + k;
+      cp_async16(sg.k + c * kD + pc * 16, pool.k_codes + slot * kD + pc * 16);
+      cp_async16(sg.v + c * kD + pc * 16, pool.v_codes + slot * kD + pc * 16);
+    }
+    if (!half)
+      cp_async8(sg.ks + 2 * c, pool.k_scales + slot * 2);
+    else
+      cp_async8(sg.vs + 2 * c, pool.v_scales + slot * 2);
+  }
+  cp_async_commit();
+  return __ballot_sync(0xffffffffu, valid);
+}
+
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+__global__ void __launch_bounds__(kAttnThreads, 4) win_attn8_kernel(const WinAttnParams p) {
+  const int R = p.n_rows, Hkv = p.n_kv_heads;
+  const int n_pairs = R * Hkv;
+  const int pair = blockIdx.x % n_pairs, split = blockIdx.x / n_pairs;
+  const int t = pair % R, h = pair / R;
+  const int G = p.n_q_heads / Hkv;
+  const int pos = __ldg(p.row_pos + t);
+  const PoolDev& pool = p.pools[p.row_pool[t]];
+
+  __shared__ __align__(16) WarpStage ring[4][2];
+  __shared__ __align__(16) float pbuf[4][8][kSlice];
+  __shared__ float wm[4][8], wl[4][8];
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, tq = lane & 3;
+
+  // ---- q of head g: for k-step s = 4 gr + w the dims 64 gr + 16 tq + 4 w .. + 3, scaled by 2^fe
+  // (max |q 2^fe| in [64, 128)) and split into fp16 hi + lo.  q is an input of the window, so
+  // this runs before the wait for the selection.
+  uint32_t qh[8][2], ql[8][2];
+  float lam0, lam1;   // base-2 logit scale of heads 2tq and 2tq+1
+  {
+    float qv[8][4];
+    float amax = 0.f;
+    const float* qrow = p.q + ((size_t)t * p.n_q_heads + h * G + min(g, G - 1)) * kD + 16 * tq;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (g < G) v = __ldg(reinterpret_cast<const float4*>(qrow + 64 * (s >> 2) + 4 * (s & 3)));
+      qv[s][0] = v.x; qv[s][1] = v.y; qv[s][2] = v.z; qv[s][3] = v.w;
+      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const int fe = scale_exp_128(amax);
+    const float f = pow2i(fe);
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      split_pair(qv[s][0] * f, qv[s][1] * f, qh[s][0], ql[s][0]);
+      split_pair(qv[s][2] * f, qv[s][3] * f, qh[s][1], ql[s][1]);
+    }
+    const float lam = kInvSqrtD * kLog2e * pow2i(-fe);
+    lam0 = __shfl_sync(0xffffffffu, lam, 4 * (2 * tq));
+    lam1 = __shfl_sync(0xffffffffu, lam, 4 * (2 * tq + 1));
+  }
+
+  pdl_wait();   // ids and n_sel of the preceding launch
+  const int n_sel = min(__ldg(p.n_sel + t), p.k_cells);
+  const int n_act = (n_sel + p.split_cells - 1) / p.split_cells;
+  if (split >= n_act) return;   // past the selection: nothing to read, nothing the merge reads
+  const int base = split * p.split_cells;
+  const int n_cells = min(p.split_cells, n_sel - base);
+  const int n_slices = (n_cells + kSlice - 1) / kSlice;
+  const int my_n = n_slices > warp ? (n_slices - warp + 3) / 4 : 0;
+  const int32_t* row_ids = p.ids + (size_t)t * p.k_cells + base;
+  WarpStage* rg = ring[warp];
+  float(*pb)[kSlice] = pbuf[warp];
+
+  float m2[2] = {-INFINITY, -INFINITY};   // running max (base 2) of heads 2tq, 2tq+1
+  float lp[2] = {0.f, 0.f};               // this lane's share of the running sums
+  float O[8][4];
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) O[mt][i] = 0.f;
+  int kv[2] = {0, 0};
+  bool have_kv[2] = {false, false};
+  uint32_t vmask[2] = {0u, 0u};
+  if (my_n > 0) vmask[0] = prefetch_slice(p, pool, rg[0], row_ids, kSlice * warp, n_cells, h, pos);
+
+  for (int j = 0; j < my_n; ++j) {
+    const int st = j & 1;
+    if (j + 1 < my_n) {
+      vmask[st ^ 1] = prefetch_slice(p, pool, rg[st ^ 1], row_ids, kSlice * (warp + 4 * (j + 1)), n_cells, h, pos);
+      cp_async_wait_group1();
+    } else {
+      cp_async_wait_all();
+    }
+    __syncwarp();
+    const WarpStage& S = rg[st];
+    const uint32_t vm = vmask[st];
+
+    // ---- S^T = Kcode . (q f)^T, one accumulator per K-scale group
+    float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+    {
+      const uint4 ca0 = *reinterpret_cast<const uint4*>(S.k + g * kD + 16 * tq);
+      const uint4 ca1 = *reinterpret_cast<const uint4*>(S.k + g * kD + 64 + 16 * tq);
+      const uint4 cb0 = *reinterpret_cast<const uint4*>(S.k + (g + 8) * kD + 16 * tq);
+      const uint4 cb1 = *reinterpret_cast<const uint4*>(S.k + (g + 8) * kD + 64 + 16 * tq);
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const int w = s & 3;
+        const uint32_t wa = word_of(s < 4 ? ca0 : ca1, w) ^ 0x80808080u;
+        const uint32_t wb = word_of(s < 4 ? cb0 : cb1, w) ^ 0x80808080u;
+        uint32_t a[4];
+        a[0] = byte_pair_h2(wa, 0x4140, kBiasS8);
+        a[2] = byte_pair_h2(wa, 0x4342, kBiasS8);
+        a[1] = byte_pair_h2(wb, 0x4140, kBiasS8);
+        a[3] = byte_pair_h2(wb, 0x4342, kBiasS8);
+        if (s < 4) {
+          mma16816(d0, a, qh[s][0], qh[s][1]);
+          mma16816(d0, a, ql[s][0], ql[s][1]);
+        } else {
+          mma16816(d1, a, qh[s][0], qh[s][1]);
+          mma16816(d1, a, ql[s][0], ql[s][1]);
+        }
+      }
+    }
+    // ---- base-2 logits of cells g, g+8 for heads 2tq, 2tq+1; masked cells -> -inf
+    const bool va = (vm >> (2 * g)) & 1u, vb = (vm >> (2 * g + 16)) & 1u;
+    float z[4];
+    {
+      const float2 ka = *reinterpret_cast<const float2*>(S.ks + 2 * g);
+      const float2 kb = *reinterpret_cast<const float2*>(S.ks + 2 * (g + 8));
+      z[0] = va ? fmaf(d1[0], ka.y, d0[0] * ka.x) * lam0 : -INFINITY;
+      z[1] = va ? fmaf(d1[1], ka.y, d0[1] * ka.x) * lam1 : -INFINITY;
+      z[2] = vb ? fmaf(d1[2], kb.y, d0[2] * kb.x) * lam0 : -INFINITY;
+      z[3] = vb ? fmaf(d1[3], kb.y, d0[3] * kb.x) * lam1 : -INFINITY;
+    }
+    float mx0 = fmaxf(z[0], z[2]), mx1 = fmaxf(z[1], z[3]);
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
+    const float mn0 = fmaxf(m2[0], mx0), mn1 = fmaxf(m2[1], mx1);
+    const float al0 = (mn0 == -INFINITY) ? 1.f : ex2f(m2[0] - mn0);
+    const float al1 = (mn1 == -INFINITY) ? 1.f : ex2f(m2[1] - mn1);
+    const float p0 = (z[0] == -INFINITY) ? 0.f : ex2f(z[0] - mn0);
+    const float p1 = (z[1] == -INFINITY) ? 0.f : ex2f(z[1] - mn1);
+    const float p2 = (z[2] == -INFINITY) ? 0.f : ex2f(z[2] - mn0);
+    const float p3 = (z[3] == -INFINITY) ? 0.f : ex2f(z[3] - mn1);
+    lp[0] = fmaf(lp[0], al0, p0 + p2);
+    lp[1] = fmaf(lp[1], al1, p1 + p3);
+    m2[0] = mn0;
+    m2[1] = mn1;
+
+    // ---- p to the B layout: this lane needs cells 2tq, 2tq+1, 2tq+8, 2tq+9 of head g
+    pb[2 * tq][g] = p0;
+    pb[2 * tq + 1][g] = p1;
+    pb[2 * tq][g + 8] = p2;
+    pb[2 * tq + 1][g + 8] = p3;
+    __syncwarp();
+    const float2 pA = *reinterpret_cast<const float2*>(&pb[g][2 * tq]);
+    const float2 pB = *reinterpret_cast<const float2*>(&pb[g][2 * tq + 8]);
+    const float4 vsA = *reinterpret_cast<const float4*>(S.vs + 4 * tq);         // cells 2tq, 2tq+1: (g0, g1)
+    const float4 vsB = *reinterpret_cast<const float4*>(S.vs + 4 * tq + 16);    // cells 2tq+8, 2tq+9
+    const bool c0 = (vm >> (4 * tq)) & 1u, c1 = (vm >> (4 * tq + 2)) & 1u;
+    const bool c2 = (vm >> (4 * tq + 16)) & 1u, c3 = (vm >> (4 * tq + 18)) & 1u;
+
+    // ---- V-scale exponent per group (slice maximum over visible cells; kv only decreases)
+    float fac[2] = {1.f, 1.f};
+    {
+      float vx0 = 0.f, vx1 = 0.f;
+      if (c0) { vx0 = fmaxf(vx0, fabsf(vsA.x)); vx1 = fmaxf(vx1, fabsf(vsA.y)); }
+      if (c1) { vx0 = fmaxf(vx0, fabsf(vsA.z)); vx1 = fmaxf(vx1, fabsf(vsA.w)); }
+      if (c2) { vx0 = fmaxf(vx0, fabsf(vsB.x)); vx1 = fmaxf(vx1, fabsf(vsB.y)); }
+      if (c3) { vx0 = fmaxf(vx0, fabsf(vsB.z)); vx1 = fmaxf(vx1, fabsf(vsB.w)); }
+      vx0 = fmaxf(vx0, __shfl_xor_sync(0xffffffffu, vx0, 1));
+      vx0 = fmaxf(vx0, __shfl_xor_sync(0xffffffffu, vx0, 2));
+      vx1 = fmaxf(vx1, __shfl_xor_sync(0xffffffffu, vx1, 1));
+      vx1 = fmaxf(vx1, __shfl_xor_sync(0xffffffffu, vx1, 2));
+      const float vx[2] = {vx0, vx1};
+#pragma unroll
+      for (int gv = 0; gv < 2; ++gv) {
+        if (vx[gv] > 0.f) {   // warp-uniform
+          int e = 0;
+          frexpf(vx[gv], &e);
+          const int k = max(-126, min(127, 4 - e));
+          if (!have_kv[gv]) {
+            kv[gv] = k;
+            have_kv[gv] = true;
+          } else if (k < kv[gv]) {
+            fac[gv] = pow2i(k - kv[gv]);
+            kv[gv] = k;
+          }
+        }
+      }
+    }
+    // ---- O = O * alpha (columns) * 2^(kv change) (rows of the group), when anything changed
+    if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f) || fac[0] != 1.f || fac[1] != 1.f) {
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        const float f = fac[mt >> 2];
+        O[mt][0] *= al0 * f;
+        O[mt][1] *= al1 * f;
+        O[mt][2] *= al0 * f;
+        O[mt][3] *= al1 * f;
+      }
+    }
+    // ---- W = p vscale 2^kv per group, fp16 hi + lo: b0 = cells (2tq, 2tq+1), b1 = (2tq+8, 2tq+9)
+    uint32_t bh[2][2], bl[2][2];
+    {
+      const float s0 = pow2i(kv[0]), s1 = pow2i(kv[1]);
+      const float w00 = c0 ? pA.x * (vsA.x * s0) : 0.f, w01 = c1 ? pA.y * (vsA.z * s0) : 0.f;
+      const float w02 = c2 ? pB.x * (vsB.x * s0) : 0.f, w03 = c3 ? pB.y * (vsB.z * s0) : 0.f;
+      const float w10 = c0 ? pA.x * (vsA.y * s1) : 0.f, w11 = c1 ? pA.y * (vsA.w * s1) : 0.f;
+      const float w12 = c2 ? pB.x * (vsB.y * s1) : 0.f, w13 = c3 ? pB.y * (vsB.w * s1) : 0.f;
+      split_pair(w00, w01, bh[0][0], bl[0][0]);
+      split_pair(w02, w03, bh[0][1], bl[0][1]);
+      split_pair(w10, w11, bh[1][0], bl[1][0]);
+      split_pair(w12, w13, bh[1][1], bl[1][1]);
+    }
+    // ---- O^T += V^T . W: lane (g, tq) reads dims 8g .. 8g+7 and 64 + 8g .. of cells 2tq, 2tq+1,
+    // 2tq+8, 2tq+9
+    {
+      const int8_t* vr = S.v + 8 * g;
+      const uint2 x0a = *reinterpret_cast<const uint2*>(vr + (2 * tq) * kD);
+      const uint2 x0b = *reinterpret_cast<const uint2*>(vr + (2 * tq) * kD + 64);
+      const uint2 x1a = *reinterpret_cast<const uint2*>(vr + (2 * tq + 1) * kD);
+      const uint2 x1b = *reinterpret_cast<const uint2*>(vr + (2 * tq + 1) * kD + 64);
+      const uint2 x2a = *reinterpret_cast<const uint2*>(vr + (2 * tq + 8) * kD);
+      const uint2 x2b = *reinterpret_cast<const uint2*>(vr + (2 * tq + 8) * kD + 64);
+      const uint2 x3a = *reinterpret_cast<const uint2*>(vr + (2 * tq + 9) * kD);
+      const uint2 x3b = *reinterpret_cast<const uint2*>(vr + (2 * tq + 9) * kD + 64);
+      // words of each group: [gv][half word] for the four cells
+      const uint32_t wc0[2][2] = {{x0a.x, x0a.y}, {x0b.x, x0b.y}};
+      const uint32_t wc1[2][2] = {{x1a.x, x1a.y}, {x1b.x, x1b.y}};
+      const uint32_t wc2[2][2] = {{x2a.x, x2a.y}, {x2b.x, x2b.y}};
+      const uint32_t wc3[2][2] = {{x3a.x, x3a.y}, {x3b.x, x3b.y}};
+#pragma unroll
+      for (int gv = 0; gv < 2; ++gv) {
+#pragma unroll
+        for (int hw = 0; hw < 2; ++hw) {
+          const uint32_t u0 = wc0[gv][hw] ^ 0x80808080u, u1 = wc1[gv][hw] ^ 0x80808080u;
+          const uint32_t u2 = wc2[gv][hw] ^ 0x80808080u, u3 = wc3[gv][hw] ^ 0x80808080u;
+          // bytes 0,1 -> m-tile j = 2 hw; bytes 2,3 -> j = 2 hw + 1
+          const uint32_t ylo = __byte_perm(u0, u1, 0x5140), yhi = __byte_perm(u0, u1, 0x7362);
+          const uint32_t zlo = __byte_perm(u2, u3, 0x5140), zhi = __byte_perm(u2, u3, 0x7362);
+#pragma unroll
+          for (int jj = 0; jj < 2; ++jj) {
+            const uint32_t y = jj ? yhi : ylo, zz = jj ? zhi : zlo;
+            uint32_t a[4];
+            a[0] = byte_pair_h2(y, 0x4140, kBiasS8);
+            a[1] = byte_pair_h2(y, 0x4342, kBiasS8);
+            a[2] = byte_pair_h2(zz, 0x4140, kBiasS8);
+            a[3] = byte_pair_h2(zz, 0x4342, kBiasS8);
+            const int mt = 4 * gv + 2 * hw + jj;
+            mma16816(O[mt], a, bh[gv][0], bh[gv][1]);
+            mma16816(O[mt], a, bl[gv][0], bl[gv][1]);
+          }
+        }
+      }
+    }
+    __syncwarp();   // the stage and pb are rewritten by the slice after next
+  }
+
+  // ---- combine the warps (in warp order) and write the split's partial
+  lp[0] += __shfl_xor_sync(0xffffffffu, lp[0], 4);
+  lp[0] += __shfl_xor_sync(0xffffffffu, lp[0], 8);
+  lp[0] += __shfl_xor_sync(0xffffffffu, lp[0], 16);
+  lp[1] += __shfl_xor_sync(0xffffffffu, lp[1], 4);
+  lp[1] += __shfl_xor_sync(0xffffffffu, lp[1], 8);
+  lp[1] += __shfl_xor_sync(0xffffffffu, lp[1], 16);
+  cp_async_wait_all();
+  __syncwarp();
+  float* wo = reinterpret_cast<float*>(rg);   // this warp's ring: O^T as [head][128]
+  {
+    const float u0 = pow2i(-kv[0]), u1 = pow2i(-kv[1]);
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      const float u = mt < 4 ? u0 : u1;
+      const int dim = 64 * (mt >> 2) + 8 * g + 2 * (mt & 3);
+      wo[(2 * tq) * kD + dim] = O[mt][0] * u;
+      wo[(2 * tq + 1) * kD + dim] = O[mt][1] * u;
+      wo[(2 * tq) * kD + dim + 1] = O[mt][2] * u;
+      wo[(2 * tq + 1) * kD + dim + 1] = O[mt][3] * u;
+    }
+    if (g == 0) {
+      wm[warp][2 * tq] = m2[0];
+      wm[warp][2 * tq + 1] = m2[1];
+      wl[warp][2 * tq] = lp[0];
+      wl[warp][2 * tq + 1] = lp[1];
+    }
+  }
+  __syncthreads();
+  const size_t cbase = ((size_t)t * p.n_q_heads + h * G) * p.n_splits + split;
+  for (int hh = 0; hh < G; ++hh) {
+    float M = wm[0][hh];
+#pragma unroll
+    for (int w = 1; w < 4; ++w) M = fmaxf(M, wm[w][hh]);
+    float o = 0.f, l = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const float mw = wm[w][hh];
+        const float sc = (mw == -INFINITY) ? 0.f : ex2f(mw - M);
+        o = fmaf(reinterpret_cast<const float*>(ring[w])[hh * kD + tid], sc, o);
+        l = fmaf(wl[w][hh], sc, l);
+      }
+    }
+    const size_t ci = cbase + (size_t)hh * p.n_splits;
+    p.part_o[ci * kD + tid] = o;
+    if (tid == 0) *reinterpret_cast<float2*>(p.part_ml + ci * 2) = make_float2(M * kLn2, l);
+  }
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------------------------
 // Host side
 
 int window_split_cells(int n_rows, int n_kv_heads, int k_cells, int n_sm) {
-  // about five 128-thread CTAs per SM in one wave, splits a multiple of the 64-cell sub-tile, at
-  // most kMaxSplits splits per (row, KV head)
+  // about four 128-thread CTAs per SM in one wave, splits a multiple of the 16-cell slice, at most
+  // kMaxSplits splits per (row, KV head)
   const long long total = (long long)n_rows * n_kv_heads * (k_cells > 0 ? k_cells : 1);
-  const long long target = 5LL * (n_sm > 0 ? n_sm : 1);
-  long long sc = kSub * ((total + kSub * target - 1) / (kSub * target));
-  const long long min_sc = kSub * (((long long)k_cells + (long long)kSub * kMaxSplits - 1) / ((long long)kSub * kMaxSplits));
+  const long long target = 4LL * (n_sm > 0 ? n_sm : 1);
+  long long sc = 16 * ((total + 16 * target - 1) / (16 * target));
+  const long long min_sc = 16 * (((long long)k_cells + 16LL * kMaxSplits - 1) / (16LL * kMaxSplits));
   if (sc < min_sc) sc = min_sc;
-  if (sc < kSub) sc = kSub;
+  if (sc < 16) sc = 16;
   return (int)sc;
 }
 
@@ -575,8 +933,13 @@ cudaError_t launch_decode_window(const WindowArgs& a, cudaStream_t stream) {
   // 3. top-k
   e = launch_topk_ex(a.topk, a.max_nb, stream, true);
   if (e != cudaSuccess) return e;
-  // 4. split attention
-  e = launch_ex(win_attn_kernel, dim3(n_pairs * ap.n_splits), dim3(kAttnThreads), 0, stream, true, ap);
+  // 4. split attention (warp-owned cells for int8 V; the chunk-style kernel when a pool has 4-bit V)
+  bool all_int8 = true;
+  for (int i = 0; i < sp.n_pools; ++i) all_int8 = all_int8 && sp.pools[i].v_bits == 8;
+  if (all_int8)
+    e = launch_ex(win_attn8_kernel, dim3(n_pairs * ap.n_splits), dim3(kAttnThreads), 0, stream, true, ap);
+  else
+    e = launch_ex(win_attn_kernel, dim3(n_pairs * ap.n_splits), dim3(kAttnThreads), 0, stream, true, ap);
   if (e != cudaSuccess) return e;
   // 5. merge of the splits
   MergeParams mp{};

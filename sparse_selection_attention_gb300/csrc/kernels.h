@@ -68,7 +68,7 @@ struct WinAttnParams {
   const int32_t* ids;
   const int32_t* n_sel;
   int n_rows, n_q_heads, n_kv_heads, k_cells;
-  int split_cells;   // cells of one split (multiple of 64)
+  int split_cells;   // cells of one split (multiple of 16)
   int n_splits;      // splits per (row, q head) in the workspace
   float* part_ml;    // [n_rows][n_q_heads][n_splits][2]
   float* part_o;     // [n_rows][n_q_heads][n_splits][128]
