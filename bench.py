@@ -1,19 +1,24 @@
 #!/usr/bin/env python3
 """Benchmark of the QSA hot path on one GB300 (or N independent replicas).
 
-One step = one decode verify window of QSA attention: block scores -> top-k
--> split-KV chunk attention -> log-sum-exp merge (four launches), on the
-workload "5 rows (4 drafts + 1), 24 q heads / 4 KV heads, head_dim 128,
-32,768 filled int8 K/V cells, 64-cell blocks, top-k 4,096 cells, 64-cell
-chunks".  The metric is decode KV GB/s: the algorithmic bytes a window must
-read (every filled K code and scale for the scores, plus the union of the
-selected visible cells' K+V codes and scales for the attention) per second.
-L2 (129 MB) is flushed before every timed step, outside the timed events, by
-writing a 256 MB buffer and then reading another 256 MB buffer (so the dirty
-lines of the write are already written back when the step starts).
+One step = one decode verify window of QSA attention in one call of the
+library (qsa_decode_window: q fragments -> block scores -> top-k -> split-KV
+attention -> log-sum-exp merge, five chained launches), on the workload
+"5 rows (4 drafts + 1), 24 q heads / 4 KV heads, head_dim 128, 32,768 filled
+int8 K/V cells, 64-cell blocks, top-k 4,096 cells".  The metric is decode KV
+GB/s: the algorithmic bytes a window must read (every filled K code and scale
+for the scores, plus the union of the selected visible cells' K+V codes and
+scales for the attention) per second.  L2 (129 MB) is flushed before every
+timed step, outside the timed events, by writing a 256 MB buffer and then
+reading another 256 MB buffer (so the dirty lines of the write are already
+written back when the step starts).
 
-The prompt side (2,048 queries against 32,768 cells, 24/4 heads, int8 K/V,
-on the tensor cores) is reported in the "prompt" object of the same line.
+Per-kernel times (and the roofline of the dominant kernel) come from
+qsa_decode_window_profile, which runs the same launches one after another with
+events between them.  The batched long-context window (2 slots x 2 rows,
+65,536 / 131,072 cells, top-k 8,192) is reported in "decode_long", and the
+prompt side (2,048 queries against 32,768 cells, 24/4 heads, int8 K/V, on the
+tensor cores) in "prompt", both on the same line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -45,7 +50,7 @@ import workloads as W  # noqa: E402
 
 METRIC = "QSA attn: decode KV GB/s (% HBM peak); prompt int8 TOPS (% peak)"
 WORKLOAD = ("decode verify window: 5 rows, 24 q heads / 4 KV heads, head_dim 128, 32,768 int8 K/V cells, "
-            "64-cell blocks, top-k 4,096 cells, 64-cell chunks")
+            "64-cell blocks, top-k 4,096 cells")
 PROMPT_WORKLOAD = "prompt chunk: 2,048 queries at 30,720..32,767 over 32,768 int8 K/V cells, 24/4 heads"
 L2_FLUSH_BYTES = 256 << 20
 K_ROW, KS_ROW, V_ROW, VS_ROW = 128, 8, 128, 8
@@ -233,10 +238,23 @@ def gpu_sleep(us: float = 400.0):
     torch.cuda._sleep(int(us * 2.1e3))
 
 
-def run_ours(args):
+def window_of(case, dev):
     import torch
 
     import sparse_selection_attention_gb300 as qsa
+    pools = [qsa.DevicePool.upload(p, dev) for p in case.pools]
+    win = qsa.DecodeWindow(pools, case.row_pool, case.n_q_heads, case.block_cells, case.k_cells, case.chunk_cells,
+                           n_chunks=case.n_chunks, max_blocks=case.max_blocks, device=dev)
+    return win, torch.from_numpy(case.q).to(dev), torch.from_numpy(case.row_pos).to(dev)
+
+
+KERNELS = ["q_prep", "block_scores", "topk", "split_attn", "merge"]
+
+
+def run_ours(args):
+    import torch
+
+    import sparse_selection_attention_gb300 as qsa  # noqa: F401  (fails loudly without the CUDA library)
 
     rank, ws, local = dist_init()
     dev = torch.device("cuda", local)
@@ -244,11 +262,7 @@ def run_ours(args):
     hbm_peak, tc_peak, peak_src = peaks()
 
     case = W.verify_window()
-    pools = [qsa.DevicePool.upload(p, dev) for p in case.pools]
-    win = qsa.DecodeWindow(pools, case.row_pool, case.n_q_heads, case.block_cells, case.k_cells, case.chunk_cells,
-                           n_chunks=case.n_chunks, max_blocks=case.max_blocks, device=dev)
-    q = torch.from_numpy(case.q).to(dev)
-    row_pos = torch.from_numpy(case.row_pos).to(dev)
+    win, q, row_pos = window_of(case, dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     clean = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
@@ -261,7 +275,7 @@ def run_ours(args):
 
     clocks = ClockSampler(local).__enter__()
     for _ in range(args.warmup):
-        win.run(q, row_pos)
+        win.run_window(q, row_pos)
     torch.cuda.synchronize()
     clocks.wait_first_sample()
     ids = win.ids.cpu().numpy()
@@ -269,50 +283,58 @@ def run_ours(args):
     a1, a3 = algorithmic_bytes(case, [ids[t] for t in range(case.n_rows)], n_sel)
     bytes_step = a1 + a3
 
-    # ---- device-timed steps, per-kernel events on the launching stream
+    # ---- device-timed steps: one qsa_decode_window call each, events on the launching stream
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     barrier(ws)
     torch.cuda.synchronize()
     for k in range(K):
         flush_l2()
-        gpu_sleep()   # the GPU idles here, outside the events, while the CPU enqueues the whole step
-        e = ev[k]
-        e[0].record(stream)
-        win.scores_step(q)
-        e[1].record(stream)
-        win.topk_step()
-        e[2].record(stream)
-        win.attn_step(q, row_pos)
-        e[3].record(stream)
-        win.merge_step()
-        e[4].record(stream)
+        gpu_sleep()   # the GPU idles here, outside the events, while the CPU enqueues the step
+        ev[k][0].record(stream)
+        win.run_window(q, row_pos)
+        ev[k][1].record(stream)
     torch.cuda.synchronize()
     barrier(ws)
-    per = np.array([[ev[k][j].elapsed_time(ev[k][j + 1]) for j in range(4)] for k in range(K)])  # ms
-    step_ms = float(per.sum(axis=1).mean())
+    step_ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
     step_ms = max_over_ranks(step_ms, ws)
-    names = ["block_scores", "topk", "decode_attn", "attn_merge"]
-    kern_ms = per.mean(axis=0)
     value = bytes_step * ws / (step_ms * 1e-3) / 1e9
 
-    dom = int(np.argmax(kern_ms))
-    dom_bytes = {0: a1, 2: a3}.get(dom)
-    roofline = None
-    if dom_bytes is not None:
-        ach = dom_bytes / (kern_ms[dom] * 1e-3) / 1e9
-        roofline = {"kernel": names[dom], "bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
-                    "frac": ach / hbm_peak, "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes": dom_bytes,
-                    "traffic": kernel_traffic(names[dom])}
+    # ---- per-kernel times: the same launches without overlap, events between them
+    P = max(5, min(50, K // 4))
+    per = []
+    for _ in range(P):
+        flush_l2()
+        gpu_sleep()
+        per.append(win.run_window_profile(q, row_pos))
+    kern_us = np.median(np.array(per), axis=0)
+    byte_of = {"block_scores": a1, "split_attn": a3}
     kernels = {}
-    for j, n in enumerate(names):
-        d = {"us": float(kern_ms[j] * 1e3), "share": float(kern_ms[j] / kern_ms.sum())}
-        b = {0: a1, 2: a3}.get(j)
-        if b is not None:
-            d["algorithmic_bytes"] = b
-            d["GB/s"] = b / (kern_ms[j] * 1e-3) / 1e9
+    for j, n in enumerate(KERNELS):
+        d = {"us": float(kern_us[j]), "share": float(kern_us[j] / kern_us.sum())}
+        if n in byte_of:
+            d["algorithmic_bytes"] = byte_of[n]
+            d["GB/s"] = byte_of[n] / (kern_us[j] * 1e-6) / 1e9
             d["frac_hbm"] = d["GB/s"] / hbm_peak
         kernels[n] = d
+    dom = max(byte_of, key=lambda n: kern_us[KERNELS.index(n)])
+    ach = byte_of[dom] / (kern_us[KERNELS.index(dom)] * 1e-6) / 1e9
+    roofline = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
+                "frac": ach / hbm_peak, "peak_source": f"{peak_src} hbm_gbs (burst copy; kernel timed alone)",
+                "algorithmic_bytes": byte_of[dom], "traffic": kernel_traffic(dom),
+                "timing": "qsa_decode_window_profile: CUDA events around the launch, no overlap with its neighbours"}
+
+    # ---- the four separate calls (qsa_block_scores, qsa_topk, qsa_decode_attn, qsa_attn_merge), for context
+    sep = []
+    for _ in range(P):
+        flush_l2()
+        gpu_sleep()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        win.run(q, row_pos)
+        b.record(stream)
+        torch.cuda.synchronize()
+        sep.append(a.elapsed_time(b))
 
     # ---- end to end through the public API with pinned host buffers
     q_h = torch.from_numpy(case.q).pin_memory()
@@ -328,7 +350,7 @@ def run_ours(args):
         e2e_ev[k][0].record(stream)
         q_d.copy_(q_h, non_blocking=True)
         pos_d.copy_(pos_h, non_blocking=True)
-        win.run(q_d, pos_d)
+        win.run_window(q_d, pos_d)
         out_h.copy_(win.out, non_blocking=True)
         lse_h.copy_(win.lse, non_blocking=True)
         e2e_ev[k][1].record(stream)
@@ -338,9 +360,39 @@ def run_ours(args):
     h2d = q_h.numel() * 4 + pos_h.numel() * 4
     d2h = out_h.numel() * 4 + lse_h.numel() * 4
 
+    # ---- batched long-context window (secondary)
+    decode_long = None
+    if not args.no_long:
+        lcase = W.batched_long_context()
+        lwin, lq, lpos = window_of(lcase, dev)
+        for _ in range(3):
+            lwin.run_window(lq, lpos)
+        torch.cuda.synchronize()
+        lids = lwin.ids.cpu().numpy()
+        lsel = lwin.n_sel.cpu().numpy()
+        l1, l3 = algorithmic_bytes(lcase, [lids[t] for t in range(lcase.n_rows)], lsel)
+        lt = []
+        for _ in range(P):
+            flush_l2()
+            gpu_sleep()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            lwin.run_window(lq, lpos)
+            b.record(stream)
+            torch.cuda.synchronize()
+            lt.append(a.elapsed_time(b))
+        lper = np.median(np.array([lwin.run_window_profile(lq, lpos) for _ in range(5)]), axis=0)
+        lms = float(np.mean(lt))
+        decode_long = {"workload": "batched long-context window: 2 slots x 2 rows, 24/4 heads, 65,536 and 131,072 "
+                                   "int8 K/V cells, top-k 8,192, one call", "ms_per_step": lms,
+                       "value": (l1 + l3) / (lms * 1e-3) / 1e9, "unit": "GB/s",
+                       "frac_of_hbm_peak": (l1 + l3) / (lms * 1e-3) / 1e9 / hbm_peak,
+                       "bytes_per_step": l1 + l3, "kernels_us": dict(zip(KERNELS, [float(x) for x in lper]))}
+
     # ---- prompt side
     prompt = None
     if not args.no_prompt:
+        import sparse_selection_attention_gb300 as qsa
         pcase = W.prompt_int8()
         call = pcase.calls[0]
         ppool = qsa.DevicePool.upload(pcase.pool, dev)
@@ -352,9 +404,9 @@ def run_ours(args):
         for _ in range(2):
             qsa.prompt_attn(ppool, pq, call[2], pout, plse, scratch=pscratch)
         torch.cuda.synchronize()
-        P = max(3, min(20, args.steps // 10))
-        pev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(P)]
-        for k in range(P):
+        PP = max(3, min(20, args.steps // 10))
+        pev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(PP)]
+        for k in range(PP):
             flush_l2()
             pev[k][0].record(stream)
             qsa.prompt_attn(ppool, pq, call[2], pout, plse, scratch=pscratch)
@@ -364,11 +416,11 @@ def run_ours(args):
             raise RuntimeError("prompt kernel reported a device error")
         p_ms = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in pev])), ws)
         issued, logical = prompt_flops(pcase, call)
-        ach = issued / (p_ms * 1e-3) / 1e12
-        prompt = {"workload": PROMPT_WORKLOAD, "ms_per_call": p_ms, "value": ach * ws, "unit": "TFLOP/s",
+        ach_p = issued / (p_ms * 1e-3) / 1e12
+        prompt = {"workload": PROMPT_WORKLOAD, "ms_per_call": p_ms, "value": ach_p * ws, "unit": "TFLOP/s",
                   "logical_TFLOP/s": logical / (p_ms * 1e-3) / 1e12 * ws, "dtype": "f16 (exact int8 codes)",
-                  "roofline": {"kernel": "prompt_attn", "bound": "tensor", "achieved": ach, "peak": tc_peak,
-                               "unit": "TFLOP/s", "frac": ach / tc_peak,
+                  "roofline": {"kernel": "prompt_attn", "bound": "tensor", "achieved": ach_p, "peak": tc_peak,
+                               "unit": "TFLOP/s", "frac": ach_p / tc_peak,
                                "peak_source": f"{peak_src} bf16_tflops (fp16 dense rate = bf16)",
                                "traffic": kernel_traffic("prompt_attn")}}
         if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -380,17 +432,20 @@ def run_ours(args):
         "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded; shapes of the pages' workloads)",
         "config": {"workload": WORKLOAD, "rows": case.n_rows, "q_heads": case.n_q_heads, "kv_heads": 4,
-                   "cells": 32768, "k_cells": case.k_cells, "chunk_cells": case.chunk_cells,
+                   "cells": 32768, "k_cells": case.k_cells, "block_cells": case.block_cells,
                    "bytes_per_step": bytes_step, "scores_bytes": a1, "attention_union_bytes": a3,
+                   "call": "qsa_decode_window (5 launches chained by programmatic dependent launch)",
                    "l2": "flushed before every timed step, outside the events: 256 MB write, then 256 MB read",
                    "parallelism": f"{ws} independent replica(s)" if ws > 1 else "1 GPU"},
         "frac_of_hbm_peak": value / ws / hbm_peak,
         "roofline": roofline,
         "kernels": kernels,
+        "separate_calls_ms": float(np.mean(sep)),
         "e2e": {"value": bytes_step * ws / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 4 * K,
+        "gpu_launches": 5 * K,
         "clocks": clocks.summary(),
+        "decode_long": decode_long,
         "prompt": prompt,
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -439,6 +494,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prompt", action="store_true")
+    ap.add_argument("--no-long", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -220,6 +220,21 @@ qsa_status qsa_decode_window(const qsa_pool* pools, int n_pools, const int32_t* 
                              void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * qsa_decode_window_profile -- qsa_decode_window for measurement: the same
+ * five launches (q fragments, block scores, top-k, split attention, merge),
+ * each started only after the previous one has finished, with CUDA events
+ * between them.  Synchronises `stream`, then writes the launches' times in
+ * microseconds to kernel_us (host, 5 floats).  Outputs as qsa_decode_window.
+ * Errors: as qsa_decode_window; QSA_ERR_ARG when kernel_us is NULL.
+ */
+qsa_status qsa_decode_window_profile(const qsa_pool* pools, int n_pools, const int32_t* row_pool,
+                                     const float* q, const int32_t* row_pos, int n_rows,
+                                     int n_q_heads, int block_cells, int k_cells, float* scores,
+                                     int max_blocks, int32_t* ids, int32_t* n_sel, float* out,
+                                     float* lse, void* workspace, size_t workspace_bytes,
+                                     void* stream, float* kernel_us);
+
+/*
  * qsa_prompt_attn -- causal attention of a chunk of n_q queries over the
  * cached context, on the tensor cores (#1367 What it does: both products on
  * the tensor cores with an exact split of the non-code operand; #600

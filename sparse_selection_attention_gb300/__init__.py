@@ -26,6 +26,7 @@ EXPORTS = [
     "qsa_block_scores", "qsa_topk", "qsa_decode_partials_bytes", "qsa_decode_attn", "qsa_attn_merge",
     "qsa_prompt_attn", "qsa_prompt_scratch_bytes", "qsa_get_device_error", "qsa_set_wait_limit_ns", "qsa_status_str", "qsa_abi_version",
     "qsa_decode_attn_noalloc", "qsa_decode_window", "qsa_decode_window_workspace_bytes",
+    "qsa_decode_window_profile",
 ]
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -70,6 +71,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qsa_prompt_scratch_bytes.restype = sz
     lib.qsa_decode_attn_noalloc.argtypes = [pool_p, i, i32p, p, p, p, p, i, i, i, i, p, p, p]
     lib.qsa_decode_window.argtypes = [pool_p, i, i32p, p, p, i, i, i, i, p, i, p, p, p, p, p, sz, p]
+    lib.qsa_decode_window_profile.argtypes = [pool_p, i, i32p, p, p, i, i, i, i, p, i, p, p, p, p, p, sz, p,
+                                              ctypes.POINTER(ctypes.c_float)]
     lib.qsa_decode_window_workspace_bytes.argtypes = [i, i, i, i]
     lib.qsa_decode_window_workspace_bytes.restype = sz
     lib.qsa_get_device_error.argtypes = [i32p, p]
@@ -79,7 +82,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qsa_status_str.restype = ctypes.c_char_p
     lib.qsa_abi_version.argtypes = []
     for name in ("qsa_block_scores", "qsa_topk", "qsa_decode_attn", "qsa_attn_merge", "qsa_prompt_attn",
-                 "qsa_get_device_error", "qsa_abi_version", "qsa_decode_attn_noalloc", "qsa_decode_window"):
+                 "qsa_get_device_error", "qsa_abi_version", "qsa_decode_attn_noalloc", "qsa_decode_window",
+                 "qsa_decode_window_profile"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -276,15 +280,25 @@ class DecodeWindow:
 
     def run_window(self, q: torch.Tensor, row_pos: torch.Tensor, stream=None) -> None:
         """The whole window in one call (qsa_decode_window): scores, ids, n_sel, out and lse."""
+        _check(load().qsa_decode_window(*self._window_args(q, row_pos, stream)), "qsa_decode_window")
+
+    def _window_args(self, q, row_pos, stream):
         if self._ws is None:
             nbytes = int(load().qsa_decode_window_workspace_bytes(self.n_rows, self.n_q_heads,
                                                                   self.pools[0].n_kv_heads, self.k_cells))
             self._ws = torch.empty((max(nbytes, 256),), dtype=torch.uint8, device=self.out.device)
-        _check(load().qsa_decode_window(self._c_pools, len(self.pools), self._c_row_pool, _ptr(q), _ptr(row_pos),
-                                        self.n_rows, self.n_q_heads, self.block_cells, self.k_cells,
-                                        self.scores.data_ptr(), self.max_blocks, self.ids.data_ptr(),
-                                        self.n_sel.data_ptr(), self.out.data_ptr(), self.lse.data_ptr(),
-                                        self._ws.data_ptr(), self._ws.numel(), _stream(stream)), "qsa_decode_window")
+        return (self._c_pools, len(self.pools), self._c_row_pool, _ptr(q), _ptr(row_pos), self.n_rows,
+                self.n_q_heads, self.block_cells, self.k_cells, self.scores.data_ptr(), self.max_blocks,
+                self.ids.data_ptr(), self.n_sel.data_ptr(), self.out.data_ptr(), self.lse.data_ptr(),
+                self._ws.data_ptr(), self._ws.numel(), _stream(stream))
+
+    def run_window_profile(self, q: torch.Tensor, row_pos: torch.Tensor, stream=None) -> List[float]:
+        """qsa_decode_window_profile: the window's five launches without overlap; returns their times in
+        microseconds (q fragments, block scores, top-k, split attention, merge).  Synchronises."""
+        us = (ctypes.c_float * 5)()
+        _check(load().qsa_decode_window_profile(*self._window_args(q, row_pos, stream), us),
+               "qsa_decode_window_profile")
+        return [float(x) for x in us]
 
     def run(self, q: torch.Tensor, row_pos: torch.Tensor, stream=None) -> None:
         """block scores -> top-k -> chunk attention -> merge, enqueued on one stream."""

@@ -243,10 +243,10 @@ size_t qsa_decode_window_workspace_bytes(int n_rows, int n_q_heads, int n_kv_hea
   return window_layout(n_rows, n_q_heads, n_kv_heads, k_cells, device_sm_count()).total;
 }
 
-qsa_status qsa_decode_window(const qsa_pool* pools, int n_pools, const int32_t* row_pool, const float* q,
-                             const int32_t* row_pos, int n_rows, int n_q_heads, int block_cells, int k_cells,
-                             float* scores, int max_blocks, int32_t* ids, int32_t* n_sel, float* out, float* lse,
-                             void* workspace, size_t workspace_bytes, void* stream) {
+static qsa_status decode_window_impl(const qsa_pool* pools, int n_pools, const int32_t* row_pool, const float* q,
+                              const int32_t* row_pos, int n_rows, int n_q_heads, int block_cells, int k_cells,
+                              float* scores, int max_blocks, int32_t* ids, int32_t* n_sel, float* out, float* lse,
+                              void* workspace, size_t workspace_bytes, void* stream, float* kernel_us) {
   qsa_status s = check_window(pools, n_pools, row_pool, n_rows, n_q_heads, true);
   if (s != QSA_OK) return s;
   if (!q || !row_pos || !scores || !ids || !n_sel || !out || !workspace) return QSA_ERR_ARG;
@@ -315,7 +315,38 @@ qsa_status qsa_decode_window(const qsa_pool* pools, int n_pools, const int32_t* 
   ap.out = out;
   ap.lse = lse;
   a.workspace = workspace;
-  return from_cuda(launch_decode_window(a, static_cast<cudaStream_t>(stream)));
+  if (!kernel_us) return from_cuda(launch_decode_window(a, static_cast<cudaStream_t>(stream)));
+  cudaEvent_t ev[6] = {};
+  cudaError_t e = cudaSuccess;
+  for (int i = 0; i < 6 && e == cudaSuccess; ++i) e = cudaEventCreate(&ev[i]);
+  if (e == cudaSuccess) e = launch_decode_window(a, static_cast<cudaStream_t>(stream), ev);
+  if (e == cudaSuccess) e = cudaEventSynchronize(ev[5]);
+  for (int i = 0; i < 5 && e == cudaSuccess; ++i) {
+    float ms = 0.f;
+    e = cudaEventElapsedTime(&ms, ev[i], ev[i + 1]);
+    kernel_us[i] = 1000.f * ms;
+  }
+  for (int i = 0; i < 6; ++i)
+    if (ev[i]) cudaEventDestroy(ev[i]);
+  return from_cuda(e);
+}
+
+qsa_status qsa_decode_window(const qsa_pool* pools, int n_pools, const int32_t* row_pool, const float* q,
+                             const int32_t* row_pos, int n_rows, int n_q_heads, int block_cells, int k_cells,
+                             float* scores, int max_blocks, int32_t* ids, int32_t* n_sel, float* out, float* lse,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_window_impl(pools, n_pools, row_pool, q, row_pos, n_rows, n_q_heads, block_cells, k_cells, scores,
+                            max_blocks, ids, n_sel, out, lse, workspace, workspace_bytes, stream, nullptr);
+}
+
+qsa_status qsa_decode_window_profile(const qsa_pool* pools, int n_pools, const int32_t* row_pool, const float* q,
+                                     const int32_t* row_pos, int n_rows, int n_q_heads, int block_cells,
+                                     int k_cells, float* scores, int max_blocks, int32_t* ids, int32_t* n_sel,
+                                     float* out, float* lse, void* workspace, size_t workspace_bytes, void* stream,
+                                     float* kernel_us) {
+  if (!kernel_us) return QSA_ERR_ARG;
+  return decode_window_impl(pools, n_pools, row_pool, q, row_pos, n_rows, n_q_heads, block_cells, k_cells, scores,
+                            max_blocks, ids, n_sel, out, lse, workspace, workspace_bytes, stream, kernel_us);
 }
 
 size_t qsa_prompt_scratch_bytes(const qsa_pool* pool, int n_q, int q_pos0) {

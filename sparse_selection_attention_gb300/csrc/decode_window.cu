@@ -899,7 +899,11 @@ static cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, si
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-cudaError_t launch_decode_window(const WindowArgs& a, cudaStream_t stream) {
+cudaError_t launch_decode_window(const WindowArgs& a, cudaStream_t stream, cudaEvent_t* ev) {
+  // With `ev` (6 events) the launches are not chained (each starts after the previous one ends) and
+  // ev[i] is recorded before launch i, ev[5] after the last: per-kernel times.
+  const bool pdl = ev == nullptr;
+  auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], stream) : cudaSuccess; };
   const ScoresParams& sp = a.scores;
   const int R = sp.n_rows, Hkv = sp.n_kv_heads, NT = (R + 7) / 8;
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
@@ -914,8 +918,12 @@ cudaError_t launch_decode_window(const WindowArgs& a, cudaStream_t stream) {
 
   // 1. q fragments: an ordinary launch, ordered after everything before it on the stream (the
   //    previous window may still read the workspace).
-  cudaError_t e = launch_ex(win_qprep_kernel, dim3(NT * 8, Hkv), dim3(32), 0, stream, false, sp.q, R, sp.n_q_heads,
-                            Hkv, NT, frag, inv_f);
+  cudaError_t e = mark(0);
+  if (e != cudaSuccess) return e;
+  e = launch_ex(win_qprep_kernel, dim3(NT * 8, Hkv), dim3(32), 0, stream, false, sp.q, R, sp.n_q_heads, Hkv, NT, frag,
+                inv_f);
+  if (e != cudaSuccess) return e;
+  e = mark(1);
   if (e != cudaSuccess) return e;
   // 2. block scores
   if (sp.total_units > 0) {
@@ -926,20 +934,26 @@ cudaError_t launch_decode_window(const WindowArgs& a, cudaStream_t stream) {
                                                                          : win_scores_kernel<4>;
     e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
-    e = launch_ex(kern, dim3(sp.total_units), dim3(kScoreThreads), smem, stream, true, sp, (const uint4*)frag,
+    e = launch_ex(kern, dim3(sp.total_units), dim3(kScoreThreads), smem, stream, pdl, sp, (const uint4*)frag,
                   (const float*)inv_f);
     if (e != cudaSuccess) return e;
   }
+  e = mark(2);
+  if (e != cudaSuccess) return e;
   // 3. top-k
-  e = launch_topk_ex(a.topk, a.max_nb, stream, true);
+  e = launch_topk_ex(a.topk, a.max_nb, stream, pdl);
+  if (e != cudaSuccess) return e;
+  e = mark(3);
   if (e != cudaSuccess) return e;
   // 4. split attention (warp-owned cells for int8 V; the chunk-style kernel when a pool has 4-bit V)
   bool all_int8 = true;
   for (int i = 0; i < sp.n_pools; ++i) all_int8 = all_int8 && sp.pools[i].v_bits == 8;
   if (all_int8)
-    e = launch_ex(win_attn8_kernel, dim3(n_pairs * ap.n_splits), dim3(kAttnThreads), 0, stream, true, ap);
+    e = launch_ex(win_attn8_kernel, dim3(n_pairs * ap.n_splits), dim3(kAttnThreads), 0, stream, pdl, ap);
   else
-    e = launch_ex(win_attn_kernel, dim3(n_pairs * ap.n_splits), dim3(kAttnThreads), 0, stream, true, ap);
+    e = launch_ex(win_attn_kernel, dim3(n_pairs * ap.n_splits), dim3(kAttnThreads), 0, stream, pdl, ap);
+  if (e != cudaSuccess) return e;
+  e = mark(4);
   if (e != cudaSuccess) return e;
   // 5. merge of the splits
   MergeParams mp{};
@@ -952,7 +966,9 @@ cudaError_t launch_decode_window(const WindowArgs& a, cudaStream_t stream) {
   mp.n_chunks = ap.n_splits;
   mp.out = ap.out;
   mp.lse = ap.lse;
-  return launch_attn_merge_ex(mp, stream, true);
+  e = launch_attn_merge_ex(mp, stream, pdl);
+  if (e != cudaSuccess) return e;
+  return mark(5);
 }
 
 }  // namespace qsa

@@ -93,7 +93,7 @@ struct WindowArgs {
 
 WindowLayout window_layout(int n_rows, int n_q_heads, int n_kv_heads, int k_cells, int n_sm);
 bool window_scores_supported(int n_rows, int n_kv_heads, int block_cells);
-cudaError_t launch_decode_window(const WindowArgs& a, cudaStream_t stream);
+cudaError_t launch_decode_window(const WindowArgs& a, cudaStream_t stream, cudaEvent_t* ev = nullptr);
 // Top-k launch; with pdl the launch may start before the preceding kernel of the stream ends.
 cudaError_t launch_topk_ex(const TopkParams& p, int max_nb, cudaStream_t stream, bool pdl);
 
