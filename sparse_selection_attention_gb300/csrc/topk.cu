@@ -9,9 +9,10 @@
 //
 // One CTA per row; thread i holds the keys of blocks [i*K, (i+1)*K) in
 // registers.  The threshold T (the kb-th largest key) is found one 8-bit digit
-// at a time from the most significant: for the keys that share the digits
-// found so far, a 256-bin histogram of the next digit (warp-aggregated shared
-// memory counts) is scanned from the top by one warp, which picks the digit
+// at a time from the most significant byte in which the largest and the
+// smallest key differ (the bytes above it are common to every key): for the
+// keys that share the digits found so far, a 256-bin shared-memory histogram
+// of the next digit is scanned from the top by one warp, which picks the digit
 // where the running count reaches the number still needed.  Blocks with key > T
 // are taken, then the lowest-id blocks with key == T.  Two CTA prefix sums in
 // block-id order give each chosen block its rank j; every block but the row's
@@ -64,14 +65,9 @@ __device__ __forceinline__ int cta_exclusive_scan(int v, int* warp_tot, int& tot
 template <int KK>
 __device__ __forceinline__ void add_digits(const uint32_t (&key)[KK], int b0, int nb, uint32_t mask, uint32_t prefix,
                                            int shift, unsigned* hist) {
-  const int lane = threadIdx.x & 31;
 #pragma unroll
-  for (int i = 0; i < KK; ++i) {
-    const bool live = b0 + i < nb && (key[i] & mask) == prefix;
-    const uint32_t digit = (key[i] >> shift) & 255u;
-    const unsigned peers = __match_any_sync(0xffffffffu, live ? digit : 256u + lane);
-    if (live && lane == __ffs(peers) - 1) atomicAdd(hist + digit, (unsigned)__popc(peers));
-  }
+  for (int i = 0; i < KK; ++i)
+    if (b0 + i < nb && (key[i] & mask) == prefix) atomicAdd(hist + ((key[i] >> shift) & 255u), 1u);
 }
 
 // Warp 0: the largest digit d whose count of keys with digit >= d reaches `need`; returns (d, need
@@ -114,6 +110,7 @@ __global__ void __launch_bounds__(kMaxThreads) topk_kernel(const TopkParams p) {
   __shared__ int warp_tot[32];
   __shared__ unsigned hist[4][256];
   __shared__ int s_pick[2];
+  __shared__ uint32_t s_mm[2][32];
   const int t = blockIdx.x, tid = threadIdx.x;
   for (int i = tid; i < 4 * 256; i += blockDim.x) (&hist[0][0])[i] = 0u;
   // Scores come from the preceding launch of the stream (a no-op without that dependency); the next
@@ -135,15 +132,37 @@ __global__ void __launch_bounds__(kMaxThreads) topk_kernel(const TopkParams p) {
   uint32_t key[KK];
 #pragma unroll
   for (int i = 0; i < KK; ++i) key[i] = (b0 + i < nb) ? score_key(__ldg(sc + b0 + i)) : 0u;
-  __syncthreads();   // histograms zeroed
 
   const bool take_all = (kb == nb);
   uint32_t T = 0;
   int need = 0;
   if (!take_all) {
+    // The leading bytes that the largest and the smallest key share are common to every key: the
+    // passes start at the first byte where they differ.
+    uint32_t mn = 0xFFFFFFFFu, mx = 0u;
+#pragma unroll
+    for (int i = 0; i < KK; ++i)
+      if (b0 + i < nb) {
+        mn = min(mn, key[i]);
+        mx = max(mx, key[i]);
+      }
+    mn = __reduce_min_sync(0xffffffffu, mn);
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    if ((tid & 31) == 0) {
+      s_mm[0][tid >> 5] = mn;
+      s_mm[1][tid >> 5] = mx;
+    }
+    __syncthreads();   // also: histograms zeroed
+    {
+      const int lane = tid & 31, n_warps = blockDim.x >> 5;
+      mn = __reduce_min_sync(0xffffffffu, lane < n_warps ? s_mm[0][lane] : 0xFFFFFFFFu);
+      mx = __reduce_max_sync(0xffffffffu, lane < n_warps ? s_mm[1][lane] : 0u);
+    }
+    const int first = (mn == mx) ? 4 : __clz(mn ^ mx) >> 3;   // leading bytes shared by every key
+    uint32_t mask = first == 0 ? 0u : (first >= 4 ? 0xFFFFFFFFu : ~(0xFFFFFFFFu >> (8 * first)));
+    T = mx & mask;
     need = kb;
-    uint32_t mask = 0;
-    for (int pass = 0; pass < 4; ++pass) {
+    for (int pass = first; pass < 4; ++pass) {
       const int shift = 24 - 8 * pass;
       add_digits<KK>(key, b0, nb, mask, T, shift, hist[pass]);
       __syncthreads();
