@@ -871,8 +871,8 @@ WindowLayout window_layout(int n_rows, int n_q_heads, int n_kv_heads, int k_cell
   off = up(off + (size_t)16 * n_kv_heads * NT * 8 * 32);
   L.inv_f = off;
   off = up(off + sizeof(float) * (size_t)n_rows * n_kv_heads);
-  L.part_ml = off;   // the qsa_decode_attn partials layout: ml, then o, back to back
-  off += sizeof(float) * 2 * (size_t)n_rows * n_q_heads * L.n_splits;
+  L.part_ml = off;   // the qsa_decode_attn partials layout (ml, then o), o 256-byte aligned for vector access
+  off = up(off + sizeof(float) * 2 * (size_t)n_rows * n_q_heads * L.n_splits);
   L.part_o = off;
   off = up(off + sizeof(float) * kD * (size_t)n_rows * n_q_heads * L.n_splits);
   L.total = off;
