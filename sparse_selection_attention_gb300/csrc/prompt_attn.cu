@@ -524,45 +524,39 @@ namespace ws {
 //    stored [cell][dim] order, two 64-dim blocks each in the 128-byte swizzle, then the tile's K
 //    and V scales group-major ([group][cell], 0 past n_filled).  It also takes the head's
 //    largest |V scale| (atomic max on its bits).
-// 2. prompt_attn_ws_kernel, one CTA per (128 rows, KV head), 12 warps in three warpgroups; the
-//    first gives registers to the other two (setmaxnreg):
-//      warp 0      one thread copies each tile image (one bulk copy) into a 6-stage ring;
+// 2. prompt_attn_ws_kernel, one CTA per (128 rows, KV head), 8 warps:
+//      warp 0      one thread copies each tile image (one bulk copy) into a 4-stage ring;
 //      warp 1      issues every tcgen05.mma from one elected lane: S(i) = Q K(i)^T with Q (hi and
-//                  lo) held in tensor memory, into one of two S slots; then P += W(i-1) V(i-1)
-//                  with W read from the S slot it was written over (V the MN-major B operand);
-//      warps 4-11  softmax, two threads per row (warps w and w+4 share TMEM lanes 32 (w % 4)..,
-//                  rows; 32 cells and 64 output dims each): logits, running max (lazy, past 2^8),
-//                  p = 2^(y - m + k) with k the head's V-scale exponent (max |vs| 2^k in
-//                  [8, 16)), W = p vscale split into fp16 hi + lo, stored over S(i).
+//                  lo, in shared memory) into one of two S slots of tensor memory; then
+//                  P += W(i-1) V(i-1) with W read from the S slot it was written over (V the
+//                  MN-major B operand);
+//      warps 4-7   softmax, one thread per row (TMEM lane = row) over all 64 cells of a tile:
+//                  logits, running max (lazy, past 2^8), p = 2^(y - m + k) with k the head's
+//                  V-scale exponent (max |vs| 2^k in [8, 16)), W = p vscale split into fp16 hi +
+//                  lo, stored over S(i).
 //    S(i+1) overlaps the softmax of tile i and P.V of tile i-1.  P holds at most kFoldEvery tiles
-//    in tensor memory: a warp folds its rows' P into the output O, kept in registers
-//    (O = O * factor + P), and zeroes P when one of its rows changes its running max and every
-//    kFoldEvery tiles.  The only thread barrier in the loop joins the two warps of a row pair;
-//    every other hand-off is an mbarrier with a bounded wait.  A wait that runs out sets the
-//    device error word; every role then stops at its next wait and the CTA drains its copies and
-//    MMAs before it exits.
-constexpr int kThreads = 384;
-// Register split: launched at kLaunchRegs a thread (the compiler's count, checked on the host
-// before every launch), warpgroup 0 drops to kRegsLow and the softmax warpgroups rise to
-// kRegsHigh; 128 kRegsLow + 256 kRegsHigh = 384 kLaunchRegs.
-constexpr int kLaunchRegs = 168, kRegsLow = 56, kRegsHigh = 224;
-static_assert(128 * kRegsLow + 256 * kRegsHigh <= kThreads * kLaunchRegs, "register split exceeds the launch");
+//    in tensor memory: a warp folds its rows' P into the output O, also in tensor memory, with
+//    fp32 FMAs (O = O * factor + P) and zeroes P when one of its rows changes its running max and
+//    every kFoldEvery tiles (the tensor core's own accumulation over thousands of steps would not
+//    round to nearest).  No thread barrier sits in the loop: every hand-off is an mbarrier with a
+//    bounded wait.  A wait that runs out sets the device error word; every role then stops at
+//    its next wait and the CTA drains its copies and MMAs before it exits.
+constexpr int kThreads = 256;
 constexpr int kM = 128;
 constexpr int kN = 64;
-constexpr int kStages = 6;
+constexpr int kStages = 4;
 constexpr int kFoldEvery = 8;
 // Tile image (global scratch and shared-memory stage alike).
 constexpr int kImgK = 0, kImgV = 16384, kImgKs = 32768, kImgVs = 33280, kImgBytes = 33792;
 constexpr int kScratchHeader = 256;   // uint32 max |V scale| bits per KV head
 // Tensor memory columns (512 allocated).
-constexpr uint32_t kTQ = 0;     // Q of dim group g: hi at 64g, lo at 64g + 32 (fp16 pairs)
-constexpr uint32_t kTS = 128;   // S slot s at 128 + 128s: S_g at +64g (fp32); W_g hi at +64g, lo at +64g+32
-constexpr uint32_t kTP = 384;   // P: output dim d at 384 + d (fp32)
+constexpr uint32_t kTS = 0;     // S slot s at 128s: S_g at +64g (fp32); W_g hi at +64g, lo at +64g+32
+constexpr uint32_t kTP = 256;   // P: output dim d at 256 + d (fp32)
+constexpr uint32_t kTO = 384;   // O: output dim d at 384 + d (fp32)
 // Shared memory map (offsets from a 1024-byte aligned base).
-constexpr int kStage0 = 0;
-constexpr int kRed = kStage0 + kStages * kImgBytes;     // row maxima [2][2][128], row sums [2][128], flags [2][8]
-constexpr int kRedMax = 0, kRedSum = 512, kRedFlag = 768;   // in 4-byte words
-constexpr int kCtl = kRed + 4096;
+constexpr int kQhi = 0, kQlo = 32768;   // Q, 2 K-blocks x [128 rows][128 B] each, 128-byte swizzle
+constexpr int kStage0 = 65536;
+constexpr int kCtl = kStage0 + kStages * kImgBytes;
 constexpr int kSmemBytes = kCtl + 512 + 1024;           // + alignment slack
 
 constexpr int FULL = 0, EMPTY = kStages, S_FULL = 2 * kStages, S_EMPTY = S_FULL + 2, W_FULL = S_EMPTY + 2,
@@ -696,8 +690,6 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
   Ctl c;
   c.bars = sbase + kCtl;
   c.w = reinterpret_cast<volatile int*>(smem + kCtl + 8 * N_BARS);
-  float* red = reinterpret_cast<float*>(smem + kRed);
-  volatile int* wflag = reinterpret_cast<volatile int*>(red + kRedFlag);
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -707,31 +699,25 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(c.bars + 8 * (S_FULL + s), 1);
       tc::mbar_init(c.bars + 8 * (S_EMPTY + s), 1);
-      tc::mbar_init(c.bars + 8 * (W_FULL + s), 8);
+      tc::mbar_init(c.bars + 8 * (W_FULL + s), 4);
     }
     tc::mbar_fence_init();
     for (int i = 0; i < N_CTL; ++i) c.w[i] = 0;
   }
   if (warp == 1) tc::tmem_alloc(tc::smem_u32(const_cast<int*>(c.w) + C_TMEM), 512);
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = static_cast<uint32_t>(c.w[C_TMEM]);
 
-  // Softmax threads: row r of the CTA (TMEM lane r), half h (cells 32h.., output dims 64h..).
+  // Softmax threads: row r of the CTA = TMEM lane r.
   const bool is_sm = warp >= 4;
   const int quarter = warp & 3;
   const int r = 32 * quarter + lane;
-  const int half = (warp - 4) >> 2;
   const int qi = q_begin + r / G;
-  const bool row_valid = (r < QPC * G) && (qi < q_end);
+  const bool row_valid = is_sm && (r < QPC * G) && (qi < q_end);
   const int head = kvh * G + (r % G);
   const int pos = row_valid ? p.q_pos0 + qi : p.q_pos0;
-  const uint32_t tl = tmem + ((uint32_t)(32 * quarter) << 16);
   float lambda = 0.f;
   if (is_sm) {
-    // Q row scaled by a power of two f (max |q f| in [64, 128)); dim group `half` split hi/lo into
-    // tensor memory, element pairs packed two per column.
+    // Q row scaled by a power of two f (max |q f| in [64, 128)), split into fp16 hi + lo and stored
+    // as the K-major A operand (two 64-dim blocks of [128 rows][128 B], 128-byte swizzle).
     const float4* q4 = reinterpret_cast<const float4*>(p.q + ((size_t)qi * p.n_q_heads + head) * kD);
     float amax = 0.f;
     if (row_valid) {
@@ -744,27 +730,32 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
     if (amax > 0.f) frexpf(amax, &e);
     const int fexp = amax > 0.f ? max(-126, min(127, 7 - e)) : 0;
     const float f = pow2f(fexp);
+#pragma unroll 4
+    for (int ch = 0; ch < 16; ++ch) {
+      float x[8];
+      if (row_valid) {
+        const float4 a = __ldg(q4 + 2 * ch), bq = __ldg(q4 + 2 * ch + 1);
+        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = bq.x; x[5] = bq.y; x[6] = bq.z; x[7] = bq.w;
+      } else {
 #pragma unroll
-    for (int part = 0; part < 2; ++part) {
-      uint32_t hi[16], lo[16];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (row_valid) v = __ldg(q4 + 16 * half + 8 * part + k);
-        split2(v.x * f, v.y * f, hi[2 * k], lo[2 * k]);
-        split2(v.z * f, v.w * f, hi[2 * k + 1], lo[2 * k + 1]);
+        for (int k = 0; k < 8; ++k) x[k] = 0.f;
       }
-      tc::tmem_st16(tl + kTQ + 64 * half + 16 * part, hi);
-      tc::tmem_st16(tl + kTQ + 64 * half + 32 + 16 * part, lo);
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) split2(x[2 * k] * f, x[2 * k + 1] * f, hi[k], lo[k]);
+      const int off = (ch >> 3) * 16384 + sw128(r, ch & 7);
+      *reinterpret_cast<uint4*>(smem + kQhi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(smem + kQlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
-    tc::tmem_wait_st();
     lambda = kLog2e * kInvSqrtD * pow2f(-fexp);
   }
+  tc::fence_proxy_async_smem();   // the tensor core reads Q through the async proxy
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
+  const uint32_t tmem = static_cast<uint32_t>(c.w[C_TMEM]);
+
   if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
   // =========================================================== producer
     if (warp == 0) {
       if (lane == 0) {
@@ -782,13 +773,11 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
       }
     }
   // =========================================================== MMA issuer
-    // The whole warp runs the loop and waits; one elected lane issues (converged issue keeps the
-    // operands in uniform registers).  Descriptors step by 32-bit adds on their low word.
+    // The whole warp runs the loop and waits; one elected lane issues.
     else if (warp == 1) {
-      const uint32_t idesc = tc::idesc_f16_f32(kM, 64);
+      const uint32_t idesc_s = tc::idesc_f16_f32(kM, kN);
       const uint32_t idesc_v = tc::idesc_f16_f32_bmn(kM, 64);
       const uint32_t d_hi = tc::sw128_desc_hi();
-      const uint32_t k_lo0 = tc::sw128_desc_lo(sbase + kStage0 + kImgK, 16);
       const uint32_t v_lo0 = tc::sw128_desc_lo(sbase + kStage0 + kImgV, 8192);
       int last_bar = -1;
       uint32_t last_par = 0;
@@ -800,15 +789,16 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
           if (!__all_sync(0xffffffffu, ok)) break;
           tc::fence_after_sync();
           if (tc::elect_one()) {
-            const uint32_t k_lo = k_lo0 + (uint32_t)(st * (kImgBytes >> 4));
             const uint32_t d = tmem + kTS + 128 * sl;
-  #pragma unroll
+#pragma unroll
             for (int g = 0; g < 2; ++g) {
-  #pragma unroll
+              const uint64_t ah = tc::sw128_desc(sbase + kQhi + g * 16384);
+              const uint64_t al = tc::sw128_desc(sbase + kQlo + g * 16384);
+              const uint64_t bk = tc::sw128_desc(sbase + kStage0 + st * kImgBytes + kImgK + g * 8192);
+#pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
-                const uint32_t b_lo = k_lo + (uint32_t)((g * 8192 + kk * 32) >> 4);
-                tc::mma_f16_tmem_a_w(d + 64 * g, tmem + kTQ + 64 * g + 8 * kk, b_lo, d_hi, idesc, kk > 0 ? 1u : 0u);
-                tc::mma_f16_tmem_a_w(d + 64 * g, tmem + kTQ + 64 * g + 32 + 8 * kk, b_lo, d_hi, idesc, 1u);
+                tc::mma_f16(d + 64 * g, ah + 2 * kk, bk + 2 * kk, idesc_s, kk > 0 ? 1u : 0u);
+                tc::mma_f16(d + 64 * g, al + 2 * kk, bk + 2 * kk, idesc_s, 1u);
               }
             }
             tc::mma_commit(c.bars + 8 * (S_FULL + sl));
@@ -825,9 +815,9 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
             const uint32_t v_lo = v_lo0 + (uint32_t)(sv * (kImgBytes >> 4));
             const uint32_t aw = tmem + kTS + 128 * sj;
             const uint32_t acc0 = j > 0 ? 1u : 0u;
-  #pragma unroll
+#pragma unroll
             for (int g = 0; g < 2; ++g) {
-  #pragma unroll
+#pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
                 const uint32_t b_lo = v_lo + (uint32_t)((g * 8192 + kk * 2048) >> 4);
                 tc::mma_f16_tmem_a_w(tmem + kTP + 64 * g, aw + 64 * g + 8 * kk, b_lo, d_hi, idesc_v, kk > 0 ? 1u : acc0);
@@ -849,7 +839,7 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
     }
     // After an abort (seen by every role at the first barrier), nothing may still write this
     // CTA's shared or tensor memory when it exits: wait for the latest fill of every stage and the
-    // last MMA commit.  (The softmax warpgroups meet these two barriers at the end of their branch.)
+    // last MMA commit.  (The softmax warpgroup meets these two barriers at the end of its branch.)
     __syncthreads();
     if (c.w[C_ABORT] && lane == 0) {
       const int issued = c.w[C_ISSUED], last_bar = c.w[C_LAST_BAR];
@@ -871,11 +861,9 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
     return;
   }
 
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
-  // =========================================================== softmax
+  // =========================================================== softmax (warps 4-7)
   {
-    const int pair_bar = 1 + quarter;          // the two warps on TMEM lanes 32 quarter ..
-    const int widx = warp - 4, partner = widx ^ 4;
+    const uint32_t tl = tmem + ((uint32_t)(32 * quarter) << 16);
     // V-scale exponent of the head: max |vs| 2^k in [8, 16); p carries the factor 2^k, which
     // cancels between the output and the row sum.
     int kv_exp = 0;
@@ -885,9 +873,6 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
       if (vmax > 0.f) frexpf(vmax, &e);
       kv_exp = vmax > 0.f ? 4 - e : 0;
     }
-    float O[64];
-#pragma unroll
-    for (int j = 0; j < 64; ++j) O[j] = 0.f;
     float m_P = -INFINITY, m_O = -INFINITY, l = 0.f;
     bool o_empty = true, alive = true;
     const float zero16[16] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -895,66 +880,62 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
       const int sl = i & 1, st = i % kStages;
       bool ok = wait_b(c, FULL + st, (i / kStages) & 1, limit);
       if (ok) ok = wait_b(c, S_FULL + sl, (i >> 1) & 1, limit);
-      ok = __all_sync(0xffffffffu, ok && !c.w[C_ABORT]);
+      if (!__all_sync(0xffffffffu, ok && !c.w[C_ABORT])) { alive = false; break; }
+      tc::fence_after_sync();
       const uint8_t* img = smem + kStage0 + st * kImgBytes;
       const int cell0 = i * kN;
-      float X[32];
-      float xmax = -INFINITY;
-      if (ok) {
-        tc::fence_after_sync();
-        const float* ksa = reinterpret_cast<const float*>(img + kImgKs);
+      const uint32_t ts = tl + kTS + 128 * sl;
+      // ---- logits of the tile's 64 cells: X = S_0 ks_0 + S_1 ks_1
+      float X[64];
+      const float* ksa = reinterpret_cast<const float*>(img + kImgKs);
 #pragma unroll
-        for (int q2 = 0; q2 < 2; ++q2) {
-          float s0[16], s1[16];
-          tc::tmem_ld16(tl + kTS + 128 * sl + 32 * half + 16 * q2, s0);
-          tc::tmem_ld16(tl + kTS + 128 * sl + 64 + 32 * half + 16 * q2, s1);
-          tc::tmem_wait_ld();
+      for (int h4 = 0; h4 < 4; ++h4) {
+        float s0[16], s1[16];
+        tc::tmem_ld16(ts + 16 * h4, s0);
+        tc::tmem_ld16(ts + 64 + 16 * h4, s1);
+        tc::tmem_wait_ld();
 #pragma unroll
-          for (int j4 = 0; j4 < 4; ++j4) {
-            const float4 k0 = reinterpret_cast<const float4*>(ksa + 32 * half + 16 * q2)[j4];
-            const float4 k1 = reinterpret_cast<const float4*>(ksa + 64 + 32 * half + 16 * q2)[j4];
-            const int j = 4 * j4;
-            const float2 xa = upk(ffma2(pk(s1[j], s1[j + 1]), pk(k1.x, k1.y), fmul2(pk(s0[j], s0[j + 1]), pk(k0.x, k0.y))));
-            const float2 xb = upk(ffma2(pk(s1[j + 2], s1[j + 3]), pk(k1.z, k1.w),
-                                        fmul2(pk(s0[j + 2], s0[j + 3]), pk(k0.z, k0.w))));
-            X[16 * q2 + j] = xa.x;
-            X[16 * q2 + j + 1] = xa.y;
-            X[16 * q2 + j + 2] = xb.x;
-            X[16 * q2 + j + 3] = xb.y;
-          }
+        for (int j4 = 0; j4 < 4; ++j4) {
+          const float4 k0 = reinterpret_cast<const float4*>(ksa + 16 * h4)[j4];
+          const float4 k1 = reinterpret_cast<const float4*>(ksa + 64 + 16 * h4)[j4];
+          const int j = 4 * j4;
+          const float2 xa = upk(ffma2(pk(s1[j], s1[j + 1]), pk(k1.x, k1.y), fmul2(pk(s0[j], s0[j + 1]), pk(k0.x, k0.y))));
+          const float2 xb = upk(ffma2(pk(s1[j + 2], s1[j + 3]), pk(k1.z, k1.w),
+                                      fmul2(pk(s0[j + 2], s0[j + 3]), pk(k0.z, k0.w))));
+          X[16 * h4 + j] = xa.x;
+          X[16 * h4 + j + 1] = xa.y;
+          X[16 * h4 + j + 2] = xb.x;
+          X[16 * h4 + j + 3] = xb.y;
         }
-        if (cell0 + kN - 1 > pos_first) {   // tile reaches past some row's position: causal mask
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (cell0 + 32 * half + j > pos) X[j] = -INFINITY;
-        }
-#pragma unroll
-        for (int j = 0; j < 32; ++j) xmax = fmaxf(xmax, X[j]);
       }
-      // Row maximum over the two halves; the pair also agrees on whether to go on.
-      red[kRedMax + (sl * 2 + half) * 128 + r] = xmax;
-      if (lane == 0) wflag[sl * 8 + widx] = ok ? 1 : 0;
-      tc::named_barrier(pair_bar, 64);
-      if (!ok || !wflag[sl * 8 + partner]) { alive = false; break; }
-      xmax = fmaxf(xmax, red[kRedMax + (sl * 2 + (half ^ 1)) * 128 + r]);
+      if (cell0 + kN - 1 > pos_first) {   // tile reaches past some row's position: causal mask
+#pragma unroll
+        for (int j = 0; j < 64; ++j)
+          if (cell0 + j > pos) X[j] = -INFINITY;
+      }
+      float xmax = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 64; ++j) xmax = fmaxf(xmax, X[j]);
       const float ymax = xmax * lambda;   // lambda > 0
       const float m_new = (ymax > m_P + 8.0f) ? ymax : m_P;
       const bool fold = __any_sync(0xffffffffu, i > 0 && (m_new != m_P || i % kFoldEvery == 0));
       if (fold) {
         // P holds this warp's rows since their last fold, referenced to m_P; after P.V(i-1):
         // O = O 2^(m_O - m_P) + P, then P = 0.  (A wait that runs out only raises the abort: the
-        // pair stops at its next barrier.)
+        // warp stops at its next wait.)
         wait_b(c, S_EMPTY + ((i - 1) & 1), ((i - 1) >> 1) & 1, limit);
         tc::fence_after_sync();
         const float fo = o_empty ? 0.f : ex2(m_O - m_P);
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          float pv[16];
-          tc::tmem_ld16(tl + kTP + 64 * half + 16 * c4, pv);
+        for (int c4 = 0; c4 < 8; ++c4) {
+          float pv[16], ov[16];
+          tc::tmem_ld16(tl + kTP + 16 * c4, pv);
+          if (!o_empty) tc::tmem_ld16(tl + kTO + 16 * c4, ov);   // O holds nothing before the first fold
           tc::tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) O[16 * c4 + j] = fmaf(O[16 * c4 + j], fo, pv[j]);
-          tc::tmem_st16f(tl + kTP + 64 * half + 16 * c4, zero16);
+          for (int j = 0; j < 16; ++j) ov[j] = o_empty ? pv[j] : fmaf(ov[j], fo, pv[j]);
+          tc::tmem_st16f(tl + kTO + 16 * c4, ov);
+          tc::tmem_st16f(tl + kTP + 16 * c4, zero16);
         }
         o_empty = false;
         m_O = m_P;
@@ -963,33 +944,39 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
         if (m_P != -INFINITY) l *= ex2(m_P - m_new);
         m_P = m_new;
       }
-      // p = 2^(X lambda - m + k), this half's row sum, W = p vscale in fp16 hi/lo over S(i).
+      // ---- p = 2^(X lambda - m + k) and the row sum
       {
         const uint64_t lam2 = pk(lambda, lambda);
         const float nm = (float)kv_exp - m_P;
         const uint64_t nm2 = pk(nm, nm);
-        float psum = 0.f;
+        float psum0 = 0.f, psum1 = 0.f;
 #pragma unroll
-        for (int j = 0; j < 32; j += 2) {
+        for (int j = 0; j < 64; j += 2) {
           const float2 y = upk(ffma2(pk(X[j], X[j + 1]), lam2, nm2));
           X[j] = ex2(y.x);
           X[j + 1] = ex2(y.y);
-          psum += X[j] + X[j + 1];
+          psum0 += X[j];
+          psum1 += X[j + 1];
         }
-        l += psum;
+        l += psum0 + psum1;
       }
+      // ---- W_g = p vscale_g in fp16 hi + lo, stored over S(i): hi at +64g, lo at +64g + 32
       const float* vsa = reinterpret_cast<const float*>(img + kImgVs);
 #pragma unroll
       for (int g = 0; g < 2; ++g) {
-        uint32_t hi[16], lo[16];
 #pragma unroll
-        for (int j4 = 0; j4 < 8; ++j4) {
-          const float4 v = reinterpret_cast<const float4*>(vsa + 64 * g + 32 * half)[j4];
-          split_pair(fmul2(pk(X[4 * j4], X[4 * j4 + 1]), pk(v.x, v.y)), hi[2 * j4], lo[2 * j4]);
-          split_pair(fmul2(pk(X[4 * j4 + 2], X[4 * j4 + 3]), pk(v.z, v.w)), hi[2 * j4 + 1], lo[2 * j4 + 1]);
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t hi[16], lo[16];
+#pragma unroll
+          for (int j4 = 0; j4 < 8; ++j4) {
+            const float4 v = reinterpret_cast<const float4*>(vsa + 64 * g + 32 * h2)[j4];
+            const int j = 32 * h2 + 4 * j4;
+            split_pair(fmul2(pk(X[j], X[j + 1]), pk(v.x, v.y)), hi[2 * j4], lo[2 * j4]);
+            split_pair(fmul2(pk(X[j + 2], X[j + 3]), pk(v.z, v.w)), hi[2 * j4 + 1], lo[2 * j4 + 1]);
+          }
+          tc::tmem_st16(ts + 64 * g + 16 * h2, hi);
+          tc::tmem_st16(ts + 64 * g + 32 + 16 * h2, lo);
         }
-        tc::tmem_st16(tl + kTS + 128 * sl + 64 * g + 16 * half, hi);
-        tc::tmem_st16(tl + kTS + 128 * sl + 64 * g + 32 + 16 * half, lo);
       }
       tc::tmem_wait_st();
       tc::fence_before_sync();
@@ -1000,29 +987,26 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
     if (alive) {
       wait_b(c, S_EMPTY + ((n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1, limit);
       tc::fence_after_sync();
-      red[kRedSum + half * 128 + r] = l;
-      tc::named_barrier(pair_bar, 64);
-      const float lt = red[kRedSum + r] + red[kRedSum + 128 + r];
       const float fo = o_empty ? 0.f : ex2(m_O - m_P);
-      const float scale = 1.f / lt;
-      float* orow = p.out + ((size_t)qi * p.n_q_heads + head) * kD + 64 * half;
+      const float scale = 1.f / l;
+      float* orow = p.out + ((size_t)qi * p.n_q_heads + head) * kD;
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        float pv[16];
-        tc::tmem_ld16(tl + kTP + 64 * half + 16 * c4, pv);
+      for (int c4 = 0; c4 < 8; ++c4) {
+        float pv[16], ov[16];
+        tc::tmem_ld16(tl + kTP + 16 * c4, pv);
+        if (!o_empty) tc::tmem_ld16(tl + kTO + 16 * c4, ov);
         tc::tmem_wait_ld();
         if (row_valid) {
 #pragma unroll
           for (int j = 0; j < 16; j += 4) {
             float v[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) v[u] = fmaf(O[16 * c4 + j + u], fo, pv[j + u]) * scale;
+            for (int u = 0; u < 4; ++u) v[u] = (o_empty ? pv[j + u] : fmaf(ov[j + u], fo, pv[j + u])) * scale;
             *reinterpret_cast<float4*>(orow + 16 * c4 + j) = make_float4(v[0], v[1], v[2], v[3]);
           }
         }
       }
-      if (row_valid && half == 0 && p.lse)
-        p.lse[(size_t)qi * p.n_q_heads + head] = (m_P - (float)kv_exp + log2f(lt)) * kLn2;
+      if (row_valid && p.lse) p.lse[(size_t)qi * p.n_q_heads + head] = (m_P - (float)kv_exp + log2f(l)) * kLn2;
     }
   }
   tc::fence_before_sync();
@@ -1044,16 +1028,6 @@ cudaError_t launch_prompt_attn(const PromptParams& p, cudaStream_t stream) {
   const int qpc = kM / G;
   dim3 grid((p.n_q + qpc - 1) / qpc, p.n_kv_heads);
   if (p.pool.v_bits == 8) {
-    // The register split inside the kernel assumes the compiled per-thread count: refuse to launch
-    // a build that differs (its setmaxnreg.inc could otherwise never be satisfied).
-    static int regs_checked = -1;
-    if (regs_checked < 0) {
-      cudaFuncAttributes fa{};
-      cudaError_t e = cudaFuncGetAttributes(&fa, reinterpret_cast<const void*>(ws::prompt_attn_ws_kernel));
-      if (e != cudaSuccess) return e;
-      regs_checked = fa.numRegs;
-    }
-    if (regs_checked != ws::kLaunchRegs) return cudaErrorInvalidConfiguration;
     cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(ws::prompt_attn_ws_kernel), (size_t)ws::kSmemBytes);
     if (e != cudaSuccess) return e;
     e = cudaMemsetAsync(p.scratch, 0, ws::kScratchHeader, stream);
