@@ -517,40 +517,43 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const PromptPa
 
 namespace ws {
 
-// Warp-specialised prompt attention for int8 V, in two launches.
+// Warp-specialised prompt attention for int8 V, in three launches.
 //
-// 1. prompt_stage_kernel converts each 64-cell tile of the context once per KV head into the
-//    exact shared-memory image the tensor cores read: K and V codes as fp16 (exact) in their
-//    stored [cell][dim] order, two 64-dim blocks each in the 128-byte swizzle, then the tile's K
-//    and V scales group-major ([group][cell], 0 past n_filled).  It also takes the head's
-//    largest |V scale| (atomic max on its bits).
-// 2. prompt_attn_ws_kernel, one CTA per (128 rows, KV head), 8 warps:
-//      warp 0      one thread copies each tile image (one bulk copy) into a 4-stage ring;
+// 1. prompt_vmax_kernel takes each KV head's largest |V scale| over the cells the call reads
+//    (atomic max on its bits): the head's exponent k_h with max |vs| 2^k_h in [8, 16).
+// 2. prompt_stage_kernel converts each 64-cell tile of the context once per KV head into the
+//    exact shared-memory image the tensor cores read: K codes as fp16 (exact), and V' = vcode *
+//    vscale * 2^k_h split into fp16 hi + lo (22 significant bits), each in the stored [cell][dim]
+//    order as two 64-dim blocks in the 128-byte swizzle; then the tile's K scales group-major
+//    ([group][cell], 0 past n_filled).
+// 3. prompt_attn_ws_kernel, one CTA per (128 rows, KV head), 8 warps:
+//      warp 0      one thread copies each tile image (one bulk copy) into a 3-stage ring;
 //      warp 1      issues every tcgen05.mma from one elected lane: S(i) = Q K(i)^T with Q (hi and
 //                  lo, in shared memory) into one of two S slots of tensor memory; then
-//                  P += W(i-1) V(i-1) with W read from the S slot it was written over (V the
-//                  MN-major B operand);
+//                  P += P'(i-1) V'(i-1) as hi.hi + hi.lo + lo.hi over all 128 output dims, with P'
+//                  read from the S slot it was written over (V' the MN-major B operand);
 //      warps 4-7   softmax, one thread per row (TMEM lane = row) over all 64 cells of a tile:
-//                  logits, running max (lazy, past 2^8), p = 2^(y - m + k) with k the head's
-//                  V-scale exponent (max |vs| 2^k in [8, 16)), W = p vscale split into fp16 hi +
-//                  lo, stored over S(i).
+//                  logits, running max (lazy, past 2^8), P' = 2^(y - m + 5) split into fp16
+//                  hi + lo, stored over S(i).  The V scale lives in V', so no per-group work.
 //    S(i+1) overlaps the softmax of tile i and P.V of tile i-1.  P holds at most kFoldEvery tiles
 //    in tensor memory: a warp folds its rows' P into the output O, also in tensor memory, with
 //    fp32 FMAs (O = O * factor + P) and zeroes P when one of its rows changes its running max and
 //    every kFoldEvery tiles (the tensor core's own accumulation over thousands of steps would not
-//    round to nearest).  No thread barrier sits in the loop: every hand-off is an mbarrier with a
-//    bounded wait.  A wait that runs out sets the device error word; every role then stops at
-//    its next wait and the CTA drains its copies and MMAs before it exits.
+//    round to nearest).  out = O 2^-(k_h + 5) / l.  No thread barrier sits in the loop: every
+//    hand-off is an mbarrier with a bounded wait.  A wait that runs out sets the device error
+//    word; every role then stops at its next wait and the CTA drains its copies and MMAs before
+//    it exits.
 constexpr int kThreads = 256;
 constexpr int kM = 128;
 constexpr int kN = 64;
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 constexpr int kFoldEvery = 8;
+constexpr int kPShift = 5;   // P' = p 2^5 <= 2^13 (p <= 2^8 under the lazy running max)
 // Tile image (global scratch and shared-memory stage alike).
-constexpr int kImgK = 0, kImgV = 16384, kImgKs = 32768, kImgVs = 33280, kImgBytes = 33792;
+constexpr int kImgK = 0, kImgVhi = 16384, kImgVlo = 32768, kImgKs = 49152, kImgBytes = 50176;
 constexpr int kScratchHeader = 256;   // uint32 max |V scale| bits per KV head
 // Tensor memory columns (512 allocated).
-constexpr uint32_t kTS = 0;     // S slot s at 128s: S_g at +64g (fp32); W_g hi at +64g, lo at +64g+32
+constexpr uint32_t kTS = 0;     // S slot s at 128s: S_g at +64g (fp32); P' hi at +0, lo at +32 (fp16 pairs)
 constexpr uint32_t kTP = 256;   // P: output dim d at 256 + d (fp32)
 constexpr uint32_t kTO = 384;   // O: output dim d at 384 + d (fp32)
 // Shared memory map (offsets from a 1024-byte aligned base).
@@ -633,20 +636,42 @@ __device__ __forceinline__ void split_pair(uint64_t ab, uint32_t& hi, uint32_t& 
   lo = h2_bits(__floats2half2_rn(rem.x, rem.y));
 }
 
+// One CTA per (64-cell tile, KV head), 64 threads (one per cell): the head's largest |V scale|.
+__global__ void __launch_bounds__(64) prompt_vmax_kernel(const PoolDev pool, int n_kv_heads, uint8_t* scratch) {
+  const int t = blockIdx.x, h = blockIdx.y, c = threadIdx.x;
+  const int cell = t * kN + c;
+  float mx = 0.f;
+  if (cell < pool.n_filled) {
+    const long long slot = cell_slot(pool, n_kv_heads, h, cell);
+    const float2 vs = __ldg(reinterpret_cast<const float2*>(pool.v_scales) + slot);
+    mx = fmaxf(fabsf(vs.x), fabsf(vs.y));
+  }
+  mx = warp_max(mx);
+  if ((c & 31) == 0) atomicMax(reinterpret_cast<unsigned int*>(scratch) + h, __float_as_uint(mx));
+}
+
+// Exponent k with max |vs| 2^k in [8, 16) for the head's largest |V scale| (0 when all are 0).
+__device__ __forceinline__ int head_v_exp(const uint8_t* scratch, int h) {
+  const float vmax = __uint_as_float(reinterpret_cast<const unsigned int*>(scratch)[h]);
+  int e = 0;
+  if (vmax > 0.f) frexpf(vmax, &e);
+  return vmax > 0.f ? max(-126, min(127, 4 - e)) : 0;
+}
+
 // One CTA per (64-cell tile, KV head), 128 threads: thread (cell ct / 2, dim block ct % 2).
 __global__ void __launch_bounds__(128) prompt_stage_kernel(const PoolDev pool, int n_kv_heads, int n_tiles,
                                                            uint8_t* scratch) {
-  const int t = blockIdx.x, h = blockIdx.y, ct = threadIdx.x, lane = ct & 31;
+  const int t = blockIdx.x, h = blockIdx.y, ct = threadIdx.x;
   uint8_t* img = scratch + kScratchHeader + ((size_t)h * n_tiles + t) * kImgBytes;
   const int cell0 = t * kN;
   const int page = __ldg(pool.page_table + cell0 / pool.page_cells);
   const long long slot0 = ((long long)page * n_kv_heads + h) * pool.page_cells + (cell0 % pool.page_cells);
   const int cc = ct >> 1, hf = ct & 1;
-#pragma unroll
-  for (int kv = 0; kv < 2; ++kv) {
-    const uint4* src = reinterpret_cast<const uint4*>(
-        (kv ? pool.v_codes : reinterpret_cast<const uint8_t*>(pool.k_codes)) + (slot0 + cc) * kD + hf * 64);
-    uint8_t* dst = img + (kv ? kImgV : kImgK) + hf * 8192;
+  const bool valid = cell0 + cc < pool.n_filled;
+  // K codes -> fp16 (exact)
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(pool.k_codes + (slot0 + cc) * kD + hf * 64);
+    uint8_t* dst = img + kImgK + hf * 8192;
     uint4 v[4];
 #pragma unroll
     for (int s4 = 0; s4 < 4; ++s4) v[s4] = __ldg(src + s4);
@@ -661,14 +686,35 @@ __global__ void __launch_bounds__(128) prompt_stage_kernel(const PoolDev pool, i
       *reinterpret_cast<uint4*>(dst + sw128(cc, 2 * s4 + 1)) = make_uint4(hh[4], hh[5], hh[6], hh[7]);
     }
   }
-  const int g = ct & 1;
-  const bool valid = cell0 + cc < pool.n_filled;
-  const float ksv = valid ? __ldg(pool.k_scales + (slot0 + cc) * 2 + g) : 0.f;
-  const float vsv = valid ? __ldg(pool.v_scales + (slot0 + cc) * 2 + g) : 0.f;
-  reinterpret_cast<float*>(img + kImgKs)[g * 64 + cc] = ksv;
-  reinterpret_cast<float*>(img + kImgVs)[g * 64 + cc] = vsv;
-  const float mx = warp_max(fabsf(vsv));
-  if (lane == 0) atomicMax(reinterpret_cast<unsigned int*>(scratch) + h, __float_as_uint(mx));
+  // V' = vcode * vscale * 2^k_h (V-scale group hf = this thread's 64 dims), fp16 hi + lo
+  {
+    const float vsc = valid ? __ldg(pool.v_scales + (slot0 + cc) * 2 + hf) * pow2f(head_v_exp(scratch, h)) : 0.f;
+    const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(pool.v_codes) +
+                                                      (slot0 + cc) * kD + hf * 64);
+    uint8_t* dhi = img + kImgVhi + hf * 8192;
+    uint8_t* dlo = img + kImgVlo + hf * 8192;
+#pragma unroll
+    for (int s4 = 0; s4 < 4; ++s4) {
+      const uint4 v = valid ? __ldg(src + s4) : make_uint4(0u, 0u, 0u, 0u);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t hi[8], lo[8];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+#pragma unroll
+        for (int b2 = 0; b2 < 2; ++b2) {
+          const float a0 = (float)(int8_t)((w[k] >> (16 * b2)) & 0xFF) * vsc;
+          const float a1 = (float)(int8_t)((w[k] >> (16 * b2 + 8)) & 0xFF) * vsc;
+          split2(a0, a1, hi[2 * k + b2], lo[2 * k + b2]);
+        }
+      }
+      *reinterpret_cast<uint4*>(dhi + sw128(cc, 2 * s4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(dhi + sw128(cc, 2 * s4 + 1)) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+      *reinterpret_cast<uint4*>(dlo + sw128(cc, 2 * s4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      *reinterpret_cast<uint4*>(dlo + sw128(cc, 2 * s4 + 1)) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+    }
+  }
+  const float ksv = valid ? __ldg(pool.k_scales + (slot0 + cc) * 2 + hf) : 0.f;
+  reinterpret_cast<float*>(img + kImgKs)[hf * 64 + cc] = ksv;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const PromptParams p) {
@@ -776,9 +822,10 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
     // The whole warp runs the loop and waits; one elected lane issues.
     else if (warp == 1) {
       const uint32_t idesc_s = tc::idesc_f16_f32(kM, kN);
-      const uint32_t idesc_v = tc::idesc_f16_f32_bmn(kM, 64);
+      const uint32_t idesc_v = tc::idesc_f16_f32_bmn(kM, 128);
       const uint32_t d_hi = tc::sw128_desc_hi();
-      const uint32_t v_lo0 = tc::sw128_desc_lo(sbase + kStage0 + kImgV, 8192);
+      const uint32_t vhi_lo0 = tc::sw128_desc_lo(sbase + kStage0 + kImgVhi, 8192);
+      const uint32_t vlo_lo0 = tc::sw128_desc_lo(sbase + kStage0 + kImgVlo, 8192);
       int last_bar = -1;
       uint32_t last_par = 0;
       for (int i = 0; i <= n_tiles; ++i) {
@@ -812,17 +859,16 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
           if (!__all_sync(0xffffffffu, wait_b(c, W_FULL + sj, (j >> 1) & 1, limit))) break;
           tc::fence_after_sync();
           if (tc::elect_one()) {
-            const uint32_t v_lo = v_lo0 + (uint32_t)(sv * (kImgBytes >> 4));
+            const uint32_t so = (uint32_t)(sv * (kImgBytes >> 4));
             const uint32_t aw = tmem + kTS + 128 * sj;
             const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
-            for (int g = 0; g < 2; ++g) {
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint32_t b_lo = v_lo + (uint32_t)((g * 8192 + kk * 2048) >> 4);
-                tc::mma_f16_tmem_a_w(tmem + kTP + 64 * g, aw + 64 * g + 8 * kk, b_lo, d_hi, idesc_v, kk > 0 ? 1u : acc0);
-                tc::mma_f16_tmem_a_w(tmem + kTP + 64 * g, aw + 64 * g + 32 + 8 * kk, b_lo, d_hi, idesc_v, 1u);
-              }
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint32_t bh = vhi_lo0 + so + (uint32_t)((kk * 2048) >> 4);
+              const uint32_t bl = vlo_lo0 + so + (uint32_t)((kk * 2048) >> 4);
+              tc::mma_f16_tmem_a_w(tmem + kTP, aw + 8 * kk, bh, d_hi, idesc_v, kk > 0 ? 1u : acc0);
+              tc::mma_f16_tmem_a_w(tmem + kTP, aw + 8 * kk, bl, d_hi, idesc_v, 1u);
+              tc::mma_f16_tmem_a_w(tmem + kTP, aw + 32 + 8 * kk, bh, d_hi, idesc_v, 1u);
             }
             tc::mma_commit(c.bars + 8 * (S_EMPTY + sj));
             tc::mma_commit(c.bars + 8 * (EMPTY + sv));
@@ -864,15 +910,8 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
   // =========================================================== softmax (warps 4-7)
   {
     const uint32_t tl = tmem + ((uint32_t)(32 * quarter) << 16);
-    // V-scale exponent of the head: max |vs| 2^k in [8, 16); p carries the factor 2^k, which
-    // cancels between the output and the row sum.
-    int kv_exp = 0;
-    {
-      const float vmax = __uint_as_float(reinterpret_cast<const unsigned int*>(p.scratch)[kvh]);
-      int e = 0;
-      if (vmax > 0.f) frexpf(vmax, &e);
-      kv_exp = vmax > 0.f ? 4 - e : 0;
-    }
+    // V' carries 2^k_h and P' carries 2^kPShift: out = O 2^-(k_h + kPShift) / l.
+    const float out_scale = pow2f(-(head_v_exp(p.scratch, kvh) + kPShift));
     float m_P = -INFINITY, m_O = -INFINITY, l = 0.f;
     bool o_empty = true, alive = true;
     const float zero16[16] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -944,39 +983,29 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
         if (m_P != -INFINITY) l *= ex2(m_P - m_new);
         m_P = m_new;
       }
-      // ---- p = 2^(X lambda - m + k) and the row sum
+      // ---- P' = 2^(X lambda - m + kPShift) in fp16 hi + lo over S(i) (hi at +0, lo at +32), and the
+      // row sum of p = P' 2^-kPShift
       {
         const uint64_t lam2 = pk(lambda, lambda);
-        const float nm = (float)kv_exp - m_P;
+        const float nm = (float)kPShift - m_P;
         const uint64_t nm2 = pk(nm, nm);
         float psum0 = 0.f, psum1 = 0.f;
-#pragma unroll
-        for (int j = 0; j < 64; j += 2) {
-          const float2 y = upk(ffma2(pk(X[j], X[j + 1]), lam2, nm2));
-          X[j] = ex2(y.x);
-          X[j + 1] = ex2(y.y);
-          psum0 += X[j];
-          psum1 += X[j + 1];
-        }
-        l += psum0 + psum1;
-      }
-      // ---- W_g = p vscale_g in fp16 hi + lo, stored over S(i): hi at +64g, lo at +64g + 32
-      const float* vsa = reinterpret_cast<const float*>(img + kImgVs);
-#pragma unroll
-      for (int g = 0; g < 2; ++g) {
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
           uint32_t hi[16], lo[16];
 #pragma unroll
-          for (int j4 = 0; j4 < 8; ++j4) {
-            const float4 v = reinterpret_cast<const float4*>(vsa + 64 * g + 32 * h2)[j4];
-            const int j = 32 * h2 + 4 * j4;
-            split_pair(fmul2(pk(X[j], X[j + 1]), pk(v.x, v.y)), hi[2 * j4], lo[2 * j4]);
-            split_pair(fmul2(pk(X[j + 2], X[j + 3]), pk(v.z, v.w)), hi[2 * j4 + 1], lo[2 * j4 + 1]);
+          for (int j2 = 0; j2 < 16; ++j2) {
+            const int j = 32 * h2 + 2 * j2;
+            const float2 y = upk(ffma2(pk(X[j], X[j + 1]), lam2, nm2));
+            const float e0 = ex2(y.x), e1 = ex2(y.y);
+            psum0 += e0;
+            psum1 += e1;
+            split_pair(pk(e0, e1), hi[j2], lo[j2]);
           }
-          tc::tmem_st16(ts + 64 * g + 16 * h2, hi);
-          tc::tmem_st16(ts + 64 * g + 32 + 16 * h2, lo);
+          tc::tmem_st16(ts + 16 * h2, hi);
+          tc::tmem_st16(ts + 32 + 16 * h2, lo);
         }
+        l += (psum0 + psum1) * (1.f / (float)(1 << kPShift));
       }
       tc::tmem_wait_st();
       tc::fence_before_sync();
@@ -988,7 +1017,7 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
       wait_b(c, S_EMPTY + ((n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1, limit);
       tc::fence_after_sync();
       const float fo = o_empty ? 0.f : ex2(m_O - m_P);
-      const float scale = 1.f / l;
+      const float scale = out_scale / l;
       float* orow = p.out + ((size_t)qi * p.n_q_heads + head) * kD;
 #pragma unroll
       for (int c4 = 0; c4 < 8; ++c4) {
@@ -1006,7 +1035,7 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
           }
         }
       }
-      if (row_valid && p.lse) p.lse[(size_t)qi * p.n_q_heads + head] = (m_P - (float)kv_exp + log2f(l)) * kLn2;
+      if (row_valid && p.lse) p.lse[(size_t)qi * p.n_q_heads + head] = (m_P + log2f(l)) * kLn2;
     }
   }
   tc::fence_before_sync();
@@ -1031,6 +1060,9 @@ cudaError_t launch_prompt_attn(const PromptParams& p, cudaStream_t stream) {
     cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(ws::prompt_attn_ws_kernel), (size_t)ws::kSmemBytes);
     if (e != cudaSuccess) return e;
     e = cudaMemsetAsync(p.scratch, 0, ws::kScratchHeader, stream);
+    if (e != cudaSuccess) return e;
+    ws::prompt_vmax_kernel<<<dim3(p.n_tiles, p.n_kv_heads), 64, 0, stream>>>(p.pool, p.n_kv_heads, p.scratch);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     ws::prompt_stage_kernel<<<dim3(p.n_tiles, p.n_kv_heads), 128, 0, stream>>>(p.pool, p.n_kv_heads, p.n_tiles,
                                                                                 p.scratch);
