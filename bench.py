@@ -85,11 +85,12 @@ def algorithmic_bytes(case, ids, n_sel):
 
 def prompt_flops(case, call):
     """(issued, logical) FLOPs of one prompt call.  Logical: unmasked (query, cell) pairs x q heads x
-    2 products x 2 * 128 FLOP.  Issued on the tensor cores: QK^T twice (fp16 hi and lo parts of q) and
-    P.V three times (hi.hi, hi.lo and lo.hi parts of P' and V')."""
+    2 products x 2 * 128 FLOP.  Issued on the tensor cores: each product three times (the hi.hi, hi.lo
+    and lo.hi parts of the fp16 hi + lo operands), six passes in all (the pages' int8 form is the same
+    count: three 8-bit planes of the non-code operand per product)."""
     _, n_q, pos0 = call
     pairs = sum(pos0 + i + 1 for i in range(n_q)) * case.n_q_heads
-    return pairs * 2 * 128 * (2 + 3), pairs * 2 * 2 * 128
+    return pairs * 2 * 128 * 6, pairs * 2 * 2 * 128
 
 
 class ClockSampler:

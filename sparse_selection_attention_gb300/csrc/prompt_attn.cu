@@ -519,27 +519,27 @@ namespace ws {
 
 // Warp-specialised prompt attention for int8 V, in three launches.
 //
-// 1. prompt_vmax_kernel takes each KV head's largest |V scale| over the cells the call reads
-//    (atomic max on its bits): the head's exponent k_h with max |vs| 2^k_h in [8, 16).
+// 1. prompt_vmax_kernel takes each KV head's largest |V scale| and |K scale| over the cells the
+//    call reads (atomic max on their bits): exponents kv_h, kk_h with max |scale| 2^k in [8, 16).
 // 2. prompt_stage_kernel converts each 64-cell tile of the context once per KV head into the
-//    exact shared-memory image the tensor cores read: K codes as fp16 (exact), and V' = vcode *
-//    vscale * 2^k_h split into fp16 hi + lo (22 significant bits), each in the stored [cell][dim]
-//    order as two 64-dim blocks in the 128-byte swizzle; then the tile's K scales group-major
-//    ([group][cell], 0 past n_filled).
+//    shared-memory image the tensor cores read: K' = kcode * kscale * 2^kk_h and V' = vcode *
+//    vscale * 2^kv_h, each split into fp16 hi + lo (22 significant bits), in the stored
+//    [cell][dim] order as two 64-dim blocks in the 128-byte swizzle (0 past n_filled).
 // 3. prompt_attn_ws_kernel, one CTA per (128 rows, KV head), 8 warps:
 //      warp 0      one thread copies each tile image (one bulk copy) into a 3-stage ring;
-//      warp 1      issues every tcgen05.mma from one elected lane: S(i) = Q K(i)^T with Q (hi and
-//                  lo, in shared memory) into one of two S slots of tensor memory; then
-//                  P += P'(i-1) V'(i-1) as hi.hi + hi.lo + lo.hi over all 128 output dims, with P'
-//                  read from the S slot it was written over (V' the MN-major B operand);
+//      warp 1      issues every tcgen05.mma from one elected lane: S(i) = Q K'(i)^T as hi.hi +
+//                  hi.lo + lo.hi (Q in tensor memory) into one of two S slots of tensor memory;
+//                  then P += P'(i-1) V'(i-1) as hi.hi + hi.lo + lo.hi over all 128 output dims,
+//                  with P' read from the S slot it was written over (V' the MN-major B operand);
 //      warps 4-7   softmax, one thread per row (TMEM lane = row) over all 64 cells of a tile:
 //                  logits, running max (lazy, past 2^8), P' = 2^(y - m + 5) split into fp16
-//                  hi + lo, stored over S(i).  The V scale lives in V', so no per-group work.
+//                  hi + lo, stored over S(i).  The scales live in K' and V', so the softmax reads
+//                  one accumulator and does no per-group work.
 //    S(i+1) overlaps the softmax of tile i and P.V of tile i-1.  P holds at most kFoldEvery tiles
 //    in tensor memory: a warp folds its rows' P into the output O, also in tensor memory, with
 //    fp32 FMAs (O = O * factor + P) and zeroes P when one of its rows changes its running max and
 //    every kFoldEvery tiles (the tensor core's own accumulation over thousands of steps would not
-//    round to nearest).  out = O 2^-(k_h + 5) / l.  No thread barrier sits in the loop: every
+//    round to nearest).  out = O 2^-(kv_h + 5) / l.  No thread barrier sits in the loop: every
 //    hand-off is an mbarrier with a bounded wait.  A wait that runs out sets the device error
 //    word; every role then stops at its next wait and the CTA drains its copies and MMAs before
 //    it exits.
@@ -549,16 +549,18 @@ constexpr int kN = 64;
 constexpr int kStages = 3;
 constexpr int kFoldEvery = 8;
 constexpr int kPShift = 5;   // P' = p 2^5 <= 2^13 (p <= 2^8 under the lazy running max)
-// Tile image (global scratch and shared-memory stage alike).
-constexpr int kImgK = 0, kImgVhi = 16384, kImgVlo = 32768, kImgKs = 49152, kImgBytes = 50176;
-constexpr int kScratchHeader = 256;   // uint32 max |V scale| bits per KV head
+// Tile image (global scratch and shared-memory stage alike): K' and V' in fp16 hi + lo, each two
+// 64-dim blocks of [64 cells][128 B] in the 128-byte swizzle.
+constexpr int kImgKhi = 0, kImgKlo = 16384, kImgVhi = 32768, kImgVlo = 49152, kImgBytes = 65536;
+constexpr int kScratchHeader = 256;   // uint32 max |V scale| bits per KV head, then max |K scale| bits
+constexpr int kMaxHeadsHeader = kScratchHeader / 8;
 // Tensor memory columns (512 allocated).
-constexpr uint32_t kTS = 0;     // S slot s at 128s: S_g at +64g (fp32); P' hi at +0, lo at +32 (fp16 pairs)
+constexpr uint32_t kTQ = 0;     // Q of dim group g: hi at 64g, lo at 64g + 32 (fp16 pairs)
+constexpr uint32_t kTS = 128;   // S slot s at 128 + 64s (fp32 logits of 64 cells); P' hi at +0, lo at +32
 constexpr uint32_t kTP = 256;   // P: output dim d at 256 + d (fp32)
 constexpr uint32_t kTO = 384;   // O: output dim d at 384 + d (fp32)
 // Shared memory map (offsets from a 1024-byte aligned base).
-constexpr int kQhi = 0, kQlo = 32768;   // Q, 2 K-blocks x [128 rows][128 B] each, 128-byte swizzle
-constexpr int kStage0 = 65536;
+constexpr int kStage0 = 0;
 constexpr int kCtl = kStage0 + kStages * kImgBytes;
 constexpr int kSmemBytes = kCtl + 512 + 1024;           // + alignment slack
 
@@ -614,6 +616,11 @@ __device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
   return d;
 }
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 __device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
   uint64_t d;
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
@@ -636,29 +643,59 @@ __device__ __forceinline__ void split_pair(uint64_t ab, uint32_t& hi, uint32_t& 
   lo = h2_bits(__floats2half2_rn(rem.x, rem.y));
 }
 
-// One CTA per (64-cell tile, KV head), 64 threads (one per cell): the head's largest |V scale|.
+// One CTA per (64-cell tile, KV head), 64 threads (one per cell): the head's largest |V scale| and
+// |K scale| (header words h and kMaxHeadsHeader + h).
 __global__ void __launch_bounds__(64) prompt_vmax_kernel(const PoolDev pool, int n_kv_heads, uint8_t* scratch) {
   const int t = blockIdx.x, h = blockIdx.y, c = threadIdx.x;
   const int cell = t * kN + c;
-  float mx = 0.f;
+  float mv = 0.f, mk = 0.f;
   if (cell < pool.n_filled) {
     const long long slot = cell_slot(pool, n_kv_heads, h, cell);
     const float2 vs = __ldg(reinterpret_cast<const float2*>(pool.v_scales) + slot);
-    mx = fmaxf(fabsf(vs.x), fabsf(vs.y));
+    const float2 ks = __ldg(reinterpret_cast<const float2*>(pool.k_scales) + slot);
+    mv = fmaxf(fabsf(vs.x), fabsf(vs.y));
+    mk = fmaxf(fabsf(ks.x), fabsf(ks.y));
   }
-  mx = warp_max(mx);
-  if ((c & 31) == 0) atomicMax(reinterpret_cast<unsigned int*>(scratch) + h, __float_as_uint(mx));
+  mv = warp_max(mv);
+  mk = warp_max(mk);
+  if ((c & 31) == 0) {
+    atomicMax(reinterpret_cast<unsigned int*>(scratch) + h, __float_as_uint(mv));
+    atomicMax(reinterpret_cast<unsigned int*>(scratch) + kMaxHeadsHeader + h, __float_as_uint(mk));
+  }
 }
 
-// Exponent k with max |vs| 2^k in [8, 16) for the head's largest |V scale| (0 when all are 0).
-__device__ __forceinline__ int head_v_exp(const uint8_t* scratch, int h) {
-  const float vmax = __uint_as_float(reinterpret_cast<const unsigned int*>(scratch)[h]);
+// Exponent k with max |scale| 2^k in [8, 16) for header word w (0 when every scale is 0).
+__device__ __forceinline__ int head_scale_exp(const uint8_t* scratch, int w) {
+  const float vmax = __uint_as_float(reinterpret_cast<const unsigned int*>(scratch)[w]);
   int e = 0;
   if (vmax > 0.f) frexpf(vmax, &e);
   return vmax > 0.f ? max(-126, min(127, 4 - e)) : 0;
 }
 
-// One CTA per (64-cell tile, KV head), 128 threads: thread (cell ct / 2, dim block ct % 2).
+// codes (int8, 64 of them in v[4]) * sc -> fp16 hi + lo, written as one cell row of two images.
+__device__ __forceinline__ void write_scaled_row(const uint4 (&v)[4], float sc, uint8_t* dhi, uint8_t* dlo, int cc) {
+#pragma unroll
+  for (int s4 = 0; s4 < 4; ++s4) {
+    const uint32_t w[4] = {v[s4].x, v[s4].y, v[s4].z, v[s4].w};
+    uint32_t hi[8], lo[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+#pragma unroll
+      for (int b2 = 0; b2 < 2; ++b2) {
+        const float a0 = (float)(int8_t)((w[k] >> (16 * b2)) & 0xFF) * sc;
+        const float a1 = (float)(int8_t)((w[k] >> (16 * b2 + 8)) & 0xFF) * sc;
+        split2(a0, a1, hi[2 * k + b2], lo[2 * k + b2]);
+      }
+    }
+    *reinterpret_cast<uint4*>(dhi + sw128(cc, 2 * s4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4*>(dhi + sw128(cc, 2 * s4 + 1)) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+    *reinterpret_cast<uint4*>(dlo + sw128(cc, 2 * s4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    *reinterpret_cast<uint4*>(dlo + sw128(cc, 2 * s4 + 1)) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+  }
+}
+
+// One CTA per (64-cell tile, KV head), 128 threads: thread (cell ct / 2, dim block ct % 2 = scale
+// group).
 __global__ void __launch_bounds__(128) prompt_stage_kernel(const PoolDev pool, int n_kv_heads, int n_tiles,
                                                            uint8_t* scratch) {
   const int t = blockIdx.x, h = blockIdx.y, ct = threadIdx.x;
@@ -668,53 +705,25 @@ __global__ void __launch_bounds__(128) prompt_stage_kernel(const PoolDev pool, i
   const long long slot0 = ((long long)page * n_kv_heads + h) * pool.page_cells + (cell0 % pool.page_cells);
   const int cc = ct >> 1, hf = ct & 1;
   const bool valid = cell0 + cc < pool.n_filled;
-  // K codes -> fp16 (exact)
+  uint4 v[4];
+  // K' = kcode * kscale * 2^kk_h
   {
+    const float sc = valid ? __ldg(pool.k_scales + (slot0 + cc) * 2 + hf) * pow2f(head_scale_exp(scratch, kMaxHeadsHeader + h))
+                           : 0.f;
     const uint4* src = reinterpret_cast<const uint4*>(pool.k_codes + (slot0 + cc) * kD + hf * 64);
-    uint8_t* dst = img + kImgK + hf * 8192;
-    uint4 v[4];
 #pragma unroll
-    for (int s4 = 0; s4 < 4; ++s4) v[s4] = __ldg(src + s4);
-#pragma unroll
-    for (int s4 = 0; s4 < 4; ++s4) {
-      uint32_t hh[8];
-      s8x4_to_h2x2(v[s4].x, hh[0], hh[1]);
-      s8x4_to_h2x2(v[s4].y, hh[2], hh[3]);
-      s8x4_to_h2x2(v[s4].z, hh[4], hh[5]);
-      s8x4_to_h2x2(v[s4].w, hh[6], hh[7]);
-      *reinterpret_cast<uint4*>(dst + sw128(cc, 2 * s4)) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
-      *reinterpret_cast<uint4*>(dst + sw128(cc, 2 * s4 + 1)) = make_uint4(hh[4], hh[5], hh[6], hh[7]);
-    }
+    for (int s4 = 0; s4 < 4; ++s4) v[s4] = valid ? __ldg(src + s4) : make_uint4(0u, 0u, 0u, 0u);
+    write_scaled_row(v, sc, img + kImgKhi + hf * 8192, img + kImgKlo + hf * 8192, cc);
   }
-  // V' = vcode * vscale * 2^k_h (V-scale group hf = this thread's 64 dims), fp16 hi + lo
+  // V' = vcode * vscale * 2^kv_h
   {
-    const float vsc = valid ? __ldg(pool.v_scales + (slot0 + cc) * 2 + hf) * pow2f(head_v_exp(scratch, h)) : 0.f;
+    const float sc = valid ? __ldg(pool.v_scales + (slot0 + cc) * 2 + hf) * pow2f(head_scale_exp(scratch, h)) : 0.f;
     const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(pool.v_codes) +
                                                       (slot0 + cc) * kD + hf * 64);
-    uint8_t* dhi = img + kImgVhi + hf * 8192;
-    uint8_t* dlo = img + kImgVlo + hf * 8192;
 #pragma unroll
-    for (int s4 = 0; s4 < 4; ++s4) {
-      const uint4 v = valid ? __ldg(src + s4) : make_uint4(0u, 0u, 0u, 0u);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      uint32_t hi[8], lo[8];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-#pragma unroll
-        for (int b2 = 0; b2 < 2; ++b2) {
-          const float a0 = (float)(int8_t)((w[k] >> (16 * b2)) & 0xFF) * vsc;
-          const float a1 = (float)(int8_t)((w[k] >> (16 * b2 + 8)) & 0xFF) * vsc;
-          split2(a0, a1, hi[2 * k + b2], lo[2 * k + b2]);
-        }
-      }
-      *reinterpret_cast<uint4*>(dhi + sw128(cc, 2 * s4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4*>(dhi + sw128(cc, 2 * s4 + 1)) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
-      *reinterpret_cast<uint4*>(dlo + sw128(cc, 2 * s4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-      *reinterpret_cast<uint4*>(dlo + sw128(cc, 2 * s4 + 1)) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
-    }
+    for (int s4 = 0; s4 < 4; ++s4) v[s4] = valid ? __ldg(src + s4) : make_uint4(0u, 0u, 0u, 0u);
+    write_scaled_row(v, sc, img + kImgVhi + hf * 8192, img + kImgVlo + hf * 8192, cc);
   }
-  const float ksv = valid ? __ldg(pool.k_scales + (slot0 + cc) * 2 + hf) : 0.f;
-  reinterpret_cast<float*>(img + kImgKs)[hf * 64 + cc] = ksv;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const PromptParams p) {
@@ -751,6 +760,9 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
     for (int i = 0; i < N_CTL; ++i) c.w[i] = 0;
   }
   if (warp == 1) tc::tmem_alloc(tc::smem_u32(const_cast<int*>(c.w) + C_TMEM), 512);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
 
   // Softmax threads: row r of the CTA = TMEM lane r.
   const bool is_sm = warp >= 4;
@@ -763,7 +775,7 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
   float lambda = 0.f;
   if (is_sm) {
     // Q row scaled by a power of two f (max |q f| in [64, 128)), split into fp16 hi + lo and stored
-    // as the K-major A operand (two 64-dim blocks of [128 rows][128 B], 128-byte swizzle).
+    // in tensor memory as the A operand (element pairs packed two per column).
     const float4* q4 = reinterpret_cast<const float4*>(p.q + ((size_t)qi * p.n_q_heads + head) * kD);
     float amax = 0.f;
     if (row_valid) {
@@ -776,28 +788,26 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
     if (amax > 0.f) frexpf(amax, &e);
     const int fexp = amax > 0.f ? max(-126, min(127, 7 - e)) : 0;
     const float f = pow2f(fexp);
-#pragma unroll 4
-    for (int ch = 0; ch < 16; ++ch) {
-      float x[8];
-      if (row_valid) {
-        const float4 a = __ldg(q4 + 2 * ch), bq = __ldg(q4 + 2 * ch + 1);
-        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = bq.x; x[5] = bq.y; x[6] = bq.z; x[7] = bq.w;
-      } else {
+    const uint32_t tq = static_cast<uint32_t>(c.w[C_TMEM]) + ((uint32_t)(32 * quarter) << 16);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) x[k] = 0.f;
+    for (int part = 0; part < 4; ++part) {   // dims 32 part .. + 31
+      uint32_t hi[16], lo[16];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (row_valid) v = __ldg(q4 + 8 * part + k);
+        split2(v.x * f, v.y * f, hi[2 * k], lo[2 * k]);
+        split2(v.z * f, v.w * f, hi[2 * k + 1], lo[2 * k + 1]);
       }
-      uint32_t hi[4], lo[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) split2(x[2 * k] * f, x[2 * k + 1] * f, hi[k], lo[k]);
-      const int off = (ch >> 3) * 16384 + sw128(r, ch & 7);
-      *reinterpret_cast<uint4*>(smem + kQhi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4*>(smem + kQlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      const uint32_t col = kTQ + 64 * (part >> 1) + 16 * (part & 1);
+      tc::tmem_st16(tq + col, hi);
+      tc::tmem_st16(tq + col + 32, lo);
     }
+    tc::tmem_wait_st();
     lambda = kLog2e * kInvSqrtD * pow2f(-fexp);
   }
-  tc::fence_proxy_async_smem();   // the tensor core reads Q through the async proxy
   tc::fence_before_sync();
-  __syncthreads();
+  __syncthreads();   // Q is in tensor memory
   tc::fence_after_sync();
   const uint32_t tmem = static_cast<uint32_t>(c.w[C_TMEM]);
 
@@ -825,6 +835,8 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
       const uint32_t idesc_v = tc::idesc_f16_f32_bmn(kM, 128);
       const uint32_t d_hi = tc::sw128_desc_hi();
       const uint32_t vhi_lo0 = tc::sw128_desc_lo(sbase + kStage0 + kImgVhi, 8192);
+      const uint32_t khi_lo0 = tc::sw128_desc_lo(sbase + kStage0 + kImgKhi, 16);
+      const uint32_t klo_lo0 = tc::sw128_desc_lo(sbase + kStage0 + kImgKlo, 16);
       const uint32_t vlo_lo0 = tc::sw128_desc_lo(sbase + kStage0 + kImgVlo, 8192);
       int last_bar = -1;
       uint32_t last_par = 0;
@@ -836,16 +848,18 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
           if (!__all_sync(0xffffffffu, ok)) break;
           tc::fence_after_sync();
           if (tc::elect_one()) {
-            const uint32_t d = tmem + kTS + 128 * sl;
+            const uint32_t d = tmem + kTS + 64 * sl;
+            const uint32_t so = (uint32_t)(st * (kImgBytes >> 4));
 #pragma unroll
             for (int g = 0; g < 2; ++g) {
-              const uint64_t ah = tc::sw128_desc(sbase + kQhi + g * 16384);
-              const uint64_t al = tc::sw128_desc(sbase + kQlo + g * 16384);
-              const uint64_t bk = tc::sw128_desc(sbase + kStage0 + st * kImgBytes + kImgK + g * 8192);
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
-                tc::mma_f16(d + 64 * g, ah + 2 * kk, bk + 2 * kk, idesc_s, kk > 0 ? 1u : 0u);
-                tc::mma_f16(d + 64 * g, al + 2 * kk, bk + 2 * kk, idesc_s, 1u);
+                const uint32_t bh = khi_lo0 + so + (uint32_t)((g * 8192 + kk * 32) >> 4);
+                const uint32_t bl = klo_lo0 + so + (uint32_t)((g * 8192 + kk * 32) >> 4);
+                const uint32_t ah = tmem + kTQ + 64 * g + 8 * kk, al = ah + 32;
+                tc::mma_f16_tmem_a_w(d, ah, bh, d_hi, idesc_s, (g > 0 || kk > 0) ? 1u : 0u);
+                tc::mma_f16_tmem_a_w(d, ah, bl, d_hi, idesc_s, 1u);
+                tc::mma_f16_tmem_a_w(d, al, bh, d_hi, idesc_s, 1u);
               }
             }
             tc::mma_commit(c.bars + 8 * (S_FULL + sl));
@@ -860,7 +874,7 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
           tc::fence_after_sync();
           if (tc::elect_one()) {
             const uint32_t so = (uint32_t)(sv * (kImgBytes >> 4));
-            const uint32_t aw = tmem + kTS + 128 * sj;
+            const uint32_t aw = tmem + kTS + 64 * sj;
             const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
@@ -910,8 +924,9 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
   // =========================================================== softmax (warps 4-7)
   {
     const uint32_t tl = tmem + ((uint32_t)(32 * quarter) << 16);
-    // V' carries 2^k_h and P' carries 2^kPShift: out = O 2^-(k_h + kPShift) / l.
-    const float out_scale = pow2f(-(head_v_exp(p.scratch, kvh) + kPShift));
+    // K' carries 2^kk_h (folded into lambda), V' 2^kv_h and P' 2^kPShift: out = O 2^-(kv_h + kPShift) / l.
+    lambda *= pow2f(-head_scale_exp(p.scratch, kMaxHeadsHeader + kvh));
+    const float out_scale = pow2f(-(head_scale_exp(p.scratch, kvh) + kPShift));
     float m_P = -INFINITY, m_O = -INFINITY, l = 0.f;
     bool o_empty = true, alive = true;
     const float zero16[16] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -923,38 +938,25 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
       tc::fence_after_sync();
       const uint8_t* img = smem + kStage0 + st * kImgBytes;
       const int cell0 = i * kN;
-      const uint32_t ts = tl + kTS + 128 * sl;
-      // ---- logits of the tile's 64 cells: X = S_0 ks_0 + S_1 ks_1
+      const uint32_t ts = tl + kTS + 64 * sl;
+      // ---- logits of the tile's 64 cells (scaled by lambda below)
       float X[64];
-      const float* ksa = reinterpret_cast<const float*>(img + kImgKs);
-#pragma unroll
-      for (int h4 = 0; h4 < 4; ++h4) {
-        float s0[16], s1[16];
-        tc::tmem_ld16(ts + 16 * h4, s0);
-        tc::tmem_ld16(ts + 64 + 16 * h4, s1);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int j4 = 0; j4 < 4; ++j4) {
-          const float4 k0 = reinterpret_cast<const float4*>(ksa + 16 * h4)[j4];
-          const float4 k1 = reinterpret_cast<const float4*>(ksa + 64 + 16 * h4)[j4];
-          const int j = 4 * j4;
-          const float2 xa = upk(ffma2(pk(s1[j], s1[j + 1]), pk(k1.x, k1.y), fmul2(pk(s0[j], s0[j + 1]), pk(k0.x, k0.y))));
-          const float2 xb = upk(ffma2(pk(s1[j + 2], s1[j + 3]), pk(k1.z, k1.w),
-                                      fmul2(pk(s0[j + 2], s0[j + 3]), pk(k0.z, k0.w))));
-          X[16 * h4 + j] = xa.x;
-          X[16 * h4 + j + 1] = xa.y;
-          X[16 * h4 + j + 2] = xb.x;
-          X[16 * h4 + j + 3] = xb.y;
-        }
-      }
+      tc::tmem_ld64(ts, X);
+      tc::tmem_wait_ld();
       if (cell0 + kN - 1 > pos_first) {   // tile reaches past some row's position: causal mask
 #pragma unroll
         for (int j = 0; j < 64; ++j)
           if (cell0 + j > pos) X[j] = -INFINITY;
       }
-      float xmax = -INFINITY;
+      // row maximum by a tree (independent pairs)
+      float mx[32];
 #pragma unroll
-      for (int j = 0; j < 64; ++j) xmax = fmaxf(xmax, X[j]);
+      for (int j = 0; j < 32; ++j) mx[j] = fmaxf(X[2 * j], X[2 * j + 1]);
+#pragma unroll
+      for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+        for (int j = 0; j < w; ++j) mx[j] = fmaxf(mx[j], mx[j + w]);
+      const float xmax = mx[0];
       const float ymax = xmax * lambda;   // lambda > 0
       const float m_new = (ymax > m_P + 8.0f) ? ymax : m_P;
       const bool fold = __any_sync(0xffffffffu, i > 0 && (m_new != m_P || i % kFoldEvery == 0));
@@ -989,7 +991,7 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
         const uint64_t lam2 = pk(lambda, lambda);
         const float nm = (float)kPShift - m_P;
         const uint64_t nm2 = pk(nm, nm);
-        float psum0 = 0.f, psum1 = 0.f;
+        uint64_t ps[4] = {0ull, 0ull, 0ull, 0ull};   // packed partial sums, four independent chains
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
           uint32_t hi[16], lo[16];
@@ -997,15 +999,15 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
           for (int j2 = 0; j2 < 16; ++j2) {
             const int j = 32 * h2 + 2 * j2;
             const float2 y = upk(ffma2(pk(X[j], X[j + 1]), lam2, nm2));
-            const float e0 = ex2(y.x), e1 = ex2(y.y);
-            psum0 += e0;
-            psum1 += e1;
-            split_pair(pk(e0, e1), hi[j2], lo[j2]);
+            const uint64_t e = pk(ex2(y.x), ex2(y.y));
+            ps[j2 & 3] = fadd2(ps[j2 & 3], e);
+            split_pair(e, hi[j2], lo[j2]);
           }
           tc::tmem_st16(ts + 16 * h2, hi);
           tc::tmem_st16(ts + 32 + 16 * h2, lo);
         }
-        l += (psum0 + psum1) * (1.f / (float)(1 << kPShift));
+        const float2 sa = upk(fadd2(fadd2(ps[0], ps[1]), fadd2(ps[2], ps[3])));
+        l += (sa.x + sa.y) * (1.f / (float)(1 << kPShift));
       }
       tc::tmem_wait_st();
       tc::fence_before_sync();

@@ -99,7 +99,7 @@ def test_decode_attn_validation(lib):
 def test_prompt_validation(lib):
     pool = _pool(n_filled=1000, capacity=1024)
     need = lib.qsa_prompt_scratch_bytes(ctypes.byref(pool), 100, 900)
-    assert need == 256 + 4 * (999 // 64 + 1) * 50176                # int8 V: one tile image per tile and head
+    assert need == 256 + 4 * (999 // 64 + 1) * 65536                # int8 V: one tile image per tile and head
     assert lib.qsa_prompt_scratch_bytes(ctypes.byref(_pool(v_bits=4, n_filled=1000, capacity=1024)), 100, 900) == 0
     ok = dict(scratch=1 << 20, nbytes=need)
 
