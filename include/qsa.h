@@ -246,8 +246,7 @@ qsa_status qsa_decode_window_profile(const qsa_pool* pools, int n_pools, const i
  *   q          (dev)  fp32 [n_q][n_q_heads][128], 16-byte aligned
  *   scratch    (dev)  caller-owned work space of scratch_bytes >=
  *                     qsa_prompt_scratch_bytes(pool, n_q, q_pos0), 256-byte
- *                     aligned; may be NULL when that size is 0.  With int8 V
- *                     the call first converts every 64-cell tile it reads,
+ *                     aligned.  The call first converts every 64-cell tile it reads,
  *                     once per KV head, into the operand images the tensor
  *                     cores load: K' = kcode * kscale * 2^a and V' = vcode *
  *                     vscale * 2^b as fp16 hi + lo, with powers of two a, b
@@ -268,7 +267,7 @@ qsa_status qsa_prompt_attn(const qsa_pool* pool, const float* q, int n_q, int q_
  * qsa_prompt_scratch_bytes -- device scratch bytes qsa_prompt_attn needs for
  * a call of n_q queries from position q_pos0 over `pool`: a 256-byte header
  * plus 65,536 bytes per 64-cell tile of cells 0 .. q_pos0 + n_q - 1 per KV
- * head with int8 V; 0 with 4-bit V.  Returns 0 for invalid arguments.
+ * head (int8 and 4-bit V alike).  Returns 0 for invalid arguments.
  */
 size_t qsa_prompt_scratch_bytes(const qsa_pool* pool, int n_q, int q_pos0);
 

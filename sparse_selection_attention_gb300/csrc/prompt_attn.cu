@@ -1,35 +1,14 @@
 // Causal prompt attention on the tcgen05 tensor cores (qsa_prompt_attn).
 //
 // Method ("#1367 prompt attention: STRATA_PROMPT_ATTN_IMMA=1", What it does):
-// both products run on the tensor cores directly on the stored K/V codes; the
-// other operand (q, and p times the V scale) is split into exact parts whose
-// partial sums are combined in fp32, and softmax is online over K/V tiles.
-// On this GPU the 16-bit tensor path is the fast one, so the split is into two
-// fp16 parts (hi + lo, 22 significant bits) instead of three 8-bit parts; int8
-// and 4-bit codes are exact in fp16.
-//
-// One CTA = 128 rows x one KV head, row r = (query q0 + r / G, q head
-// kvh*G + r % G): the G q heads of a KV head share every K/V tile.  Per
-// 64-cell tile:
-//   1. TMA bulk copies (prefetched one tile ahead) bring the tile's int8 K,
-//      V codes and their scales into a staging buffer;
-//   2. threads convert K to fp16 (K-major, 128-byte swizzle) and V to fp16
-//      transposed (dims x cells, K-major for the second product);
-//   3. S_g = (Qhi + Qlo) . Kcode over the 64 dims of K-scale group g,
-//      accumulated in tensor memory (one fp32 column per cell);
-//   4. thread r (row r): logit = (S_0 ks_0 + S_1 ks_1) / (f sqrt(D)),
-//      causal mask, running max (rescaled lazily, only when it grows by more
-//      than 2^8), p = 2^(y - m), W_g = p * vscale_g * 2^k (k a per-tile power
-//      of two), W split into fp16 hi + lo;
-//   5. P[:, group g] = (Whi_g + Wlo_g) . Vcode[:, group g], a fresh tensor-
-//      memory accumulator per tile (8 MMA steps), folded into the running
-//      output O (also in tensor memory) with fp32 FMAs on the CUDA cores:
-//      O = O * factor + P, factor = the tile's change of running max and of
-//      the V-scale power of two.  Keeping the long sum over thousands of
-//      tiles out of the tensor-core accumulator keeps its rounding at fp32
-//      round-to-nearest level.
-// Waits are bounded: a wait that runs out sets the device error word, drains
-// the CTA's copies and exits.
+// both products run on the tensor cores with the stored codes as one operand
+// and an exact split of the other; partial sums are combined in fp32, and the
+// softmax is online over K/V tiles.  On this GPU the 16-bit tensor path is the
+// fast one, so every operand is an fp16 hi + lo pair (22 significant bits):
+// K' = kcode * kscale and V' = vcode * vscale (scaled per KV head by a power
+// of two into fp16 range) are split once per tile into operand images, q and
+// p inside the kernel; each product is issued as hi.hi + hi.lo + lo.hi.
+// int8 and 4-bit V codes take the same path (the image holds V').
 #include <cuda_fp16.h>
 
 #include "kernels.h"
@@ -41,44 +20,10 @@ __device__ int g_device_error = 0;
 
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kM = 128;
-constexpr int kTileN = 64;
-
-// Shared memory map (offsets from a 1024-byte aligned base).
-constexpr int kQhiOff = 0;          // 2 K-blocks x [128 rows][128 B]
-constexpr int kQloOff = 32768;
-constexpr int kKfOff = 65536;       // 2 K-blocks x [64 cells][128 B]
-constexpr int kVfOff = 81920;       // [128 dims][64 cells x 2 B]
-constexpr int kWOff = 98304;        // 2 slots x (hi [128][128 B] + lo [128][128 B])
-constexpr int kWSlot = 32768;
-constexpr int kStageOff = 163840;   // 2 stages
-constexpr int kStK = 0, kStV = 8192, kStKs = 16384, kStVs = 16896, kStBytes = 17920;
-constexpr int kVspOff = kStageOff + 2 * kStBytes;   // float [4][64]
-constexpr int kBarOff = kVspOff + 1024;
-constexpr int kSmemBytes = kBarOff + 128 + 1024;    // + alignment slack
-
-constexpr uint32_t kTmemCols = 512;  // S: [0,128), tile P.V: [128,256), O: [256,384)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr uint64_t kDrainLimitNs = 2000000000ull;
 
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
-__device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
-
-// Four int8 codes (w) -> two fp16 pairs, exact: bias to unsigned, place the
-// byte in the mantissa of 1024 (0x6400), subtract 1152.
-__device__ __forceinline__ void s8x4_to_h2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t u = w ^ 0x80808080u;
-  const __half2 bias = bits_h2(0x64806480u);  // 1152, 1152
-  lo = h2_bits(__hsub2(bits_h2(__byte_perm(u, 0x64646464u, 0x4140)), bias));
-  hi = h2_bits(__hsub2(bits_h2(__byte_perm(u, 0x64646464u, 0x4342)), bias));
-}
-
-// Two bytes (b0, b1) of an already-biased word -> fp16 pair 1024 + b, minus `bias`.
-__device__ __forceinline__ uint32_t bytes_to_h2(uint32_t u, uint32_t sel, uint32_t bias) {
-  return h2_bits(__hsub2(bits_h2(__byte_perm(u, 0x64646464u, sel)), bits_h2(bias)));
-}
 
 // x -> (hi, lo) fp16 with hi + lo = x to ~2^-22 relative.
 __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
@@ -88,430 +33,12 @@ __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t&
   lo = h2_bits(__floats2half2_rn(a - back.x, b - back.y));
 }
 
+// Byte offset of 16-byte chunk `chunk` of row `row` in the 128-byte swizzle (8-row atoms of 1 KB).
 __device__ __forceinline__ int sw128(int row, int chunk) {
   return (row >> 3) * 1024 + (row & 7) * 128 + ((chunk ^ (row & 7)) << 4);
 }
 
-template <int N>
-__device__ __forceinline__ uint4 pick(const uint4 (&v)[N], int j) {
-  uint4 r = v[0];
-#pragma unroll
-  for (int i = 1; i < N; ++i)
-    if (j == i) r = v[i];
-  return r;
-}
-
 __device__ __forceinline__ void raise_device_error(int code) { atomicCAS(&g_device_error, 0, code); }
-
-__global__ void __launch_bounds__(kThreads, 1) prompt_attn_kernel(const PromptParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t sbase = tc::smem_u32(smem);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int Hkv = p.n_kv_heads;
-  const int G = p.n_q_heads / Hkv;
-  const int QPC = kM / G;
-  const int kvh = blockIdx.y;
-  const int q_begin = blockIdx.x * QPC;
-  const int q_end = min(p.n_q, q_begin + QPC);
-  const PoolDev& pool = p.pool;
-  const int n_vg = pool.v_bits == 8 ? 2 : 4;
-  const int vg_dims = kD / n_vg;
-  const int v_row_bytes = pool.v_bits == 8 ? 128 : 64;
-
-  const int r = tid;
-  const int qi = q_begin + r / G;
-  const bool row_valid = (r < QPC * G) && (qi < q_end);
-  const int head = kvh * G + (r % G);
-  const int pos = row_valid ? p.q_pos0 + qi : p.q_pos0;
-  const int pos_first = p.q_pos0 + q_begin;
-  const int pos_last = p.q_pos0 + q_end - 1;
-  const int n_tiles = pos_last / kTileN + 1;
-
-  const uint32_t bar_st0 = sbase + kBarOff, bar_mma = sbase + kBarOff + 16;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + kBarOff + 32);
-  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kBarOff + 40);
-  volatile int* s_rho = reinterpret_cast<volatile int*>(smem + kBarOff + 44);
-  volatile int* s_kref = reinterpret_cast<volatile int*>(smem + kBarOff + 48);
-  float* vsp = reinterpret_cast<float*>(smem + kVspOff);
-
-  if (tid == 0) {
-    tc::mbar_init(bar_st0, 1);
-    tc::mbar_init(bar_st0 + 8, 1);
-    tc::mbar_init(bar_mma, 1);
-    tc::mbar_fence_init();
-    *s_abort = 0;
-  }
-  if (warp == 0) tc::tmem_alloc(tc::smem_u32(tmem_holder), kTmemCols);
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = *tmem_holder;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-  const uint32_t tS = tmem + lane_base;
-  const uint32_t tP = tmem + lane_base + 128;
-  const uint32_t tO = tmem + lane_base + 256;
-
-  // ---- Q: scale row by a power of two f (max |q f| in [64, 128)), split hi/lo.
-  float lambda;
-  {
-    const float4* q4 = reinterpret_cast<const float4*>(p.q + ((size_t)qi * p.n_q_heads + head) * kD);
-    float amax = 0.f;
-    if (row_valid) {
-      for (int k = 0; k < 32; ++k) {
-        const float4 v = __ldg(q4 + k);
-        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
-      }
-    }
-    int e = 0;
-    if (amax > 0.f) frexpf(amax, &e);
-    const int fexp = amax > 0.f ? 7 - e : 0;
-    for (int c = 0; c < 16; ++c) {
-      float x[8];
-      if (row_valid) {
-        const float4 a = __ldg(q4 + 2 * c), b = __ldg(q4 + 2 * c + 1);
-        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-      } else {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) x[k] = 0.f;
-      }
-      uint32_t hi[4], lo[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) split2(ldexpf(x[2 * k], fexp), ldexpf(x[2 * k + 1], fexp), hi[k], lo[k]);
-      const int off = (c >> 3) * 16384 + sw128(r, c & 7);
-      *reinterpret_cast<uint4*>(smem + kQhiOff + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4*>(smem + kQloOff + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    }
-    lambda = ldexpf(kLog2e * kInvSqrtD, -fexp);
-  }
-  tc::fence_proxy_async_smem();
-
-  // Thread 0 owns the copy / MMA issue and tracks what is in flight.
-  uint32_t st_par[2] = {0u, 0u};
-  uint32_t mma_par = 0u;
-  bool st_busy[2] = {false, false};
-  bool mma_busy = false;
-  auto issue_tile = [&](int tile, int stage) {
-    const int cell0 = tile * kTileN;
-    const int page = __ldg(pool.page_table + cell0 / pool.page_cells);
-    const long long slot0 = ((long long)page * Hkv + kvh) * pool.page_cells + (cell0 % pool.page_cells);
-    const uint32_t st = sbase + kStageOff + stage * kStBytes;
-    const uint32_t vbytes = kTileN * v_row_bytes, vsbytes = kTileN * n_vg * 4;
-    const uint32_t bar = bar_st0 + 8 * stage;
-    tc::mbar_expect_tx(bar, 8192 + vbytes + 512 + vsbytes);
-    tc::bulk_g2s(st + kStK, pool.k_codes + slot0 * kD, 8192, bar);
-    tc::bulk_g2s(st + kStV, pool.v_codes + slot0 * v_row_bytes, vbytes, bar);
-    tc::bulk_g2s(st + kStKs, pool.k_scales + slot0 * 2, 512, bar);
-    tc::bulk_g2s(st + kStVs, pool.v_scales + slot0 * n_vg, vsbytes, bar);
-    st_busy[stage] = true;
-  };
-  if (tid == 0) issue_tile(0, 0);
-  __syncthreads();
-
-  // Every thread waits; the CTA then agrees on whether any wait ran out.
-  auto cta_wait = [&](uint32_t bar, uint32_t parity) -> bool {
-    const bool ok = tc::mbar_wait(bar, parity, p.wait_limit_ns);
-    if (!ok) *s_abort = 1;
-    __syncthreads();
-    const bool go = (*s_abort == 0);
-    __syncthreads();
-    return go;
-  };
-
-  float m_ref = -INFINITY, l_run = 0.f;
-  int k_ref = 0;   // V-scale exponent (warp 0 keeps it; the CTA sees s_rho)
-  bool aborted = false;
-  const uint32_t idesc_s = tc::idesc_f16_f32(kM, kTileN);
-  const uint32_t idesc_o = tc::idesc_f16_f32(kM, vg_dims);
-
-  for (int i = 0; i < n_tiles; ++i) {
-    const int stage = i & 1;
-    const int cell0 = i * kTileN;
-    if (tid == 0 && i + 1 < n_tiles) issue_tile(i + 1, stage ^ 1);
-    if (!cta_wait(bar_st0 + 8 * stage, st_par[stage])) { aborted = true; break; }
-    st_par[stage] ^= 1u;
-    if (tid == 0) st_busy[stage] = false;
-    const uint8_t* st = smem + kStageOff + stage * kStBytes;
-
-    // ---- K codes -> fp16, K-major [cell][dim] in two 64-dim blocks.
-    {
-      const int c = tid >> 1, hf = tid & 1;
-      const uint8_t* src = st + kStK + c * 128 + hf * 64;
-      uint8_t* dst = smem + kKfOff + hf * 8192;
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        const int i4 = (s + c) & 3;
-        const uint4 v = *reinterpret_cast<const uint4*>(src + i4 * 16);
-        uint32_t h[8];
-        s8x4_to_h2x2(v.x, h[0], h[1]);
-        s8x4_to_h2x2(v.y, h[2], h[3]);
-        s8x4_to_h2x2(v.z, h[4], h[5]);
-        s8x4_to_h2x2(v.w, h[6], h[7]);
-        *reinterpret_cast<uint4*>(dst + sw128(c, 2 * i4)) = make_uint4(h[0], h[1], h[2], h[3]);
-        *reinterpret_cast<uint4*>(dst + sw128(c, 2 * i4 + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
-      }
-    }
-    // ---- V codes -> fp16 transposed [dim][cell] (K-major for p.V).
-    if (pool.v_bits == 8) {
-      const int dq = tid & 31, co = tid >> 5;
-#pragma unroll
-      for (int oi = 0; oi < 2; ++oi) {
-        const int oct = co + 4 * oi;
-        uint32_t w[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          w[k] = *reinterpret_cast<const uint32_t*>(st + kStV + (8 * oct + k) * 128 + 4 * dq) ^ 0x80808080u;
-        uint4 out[4];
-        uint32_t a[4], b[4];
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          a[kk] = __byte_perm(w[2 * kk], w[2 * kk + 1], 0x5140);  // dims 0,1 of cells 2kk, 2kk+1
-          b[kk] = __byte_perm(w[2 * kk], w[2 * kk + 1], 0x7362);  // dims 2,3
-        }
-        out[0] = make_uint4(bytes_to_h2(a[0], 0x4140, 0x64806480u), bytes_to_h2(a[1], 0x4140, 0x64806480u),
-                            bytes_to_h2(a[2], 0x4140, 0x64806480u), bytes_to_h2(a[3], 0x4140, 0x64806480u));
-        out[1] = make_uint4(bytes_to_h2(a[0], 0x4342, 0x64806480u), bytes_to_h2(a[1], 0x4342, 0x64806480u),
-                            bytes_to_h2(a[2], 0x4342, 0x64806480u), bytes_to_h2(a[3], 0x4342, 0x64806480u));
-        out[2] = make_uint4(bytes_to_h2(b[0], 0x4140, 0x64806480u), bytes_to_h2(b[1], 0x4140, 0x64806480u),
-                            bytes_to_h2(b[2], 0x4140, 0x64806480u), bytes_to_h2(b[3], 0x4140, 0x64806480u));
-        out[3] = make_uint4(bytes_to_h2(b[0], 0x4342, 0x64806480u), bytes_to_h2(b[1], 0x4342, 0x64806480u),
-                            bytes_to_h2(b[2], 0x4342, 0x64806480u), bytes_to_h2(b[3], 0x4342, 0x64806480u));
-#pragma unroll
-        for (int s = 0; s < 4; ++s) {
-          const int j = (s + (dq >> 1)) & 3;
-          const int d = 4 * dq + j;
-          *reinterpret_cast<uint4*>(smem + kVfOff + sw128(d, oct)) = pick(out, j);
-        }
-      }
-    } else {
-      const int dq = tid & 15, oct = tid >> 4;
-      uint32_t e[8], o[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(st + kStV + (8 * oct + k) * 64 + 4 * dq);
-        e[k] = w & 0x0F0F0F0Fu;          // even dims 8dq + 0,2,4,6 as nibble values
-        o[k] = (w >> 4) & 0x0F0F0F0Fu;   // odd dims 8dq + 1,3,5,7
-      }
-      uint4 out[8];
-#pragma unroll
-      for (int par = 0; par < 2; ++par) {
-        const uint32_t* src = par ? o : e;
-        uint32_t a[4], b[4];
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          a[kk] = __byte_perm(src[2 * kk], src[2 * kk + 1], 0x5140);
-          b[kk] = __byte_perm(src[2 * kk], src[2 * kk + 1], 0x7362);
-        }
-        // byte j of the word -> dim 8dq + 2j + par; nibble n -> 1024 + n - 1032
-        out[0 + par] = make_uint4(bytes_to_h2(a[0], 0x4140, 0x64086408u), bytes_to_h2(a[1], 0x4140, 0x64086408u),
-                                  bytes_to_h2(a[2], 0x4140, 0x64086408u), bytes_to_h2(a[3], 0x4140, 0x64086408u));
-        out[2 + par] = make_uint4(bytes_to_h2(a[0], 0x4342, 0x64086408u), bytes_to_h2(a[1], 0x4342, 0x64086408u),
-                                  bytes_to_h2(a[2], 0x4342, 0x64086408u), bytes_to_h2(a[3], 0x4342, 0x64086408u));
-        out[4 + par] = make_uint4(bytes_to_h2(b[0], 0x4140, 0x64086408u), bytes_to_h2(b[1], 0x4140, 0x64086408u),
-                                  bytes_to_h2(b[2], 0x4140, 0x64086408u), bytes_to_h2(b[3], 0x4140, 0x64086408u));
-        out[6 + par] = make_uint4(bytes_to_h2(b[0], 0x4342, 0x64086408u), bytes_to_h2(b[1], 0x4342, 0x64086408u),
-                                  bytes_to_h2(b[2], 0x4342, 0x64086408u), bytes_to_h2(b[3], 0x4342, 0x64086408u));
-      }
-#pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        const int j = (s + dq) & 7;
-        const int d = 8 * dq + j;
-        *reinterpret_cast<uint4*>(smem + kVfOff + sw128(d, oct)) = pick(out, j);
-      }
-    }
-    // ---- V scales of this tile times a power of two 2^k_ref (warp 0).
-    if (warp == 0) {
-      const float* vs = reinterpret_cast<const float*>(st + kStVs);
-      float mx = 0.f;
-      for (int idx = lane; idx < kTileN * n_vg; idx += 32)
-        if (cell0 + idx / n_vg < pool.n_filled) mx = fmaxf(mx, fabsf(vs[idx]));
-      mx = warp_max(mx);
-      int e = 0;
-      if (mx > 0.f) frexpf(mx, &e);
-      const int k = mx > 0.f ? 4 - e : k_ref;   // max |vs| 2^k in [8, 16)
-      int rho = 0;
-      if (i == 0) k_ref = k;
-      else if (k < k_ref) { rho = k - k_ref; k_ref = k; }
-      for (int idx = lane; idx < kTileN * n_vg; idx += 32) {
-        const int c = idx / n_vg, g = idx % n_vg;
-        vsp[g * kTileN + c] = (cell0 + c < pool.n_filled) ? ldexpf(vs[idx], k_ref) : 0.f;
-      }
-      if (lane == 0) {
-        *s_rho = rho;
-        *s_kref = k_ref;
-      }
-    }
-    tc::fence_proxy_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-
-    // ---- S_g = (Qhi + Qlo) . K over 64-dim group g.
-    if (tid == 0) {
-      tc::fence_after_sync();
-#pragma unroll
-      for (int g = 0; g < 2; ++g) {
-        const uint64_t ah = tc::sw128_desc(sbase + kQhiOff + g * 16384);
-        const uint64_t al = tc::sw128_desc(sbase + kQloOff + g * 16384);
-        const uint64_t bk = tc::sw128_desc(sbase + kKfOff + g * 8192);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          tc::mma_f16(tmem + g * kTileN, ah + 2 * kk, bk + 2 * kk, idesc_s, kk > 0);
-          tc::mma_f16(tmem + g * kTileN, al + 2 * kk, bk + 2 * kk, idesc_s, 1);
-        }
-      }
-      tc::mma_commit(bar_mma);
-      mma_busy = true;
-    }
-    if (!cta_wait(bar_mma, mma_par)) { aborted = true; break; }
-    mma_par ^= 1u;
-    if (tid == 0) mma_busy = false;
-    tc::fence_after_sync();
-
-    // ---- softmax of row r over the tile.
-    float X[kTileN];
-    {
-      const float2* ks = reinterpret_cast<const float2*>(st + kStKs);
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        float s0[32], s1[32];
-        tc::tmem_ld32(tS + 32 * h2, s0);
-        tc::tmem_ld32(tS + kTileN + 32 * h2, s1);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float2 kk = ks[32 * h2 + j];
-          X[32 * h2 + j] = fmaf(s1[j], kk.y, s0[j] * kk.x);
-        }
-      }
-    }
-    const bool full = (cell0 + kTileN - 1 <= pos_first);
-    float ymax = -INFINITY;
-#pragma unroll
-    for (int c = 0; c < kTileN; ++c) {
-      float y = X[c] * lambda;
-      if (!full && cell0 + c > pos) y = -INFINITY;
-      X[c] = y;
-      ymax = fmaxf(ymax, y);
-    }
-    const float m_new = (ymax > m_ref + 8.0f) ? ymax : m_ref;
-    const float alpha = (m_new == m_ref) ? 1.f : exp2f(m_ref - m_new);
-    const int rho = *s_rho;
-    const float factor = ldexpf(alpha, rho);
-    m_ref = m_new;
-    float psum = 0.f;
-#pragma unroll
-    for (int c = 0; c < kTileN; ++c) {
-      const float pc = (X[c] == -INFINITY) ? 0.f : exp2f(X[c] - m_ref);
-      X[c] = pc;
-      psum += pc;
-    }
-    l_run = fmaf(l_run, alpha, psum);
-
-    // ---- W_g = p * vscale_g * 2^k, fp16 hi/lo, then O += W . V per V group.
-    bool pv_ok = true;
-    for (int round = 0; round * 2 < n_vg; ++round) {
-      if (round > 0) {
-        if (!cta_wait(bar_mma, mma_par)) { pv_ok = false; break; }
-        mma_par ^= 1u;
-        if (tid == 0) mma_busy = false;
-        tc::fence_after_sync();
-      }
-#pragma unroll
-      for (int slot = 0; slot < 2; ++slot) {
-        const float* vg = vsp + (round * 2 + slot) * kTileN;
-        uint8_t* whi = smem + kWOff + slot * kWSlot;
-        uint8_t* wlo = whi + 16384;
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          uint32_t hi[4], lo[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            split2(X[8 * ch + 2 * k] * vg[8 * ch + 2 * k], X[8 * ch + 2 * k + 1] * vg[8 * ch + 2 * k + 1], hi[k],
-                   lo[k]);
-          *reinterpret_cast<uint4*>(whi + sw128(r, ch)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(wlo + sw128(r, ch)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        }
-      }
-      tc::fence_proxy_async_smem();
-      tc::fence_before_sync();
-      __syncthreads();
-      if (tid == 0) {
-        tc::fence_after_sync();
-#pragma unroll
-        for (int slot = 0; slot < 2; ++slot) {
-          const int g = round * 2 + slot;
-          const uint64_t ah = tc::sw128_desc(sbase + kWOff + slot * kWSlot);
-          const uint64_t al = tc::sw128_desc(sbase + kWOff + slot * kWSlot + 16384);
-          const uint64_t bv = tc::sw128_desc(sbase + kVfOff + g * vg_dims * 128);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            tc::mma_f16(tmem + 128 + g * vg_dims, ah + 2 * kk, bv + 2 * kk, idesc_o, kk > 0);
-            tc::mma_f16(tmem + 128 + g * vg_dims, al + 2 * kk, bv + 2 * kk, idesc_o, 1);
-          }
-        }
-        tc::mma_commit(bar_mma);
-        mma_busy = true;
-      }
-    }
-    if (!pv_ok) { aborted = true; break; }
-    if (!cta_wait(bar_mma, mma_par)) { aborted = true; break; }
-    mma_par ^= 1u;
-    if (tid == 0) mma_busy = false;
-    tc::fence_after_sync();
-    // ---- O = O * factor + P (row r, 128 dims), fp32 round-to-nearest.
-#pragma unroll
-    for (int h4 = 0; h4 < 4; ++h4) {
-      float pv[32], o[32];
-      tc::tmem_ld32(tP + 32 * h4, pv);
-      if (i > 0) tc::tmem_ld32(tO + 32 * h4, o);
-      tc::tmem_wait_ld();
-      if (i > 0) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) o[j] = fmaf(o[j], factor, pv[j]);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) o[j] = pv[j];
-      }
-      tc::tmem_st32(tO + 32 * h4, o);
-    }
-    tc::tmem_wait_st();
-    tc::fence_before_sync();
-    tc::fence_proxy_async_smem();
-  }
-
-  if (aborted) {
-    if (tid == 0) {
-      raise_device_error(1);
-      for (int s = 0; s < 2; ++s)
-        if (st_busy[s]) tc::mbar_wait(bar_st0 + 8 * s, st_par[s], kDrainLimitNs);
-      if (mma_busy) tc::mbar_wait(bar_mma, mma_par, kDrainLimitNs);
-    }
-    __syncthreads();
-  } else {
-    // ---- out = O 2^-k / l, lse = (m + log2 l) ln 2.
-    const float scale = ldexpf(1.f / l_run, -*s_kref);
-    float* orow = p.out + ((size_t)qi * p.n_q_heads + head) * kD;
-#pragma unroll
-    for (int h4 = 0; h4 < 4; ++h4) {
-      float o[32];
-      tc::tmem_ld32(tO + 32 * h4, o);
-      tc::tmem_wait_ld();
-      if (row_valid) {
-#pragma unroll
-        for (int j = 0; j < 32; j += 4)
-          *reinterpret_cast<float4*>(orow + 32 * h4 + j) =
-              make_float4(o[j] * scale, o[j + 1] * scale, o[j + 2] * scale, o[j + 3] * scale);
-      }
-    }
-    if (row_valid && p.lse) p.lse[(size_t)qi * p.n_q_heads + head] = (m_ref + log2f(l_run)) * kLn2;
-  }
-  tc::fence_before_sync();
-  __syncthreads();
-  if (warp == 0) {
-    tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, kTmemCols);
-  }
-}
 
 }  // namespace
 
@@ -651,9 +178,14 @@ __global__ void __launch_bounds__(64) prompt_vmax_kernel(const PoolDev pool, int
   float mv = 0.f, mk = 0.f;
   if (cell < pool.n_filled) {
     const long long slot = cell_slot(pool, n_kv_heads, h, cell);
-    const float2 vs = __ldg(reinterpret_cast<const float2*>(pool.v_scales) + slot);
+    if (pool.v_bits == 8) {
+      const float2 vs = __ldg(reinterpret_cast<const float2*>(pool.v_scales) + slot);
+      mv = fmaxf(fabsf(vs.x), fabsf(vs.y));
+    } else {
+      const float4 vs = __ldg(reinterpret_cast<const float4*>(pool.v_scales) + slot);
+      mv = fmaxf(fmaxf(fabsf(vs.x), fabsf(vs.y)), fmaxf(fabsf(vs.z), fabsf(vs.w)));
+    }
     const float2 ks = __ldg(reinterpret_cast<const float2*>(pool.k_scales) + slot);
-    mv = fmaxf(fabsf(vs.x), fabsf(vs.y));
     mk = fmaxf(fabsf(ks.x), fabsf(ks.y));
   }
   mv = warp_max(mv);
@@ -694,6 +226,28 @@ __device__ __forceinline__ void write_scaled_row(const uint4 (&v)[4], float sc, 
   }
 }
 
+// 4-bit codes (32 bytes: byte j holds dim 2j in its low nibble and 2j + 1 in its high nibble,
+// nibble = code + 8) of 64 dims, dims 0..31 scaled by sc0 and 32..63 by sc1 -> fp16 hi + lo row.
+__device__ __forceinline__ void write_scaled_row4(const uint4 (&v)[2], float sc0, float sc1, uint8_t* dhi,
+                                                  uint8_t* dlo, int cc) {
+#pragma unroll
+  for (int s4 = 0; s4 < 4; ++s4) {   // 16 dims = 8 bytes
+    const uint4& q = v[s4 >> 1];
+    const uint32_t w0 = (s4 & 1) ? q.z : q.x, w1 = (s4 & 1) ? q.w : q.y;
+    const float sc = s4 < 2 ? sc0 : sc1;
+    uint32_t hi[8], lo[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t b = ((k < 4 ? w0 : w1) >> (8 * (k & 3))) & 0xFFu;
+      split2((float)((int)(b & 15u) - 8) * sc, (float)((int)(b >> 4) - 8) * sc, hi[k], lo[k]);
+    }
+    *reinterpret_cast<uint4*>(dhi + sw128(cc, 2 * s4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4*>(dhi + sw128(cc, 2 * s4 + 1)) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+    *reinterpret_cast<uint4*>(dlo + sw128(cc, 2 * s4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    *reinterpret_cast<uint4*>(dlo + sw128(cc, 2 * s4 + 1)) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+  }
+}
+
 // One CTA per (64-cell tile, KV head), 128 threads: thread (cell ct / 2, dim block ct % 2 = scale
 // group).
 __global__ void __launch_bounds__(128) prompt_stage_kernel(const PoolDev pool, int n_kv_heads, int n_tiles,
@@ -715,14 +269,26 @@ __global__ void __launch_bounds__(128) prompt_stage_kernel(const PoolDev pool, i
     for (int s4 = 0; s4 < 4; ++s4) v[s4] = valid ? __ldg(src + s4) : make_uint4(0u, 0u, 0u, 0u);
     write_scaled_row(v, sc, img + kImgKhi + hf * 8192, img + kImgKlo + hf * 8192, cc);
   }
-  // V' = vcode * vscale * 2^kv_h
-  {
-    const float sc = valid ? __ldg(pool.v_scales + (slot0 + cc) * 2 + hf) * pow2f(head_scale_exp(scratch, h)) : 0.f;
+  // V' = vcode * vscale * 2^kv_h (int8 V: one scale per 64 dims; 4-bit V: one per 32 dims)
+  const float vsh = pow2f(head_scale_exp(scratch, h));
+  if (pool.v_bits == 8) {
+    const float sc = valid ? __ldg(pool.v_scales + (slot0 + cc) * 2 + hf) * vsh : 0.f;
     const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(pool.v_codes) +
                                                       (slot0 + cc) * kD + hf * 64);
 #pragma unroll
     for (int s4 = 0; s4 < 4; ++s4) v[s4] = valid ? __ldg(src + s4) : make_uint4(0u, 0u, 0u, 0u);
     write_scaled_row(v, sc, img + kImgVhi + hf * 8192, img + kImgVlo + hf * 8192, cc);
+  } else {
+    float2 sc = make_float2(0.f, 0.f);
+    uint4 v4[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+    if (valid) {
+      sc = __ldg(reinterpret_cast<const float2*>(pool.v_scales + (slot0 + cc) * 4 + 2 * hf));
+      const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(pool.v_codes) +
+                                                        (slot0 + cc) * 64 + hf * 32);
+      v4[0] = __ldg(src);
+      v4[1] = __ldg(src + 1);
+    }
+    write_scaled_row4(v4, sc.x * vsh, sc.y * vsh, img + kImgVhi + hf * 8192, img + kImgVlo + hf * 8192, cc);
   }
 }
 
@@ -936,7 +502,6 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
       if (ok) ok = wait_b(c, S_FULL + sl, (i >> 1) & 1, limit);
       if (!__all_sync(0xffffffffu, ok && !c.w[C_ABORT])) { alive = false; break; }
       tc::fence_after_sync();
-      const uint8_t* img = smem + kStage0 + st * kImgBytes;
       const int cell0 = i * kN;
       const uint32_t ts = tl + kTS + 64 * sl;
       // ---- logits of the tile's 64 cells (scaled by lambda below)
@@ -1048,34 +613,27 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
 }  // namespace ws
 
 size_t prompt_scratch_bytes(int v_bits, int n_kv_heads, int q_end_pos) {
-  if (v_bits != 8 || q_end_pos <= 0) return 0;
+  if ((v_bits != 8 && v_bits != 4) || q_end_pos <= 0) return 0;
   const int n_tiles = (q_end_pos - 1) / ws::kN + 1;
   return (size_t)ws::kScratchHeader + (size_t)n_kv_heads * n_tiles * ws::kImgBytes;
 }
 
-
 cudaError_t launch_prompt_attn(const PromptParams& p, cudaStream_t stream) {
   const int G = p.n_q_heads / p.n_kv_heads;
-  const int qpc = kM / G;
-  dim3 grid((p.n_q + qpc - 1) / qpc, p.n_kv_heads);
-  if (p.pool.v_bits == 8) {
-    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(ws::prompt_attn_ws_kernel), (size_t)ws::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    e = cudaMemsetAsync(p.scratch, 0, ws::kScratchHeader, stream);
-    if (e != cudaSuccess) return e;
-    ws::prompt_vmax_kernel<<<dim3(p.n_tiles, p.n_kv_heads), 64, 0, stream>>>(p.pool, p.n_kv_heads, p.scratch);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    ws::prompt_stage_kernel<<<dim3(p.n_tiles, p.n_kv_heads), 128, 0, stream>>>(p.pool, p.n_kv_heads, p.n_tiles,
-                                                                                p.scratch);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    ws::prompt_attn_ws_kernel<<<grid, ws::kThreads, ws::kSmemBytes, stream>>>(p);
-    return cudaGetLastError();
-  }
-  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(prompt_attn_kernel), (size_t)kSmemBytes);
+  const int qpc = ws::kM / G;
+  const dim3 grid((p.n_q + qpc - 1) / qpc, p.n_kv_heads);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(ws::prompt_attn_ws_kernel), (size_t)ws::kSmemBytes);
   if (e != cudaSuccess) return e;
-  prompt_attn_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p);
+  e = cudaMemsetAsync(p.scratch, 0, ws::kScratchHeader, stream);
+  if (e != cudaSuccess) return e;
+  ws::prompt_vmax_kernel<<<dim3(p.n_tiles, p.n_kv_heads), 64, 0, stream>>>(p.pool, p.n_kv_heads, p.scratch);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  ws::prompt_stage_kernel<<<dim3(p.n_tiles, p.n_kv_heads), 128, 0, stream>>>(p.pool, p.n_kv_heads, p.n_tiles,
+                                                                              p.scratch);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  ws::prompt_attn_ws_kernel<<<grid, ws::kThreads, ws::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
 

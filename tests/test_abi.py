@@ -99,8 +99,8 @@ def test_decode_attn_validation(lib):
 def test_prompt_validation(lib):
     pool = _pool(n_filled=1000, capacity=1024)
     need = lib.qsa_prompt_scratch_bytes(ctypes.byref(pool), 100, 900)
-    assert need == 256 + 4 * (999 // 64 + 1) * 65536                # int8 V: one tile image per tile and head
-    assert lib.qsa_prompt_scratch_bytes(ctypes.byref(_pool(v_bits=4, n_filled=1000, capacity=1024)), 100, 900) == 0
+    assert need == 256 + 4 * (999 // 64 + 1) * 65536                # one tile image per tile and head
+    assert lib.qsa_prompt_scratch_bytes(ctypes.byref(_pool(v_bits=4, n_filled=1000, capacity=1024)), 100, 900) == need
     ok = dict(scratch=1 << 20, nbytes=need)
 
     def call(pl, q_pos0, n_q, Hq=24, scratch=None, nbytes=None):
