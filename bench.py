@@ -401,7 +401,7 @@ def run_ours(args):
         pq = torch.from_numpy(pcase.q).to(dev)
         pout = torch.empty((call[1], pcase.n_q_heads, 128), device=dev)
         plse = torch.empty((call[1], pcase.n_q_heads), device=dev)
-        pscratch = torch.empty(max(1, qsa.prompt_scratch_bytes(ppool, call[1], call[2])), dtype=torch.uint8,
+        pscratch = torch.empty(max(1, qsa.prompt_scratch_bytes(ppool, call[1], call[2], pcase.n_q_heads)), dtype=torch.uint8,
                                device=dev)
         for _ in range(2):
             qsa.prompt_attn(ppool, pq, call[2], pout, plse, scratch=pscratch)

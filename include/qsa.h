@@ -245,12 +245,17 @@ qsa_status qsa_decode_window_profile(const qsa_pool* pools, int n_pools, const i
  *   pool       (host) one descriptor; page_cells multiple of 64
  *   q          (dev)  fp32 [n_q][n_q_heads][128], 16-byte aligned
  *   scratch    (dev)  caller-owned work space of scratch_bytes >=
- *                     qsa_prompt_scratch_bytes(pool, n_q, q_pos0), 256-byte
+ *                     qsa_prompt_scratch_bytes(pool, n_q, q_pos0, n_q_heads), 256-byte
  *                     aligned.  The call first converts every 64-cell tile it reads,
  *                     once per KV head, into the operand images the tensor
  *                     cores load: K' = kcode * kscale * 2^a and V' = vcode *
  *                     vscale * 2^b as fp16 hi + lo, with powers of two a, b
- *                     per KV head.
+ *                     per KV head.  Work runs as one CTA per (block of
+ *                     128 / group queries, KV head); when the last round of
+ *                     CTAs would leave SMs idle, its units are cut into equal
+ *                     ranges of tiles whose partial rows (unnormalised output,
+ *                     running max, row sum) also live in scratch and are
+ *                     combined by log-sum-exp in range order.
  *   out        (dev)  fp32 [n_q][n_q_heads][128], 16-byte aligned
  *   lse        (dev)  fp32 [n_q][n_q_heads], may be NULL
  *   q_pos0 >= 0, q_pos0 + n_q <= pool->n_filled
@@ -265,11 +270,14 @@ qsa_status qsa_prompt_attn(const qsa_pool* pool, const float* q, int n_q, int q_
 
 /*
  * qsa_prompt_scratch_bytes -- device scratch bytes qsa_prompt_attn needs for
- * a call of n_q queries from position q_pos0 over `pool`: a 256-byte header
- * plus 65,536 bytes per 64-cell tile of cells 0 .. q_pos0 + n_q - 1 per KV
- * head (int8 and 4-bit V alike).  Returns 0 for invalid arguments.
+ * a call of n_q >= 1 queries of n_q_heads heads from position q_pos0 over
+ * `pool`, on the current device: a 256-byte header, 65,536 bytes per 64-cell
+ * tile of cells 0 .. q_pos0 + n_q - 1 per KV head (int8 and 4-bit V alike),
+ * and 66,560 bytes per partial range of a cut unit (their number depends on
+ * the device's SM count; none without a device).  Returns 0 for invalid
+ * arguments.
  */
-size_t qsa_prompt_scratch_bytes(const qsa_pool* pool, int n_q, int q_pos0);
+size_t qsa_prompt_scratch_bytes(const qsa_pool* pool, int n_q, int q_pos0, int n_q_heads);
 
 /* Size of the library-owned scratch of qsa_decode_attn_noalloc (8 MiB). */
 #define QSA_NOALLOC_SCRATCH_BYTES (8u << 20)

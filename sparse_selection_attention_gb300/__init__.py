@@ -67,7 +67,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qsa_decode_attn.argtypes = [pool_p, i, i32p, p, p, p, p, i, i, i, i, i, p, sz, p]
     lib.qsa_attn_merge.argtypes = [p, p, i, i, i, i, p, p, p]
     lib.qsa_prompt_attn.argtypes = [pool_p, p, i, i, i, p, sz, p, p, p]
-    lib.qsa_prompt_scratch_bytes.argtypes = [pool_p, i, i]
+    lib.qsa_prompt_scratch_bytes.argtypes = [pool_p, i, i, i]
     lib.qsa_prompt_scratch_bytes.restype = sz
     lib.qsa_decode_attn_noalloc.argtypes = [pool_p, i, i32p, p, p, p, p, i, i, i, i, p, p, p]
     lib.qsa_decode_window.argtypes = [pool_p, i, i32p, p, p, i, i, i, i, p, i, p, p, p, p, p, sz, p]
@@ -179,9 +179,10 @@ def attn_merge(partials: torch.Tensor, n_sel: torch.Tensor, n_rows: int, n_q_hea
                                  _ptr(lse), _stream(stream)), "qsa_attn_merge")
 
 
-def prompt_scratch_bytes(pool: DevicePool, n_q: int, q_pos0: int) -> int:
+def prompt_scratch_bytes(pool: DevicePool, n_q: int, q_pos0: int, n_q_heads: int) -> int:
+    """Scratch bytes of a prompt call on the current device (0 for invalid arguments)."""
     pc = pool.c()
-    return int(load().qsa_prompt_scratch_bytes(ctypes.byref(pc), n_q, q_pos0))
+    return int(load().qsa_prompt_scratch_bytes(ctypes.byref(pc), n_q, q_pos0, n_q_heads))
 
 
 def prompt_attn(pool: DevicePool, q: torch.Tensor, q_pos0: int, out: torch.Tensor,
@@ -191,7 +192,7 @@ def prompt_attn(pool: DevicePool, q: torch.Tensor, q_pos0: int, out: torch.Tenso
     n_q, Hq, _ = q.shape
     pc = pool.c()
     if scratch is None:
-        need = prompt_scratch_bytes(pool, n_q, q_pos0)
+        need = prompt_scratch_bytes(pool, n_q, q_pos0, Hq)
         scratch = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     _check(load().qsa_prompt_attn(ctypes.byref(pc), _ptr(q), n_q, q_pos0, Hq, _ptr(scratch), scratch.numel(),
                                   _ptr(out), _ptr(lse), _stream(stream)), "qsa_prompt_attn")

@@ -349,9 +349,11 @@ qsa_status qsa_decode_window_profile(const qsa_pool* pools, int n_pools, const i
                             max_blocks, ids, n_sel, out, lse, workspace, workspace_bytes, stream, kernel_us);
 }
 
-size_t qsa_prompt_scratch_bytes(const qsa_pool* pool, int n_q, int q_pos0) {
-  if (!pool || n_q < 0 || q_pos0 < 0 || pool->n_kv_heads < 1) return 0;
-  return prompt_scratch_bytes(pool->v_bits, pool->n_kv_heads, q_pos0 + n_q);
+size_t qsa_prompt_scratch_bytes(const qsa_pool* pool, int n_q, int q_pos0, int n_q_heads) {
+  PromptPlan plan;
+  if (!pool || !prompt_plan(pool->v_bits, pool->n_kv_heads, n_q_heads, n_q, q_pos0, device_sm_count(), &plan))
+    return 0;
+  return plan.bytes;
 }
 
 qsa_status qsa_prompt_attn(const qsa_pool* pool, const float* q, int n_q, int q_pos0, int n_q_heads, void* scratch,
@@ -363,11 +365,19 @@ qsa_status qsa_prompt_attn(const qsa_pool* pool, const float* q, int n_q, int q_
   if (n_q_heads < 1 || n_q_heads % pool->n_kv_heads != 0) return QSA_ERR_ARG;
   if (n_q_heads / pool->n_kv_heads > 128) return QSA_ERR_UNSUPPORTED;
   if (n_q == 0) return QSA_OK;
-  const size_t need = prompt_scratch_bytes(pool->v_bits, pool->n_kv_heads, q_pos0 + n_q);
-  if (need > 0 && (!scratch || (reinterpret_cast<uintptr_t>(scratch) & 255u) != 0 || scratch_bytes < need))
+  PromptPlan plan;
+  if (!prompt_plan(pool->v_bits, pool->n_kv_heads, n_q_heads, n_q, q_pos0, device_sm_count(), &plan))
+    return QSA_ERR_ARG;
+  if (!scratch || (reinterpret_cast<uintptr_t>(scratch) & 255u) != 0 || scratch_bytes < plan.bytes)
     return QSA_ERR_SCRATCH;
   PromptParams p{};
   p.scratch = static_cast<uint8_t*>(scratch);
+  p.qpc = plan.qpc;
+  p.n_qb = plan.n_qb;
+  p.n_whole = plan.n_whole;
+  p.n_split = plan.n_split;
+  p.part_o = reinterpret_cast<float*>(p.scratch + plan.parts_offset);
+  p.part_ml = reinterpret_cast<float*>(p.scratch + plan.ml_offset);
   p.n_tiles = (q_pos0 + n_q - 1) / 64 + 1;
   p.pool = to_dev(*pool);
   p.n_kv_heads = pool->n_kv_heads;
@@ -402,6 +412,6 @@ const char* qsa_status_str(qsa_status s) {
   return "unknown status";
 }
 
-int qsa_abi_version(void) { return 102; }
+int qsa_abi_version(void) { return 103; }
 
 }  // extern "C"

@@ -54,9 +54,21 @@ struct PromptParams {
   const float* q;
   float* out;
   float* lse;
-  uint8_t* scratch;   // tile images of the int8-V path (prompt_scratch_bytes)
+  uint8_t* scratch;   // header, tile images and part records (prompt_scratch_bytes)
   int n_tiles;        // 64-cell tiles the call reads: (q_pos0 + n_q - 1) / 64 + 1
+  // Work units: (block of qpc queries, KV head), unit u = kv_head * n_qb + query block.  Units below
+  // n_whole run as one CTA each; each later unit runs as n_split CTAs over equal tile ranges whose
+  // partial rows go to part_o / part_ml and are combined by prompt_merge_kernel.
+  int qpc, n_qb, n_whole, n_split;
+  float* part_o;      // [n_parts][128 rows][128]  unnormalised O of a part, in output units
+  float* part_ml;     // [n_parts][128 rows][2]    (running max m in log2 units, row sum l)
   unsigned long long wait_limit_ns;
+};
+
+// How a prompt call is cut into CTAs for a device with n_sm SMs, and the scratch it needs.
+struct PromptPlan {
+  int qpc, n_qb, n_units, n_whole, n_split, n_parts;
+  size_t images_offset, parts_offset, ml_offset, bytes;
 };
 
 // Split attention + fused merge of a decode window (qsa_decode_window).
@@ -97,7 +109,7 @@ cudaError_t launch_decode_window(const WindowArgs& a, cudaStream_t stream, cudaE
 // Top-k launch; with pdl the launch may start before the preceding kernel of the stream ends.
 cudaError_t launch_topk_ex(const TopkParams& p, int max_nb, cudaStream_t stream, bool pdl);
 
-size_t prompt_scratch_bytes(int v_bits, int n_kv_heads, int q_end_pos);
+bool prompt_plan(int v_bits, int n_kv_heads, int n_q_heads, int n_q, int q_pos0, int n_sm, PromptPlan* plan);
 size_t block_scores_smem_bytes(int n_rows, int n_q_heads, int n_kv_heads, int block_cells);
 bool block_scores_supported(int n_kv_heads, int block_cells);
 int block_scores_q_rows_per_batch(int n_rows, int n_q_heads, int n_kv_heads, int block_cells);

@@ -11,6 +11,8 @@
 // int8 and 4-bit V codes take the same path (the image holds V').
 #include <cuda_fp16.h>
 
+#include <algorithm>
+
 #include "kernels.h"
 #include "tc.cuh"
 
@@ -297,16 +299,33 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = tc::smem_u32(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int Hkv = p.n_kv_heads;
-  const int G = p.n_q_heads / Hkv;
-  const int QPC = kM / G;
-  const int kvh = blockIdx.y;
-  const int q_begin = blockIdx.x * QPC;
+  const int G = p.n_q_heads / p.n_kv_heads;
+  const int QPC = p.qpc;
+  // This CTA's work: unit u (query block, KV head) over tiles [t0, t0 + n_tiles); part >= 0 for a
+  // unit split across n_split CTAs (part-major order, so concurrent CTAs walk the same tiles).
+  int u = blockIdx.x, part = -1;
+  if (u >= p.n_whole) {
+    const int n_tail = p.n_qb * p.n_kv_heads - p.n_whole;
+    part = u - p.n_whole;
+    u = p.n_whole + part % n_tail;
+  }
+  const int kvh = u / p.n_qb;
+  const int q_begin = (u % p.n_qb) * QPC;
   const int q_end = min(p.n_q, q_begin + QPC);
   const int pos_first = p.q_pos0 + q_begin;
   const int pos_last = p.q_pos0 + q_end - 1;
-  const int n_tiles = pos_last / kN + 1;
+  const int unit_tiles = pos_last / kN + 1;
+  int t0 = 0, n_tiles = unit_tiles;
+  if (part >= 0) {
+    const int k = part / (p.n_qb * p.n_kv_heads - p.n_whole);
+    t0 = (int)((long long)k * unit_tiles / p.n_split);
+    n_tiles = (int)((long long)(k + 1) * unit_tiles / p.n_split) - t0;
+  }
   const uint64_t limit = p.wait_limit_ns;
+
+  // The part merge (launched after this grid) may be scheduled once every CTA has started; it
+  // waits for this grid to complete before it reads anything.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   Ctl c;
   c.bars = sbase + kCtl;
@@ -381,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
   // =========================================================== producer
     if (warp == 0) {
       if (lane == 0) {
-        const uint8_t* img0 = p.scratch + kScratchHeader + (size_t)kvh * p.n_tiles * kImgBytes;
+        const uint8_t* img0 = p.scratch + kScratchHeader + ((size_t)kvh * p.n_tiles + t0) * kImgBytes;
         int issued = 0;
         for (int i = 0; i < n_tiles; ++i) {
           const int st = i % kStages;
@@ -502,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
       if (ok) ok = wait_b(c, S_FULL + sl, (i >> 1) & 1, limit);
       if (!__all_sync(0xffffffffu, ok && !c.w[C_ABORT])) { alive = false; break; }
       tc::fence_after_sync();
-      const int cell0 = i * kN;
+      const int cell0 = (t0 + i) * kN;
       const uint32_t ts = tl + kTS + 64 * sl;
       // ---- logits of the tile's 64 cells (scaled by lambda below)
       float X[64];
@@ -531,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
         // warp stops at its next wait.)
         wait_b(c, S_EMPTY + ((i - 1) & 1), ((i - 1) >> 1) & 1, limit);
         tc::fence_after_sync();
-        const float fo = o_empty ? 0.f : ex2(m_O - m_P);
+        const float fo = (o_empty || m_O == -INFINITY) ? 0.f : ex2(m_O - m_P);
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
           float pv[16], ov[16];
@@ -554,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
       // row sum of p = P' 2^-kPShift
       {
         const uint64_t lam2 = pk(lambda, lambda);
-        const float nm = (float)kPShift - m_P;
+        const float nm = m_P == -INFINITY ? 0.f : (float)kPShift - m_P;   // every X is -inf then
         const uint64_t nm2 = pk(nm, nm);
         uint64_t ps[4] = {0ull, 0ull, 0ull, 0ull};   // packed partial sums, four independent chains
 #pragma unroll
@@ -579,13 +598,15 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
       __syncwarp();
       if (lane == 0) arrive(c, W_FULL + sl);
     }
-    // ---- epilogue: after the last P.V, out = (O 2^(m_O - m) + P) / l, lse = (m - k + log2 l) ln 2.
+    // ---- epilogue: after the last P.V, out = (O 2^(m_O - m) + P) / l, lse = (m + log2 l) ln 2;
+    // a part writes (O 2^(m_O - m) + P) unnormalised with (m, l) for prompt_merge_kernel.
     if (alive) {
       wait_b(c, S_EMPTY + ((n_tiles - 1) & 1), ((n_tiles - 1) >> 1) & 1, limit);
       tc::fence_after_sync();
-      const float fo = o_empty ? 0.f : ex2(m_O - m_P);
-      const float scale = out_scale / l;
-      float* orow = p.out + ((size_t)qi * p.n_q_heads + head) * kD;
+      const float fo = (o_empty || m_O == -INFINITY) ? 0.f : ex2(m_O - m_P);
+      const float scale = part >= 0 ? out_scale : out_scale / l;
+      float* orow = part >= 0 ? p.part_o + ((size_t)part * kM + r) * kD
+                              : p.out + ((size_t)qi * p.n_q_heads + head) * kD;
 #pragma unroll
       for (int c4 = 0; c4 < 8; ++c4) {
         float pv[16], ov[16];
@@ -602,7 +623,10 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
           }
         }
       }
-      if (row_valid && p.lse) p.lse[(size_t)qi * p.n_q_heads + head] = (m_P + log2f(l)) * kLn2;
+      if (row_valid && part >= 0)
+        *reinterpret_cast<float2*>(p.part_ml + ((size_t)part * kM + r) * 2) = make_float2(m_P, l);
+      else if (row_valid && p.lse)
+        p.lse[(size_t)qi * p.n_q_heads + head] = (m_P + log2f(l)) * kLn2;
     }
   }
   tc::fence_before_sync();
@@ -610,18 +634,96 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
   __syncthreads();
 }
 
+// Combines the n_split parts of each split unit, one CTA per unit, one warp per row at a time
+// (four output dims a lane): with w_k = 2^(m_k - M), M = max_k m_k,
+//   out = sum_k w_k O_k / sum_k w_k l_k,   lse = (M + log2 sum_k w_k l_k) ln 2,
+// summed in part order (the result does not depend on which part finished first).
+__global__ void __launch_bounds__(128) prompt_merge_kernel(const PromptParams p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int n_tail = p.n_qb * p.n_kv_heads - p.n_whole;
+  const int v = blockIdx.x, u = p.n_whole + v;
+  const int G = p.n_q_heads / p.n_kv_heads;
+  const int kvh = u / p.n_qb, q_begin = (u % p.n_qb) * p.qpc;
+  const int rows = (min(p.n_q, q_begin + p.qpc) - q_begin) * G;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int r = warp; r < rows; r += 4) {
+    float M = -INFINITY;
+    for (int k = 0; k < p.n_split; ++k) M = fmaxf(M, p.part_ml[((size_t)(k * n_tail + v) * kM + r) * 2]);
+    float L = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < p.n_split; ++k) {
+      const size_t rec = (size_t)(k * n_tail + v) * kM + r;
+      const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + rec * 2);
+      const float w = ml.x == -INFINITY ? 0.f : ex2(ml.x - M);
+      const float4 ov = reinterpret_cast<const float4*>(p.part_o + rec * kD)[lane];
+      L = fmaf(w, ml.y, L);
+      o = make_float4(fmaf(w, ov.x, o.x), fmaf(w, ov.y, o.y), fmaf(w, ov.z, o.z), fmaf(w, ov.w, o.w));
+    }
+    const float inv = 1.f / L;
+    const int qi = q_begin + r / G, head = kvh * G + r % G;
+    reinterpret_cast<float4*>(p.out + ((size_t)qi * p.n_q_heads + head) * kD)[lane] =
+        make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+    if (p.lse && lane == 0) p.lse[(size_t)qi * p.n_q_heads + head] = (M + log2f(L)) * kLn2;
+  }
+}
+
+// A split unit's CTA costs this many tiles beyond its share (prologue, pipeline fill and drain).
+constexpr int kPartOverheadTiles = 4;
+constexpr int kMinPartTiles = 8;
+constexpr int kMaxSplit = 8;
+
 }  // namespace ws
 
-size_t prompt_scratch_bytes(int v_bits, int n_kv_heads, int q_end_pos) {
-  if ((v_bits != 8 && v_bits != 4) || q_end_pos <= 0) return 0;
-  const int n_tiles = (q_end_pos - 1) / ws::kN + 1;
-  return (size_t)ws::kScratchHeader + (size_t)n_kv_heads * n_tiles * ws::kImgBytes;
+// Units (query block, KV head) run in rounds of n_sm CTAs; when the last round is partly empty,
+// its units are each cut into n_split equal tile ranges (the n_split minimising the modelled
+// finish time of the tail: rounds of parts x (tiles per part + overhead)), and the parts' rows
+// are merged by one more launch.
+bool prompt_plan(int v_bits, int n_kv_heads, int n_q_heads, int n_q, int q_pos0, int n_sm, PromptPlan* plan) {
+  if ((v_bits != 8 && v_bits != 4) || n_kv_heads < 1 || n_q_heads < 1 || n_q_heads % n_kv_heads != 0 ||
+      n_q_heads / n_kv_heads > ws::kM || n_q < 1 || q_pos0 < 0 || n_sm < 1 || !plan)
+    return false;
+  PromptPlan pl{};
+  pl.qpc = ws::kM / (n_q_heads / n_kv_heads);
+  pl.n_qb = (n_q + pl.qpc - 1) / pl.qpc;
+  pl.n_units = pl.n_qb * n_kv_heads;
+  pl.n_whole = pl.n_units;
+  pl.n_split = 1;
+  const int n_tail = pl.n_units % n_sm;
+  if (n_tail > 0) {
+    int l_min = 1 << 30;
+    double l_sum = 0.0;
+    for (int u = pl.n_units - n_tail; u < pl.n_units; ++u) {
+      const int qb = u % pl.n_qb;
+      const int l = (q_pos0 + std::min(n_q, (qb + 1) * pl.qpc) - 1) / ws::kN + 1;
+      l_min = std::min(l_min, l);
+      l_sum += l;
+    }
+    const double l_avg = l_sum / n_tail;
+    double best = 0.0;
+    for (int s = 1; s <= ws::kMaxSplit && (s == 1 || l_min / s >= ws::kMinPartTiles); ++s) {
+      const double cost = (double)((n_tail * s + n_sm - 1) / n_sm) * (l_avg / s + ws::kPartOverheadTiles);
+      if (s == 1 || cost < best) {
+        best = cost;
+        pl.n_split = s;
+      }
+    }
+    if (pl.n_split > 1) {
+      pl.n_whole = pl.n_units - n_tail;
+      pl.n_parts = n_tail * pl.n_split;
+    }
+  }
+  const int n_tiles = (q_pos0 + n_q - 1) / ws::kN + 1;
+  pl.images_offset = ws::kScratchHeader;
+  pl.parts_offset = pl.images_offset + (size_t)n_kv_heads * n_tiles * ws::kImgBytes;
+  pl.ml_offset = pl.parts_offset + (size_t)pl.n_parts * ws::kM * kD * sizeof(float);
+  pl.bytes = pl.ml_offset + (size_t)pl.n_parts * ws::kM * 2 * sizeof(float);
+  *plan = pl;
+  return true;
 }
 
 cudaError_t launch_prompt_attn(const PromptParams& p, cudaStream_t stream) {
-  const int G = p.n_q_heads / p.n_kv_heads;
-  const int qpc = ws::kM / G;
-  const dim3 grid((p.n_q + qpc - 1) / qpc, p.n_kv_heads);
+  const int n_tail = p.n_qb * p.n_kv_heads - p.n_whole;
+  const dim3 grid(p.n_whole + (p.n_split > 1 ? n_tail * p.n_split : 0));
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(ws::prompt_attn_ws_kernel), (size_t)ws::kSmemBytes);
   if (e != cudaSuccess) return e;
   e = cudaMemsetAsync(p.scratch, 0, ws::kScratchHeader, stream);
@@ -634,7 +736,18 @@ cudaError_t launch_prompt_attn(const PromptParams& p, cudaStream_t stream) {
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   ws::prompt_attn_ws_kernel<<<grid, ws::kThreads, ws::kSmemBytes, stream>>>(p);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e != cudaSuccess || p.n_split <= 1) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_tail);
+  cfg.blockDim = dim3(128);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, ws::prompt_merge_kernel, p);
 }
 
 int* device_error_word() {

@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_pure_host_calls(lib):
-    assert qsa.abi_version() == 102
+    assert qsa.abi_version() == 103
     assert qsa.status_str(qsa.QSA_ERR_SCRATCH) == "scratch buffer too small"
     assert qsa.decode_partials_bytes(5, 24, 64) == 4 * 5 * 24 * 64 * 130
     assert qsa.decode_partials_bytes(0, 24, 64) == 0
@@ -98,9 +98,12 @@ def test_decode_attn_validation(lib):
 
 def test_prompt_validation(lib):
     pool = _pool(n_filled=1000, capacity=1024)
-    need = lib.qsa_prompt_scratch_bytes(ctypes.byref(pool), 100, 900)
-    assert need == 256 + 4 * (999 // 64 + 1) * 65536                # one tile image per tile and head
-    assert lib.qsa_prompt_scratch_bytes(ctypes.byref(_pool(v_bits=4, n_filled=1000, capacity=1024)), 100, 900) == need
+    need = lib.qsa_prompt_scratch_bytes(ctypes.byref(pool), 100, 900, 24)
+    # one tile image per tile and head; no partial ranges without a device (its SM count decides them)
+    assert need == 256 + 4 * (999 // 64 + 1) * 65536
+    assert lib.qsa_prompt_scratch_bytes(ctypes.byref(_pool(v_bits=4, n_filled=1000, capacity=1024)), 100, 900, 24) == need
+    assert lib.qsa_prompt_scratch_bytes(ctypes.byref(pool), 100, 900, 26) == 0      # not a multiple of the KV heads
+    assert lib.qsa_prompt_scratch_bytes(ctypes.byref(pool), 0, 900, 24) == 0
     ok = dict(scratch=1 << 20, nbytes=need)
 
     def call(pl, q_pos0, n_q, Hq=24, scratch=None, nbytes=None):

@@ -34,6 +34,10 @@ def run_prompt(case, call):
     (64, 64, 2, 1, 8, 64),         # one tile, queries from position 0
     (1000, 37, 6, 6, 8, 128),      # G = 1
     (333, 333, 16, 1, 4, 64),      # G = 16, whole context is the prompt
+    # fewer units than SMs: each unit cut into tile ranges merged by log-sum-exp
+    (2000, 300, 2, 1, 8, 64),      # G = 2: 5 units of 27..32 tiles, 3 ranges each (ragged range ends)
+    (3000, 64, 8, 2, 4, 128),      # 4-bit V, G = 4: 4 units of 47 tiles, 5 ranges each
+    (1500, 1500, 4, 4, 8, 64),     # queries from position 0: units from 1 to 24 tiles, cut by the shortest
 ])
 def test_small_prompt_full(n_ctx, n_q, Hq, Hkv, v_bits, page_cells):
     case = W.prompt_case(name="p", seed=n_ctx + n_q, n_ctx=n_ctx, n_q=n_q, n_q_heads=Hq, n_kv_heads=Hkv,
@@ -42,6 +46,17 @@ def test_small_prompt_full(n_ctx, n_q, Hq, Hkv, v_bits, page_cells):
     ref_out, ref_lse = O.prompt_attention(case.pool, case.q, case.calls[0][2])
     assert_close(out, ref_out, "out")
     assert_close(lse, ref_lse, "lse")
+
+
+def test_prompt_scratch_covers_images_and_ranges():
+    """The scratch of the bench's prompt call: header, one image per tile and KV head, and a whole
+    number of 66,560-byte partial-range records (the range count follows the SM count)."""
+    case = W.prompt_int8()
+    pool = qsa.DevicePool.upload(case.pool)
+    i0, n, pos0 = case.calls[0]
+    need = qsa.prompt_scratch_bytes(pool, n, pos0, case.n_q_heads)
+    images = 256 + case.pool.n_kv_heads * ((pos0 + n - 1) // 64 + 1) * 65536
+    assert need >= images and (need - images) % 66560 == 0
 
 
 def test_prompt_heads_with_far_apart_v_scales():
