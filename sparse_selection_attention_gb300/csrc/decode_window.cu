@@ -87,6 +87,8 @@ __global__ void __launch_bounds__(32) win_qprep_kernel(const float* __restrict__
 // every read of the CTA is in flight at once and no register is held across the wait; warp tasks
 // (KV head, 16-cell m-tile) then take their operands from shared memory.
 constexpr int kScoreThreads = 256;
+constexpr size_t kFragSmemMax = 16384;   // q fragments staged in shared memory up to this size
+constexpr int kMaxInvF = 2 * kScoreThreads;   // (row, KV head) factors in shared memory (R * Hkv <= 32 * 16)
 
 template <int NT>
 __global__ void __launch_bounds__(kScoreThreads, 4) win_scores_kernel(const ScoresParams p,
@@ -99,6 +101,8 @@ __global__ void __launch_bounds__(kScoreThreads, 4) win_scores_kernel(const Scor
   uint8_t* codes = sm;                                                    // [Hkv][B][128]
   float* kscale = reinterpret_cast<float*>(sm + (size_t)Hkv * B * kD);    // [Hkv][B][2]
   float* part = kscale + (size_t)Hkv * B * 2;                             // [tpu][NT * 8]
+  float* invf_s = part + (size_t)tpu * NT * 8;                            // [R][Hkv]
+  uint4* frag_s = reinterpret_cast<uint4*>(invf_s + kMaxInvF);            // [Hkv][NT][8][32] (frag_smem)
   const int unit = blockIdx.x;
   const int pi = pool_index(p.unit_begin, p.n_pools, unit);
   const PoolDev& pool = p.pools[pi];
@@ -115,7 +119,7 @@ __global__ void __launch_bounds__(kScoreThreads, 4) win_scores_kernel(const Scor
       if (c < n_b) {
         const long long slot = slot00 + (long long)h * pool.page_cells + c;
         const int8_t* src = pool.k_codes + slot * kD + 64 * half;
-        uint8_t* dst = codes + (size_t)hc * kD + 64 * half;
+        uint8_t* dst = codes + (size_t)hc * kD + 64 * (half ^ (c & 1));   // odd rows: halves swapped
 #pragma unroll
         for (int k = 0; k < 4; ++k) cp_async16(dst + 16 * k, src + 16 * k);
         if (!half) cp_async8(kscale + 2 * hc, pool.k_scales + slot * 2);
@@ -128,63 +132,101 @@ __global__ void __launch_bounds__(kScoreThreads, 4) win_scores_kernel(const Scor
   }
   pdl_trigger();
   pdl_wait();   // q fragments of the preceding launch
+  // The fragments every task reads, copied once into shared memory while the codes are in flight.
+  const bool fsm = p.frag_smem != 0;
+  if (fsm) {
+    for (int i = tid; i < Hkv * NT * 8 * 32; i += kScoreThreads) cp_async16(frag_s + i, frag + i);
+    cp_async_commit();
+  }
+  // per-(row, head) factors 2^-fe of the fragments, read while the codes arrive
+  const float invf0 = tid < R * Hkv ? __ldg(inv_f + tid) : 0.f;
+  const float invf1 = tid + kScoreThreads < R * Hkv ? __ldg(inv_f + tid + kScoreThreads) : 0.f;
   cp_async_wait_all();
+  if (tid < R * Hkv) invf_s[tid] = invf0;
+  if (tid + kScoreThreads < R * Hkv) invf_s[tid + kScoreThreads] = invf1;
   __syncthreads();
 
-  for (int task = warp; task < tpu; task += kScoreThreads / 32) {
-    const int h = task / mts, mt = task % mts;
-    const int row0 = h * B + 16 * mt + g;   // (head, cell) row of the lane's first cell
-    uint4 c[2][2];
-    float2 ks[2];
+  // Warp work item: TPW consecutive m-tiles of one KV head, which share every fragment load.
+  constexpr int TPW = NT == 1 ? 2 : 1;
+  const int ipb = (mts + TPW - 1) / TPW;   // items per head
+  for (int item = warp; item < Hkv * ipb; item += kScoreThreads / 32) {
+    const int h = item / ipb, mt0 = TPW * (item % ipb);
+    const int cnt = min(TPW, mts - mt0);
+    float d[TPW][NT][2][4];   // [m-tile][n-tile][K-scale group]: hi and lo parts of qbar accumulate together
 #pragma unroll
-    for (int ab = 0; ab < 2; ++ab) {
-      const uint8_t* src = codes + (size_t)(row0 + 8 * ab) * kD;
-      c[ab][0] = *reinterpret_cast<const uint4*>(src + 16 * tq);
-      c[ab][1] = *reinterpret_cast<const uint4*>(src + 64 + 16 * tq);
-      ks[ab] = *reinterpret_cast<const float2*>(kscale + 2 * (row0 + 8 * ab));
-    }
-    float d[NT][2][4];   // [n-tile][K-scale group]: hi and lo parts of qbar accumulate together
+    for (int tt = 0; tt < TPW; ++tt)
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int gr = 0; gr < 2; ++gr)
+        for (int gr = 0; gr < 2; ++gr)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) d[nt][gr][i] = 0.f;
-    const uint4* fr = frag + (size_t)h * NT * 8 * 32 + lane;
+          for (int i = 0; i < 4; ++i) d[tt][nt][gr][i] = 0.f;
+    const size_t fo = (size_t)h * NT * 8 * 32 + lane;
 #pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      const int gr = s >> 2, w = s & 3;
-      const uint32_t wa = word_of(c[0][gr], w) ^ 0x80808080u;
-      const uint32_t wb = word_of(c[1][gr], w) ^ 0x80808080u;
-      uint32_t a[4];
-      a[0] = byte_pair_h2(wa, 0x4140, kBiasS8);
-      a[2] = byte_pair_h2(wa, 0x4342, kBiasS8);
-      a[1] = byte_pair_h2(wb, 0x4140, kBiasS8);
-      a[3] = byte_pair_h2(wb, 0x4342, kBiasS8);
+    for (int gr = 0; gr < 2; ++gr) {
+      // codes of dims 64 gr .. + 63 of the lane's cells g and g + 8 (rows of odd cells hold the two
+      // 64-byte halves swapped, so the eight lanes of each load phase hit eight different chunks)
+      uint4 c[TPW][2];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const uint4 bf = __ldg(fr + (nt * 8 + s) * 32);
-        mma16816(d[nt][gr], a, bf.x, bf.y);
-        mma16816(d[nt][gr], a, bf.z, bf.w);
+      for (int tt = 0; tt < TPW; ++tt)
+#pragma unroll
+        for (int ab = 0; ab < 2; ++ab) {
+          const int row = h * B + 16 * (mt0 + tt) + g + 8 * ab;
+          c[tt][ab] = tt < cnt ? *reinterpret_cast<const uint4*>(codes + (size_t)row * kD + 64 * (gr ^ (g & 1)) + 16 * tq)
+                               : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const int s = 4 * gr + w;
+        uint32_t a[TPW][4];
+#pragma unroll
+        for (int tt = 0; tt < TPW; ++tt) {
+          const uint32_t wa = word_of(c[tt][0], w) ^ 0x80808080u;
+          const uint32_t wb = word_of(c[tt][1], w) ^ 0x80808080u;
+          a[tt][0] = byte_pair_h2(wa, 0x4140, kBiasS8);
+          a[tt][2] = byte_pair_h2(wa, 0x4342, kBiasS8);
+          a[tt][1] = byte_pair_h2(wb, 0x4140, kBiasS8);
+          a[tt][3] = byte_pair_h2(wb, 0x4342, kBiasS8);
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const uint4 bf = fsm ? frag_s[fo + (nt * 8 + s) * 32] : __ldg(frag + fo + (nt * 8 + s) * 32);
+#pragma unroll
+          for (int tt = 0; tt < TPW; ++tt) {
+            if (tt < cnt) {
+              mma16816(d[tt][nt][gr], a[tt], bf.x, bf.y);
+              mma16816(d[tt][nt][gr], a[tt], bf.z, bf.w);
+            }
+          }
+        }
       }
     }
     // cell weights by K scale, the lane's two cells summed, then a butterfly over the 8 cell pairs
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const float(&x)[2][4] = d[nt];
-      float e0 = fmaf(ks[0].y, x[1][0], ks[0].x * x[0][0]);
-      e0 += fmaf(ks[1].y, x[1][2], ks[1].x * x[0][2]);
-      float e1 = fmaf(ks[0].y, x[1][1], ks[0].x * x[0][1]);
-      e1 += fmaf(ks[1].y, x[1][3], ks[1].x * x[0][3]);
+    for (int tt = 0; tt < TPW; ++tt) {
+      if (tt < cnt) {
+        const int task = h * mts + mt0 + tt;
+        const int row0 = h * B + 16 * (mt0 + tt) + g;
+        const float2 ks0 = *reinterpret_cast<const float2*>(kscale + 2 * row0);
+        const float2 ks1 = *reinterpret_cast<const float2*>(kscale + 2 * (row0 + 8));
 #pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        e0 += __shfl_xor_sync(0xffffffffu, e0, o);
-        e1 += __shfl_xor_sync(0xffffffffu, e1, o);
-      }
-      if (g == 0) {
-        const int row = nt * 8 + 2 * tq;
-        part[task * NT * 8 + row] = row < R ? e0 * __ldg(inv_f + row * Hkv + h) : 0.f;
-        part[task * NT * 8 + row + 1] = row + 1 < R ? e1 * __ldg(inv_f + (row + 1) * Hkv + h) : 0.f;
+        for (int nt = 0; nt < NT; ++nt) {
+          const float(&x)[2][4] = d[tt][nt];
+          float e0 = fmaf(ks0.y, x[1][0], ks0.x * x[0][0]);
+          e0 += fmaf(ks1.y, x[1][2], ks1.x * x[0][2]);
+          float e1 = fmaf(ks0.y, x[1][1], ks0.x * x[0][1]);
+          e1 += fmaf(ks1.y, x[1][3], ks1.x * x[0][3]);
+#pragma unroll
+          for (int o = 4; o < 32; o <<= 1) {
+            e0 += __shfl_xor_sync(0xffffffffu, e0, o);
+            e1 += __shfl_xor_sync(0xffffffffu, e1, o);
+          }
+          if (g == 0) {
+            const int row = nt * 8 + 2 * tq;
+            part[task * NT * 8 + row] = row < R ? e0 * invf_s[row * Hkv + h] : 0.f;
+            part[task * NT * 8 + row + 1] = row + 1 < R ? e1 * invf_s[(row + 1) * Hkv + h] : 0.f;
+          }
+        }
       }
     }
   }
@@ -209,6 +251,37 @@ struct Stage {
 
 // Copies of sub-tile `st` of the split into `sg`: thread (cell c = tid / 2, half) copies half of
 // the cell's K and V pieces and one of its scale rows; invisible cells copy nothing.
+// Every filled page's V codes and scales into L2, in pieces of at most 16 KB spread over the first
+// lane of every warp of the grid.  Issued before the wait for the selection: the reads overlap
+// the top-k, and the attention then finds the V of its cells in L2.
+__device__ __noinline__ void prefetch_v_pages(const WinAttnParams& p) {
+  constexpr uint32_t kPiece = 16384;
+  const int n_issuers = gridDim.x * (kAttnThreads / 32);
+  const int issuer = blockIdx.x * (kAttnThreads / 32) + (threadIdx.x >> 5);
+  int base = 0;   // index of the pool's first piece
+  for (int pi = 0; pi < p.n_pools; ++pi) {
+    const PoolDev& pool = p.pools[pi];
+    const int n_pages = (pool.n_filled + pool.page_cells - 1) / pool.page_cells;
+    const uint32_t code_bytes = (uint32_t)(p.n_kv_heads * pool.page_cells * (pool.v_bits == 8 ? kD : kD / 2));
+    const uint32_t sc_bytes = (uint32_t)(p.n_kv_heads * pool.page_cells * (pool.v_bits == 8 ? 2 : 4) * 4);
+    const int n_code = (int)((code_bytes + kPiece - 1) / kPiece), n_sc = (int)((sc_bytes + kPiece - 1) / kPiece);
+    const int per_page = n_code + n_sc;
+    const int n = n_pages * per_page;
+    for (int c = ((issuer - base) % n_issuers + n_issuers) % n_issuers; c < n; c += n_issuers) {
+      const int pg = c / per_page, k = c % per_page;
+      const size_t phys = (size_t)__ldg(pool.page_table + pg);
+      if (k < n_code) {
+        const uint32_t off = (uint32_t)k * kPiece;
+        prefetch_l2(pool.v_codes + phys * code_bytes + off, min(kPiece, code_bytes - off));
+      } else {
+        const uint32_t off = (uint32_t)(k - n_code) * kPiece;
+        prefetch_l2(reinterpret_cast<const uint8_t*>(pool.v_scales) + phys * sc_bytes + off, min(kPiece, sc_bytes - off));
+      }
+    }
+    base += n;
+  }
+}
+
 __device__ __forceinline__ void prefetch_sub(const WinAttnParams& p, const PoolDev& pool, Stage& sg, int base, int n_cells,
                                              int st, int t, int h, int pos, bool v4) {
   const int c = threadIdx.x >> 1, half = threadIdx.x & 1;
@@ -295,6 +368,7 @@ __global__ void __launch_bounds__(kAttnThreads, 5) win_attn_kernel(const WinAttn
     lam_hi = __shfl_sync(0xffffffffu, lam, 4 * (2 * tq + 1));
   }
 
+  if (p.prefetch_v && lane == 0) prefetch_v_pages(p);
   pdl_wait();   // ids and n_sel of the preceding launch
   const int n_sel = min(__ldg(p.n_sel + t), p.k_cells);
   const int n_act = (n_sel + p.split_cells - 1) / p.split_cells;
@@ -499,6 +573,7 @@ __global__ void __launch_bounds__(kAttnThreads, 5) win_attn_kernel(const WinAttn
 //   W is scaled by 2^kv[group] (max |vscale| 2^kv in [8, 16) over the slices seen so far; kv only
 //   decreases, and O's rows of that group are rescaled when it does).
 constexpr int kSlice = 16;
+constexpr int kPageCache = 1024;   // page-table entries the int8-V attention keeps in shared memory
 
 struct WarpStage {
   int8_t k[kSlice * kD];
@@ -507,25 +582,41 @@ struct WarpStage {
   float vs[kSlice * 2];
 };
 
-// Copies slice entries [first, first + 16) of the split into `sg` (lane: cell lane / 2, half
-// lane % 2); returns the warp's ballot of visible cells (bit 2c + half for cell c).
-__device__ __forceinline__ uint32_t prefetch_slice(const WinAttnParams& p, const PoolDev& pool, WarpStage& sg,
-                                                   const int32_t* row_ids, int first, int n_cells, int h, int pos) {
+// Id of this lane's cell (lane / 2) of the slice starting at split entry `first`, or -1 past the
+// split.  The read stays inside the row's k_cells ids, so it may be issued before n_sel is known.
+__device__ __forceinline__ int slice_cell_id(const WinAttnParams& p, const int32_t* row_ids, int base, int first,
+                                             int n_cells) {
+  const int idx = first + ((threadIdx.x & 31) >> 1);
+  return (idx < n_cells && base + idx < p.k_cells) ? __ldg(row_ids + idx) : -1;
+}
+
+// Copies the slice's cells (ids from slice_cell_id; lane: cell lane / 2, half lane % 2) into `sg`,
+// pages looked up in `pt` (the pool's page table, in shared memory when it fits); returns the warp's
+// ballot of visible cells (bit 2c + half for cell c).
+__device__ __forceinline__ uint32_t prefetch_slice(const WinAttnParams& p, const PoolDev& pool, const int32_t* pt,
+                                                   WarpStage& sg, int cell, int h, int pos) {
   const int lane = threadIdx.x & 31, c = lane >> 1, half = lane & 1;
-  const int idx = first + c;
-  bool valid = false;
+  const bool valid = cell >= 0 && cell <= pos && cell < pool.n_filled;
   long long slot = 0;
-  if (idx < n_cells) {
-    const int cell = __ldg(row_ids + idx);
-    valid = cell <= pos && cell >= 0 && cell < pool.n_filled;
-    if (valid) slot = cell_slot(pool, p.n_kv_heads, h, cell);
+  if (valid) {
+    int pg, off;
+    if (pool.page_shift >= 0) {
+      pg = cell >> pool.page_shift;
+      off = cell & (pool.page_cells - 1);
+    } else {
+      pg = cell / pool.page_cells;
+      off = cell - pg * pool.page_cells;
+    }
+    slot = ((long long)pt[pg] * p.n_kv_heads + h) * pool.page_cells + off;
   }
   if (valid) {
+    // 16-byte chunks swizzled within the 128-byte row so that the fragment reads below are free of
+    // bank conflicts: K chunk pc of cell c at pc ^ 4 (c & 1), V chunk pc at pc ^ 2 ((c >> 1) & 3).
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int pc = 4 * half + k;
-      cp_async16(sg.k + c * kD + pc * 16, pool.k_codes + slot * kD + pc * 16);
-      cp_async16(sg.v + c * kD + pc * 16, pool.v_codes + slot * kD + pc * 16);
+      cp_async16(sg.k + c * kD + ((pc ^ (4 * (c & 1))) << 4), pool.k_codes + slot * kD + pc * 16);
+      cp_async16(sg.v + c * kD + ((pc ^ (2 * ((c >> 1) & 3))) << 4), pool.v_codes + slot * kD + pc * 16);
     }
     if (!half)
       cp_async8(sg.ks + 2 * c, pool.k_scales + slot * 2);
@@ -557,6 +648,7 @@ __global__ void __launch_bounds__(kAttnThreads, 4) win_attn8_kernel(const WinAtt
   __shared__ __align__(16) WarpStage ring[4][2];
   __shared__ __align__(16) float pbuf[4][8][kSlice];
   __shared__ float wm[4][8], wl[4][8];
+  __shared__ int32_t pt_s[kPageCache];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, tq = lane & 3;
@@ -591,15 +683,30 @@ __global__ void __launch_bounds__(kAttnThreads, 4) win_attn8_kernel(const WinAtt
     lam1 = __shfl_sync(0xffffffffu, lam, 4 * (2 * tq + 1));
   }
 
+  // The pool's page table (an input of the window) into shared memory when it fits.
+  const int n_pages = (pool.n_filled + pool.page_cells - 1) / pool.page_cells;
+  const int32_t* pt = pool.page_table;
+  if (n_pages <= kPageCache) {
+    for (int i = tid; i < n_pages; i += kAttnThreads) pt_s[i] = __ldg(pool.page_table + i);
+    pt = pt_s;
+  }
+  __syncthreads();
+  if (p.prefetch_v && lane == 0) prefetch_v_pages(p);
   pdl_wait();   // ids and n_sel of the preceding launch
+  const int base = split * p.split_cells;
+  const int32_t* row_ids = p.ids + (size_t)t * p.k_cells + base;
+  // The ids of the warp's first two slices are read together with n_sel (inside the row's ids, so
+  // before the split's extent is known); later ids are read one slice ahead of their copy.
+  int id_a = slice_cell_id(p, row_ids, base, kSlice * warp, p.split_cells);
+  int id_b = slice_cell_id(p, row_ids, base, kSlice * (warp + 4), p.split_cells);
   const int n_sel = min(__ldg(p.n_sel + t), p.k_cells);
   const int n_act = (n_sel + p.split_cells - 1) / p.split_cells;
   if (split >= n_act) return;   // past the selection: nothing to read, nothing the merge reads
-  const int base = split * p.split_cells;
   const int n_cells = min(p.split_cells, n_sel - base);
   const int n_slices = (n_cells + kSlice - 1) / kSlice;
   const int my_n = n_slices > warp ? (n_slices - warp + 3) / 4 : 0;
-  const int32_t* row_ids = p.ids + (size_t)t * p.k_cells + base;
+  if (kSlice * warp + (lane >> 1) >= n_cells) id_a = -1;
+  if (kSlice * (warp + 4) + (lane >> 1) >= n_cells) id_b = -1;
   WarpStage* rg = ring[warp];
   float(*pb)[kSlice] = pbuf[warp];
 
@@ -613,12 +720,13 @@ __global__ void __launch_bounds__(kAttnThreads, 4) win_attn8_kernel(const WinAtt
   int kv[2] = {0, 0};
   bool have_kv[2] = {false, false};
   uint32_t vmask[2] = {0u, 0u};
-  if (my_n > 0) vmask[0] = prefetch_slice(p, pool, rg[0], row_ids, kSlice * warp, n_cells, h, pos);
+  if (my_n > 0) vmask[0] = prefetch_slice(p, pool, pt, rg[0], id_a, h, pos);
 
   for (int j = 0; j < my_n; ++j) {
     const int st = j & 1;
     if (j + 1 < my_n) {
-      vmask[st ^ 1] = prefetch_slice(p, pool, rg[st ^ 1], row_ids, kSlice * (warp + 4 * (j + 1)), n_cells, h, pos);
+      vmask[st ^ 1] = prefetch_slice(p, pool, pt, rg[st ^ 1], id_b, h, pos);
+      id_b = slice_cell_id(p, row_ids, base, kSlice * (warp + 4 * (j + 2)), n_cells);
       cp_async_wait_group1();
     } else {
       cp_async_wait_all();
@@ -630,10 +738,11 @@ __global__ void __launch_bounds__(kAttnThreads, 4) win_attn8_kernel(const WinAtt
     // ---- S^T = Kcode . (q f)^T, one accumulator per K-scale group
     float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
     {
-      const uint4 ca0 = *reinterpret_cast<const uint4*>(S.k + g * kD + 16 * tq);
-      const uint4 ca1 = *reinterpret_cast<const uint4*>(S.k + g * kD + 64 + 16 * tq);
-      const uint4 cb0 = *reinterpret_cast<const uint4*>(S.k + (g + 8) * kD + 16 * tq);
-      const uint4 cb1 = *reinterpret_cast<const uint4*>(S.k + (g + 8) * kD + 64 + 16 * tq);
+      const int sk = 4 * (g & 1);   // rows g and g + 8 share the swizzle
+      const uint4 ca0 = *reinterpret_cast<const uint4*>(S.k + g * kD + ((tq ^ sk) << 4));
+      const uint4 ca1 = *reinterpret_cast<const uint4*>(S.k + g * kD + (((4 + tq) ^ sk) << 4));
+      const uint4 cb0 = *reinterpret_cast<const uint4*>(S.k + (g + 8) * kD + ((tq ^ sk) << 4));
+      const uint4 cb1 = *reinterpret_cast<const uint4*>(S.k + (g + 8) * kD + (((4 + tq) ^ sk) << 4));
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
         const int w = s & 3;
@@ -751,15 +860,18 @@ __global__ void __launch_bounds__(kAttnThreads, 4) win_attn8_kernel(const WinAtt
     // ---- O^T += V^T . W: lane (g, tq) reads dims 8g .. 8g+7 and 64 + 8g .. of cells 2tq, 2tq+1,
     // 2tq+8, 2tq+9
     {
-      const int8_t* vr = S.v + 8 * g;
-      const uint2 x0a = *reinterpret_cast<const uint2*>(vr + (2 * tq) * kD);
-      const uint2 x0b = *reinterpret_cast<const uint2*>(vr + (2 * tq) * kD + 64);
-      const uint2 x1a = *reinterpret_cast<const uint2*>(vr + (2 * tq + 1) * kD);
-      const uint2 x1b = *reinterpret_cast<const uint2*>(vr + (2 * tq + 1) * kD + 64);
-      const uint2 x2a = *reinterpret_cast<const uint2*>(vr + (2 * tq + 8) * kD);
-      const uint2 x2b = *reinterpret_cast<const uint2*>(vr + (2 * tq + 8) * kD + 64);
-      const uint2 x3a = *reinterpret_cast<const uint2*>(vr + (2 * tq + 9) * kD);
-      const uint2 x3b = *reinterpret_cast<const uint2*>(vr + (2 * tq + 9) * kD + 64);
+      // 8-byte column g (dims 8g..) and g + 8 (dims 64 + 8g..) of rows 2tq, 2tq+1, 2tq+8, 2tq+9,
+      // all four with the row swizzle 2 tq on 16-byte chunks = 4 tq on 8-byte columns
+      const int oa = 8 * (g ^ (4 * tq)), ob = 8 * ((g + 8) ^ (4 * tq));
+      const int8_t* vr = S.v;
+      const uint2 x0a = *reinterpret_cast<const uint2*>(vr + (2 * tq) * kD + oa);
+      const uint2 x0b = *reinterpret_cast<const uint2*>(vr + (2 * tq) * kD + ob);
+      const uint2 x1a = *reinterpret_cast<const uint2*>(vr + (2 * tq + 1) * kD + oa);
+      const uint2 x1b = *reinterpret_cast<const uint2*>(vr + (2 * tq + 1) * kD + ob);
+      const uint2 x2a = *reinterpret_cast<const uint2*>(vr + (2 * tq + 8) * kD + oa);
+      const uint2 x2b = *reinterpret_cast<const uint2*>(vr + (2 * tq + 8) * kD + ob);
+      const uint2 x3a = *reinterpret_cast<const uint2*>(vr + (2 * tq + 9) * kD + oa);
+      const uint2 x3b = *reinterpret_cast<const uint2*>(vr + (2 * tq + 9) * kD + ob);
       // words of each group: [gv][half word] for the four cells
       const uint32_t wc0[2][2] = {{x0a.x, x0a.y}, {x0b.x, x0b.y}};
       const uint32_t wc1[2][2] = {{x1a.x, x1a.y}, {x1b.x, x1b.y}};
@@ -928,13 +1040,17 @@ cudaError_t launch_decode_window(const WindowArgs& a, cudaStream_t stream, cudaE
   // 2. block scores
   if (sp.total_units > 0) {
     const int tpu = Hkv * (sp.block_cells / 16);
-    const size_t smem = (size_t)Hkv * sp.block_cells * (kD + 8) + sizeof(float) * (size_t)tpu * NT * 8;
+    const size_t frag_bytes = (size_t)Hkv * NT * 8 * 32 * sizeof(uint4);
+    ScoresParams spx = sp;
+    spx.frag_smem = frag_bytes <= kFragSmemMax;
+    const size_t smem = (size_t)Hkv * sp.block_cells * (kD + 8) + sizeof(float) * ((size_t)tpu * NT * 8 + kMaxInvF) +
+                        (spx.frag_smem ? frag_bytes : 0);
     void (*kern)(ScoresParams, const uint4*, const float*) =
         NT == 1 ? win_scores_kernel<1> : NT == 2 ? win_scores_kernel<2> : NT == 3 ? win_scores_kernel<3>
                                                                          : win_scores_kernel<4>;
     e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
-    e = launch_ex(kern, dim3(sp.total_units), dim3(kScoreThreads), smem, stream, pdl, sp, (const uint4*)frag,
+    e = launch_ex(kern, dim3(sp.total_units), dim3(kScoreThreads), smem, stream, pdl, spx, (const uint4*)frag,
                   (const float*)inv_f);
     if (e != cudaSuccess) return e;
   }

@@ -12,6 +12,7 @@ struct ScoresParams {
   int n_pools, total_units;
   int n_rows, n_q_heads, n_kv_heads, block_cells, max_blocks;
   int q_rows_per_batch;   // rows of q staged in shared memory at a time
+  int frag_smem;          // decode window: 1 when the scores kernel stages the q fragments in shared memory
   const float* q;
   float* scores;
   int* err;               // device error word (bounded waits of the staged kernel)
@@ -79,7 +80,9 @@ struct WinAttnParams {
   const int32_t* row_pos;
   const int32_t* ids;
   const int32_t* n_sel;
+  int n_pools;
   int n_rows, n_q_heads, n_kv_heads, k_cells;
+  int prefetch_v;    // 1: prefetch every filled V page into L2 before the wait for the selection
   int split_cells;   // cells of one split (multiple of 16)
   int n_splits;      // splits per (row, q head) in the workspace
   float* part_ml;    // [n_rows][n_q_heads][n_splits][2]
