@@ -35,11 +35,6 @@ __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t&
   lo = h2_bits(__floats2half2_rn(a - back.x, b - back.y));
 }
 
-// Byte offset of 16-byte chunk `chunk` of row `row` in the 128-byte swizzle (8-row atoms of 1 KB).
-__device__ __forceinline__ int sw128(int row, int chunk) {
-  return (row >> 3) * 1024 + (row & 7) * 128 + ((chunk ^ (row & 7)) << 4);
-}
-
 __device__ __forceinline__ void raise_device_error(int code) { atomicCAS(&g_device_error, 0, code); }
 
 }  // namespace
@@ -81,6 +76,7 @@ constexpr int kPShift = 5;   // P' = p 2^5 <= 2^13 (p <= 2^8 under the lazy runn
 // Tile image (global scratch and shared-memory stage alike): K' and V' in fp16 hi + lo, each two
 // 64-dim blocks of [64 cells][128 B] in the 128-byte swizzle.
 constexpr int kImgKhi = 0, kImgKlo = 16384, kImgVhi = 32768, kImgVlo = 49152, kImgBytes = 65536;
+static_assert(kImgVlo - kImgVhi == kImgKlo - kImgKhi, "lo copies sit at one offset from their hi copies");
 constexpr int kScratchHeader = 256;   // uint32 max |V scale| bits per KV head, then max |K scale| bits
 constexpr int kMaxHeadsHeader = kScratchHeader / 8;
 // Tensor memory columns (512 allocated).
@@ -206,91 +202,52 @@ __device__ __forceinline__ int head_scale_exp(const uint8_t* scratch, int w) {
   return vmax > 0.f ? max(-126, min(127, 4 - e)) : 0;
 }
 
-// codes (int8, 64 of them in v[4]) * sc -> fp16 hi + lo, written as one cell row of two images.
-__device__ __forceinline__ void write_scaled_row(const uint4 (&v)[4], float sc, uint8_t* dhi, uint8_t* dlo, int cc) {
-#pragma unroll
-  for (int s4 = 0; s4 < 4; ++s4) {
-    const uint32_t w[4] = {v[s4].x, v[s4].y, v[s4].z, v[s4].w};
-    uint32_t hi[8], lo[8];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-#pragma unroll
-      for (int b2 = 0; b2 < 2; ++b2) {
-        const float a0 = (float)(int8_t)((w[k] >> (16 * b2)) & 0xFF) * sc;
-        const float a1 = (float)(int8_t)((w[k] >> (16 * b2 + 8)) & 0xFF) * sc;
-        split2(a0, a1, hi[2 * k + b2], lo[2 * k + b2]);
-      }
-    }
-    *reinterpret_cast<uint4*>(dhi + sw128(cc, 2 * s4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-    *reinterpret_cast<uint4*>(dhi + sw128(cc, 2 * s4 + 1)) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
-    *reinterpret_cast<uint4*>(dlo + sw128(cc, 2 * s4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    *reinterpret_cast<uint4*>(dlo + sw128(cc, 2 * s4 + 1)) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
-  }
-}
-
-// 4-bit codes (32 bytes: byte j holds dim 2j in its low nibble and 2j + 1 in its high nibble,
-// nibble = code + 8) of 64 dims, dims 0..31 scaled by sc0 and 32..63 by sc1 -> fp16 hi + lo row.
-__device__ __forceinline__ void write_scaled_row4(const uint4 (&v)[2], float sc0, float sc1, uint8_t* dhi,
-                                                  uint8_t* dlo, int cc) {
-#pragma unroll
-  for (int s4 = 0; s4 < 4; ++s4) {   // 16 dims = 8 bytes
-    const uint4& q = v[s4 >> 1];
-    const uint32_t w0 = (s4 & 1) ? q.z : q.x, w1 = (s4 & 1) ? q.w : q.y;
-    const float sc = s4 < 2 ? sc0 : sc1;
-    uint32_t hi[8], lo[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const uint32_t b = ((k < 4 ? w0 : w1) >> (8 * (k & 3))) & 0xFFu;
-      split2((float)((int)(b & 15u) - 8) * sc, (float)((int)(b >> 4) - 8) * sc, hi[k], lo[k]);
-    }
-    *reinterpret_cast<uint4*>(dhi + sw128(cc, 2 * s4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-    *reinterpret_cast<uint4*>(dhi + sw128(cc, 2 * s4 + 1)) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
-    *reinterpret_cast<uint4*>(dlo + sw128(cc, 2 * s4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    *reinterpret_cast<uint4*>(dlo + sw128(cc, 2 * s4 + 1)) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
-  }
-}
-
-// One CTA per (64-cell tile, KV head), 128 threads: thread (cell ct / 2, dim block ct % 2 = scale
-// group).
-__global__ void __launch_bounds__(128) prompt_stage_kernel(const PoolDev pool, int n_kv_heads, int n_tiles,
+// One CTA per (64-cell tile, KV head), 256 threads.  The image is four 8 KB blocks (K dims 0-63,
+// K dims 64-127, V dims 0-63, V dims 64-127), each with a hi and a lo copy; a thread makes one
+// 16-byte chunk of a block (8 dims of one cell) per step, chunks in image order, so a warp reads
+// four cells' rows and writes 512 contiguous bytes of each copy.  Physical chunk p of row r holds
+// the dims of logical chunk p ^ (r & 7) (the 128-byte swizzle).
+__global__ void __launch_bounds__(256) prompt_stage_kernel(const PoolDev pool, int n_kv_heads, int n_tiles,
                                                            uint8_t* scratch) {
-  const int t = blockIdx.x, h = blockIdx.y, ct = threadIdx.x;
+  const int t = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
   uint8_t* img = scratch + kScratchHeader + ((size_t)h * n_tiles + t) * kImgBytes;
   const int cell0 = t * kN;
   const int page = __ldg(pool.page_table + cell0 / pool.page_cells);
   const long long slot0 = ((long long)page * n_kv_heads + h) * pool.page_cells + (cell0 % pool.page_cells);
-  const int cc = ct >> 1, hf = ct & 1;
-  const bool valid = cell0 + cc < pool.n_filled;
-  uint4 v[4];
-  // K' = kcode * kscale * 2^kk_h
-  {
-    const float sc = valid ? __ldg(pool.k_scales + (slot0 + cc) * 2 + hf) * pow2f(head_scale_exp(scratch, kMaxHeadsHeader + h))
-                           : 0.f;
-    const uint4* src = reinterpret_cast<const uint4*>(pool.k_codes + (slot0 + cc) * kD + hf * 64);
+  const float ksh = pow2f(head_scale_exp(scratch, kMaxHeadsHeader + h));   // K' = kcode kscale 2^kk_h
+  const float vsh = pow2f(head_scale_exp(scratch, h));                     // V' = vcode vscale 2^kv_h
 #pragma unroll
-    for (int s4 = 0; s4 < 4; ++s4) v[s4] = valid ? __ldg(src + s4) : make_uint4(0u, 0u, 0u, 0u);
-    write_scaled_row(v, sc, img + kImgKhi + hf * 8192, img + kImgKlo + hf * 8192, cc);
-  }
-  // V' = vcode * vscale * 2^kv_h (int8 V: one scale per 64 dims; 4-bit V: one per 32 dims)
-  const float vsh = pow2f(head_scale_exp(scratch, h));
-  if (pool.v_bits == 8) {
-    const float sc = valid ? __ldg(pool.v_scales + (slot0 + cc) * 2 + hf) * vsh : 0.f;
-    const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(pool.v_codes) +
-                                                      (slot0 + cc) * kD + hf * 64);
+  for (int j = 0; j < 8; ++j) {
+    const int blk = j >> 1, hf = blk & 1;
+    const int o16 = (j & 1) * 256 + tid;   // chunk of the 8 KB block, in memory order
+    const int row = o16 >> 3, lc = (o16 & 7) ^ (row & 7);
+    const int d0 = 64 * hf + 8 * lc;       // first of the chunk's 8 dims
+    const bool valid = cell0 + row < pool.n_filled;
+    const long long slot = slot0 + row;
+    float x[8];
+    if (blk < 2 || pool.v_bits == 8) {     // int8 codes, one scale per 64 dims
+      const int8_t* codes = blk < 2 ? pool.k_codes : reinterpret_cast<const int8_t*>(pool.v_codes);
+      const float* scales = blk < 2 ? pool.k_scales : pool.v_scales;
+      const uint2 w = valid ? __ldg(reinterpret_cast<const uint2*>(codes + slot * kD + d0)) : make_uint2(0u, 0u);
+      const float sc = valid ? __ldg(scales + slot * 2 + hf) * (blk < 2 ? ksh : vsh) : 0.f;
 #pragma unroll
-    for (int s4 = 0; s4 < 4; ++s4) v[s4] = valid ? __ldg(src + s4) : make_uint4(0u, 0u, 0u, 0u);
-    write_scaled_row(v, sc, img + kImgVhi + hf * 8192, img + kImgVlo + hf * 8192, cc);
-  } else {
-    float2 sc = make_float2(0.f, 0.f);
-    uint4 v4[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
-    if (valid) {
-      sc = __ldg(reinterpret_cast<const float2*>(pool.v_scales + (slot0 + cc) * 4 + 2 * hf));
-      const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(pool.v_codes) +
-                                                        (slot0 + cc) * 64 + hf * 32);
-      v4[0] = __ldg(src);
-      v4[1] = __ldg(src + 1);
+      for (int k = 0; k < 8; ++k) x[k] = (float)(int8_t)((((k < 4) ? w.x : w.y) >> (8 * (k & 3))) & 0xFFu) * sc;
+    } else {                               // 4-bit V: byte j = dims 2j (low nibble), 2j + 1; one scale per 32 dims
+      const uint32_t w = valid ? __ldg(reinterpret_cast<const uint32_t*>(pool.v_codes + slot * (kD / 2) + d0 / 2)) : 0u;
+      const float sc = valid ? __ldg(pool.v_scales + slot * 4 + d0 / 32) * vsh : 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t b = (w >> (8 * k)) & 0xFFu;
+        x[2 * k] = (float)((int)(b & 15u) - 8) * sc;
+        x[2 * k + 1] = (float)((int)(b >> 4) - 8) * sc;
+      }
     }
-    write_scaled_row4(v4, sc.x * vsh, sc.y * vsh, img + kImgVhi + hf * 8192, img + kImgVlo + hf * 8192, cc);
+    uint32_t hi[4], lo[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) split2(x[2 * k], x[2 * k + 1], hi[k], lo[k]);
+    uint8_t* dst = img + (blk < 2 ? kImgKhi : kImgVhi) + hf * 8192 + o16 * 16;
+    *reinterpret_cast<uint4*>(dst) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4*>(dst + (kImgKlo - kImgKhi)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
   }
 }
 
@@ -731,7 +688,7 @@ cudaError_t launch_prompt_attn(const PromptParams& p, cudaStream_t stream) {
   ws::prompt_vmax_kernel<<<dim3(p.n_tiles, p.n_kv_heads), 64, 0, stream>>>(p.pool, p.n_kv_heads, p.scratch);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  ws::prompt_stage_kernel<<<dim3(p.n_tiles, p.n_kv_heads), 128, 0, stream>>>(p.pool, p.n_kv_heads, p.n_tiles,
+  ws::prompt_stage_kernel<<<dim3(p.n_tiles, p.n_kv_heads), 256, 0, stream>>>(p.pool, p.n_kv_heads, p.n_tiles,
                                                                               p.scratch);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
