@@ -1,6 +1,6 @@
-"""GPU parity of the one-call decode window (qsa_decode_window: block scores ->
-top-k -> split attention with the merge fused in) against the FP64 oracle,
-through the C ABI.
+"""GPU parity of the one-call decode window (qsa_decode_window: q fragments ->
+block scores -> top-k -> split attention -> log-sum-exp merge, five chained
+launches) against the FP64 oracle, through the C ABI.
 
 Gates as for the four separate calls: ids bit-exact given the GPU's own fp32
 scores; scores, out and lse within max |gpu - oracle| / max |oracle| <= 1e-5;
@@ -110,6 +110,36 @@ def test_window_deterministic_and_reusable_workspace():
     win.run(q, row_pos)
     torch.cuda.synchronize()
     assert_close(outs[0][3].cpu().numpy(), win.out.cpu().numpy(), "window vs separate calls")
+
+
+def test_window_replays_from_a_cuda_graph():
+    """The window's five chained launches (programmatic dependent launch edges included) captured in
+    one CUDA graph: a replay gives the bits of a direct call, and a replay after new q is written into
+    the captured buffer gives the bits of a direct call with that q."""
+    case = W.verify_window()
+    win, q, row_pos = upload_case(case)
+    win.run_window(q, row_pos)
+    torch.cuda.synchronize()
+    direct = [t.clone() for t in (win.scores, win.ids, win.n_sel, win.out, win.lse)]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        win.run_window(q, row_pos)
+    for t in (win.scores, win.out, win.lse):
+        t.fill_(float("nan"))
+    graph.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(direct, (win.scores, win.ids, win.n_sel, win.out, win.lse)):
+        assert torch.equal(a, b)
+    q2 = torch.from_numpy(np.random.default_rng(7).standard_normal(tuple(q.shape)).astype(np.float32)).cuda()
+    q.copy_(q2)
+    graph.replay()
+    torch.cuda.synchronize()
+    replayed = [t.clone() for t in (win.scores, win.ids, win.n_sel, win.out, win.lse)]
+    win.run_window(q2, row_pos)
+    torch.cuda.synchronize()
+    for a, b in zip(replayed, (win.scores, win.ids, win.n_sel, win.out, win.lse)):
+        assert torch.equal(a, b)
+    assert not torch.equal(replayed[3], direct[3])
 
 
 def test_window_refuses_small_workspace():
