@@ -74,6 +74,15 @@ def test_window_many_rows_two_pools():
     run_window_and_check(case)
 
 
+def test_window_many_waves_of_blocks_two_pools():
+    """1,250 32-cell blocks over two pools (two waves and more of block-score CTAs) and 12 rows (two 8-row
+    n-tiles, one q-fragment load per m-tile)."""
+    case = W.decode_case(name="wwaves", seed=91, fills=[25000, 15000], capacity=25600, rows_per_slot=6,
+                         n_q_heads=16, n_kv_heads=4, k_cells=512, chunk_cells=64, page_cells=256,
+                         block_cells=32, bias_prob=0.05)
+    run_window_and_check(case)
+
+
 def test_window_rows_with_masked_cells():
     """Rows early in the context: selected cells past a row's position are masked; splits whose cells are
     all masked are empty and carry no weight in the merge."""
