@@ -591,43 +591,51 @@ __global__ void __launch_bounds__(kThreads, 1) prompt_attn_ws_kernel(const Promp
   __syncthreads();
 }
 
-// Combines the n_split parts of each split unit, one CTA per unit, one warp per row at a time
-// (four output dims a lane): with w_k = 2^(m_k - M), M = max_k m_k,
+// Combines the n_split parts of each split unit: one warp per row (grid (unit, 8-row group)), lane l
+// holding output dims 4l .. 4l + 3, every part's loads in flight together.  With w_k = 2^(m_k - M),
+// M = max_k m_k:
 //   out = sum_k w_k O_k / sum_k w_k l_k,   lse = (M + log2 sum_k w_k l_k) ln 2,
 // summed in part order (the result does not depend on which part finished first).
-__global__ void __launch_bounds__(128) prompt_merge_kernel(const PromptParams p) {
+constexpr int kMaxSplit = 8;
+__global__ void __launch_bounds__(256) prompt_merge_kernel(const PromptParams p) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int n_tail = p.n_qb * p.n_kv_heads - p.n_whole;
   const int v = blockIdx.x, u = p.n_whole + v;
   const int G = p.n_q_heads / p.n_kv_heads;
   const int kvh = u / p.n_qb, q_begin = (u % p.n_qb) * p.qpc;
   const int rows = (min(p.n_q, q_begin + p.qpc) - q_begin) * G;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int r = warp; r < rows; r += 4) {
-    float M = -INFINITY;
-    for (int k = 0; k < p.n_split; ++k) M = fmaxf(M, p.part_ml[((size_t)(k * n_tail + v) * kM + r) * 2]);
-    float L = 0.f;
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k = 0; k < p.n_split; ++k) {
-      const size_t rec = (size_t)(k * n_tail + v) * kM + r;
-      const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + rec * 2);
-      const float w = ml.x == -INFINITY ? 0.f : ex2(ml.x - M);
-      const float4 ov = reinterpret_cast<const float4*>(p.part_o + rec * kD)[lane];
-      L = fmaf(w, ml.y, L);
-      o = make_float4(fmaf(w, ov.x, o.x), fmaf(w, ov.y, o.y), fmaf(w, ov.z, o.z), fmaf(w, ov.w, o.w));
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.y * 8 + (threadIdx.x >> 5);
+  if (r >= rows) return;
+  const int S = p.n_split;
+  float2 ml = make_float2(-INFINITY, 0.f);   // (m, l) of part `lane`
+  if (lane < S) ml = *reinterpret_cast<const float2*>(p.part_ml + ((size_t)(lane * n_tail + v) * kM + r) * 2);
+  float4 ov[kMaxSplit];
+#pragma unroll
+  for (int k = 0; k < kMaxSplit; ++k)
+    if (k < S) ov[k] = reinterpret_cast<const float4*>(p.part_o + ((size_t)(k * n_tail + v) * kM + r) * kD)[lane];
+  const float M = warp_max(ml.x);
+  const float w = ml.x == -INFINITY ? 0.f : ex2(ml.x - M);
+  float L = 0.f;
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int k = 0; k < kMaxSplit; ++k) {
+    if (k < S) {
+      const float wk = __shfl_sync(0xffffffffu, w, k), lk = __shfl_sync(0xffffffffu, ml.y, k);
+      L = fmaf(wk, lk, L);
+      o = make_float4(fmaf(wk, ov[k].x, o.x), fmaf(wk, ov[k].y, o.y), fmaf(wk, ov[k].z, o.z), fmaf(wk, ov[k].w, o.w));
     }
-    const float inv = 1.f / L;
-    const int qi = q_begin + r / G, head = kvh * G + r % G;
-    reinterpret_cast<float4*>(p.out + ((size_t)qi * p.n_q_heads + head) * kD)[lane] =
-        make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
-    if (p.lse && lane == 0) p.lse[(size_t)qi * p.n_q_heads + head] = (M + log2f(L)) * kLn2;
   }
+  const float inv = 1.f / L;
+  const int qi = q_begin + r / G, head = kvh * G + r % G;
+  reinterpret_cast<float4*>(p.out + ((size_t)qi * p.n_q_heads + head) * kD)[lane] =
+      make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+  if (p.lse && lane == 0) p.lse[(size_t)qi * p.n_q_heads + head] = (M + log2f(L)) * kLn2;
 }
 
 // A split unit's CTA costs this many tiles beyond its share (prologue, pipeline fill and drain).
 constexpr int kPartOverheadTiles = 4;
 constexpr int kMinPartTiles = 8;
-constexpr int kMaxSplit = 8;
 
 }  // namespace ws
 
@@ -696,8 +704,8 @@ cudaError_t launch_prompt_attn(const PromptParams& p, cudaStream_t stream) {
   e = cudaGetLastError();
   if (e != cudaSuccess || p.n_split <= 1) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(n_tail);
-  cfg.blockDim = dim3(128);
+  cfg.gridDim = dim3(n_tail, ws::kM / 8);
+  cfg.blockDim = dim3(256);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
