@@ -252,6 +252,47 @@ def window_of(case, dev):
 
 
 KERNELS = ["q_prep", "block_scores", "topk", "split_attn", "merge"]
+K8V4_WORKLOAD = ("large prompt with mixed KV: 8,192 queries at 122,880..131,071 over 131,072 cells, 32/8 heads, "
+                 "int8 K / 4-bit V, four calls of 2,048 queries in one stream")
+
+
+def run_prompt_k8v4(dev, stream, flush_l2, tc_peak, ws):
+    """The four 2,048-query calls of the K8V4 prompt, one after another on one stream, timed together."""
+    import torch
+
+    import sparse_selection_attention_gb300 as qsa
+    case = W.prompt_k8v4()
+    pool = qsa.DevicePool.upload(case.pool, dev)
+    q = torch.from_numpy(case.q).to(dev)
+    n = max(c[1] for c in case.calls)
+    out = torch.empty((n, case.n_q_heads, 128), device=dev)
+    lse = torch.empty((n, case.n_q_heads), device=dev)
+    need = max(qsa.prompt_scratch_bytes(pool, c[1], c[2], case.n_q_heads) for c in case.calls)
+    scratch = torch.empty(max(1, need), dtype=torch.uint8, device=dev)
+
+    def chunked():
+        for i0, nq, pos0 in case.calls:
+            qsa.prompt_attn(pool, q[i0:i0 + nq], pos0, out[:nq], lse[:nq], scratch=scratch)
+    chunked()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(3):
+        flush_l2()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        chunked()
+        b.record(stream)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    if qsa.get_device_error() != 0:
+        raise RuntimeError("prompt kernel reported a device error")
+    ms = max_over_ranks(float(np.mean(times)), ws)
+    issued = sum(prompt_flops(case, c)[0] for c in case.calls)
+    logical = sum(prompt_flops(case, c)[1] for c in case.calls)
+    ach = issued / (ms * 1e-3) / 1e12
+    return {"workload": K8V4_WORKLOAD, "ms_per_prompt": ms, "value": ach * ws, "unit": "TFLOP/s",
+            "logical_TFLOP/s": logical / (ms * 1e-3) / 1e12 * ws, "frac_of_tensor_peak": ach / tc_peak,
+            "scratch_bytes": need}
 
 
 def run_ours(args):
@@ -447,6 +488,9 @@ def run_ours(args):
                                "traffic": kernel_traffic("prompt_attn")}}
         if rank == 0 and ws == 1 and not args.no_cpu_baseline:
             prompt["cpu_baseline"] = prompt_cpu_baseline(pcase, call, issued)
+        del pscratch
+        if not args.no_k8v4:
+            prompt["k8v4"] = run_prompt_k8v4(dev, stream, flush_l2, tc_peak, ws)
 
     clocks.__exit__()
     line = {
@@ -518,6 +562,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prompt", action="store_true")
+    ap.add_argument("--no-k8v4", action="store_true", help="skip the K8V4 prompt (four calls over 131,072 cells)")
     ap.add_argument("--no-long", action="store_true")
     ap.add_argument("--case", choices=["verify", "long"], default="verify",
                     help="decode workload of the timed step (the verify window is the headline)")
