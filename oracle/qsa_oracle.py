@@ -35,7 +35,13 @@ notes of the repository):
       visible cell is empty and the merge skips it;
   R7  chunk j of a row is entries [j*C, (j+1)*C) of its selected-id list;
   R8  4-bit V: code = nibble - 8, low nibble = even dim, one scale per
-      32-dim group; int8 V and int8 K: one scale per 64-dim group.
+      32-dim group; int8 V and int8 K: one scale per 64-dim group;
+  R14 appending a cell quantises each group of its K and V rows symmetrically
+      by the group's largest magnitude: scale = amax / 127 (int8) or amax / 7
+      (4-bit V), code = round-half-to-even(x / scale) clamped to +-127 (+-7),
+      amax = 0 giving scale 0 and codes 0; the division and rounding that
+      decide the integer codes are taken in fp32 (the stored precision), so
+      the codes are exact integers both sides agree on.
 """
 from __future__ import annotations
 
@@ -47,7 +53,7 @@ import numpy as np
 __all__ = [
     "dequantise_k", "dequantise_v", "kv_head", "block_scores", "score_key",
     "topk_select", "attention", "chunk_partials", "merge_partials",
-    "prompt_attention", "decode_window",
+    "prompt_attention", "decode_window", "quantise_group", "append_cells",
 ]
 
 
@@ -87,6 +93,58 @@ def dequantise_v(pool, h: int, cells: Sequence[int]) -> np.ndarray:
         codes[:, 1::2] = hi
     scales = pool.v_scales[phys, h, off, :].astype(np.float64)
     return codes * np.repeat(scales, pool.v_group, axis=1)
+
+
+# ---------------------------------------------------------------- append (quantise new cells)
+
+def quantise_group(x, qmax: int) -> Tuple[np.ndarray, np.float32]:
+    """Codes and scale of one group of fp32 values (reading R14).
+
+    The pages store K/V as int8 (4-bit for K8V4 V) codes with one fp32 scale
+    per (cell, KV head, group) ([1367] Operands; [1888], [2075] name the K8V4
+    format) and append new cells per row ([2806] What it leaves alone: "K/V and
+    indexer appends"), but give no quantiser; the plainest one is symmetric:
+    scale = max |x| / qmax, code = x / scale rounded to nearest (ties to even),
+    in fp32."""
+    x = np.asarray(x, dtype=np.float32)
+    amax = np.float32(np.max(np.abs(x))) if x.size else np.float32(0)
+    if amax == 0:
+        return np.zeros(x.shape, dtype=np.int64), np.float32(0)
+    scale = np.float32(amax / np.float32(qmax))          # fp32 division, rounded to nearest
+    q = np.rint(x / scale)                                # fp32 division, then ties-to-even
+    return np.clip(q, -qmax, qmax).astype(np.int64), scale
+
+
+def append_cells(pool, k_new: np.ndarray, v_new: np.ndarray, first_cell: int):
+    """A copy of `pool` with cells first_cell .. first_cell + n - 1 written from k_new, v_new (fp32
+    [n][Hkv][D]): K in int8 with one scale per 64 dims; V likewise, or in 4-bit (code + 8 in a
+    nibble, the even dim in the low nibble) with one scale per 32 dims.  n_filled becomes
+    max(n_filled, first_cell + n)."""
+    import copy
+    out = copy.deepcopy(pool)
+    n = k_new.shape[0]
+    for i in range(n):
+        cell = first_cell + i
+        phys = int(pool.page_table[cell // pool.page_cells])
+        off = cell % pool.page_cells
+        for h in range(pool.n_kv_heads):
+            for g in range(pool.head_dim // 64):
+                codes, scale = quantise_group(k_new[i, h, 64 * g:64 * (g + 1)], 127)
+                out.k_codes[phys, h, off, 64 * g:64 * (g + 1)] = codes
+                out.k_scales[phys, h, off, g] = scale
+            vg = pool.v_group
+            for g in range(pool.head_dim // vg):
+                codes, scale = quantise_group(v_new[i, h, vg * g:vg * (g + 1)], 127 if pool.v_bits == 8 else 7)
+                out.v_scales[phys, h, off, g] = scale
+                if pool.v_bits == 8:
+                    out.v_codes[phys, h, off, vg * g:vg * (g + 1)] = codes
+                else:
+                    nib = (codes + 8).astype(np.uint8)
+                    for j in range(0, vg, 2):
+                        d = vg * g + j
+                        out.v_codes[phys, h, off, d // 2] = nib[j] | (nib[j + 1] << 4)
+    out.n_filled = max(pool.n_filled, first_cell + n)
+    return out
 
 
 def kv_head(g: int, n_q_heads: int, n_kv_heads: int) -> int:

@@ -323,3 +323,73 @@ def test_workload_recipe():
     fin = p.k_scales[np.isfinite(p.k_scales)]
     assert fin.min() >= 0.005 and fin.max() <= 0.02
     assert sorted(p.page_table) == list(range(p.n_pages))
+
+
+# ---------------------------------------------------------------- append (reading R14)
+
+def _group(head, n):
+    x = np.zeros(n, np.float32)
+    x[:len(head)] = head
+    return x
+
+
+def test_append_groups_worked_by_hand():
+    """Hand-worked groups: absmax scale, ties to even (a round-half-away or a scale from the mean
+    would change codes 2, 4, -2 or 126), zeros for an all-zero group."""
+    g = json.load(open(os.path.join(GOLD, "append_quant.json")))
+    for case in g["int8_groups"]:
+        codes, scale = O.quantise_group(_group(case["x_head"], 64), 127)
+        assert scale == np.float32(case["scale"])
+        assert codes[:len(case["codes_head"])].tolist() == case["codes_head"]
+        assert not codes[len(case["codes_head"]):].any()
+    v = g["v4_group"]
+    pool = hand_pool(64, v_bits=4, page_cells=64)
+    k_new = np.zeros((1, 1, 128), np.float32)
+    v_new = np.zeros((1, 1, 128), np.float32)
+    v_new[0, 0, :len(v["x_head"])] = v["x_head"]
+    out = O.append_cells(pool, k_new, v_new, 5)
+    phys = out.page_table[0]
+    assert out.v_scales[phys, 0, 5, 0] == np.float32(v["scale"])
+    assert out.v_codes[phys, 0, 5, :2].tolist() == v["bytes_head"]
+    assert out.v_codes[phys, 0, 5, 2] == 0x88                       # zeros: code 0 -> nibble 8
+    assert (out.k_scales[phys, 0, 5] == 0).all() and not out.k_codes[phys, 0, 5].any()
+
+
+@pytest.mark.parametrize("qmax", [127, 7])
+def test_append_error_bound_and_extreme(qmax):
+    """Random fp32 groups: every code within +-qmax, the largest magnitude maps to +-qmax, and the
+    dequantised value is within half a step of the input (the bound of rounding to nearest)."""
+    rng = np.random.default_rng(3)
+    for _ in range(200):
+        x = (rng.standard_normal(64) * 10.0 ** rng.uniform(-6, 4)).astype(np.float32)
+        codes, scale = O.quantise_group(x, qmax)
+        i = int(np.argmax(np.abs(x)))
+        assert abs(codes[i]) == qmax and np.sign(codes[i]) == np.sign(x[i])
+        assert np.abs(codes).max() <= qmax
+        err = np.abs(codes.astype(np.float64) * np.float64(scale) - x.astype(np.float64))
+        assert err.max() <= 0.5 * float(scale) * (1 + 1e-5)
+
+
+@pytest.mark.parametrize("v_bits", [8, 4])
+def test_append_cells_round_trip_across_pages(v_bits):
+    """Cells appended across a page boundary of a permuted page table come back through the
+    dequantisation within half a step per group, and no other cell changes."""
+    pool = hand_pool(100, n_kv_heads=2, v_bits=v_bits, page_cells=64, capacity=256, seed=4)
+    before = (pool.k_codes.copy(), pool.v_codes.copy(), pool.k_scales.copy(), pool.v_scales.copy())
+    rng = np.random.default_rng(5)
+    k_new = rng.standard_normal((40, 2, 128)).astype(np.float32)
+    v_new = rng.standard_normal((40, 2, 128)).astype(np.float32)
+    out = O.append_cells(pool, k_new, v_new, 100)                 # cells 100..139 span pages 1 and 2
+    assert out.n_filled == 140 and pool.n_filled == 100
+    cells = list(range(100, 140))
+    for h in range(2):
+        k = O.dequantise_k(out, h, cells)
+        v = O.dequantise_v(out, h, cells)
+        for x, back, grp, qmax in ((k_new[:, h], k, 64, 127), (v_new[:, h], v, out.v_group, 127 if v_bits == 8 else 7)):
+            step = np.repeat(np.abs(x.reshape(40, -1, grp)).max(axis=2) / qmax, grp, axis=1)
+            assert (np.abs(back - x) <= 0.5 * step * (1 + 1e-5)).all()
+    touched = np.zeros(pool.k_codes.shape[:3], bool)
+    for c in cells:
+        touched[pool.page_table[c // 64], :, c % 64] = True
+    for a, b in zip(before, (out.k_codes, out.v_codes, out.k_scales, out.v_scales)):
+        assert np.array_equal(a[~touched], b[~touched])
