@@ -279,6 +279,32 @@ qsa_status qsa_prompt_attn(const qsa_pool* pool, const float* q, int n_q, int q_
  */
 size_t qsa_prompt_scratch_bytes(const qsa_pool* pool, int n_q, int q_pos0, int n_q_heads);
 
+/*
+ * qsa_kv_append -- quantise n_new new cells into a pool: cell first_cell + i
+ * of KV head h takes the rows k[i][h] and v[i][h] ("#2806 sycl: decode QSA
+ * selection and attention in fewer, shorter launches", What it leaves alone:
+ * the per-row K/V appends; storage format of "#1367 prompt attention",
+ * Operands, and "#2075 QSA decode attention", Bit for bit).  Each group of a
+ * row (64 dims; 32 for 4-bit V) is quantised symmetrically by its largest
+ * magnitude amax:
+ *   scale = amax / 127 (4-bit V: amax / 7), stored as the group's fp32 scale;
+ *   code  = x / scale rounded to nearest with ties to even, clamped to +-127
+ *           (+-7; stored as the nibble code + 8, the even dim in the low
+ *           nibble); amax = 0 gives scale 0 and codes 0.
+ * The division and rounding are IEEE fp32, so the codes are exact integers.
+ *   pool        (host) descriptor; the call WRITES its code and scale arrays
+ *                      for the appended cells (the const in qsa_pool marks
+ *                      the attention calls' read-only use).  n_filled is the
+ *                      caller's: raise it to first_cell + n_new before reading
+ *                      the new cells.
+ *   k, v        (dev)  fp32 [n_new][n_kv_heads][128], 16-byte aligned
+ *   first_cell >= 0, first_cell + n_new <= pool->capacity
+ * Errors: QSA_ERR_ARG, QSA_ERR_UNSUPPORTED (as for the pool elsewhere).
+ * Non-finite inputs give unspecified codes for their group (no fault).
+ */
+qsa_status qsa_kv_append(const qsa_pool* pool, const float* k, const float* v, int first_cell,
+                         int n_new, void* stream);
+
 /* Size of the library-owned scratch of qsa_decode_attn_noalloc (8 MiB). */
 #define QSA_NOALLOC_SCRATCH_BYTES (8u << 20)
 

@@ -26,7 +26,7 @@ EXPORTS = [
     "qsa_block_scores", "qsa_topk", "qsa_decode_partials_bytes", "qsa_decode_attn", "qsa_attn_merge",
     "qsa_prompt_attn", "qsa_prompt_scratch_bytes", "qsa_get_device_error", "qsa_set_wait_limit_ns", "qsa_status_str", "qsa_abi_version",
     "qsa_decode_attn_noalloc", "qsa_decode_window", "qsa_decode_window_workspace_bytes",
-    "qsa_decode_window_profile",
+    "qsa_decode_window_profile", "qsa_kv_append",
 ]
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -75,6 +75,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                               ctypes.POINTER(ctypes.c_float)]
     lib.qsa_decode_window_workspace_bytes.argtypes = [i, i, i, i]
     lib.qsa_decode_window_workspace_bytes.restype = sz
+    lib.qsa_kv_append.argtypes = [pool_p, p, p, i, i, p]
     lib.qsa_get_device_error.argtypes = [i32p, p]
     lib.qsa_set_wait_limit_ns.argtypes = [u64]
     lib.qsa_set_wait_limit_ns.restype = None
@@ -139,6 +140,16 @@ class DevicePool:
         return QsaPoolC(_ptr(self.k_codes), _ptr(self.v_codes), _ptr(self.k_scales), _ptr(self.v_scales),
                         _ptr(self.page_table), self.n_filled, self.capacity, self.page_cells, self.n_kv_heads,
                         self.head_dim, self.v_bits)
+
+
+def kv_append(pool: DevicePool, k: torch.Tensor, v: torch.Tensor, first_cell: int, stream=None) -> None:
+    """Quantises the new cells' K and V rows (fp32 [n_new][n_kv_heads][128]) into the pool at cells
+    first_cell .. first_cell + n_new - 1, then raises the host-side pool.n_filled to cover them."""
+    n_new = k.shape[0]
+    pc = pool.c()
+    _check(load().qsa_kv_append(ctypes.byref(pc), _ptr(k), _ptr(v), int(first_cell), n_new, _stream(stream)),
+           "qsa_kv_append")
+    pool.n_filled = max(pool.n_filled, int(first_cell) + n_new)
 
 
 def _pools_c(pools: Sequence[DevicePool]):

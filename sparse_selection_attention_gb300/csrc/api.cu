@@ -423,6 +423,27 @@ const char* qsa_status_str(qsa_status s) {
   return "unknown status";
 }
 
-int qsa_abi_version(void) { return 103; }
+qsa_status qsa_kv_append(const qsa_pool* pool, const float* k, const float* v, int first_cell, int n_new,
+                         void* stream) {
+  if (!pool || !k || !v || !aligned16(k) || !aligned16(v)) return QSA_ERR_ARG;
+  qsa_status s = check_pool(*pool, true);
+  if (s != QSA_OK) return s;
+  if (first_cell < 0 || n_new < 0 || (long long)first_cell + n_new > pool->capacity) return QSA_ERR_ARG;
+  if (n_new == 0) return QSA_OK;
+  AppendParams p{};
+  p.pool = to_dev(*pool);
+  p.k_codes = const_cast<int8_t*>(pool->k_codes);
+  p.v_codes = static_cast<uint8_t*>(const_cast<void*>(pool->v_codes));
+  p.k_scales = const_cast<float*>(pool->k_scales);
+  p.v_scales = const_cast<float*>(pool->v_scales);
+  p.k = k;
+  p.v = v;
+  p.n_kv_heads = pool->n_kv_heads;
+  p.first_cell = first_cell;
+  p.n_new = n_new;
+  return from_cuda(launch_kv_append(p, static_cast<cudaStream_t>(stream)));
+}
+
+int qsa_abi_version(void) { return 104; }
 
 }  // extern "C"

@@ -66,6 +66,19 @@ struct PromptParams {
   unsigned long long wait_limit_ns;
 };
 
+// Quantise-on-append of new cells (qsa_kv_append): the pool read through `pool`, its code and
+// scale arrays written through the other pointers.
+struct AppendParams {
+  PoolDev pool;
+  int8_t* k_codes;
+  uint8_t* v_codes;
+  float* k_scales;
+  float* v_scales;
+  const float* k;   // [n_new][n_kv_heads][128]
+  const float* v;
+  int n_kv_heads, first_cell, n_new;
+};
+
 // How a prompt call is cut into CTAs for a device with n_sm SMs, and the scratch it needs.
 struct PromptPlan {
   int qpc, n_qb, n_units, n_whole, n_split, n_parts;
@@ -123,6 +136,7 @@ cudaError_t launch_decode_attn(const AttnParams& p, cudaStream_t stream);
 cudaError_t launch_attn_merge(const MergeParams& p, cudaStream_t stream);
 cudaError_t launch_attn_merge_ex(const MergeParams& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_prompt_attn(const PromptParams& p, cudaStream_t stream);
+cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream);
 cudaError_t read_and_clear_device_error(int32_t* code, cudaStream_t stream);
 // Device address of the library's error word on the current device (for kernels of other
 // translation units), or nullptr.

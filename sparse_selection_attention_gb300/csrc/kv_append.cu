@@ -1,0 +1,85 @@
+// Quantise-on-append of new K/V cells into a paged pool (qsa_kv_append).
+//
+// The pages store the cache as int8 codes (4-bit for the V of the K8V4 format) with one fp32
+// scale per (cell, KV head, group) ("#1367 prompt attention", Operands; "#2075 QSA decode
+// attention", Bit for bit) and append the new cells of each row to it ("#2806 sycl: decode QSA
+// selection and attention in fewer, shorter launches", What it leaves alone).  They give no
+// quantiser; this one is symmetric by the group's largest magnitude:
+//   scale = amax / 127 (int8) or amax / 7 (4-bit V),
+//   code  = x / scale rounded to nearest, ties to even, clamped to +-127 (+-7),
+// with amax = 0 giving scale 0 and codes 0.  The division and the rounding are IEEE fp32
+// (round to nearest; the library is built without fast-math), so the codes are exact integers.
+#include "kernels.h"
+
+namespace qsa {
+namespace {
+
+constexpr int kAppendWarps = 8;
+
+__device__ __forceinline__ float group_scale(float amax, float qmax) { return amax > 0.f ? __fdiv_rn(amax, qmax) : 0.f; }
+
+__device__ __forceinline__ int quant_code(float x, float scale, float qmax) {
+  if (scale == 0.f) return 0;
+  return (int)fminf(fmaxf(rintf(__fdiv_rn(x, scale)), -qmax), qmax);
+}
+
+__device__ __forceinline__ float max_abs4(float4 x) {
+  return fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
+}
+
+// Largest magnitude over the `width` lanes of the lane's aligned group (width a power of two <= 32).
+__device__ __forceinline__ float group_max(float m, int width) {
+  for (int o = width >> 1; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  return m;
+}
+
+__device__ __forceinline__ uint32_t pack_s8(int a, int b, int c, int d) {
+  return (uint32_t)(a & 0xFF) | ((uint32_t)(b & 0xFF) << 8) | ((uint32_t)(c & 0xFF) << 16) | ((uint32_t)(d & 0xFF) << 24);
+}
+
+// One warp per (new cell, KV head); lane l holds dims 4l .. 4l + 3 of the K row and of the V row.
+// int8 groups of 64 dims are 16 lanes, 4-bit V groups of 32 dims are 8 lanes.
+__global__ void __launch_bounds__(32 * kAppendWarps) kv_append_kernel(const AppendParams p) {
+  const int Hkv = p.n_kv_heads;
+  const int item = blockIdx.x * kAppendWarps + (threadIdx.x >> 5);
+  if (item >= p.n_new * Hkv) return;
+  const int lane = threadIdx.x & 31;
+  const int i = item / Hkv, h = item % Hkv;
+  const long long slot = cell_slot(p.pool, Hkv, h, p.first_cell + i);
+  const size_t row = ((size_t)i * Hkv + h) * kD;
+  const float4 xk = __ldg(reinterpret_cast<const float4*>(p.k + row) + lane);
+  const float4 xv = __ldg(reinterpret_cast<const float4*>(p.v + row) + lane);
+
+  // K: int8, one scale per 64 dims
+  {
+    const float sc = group_scale(group_max(max_abs4(xk), 16), 127.f);
+    reinterpret_cast<uint32_t*>(p.k_codes + slot * kD)[lane] =
+        pack_s8(quant_code(xk.x, sc, 127.f), quant_code(xk.y, sc, 127.f), quant_code(xk.z, sc, 127.f),
+                quant_code(xk.w, sc, 127.f));
+    if ((lane & 15) == 0) p.k_scales[slot * 2 + (lane >> 4)] = sc;
+  }
+  if (p.pool.v_bits == 8) {   // V: int8, one scale per 64 dims
+    const float sc = group_scale(group_max(max_abs4(xv), 16), 127.f);
+    reinterpret_cast<uint32_t*>(p.v_codes + slot * kD)[lane] =
+        pack_s8(quant_code(xv.x, sc, 127.f), quant_code(xv.y, sc, 127.f), quant_code(xv.z, sc, 127.f),
+                quant_code(xv.w, sc, 127.f));
+    if ((lane & 15) == 0) p.v_scales[slot * 2 + (lane >> 4)] = sc;
+  } else {                    // V: 4-bit, nibble = code + 8, even dim in the low nibble, one scale per 32 dims
+    const float sc = group_scale(group_max(max_abs4(xv), 8), 7.f);
+    const uint32_t n0 = (uint32_t)(quant_code(xv.x, sc, 7.f) + 8), n1 = (uint32_t)(quant_code(xv.y, sc, 7.f) + 8);
+    const uint32_t n2 = (uint32_t)(quant_code(xv.z, sc, 7.f) + 8), n3 = (uint32_t)(quant_code(xv.w, sc, 7.f) + 8);
+    reinterpret_cast<uint16_t*>(p.v_codes + slot * (kD / 2))[lane] = (uint16_t)(n0 | (n1 << 4) | (n2 << 8) | (n3 << 12));
+    if ((lane & 7) == 0) p.v_scales[slot * 4 + (lane >> 3)] = sc;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream) {
+  const long long items = (long long)p.n_new * p.n_kv_heads;
+  if (items == 0) return cudaSuccess;
+  kv_append_kernel<<<(unsigned)((items + kAppendWarps - 1) / kAppendWarps), 32 * kAppendWarps, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace qsa

@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_pure_host_calls(lib):
-    assert qsa.abi_version() == 103
+    assert qsa.abi_version() == 104
     assert qsa.status_str(qsa.QSA_ERR_SCRATCH) == "scratch buffer too small"
     assert qsa.decode_partials_bytes(5, 24, 64) == 4 * 5 * 24 * 64 * 130
     assert qsa.decode_partials_bytes(0, 24, 64) == 0
@@ -117,3 +117,15 @@ def test_prompt_validation(lib):
     assert call(pool, 900, 100, nbytes=need - 1) == qsa.QSA_ERR_SCRATCH
     assert call(pool, 900, 100, scratch=(1 << 20) + 16) == qsa.QSA_ERR_SCRATCH   # not 256-byte aligned
     assert lib.qsa_prompt_attn(ctypes.byref(pool), 16, 100, 900, 24, None, need, 32, None, None) == qsa.QSA_ERR_SCRATCH
+
+def test_kv_append_validation(lib):
+    pool = _pool(n_filled=100, capacity=256)
+    call = lambda pl, first, n, k=16, v=32: lib.qsa_kv_append(ctypes.byref(pl), k, v, first, n, None)
+    assert call(pool, 200, 57) == qsa.QSA_ERR_ARG                   # past the capacity
+    assert call(pool, -1, 1) == qsa.QSA_ERR_ARG
+    assert call(pool, 0, -1) == qsa.QSA_ERR_ARG
+    assert call(pool, 10, 5, k=24) == qsa.QSA_ERR_ARG               # k not 16-byte aligned
+    assert call(pool, 10, 5, v=0) == qsa.QSA_ERR_ARG                # v missing
+    assert call(_pool(page_cells=96), 0, 1) == qsa.QSA_ERR_ARG       # pages of a multiple of 64 cells only
+    assert call(_pool(head_dim=64), 0, 1) == qsa.QSA_ERR_UNSUPPORTED
+    assert call(pool, 200, 0) == qsa.QSA_OK                          # nothing to append: nothing launched
