@@ -256,6 +256,41 @@ K8V4_WORKLOAD = ("large prompt with mixed KV: 8,192 queries at 122,880..131,071 
                  "int8 K / 4-bit V, four calls of 2,048 queries in one stream")
 
 
+def run_kv_append(dev, stream, flush_l2, hbm_peak, ws):
+    """qsa_kv_append of (a) one 2,048-cell prompt chunk into the int8 prompt pool's shape (4 KV heads)
+    and (b) 32,768 cells x 8 KV heads into a K8V4 pool: algorithmic bytes per (cell, KV head) are the
+    fp32 K and V rows read (1,024 B) plus the codes and scales written (136 B for int8 K; 136 B for
+    int8 V, 80 B for 4-bit V)."""
+    import torch
+
+    import sparse_selection_attention_gb300 as qsa
+    res = {}
+    for name, n, Hkv, v_bits, cap in (("prompt_chunk_2048x4_int8", 2048, 4, 8, 32768),
+                                      ("cells_32768x8_k8v4", 32768, 8, 4, 32768)):
+        rng = np.random.default_rng(n + Hkv)
+        pool = qsa.DevicePool.upload(W.make_pool(rng, capacity=cap, n_filled=0, n_kv_heads=Hkv, page_cells=256,
+                                                 v_bits=v_bits), dev)
+        k = torch.randn((n, Hkv, 128), device=dev)
+        v = torch.randn((n, Hkv, 128), device=dev)
+        for _ in range(3):
+            qsa.kv_append(pool, k, v, 0)
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(10):
+            flush_l2()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            qsa.kv_append(pool, k, v, 0)
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        us = max_over_ranks(float(np.median(ts)), ws) * 1e3
+        nbytes = n * Hkv * (1024 + 136 + (136 if v_bits == 8 else 80))
+        gbs = nbytes / (us * 1e-6) / 1e9
+        res[name] = {"us": us, "algorithmic_bytes": nbytes, "GB/s": gbs * ws, "frac_hbm": gbs / hbm_peak}
+    return res
+
+
 def run_prompt_k8v4(dev, stream, flush_l2, tc_peak, ws):
     """The four 2,048-query calls of the K8V4 prompt, one after another on one stream, timed together."""
     import torch
@@ -492,6 +527,8 @@ def run_ours(args):
         if not args.no_k8v4:
             prompt["k8v4"] = run_prompt_k8v4(dev, stream, flush_l2, tc_peak, ws)
 
+    kv_append = None if args.no_append else run_kv_append(dev, stream, flush_l2, hbm_peak, ws)
+
     clocks.__exit__()
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
@@ -509,6 +546,7 @@ def run_ours(args):
         "kernels": kernels,
         "separate_calls_ms": float(np.mean(sep)),
         "graph_replay": graph_replay,
+        "kv_append": kv_append,
         "e2e": {"value": bytes_step * ws / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 5 * K,
@@ -563,6 +601,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prompt", action="store_true")
     ap.add_argument("--no-k8v4", action="store_true", help="skip the K8V4 prompt (four calls over 131,072 cells)")
+    ap.add_argument("--no-append", action="store_true", help="skip the quantise-on-append measurement")
     ap.add_argument("--no-long", action="store_true")
     ap.add_argument("--case", choices=["verify", "long"], default="verify",
                     help="decode workload of the timed step (the verify window is the headline)")

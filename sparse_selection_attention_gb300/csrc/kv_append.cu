@@ -18,9 +18,17 @@ constexpr int kAppendWarps = 8;
 
 __device__ __forceinline__ float group_scale(float amax, float qmax) { return amax > 0.f ? __fdiv_rn(amax, qmax) : 0.f; }
 
-__device__ __forceinline__ int quant_code(float x, float scale, float qmax) {
+// code = rint(x / scale) with the quotient rounded to fp32 first (IEEE division), clamped.  y = x *
+// (1 / scale), both rounded to nearest, is within 2^-16 of the exact quotient while |x / scale| <=
+// 127 (ulp 2^-17 at most), and the rounded quotient within 2^-17: unless y lies within 2^-14 of a
+// half-integer, both round to the same integer, so the division is taken only there (and for
+// scales below 2^-120, whose reciprocals leave the range this bound assumes).
+__device__ __forceinline__ int quant_code(float x, float scale, float inv, float qmax) {
   if (scale == 0.f) return 0;
-  return (int)fminf(fmaxf(rintf(__fdiv_rn(x, scale)), -qmax), qmax);
+  const float y = x * inv;
+  const bool exact = !(inv <= 0x1p120f) || fabsf(y - floorf(y) - 0.5f) <= 0x1p-14f;
+  const float r = exact ? rintf(__fdiv_rn(x, scale)) : rintf(y);
+  return (int)fminf(fmaxf(r, -qmax), qmax);
 }
 
 __device__ __forceinline__ float max_abs4(float4 x) {
@@ -37,40 +45,52 @@ __device__ __forceinline__ uint32_t pack_s8(int a, int b, int c, int d) {
   return (uint32_t)(a & 0xFF) | ((uint32_t)(b & 0xFF) << 8) | ((uint32_t)(c & 0xFF) << 16) | ((uint32_t)(d & 0xFF) << 24);
 }
 
-// One warp per (new cell, KV head); lane l holds dims 4l .. 4l + 3 of the K row and of the V row.
+// Quantises one (cell, KV head) whose K and V rows this warp holds (lane l: dims 4l .. 4l + 3).
 // int8 groups of 64 dims are 16 lanes, 4-bit V groups of 32 dims are 8 lanes.
-__global__ void __launch_bounds__(32 * kAppendWarps) kv_append_kernel(const AppendParams p) {
+__device__ __forceinline__ void append_item(const AppendParams& p, int item, float4 xk, float4 xv, int lane) {
   const int Hkv = p.n_kv_heads;
-  const int item = blockIdx.x * kAppendWarps + (threadIdx.x >> 5);
-  if (item >= p.n_new * Hkv) return;
-  const int lane = threadIdx.x & 31;
   const int i = item / Hkv, h = item % Hkv;
   const long long slot = cell_slot(p.pool, Hkv, h, p.first_cell + i);
-  const size_t row = ((size_t)i * Hkv + h) * kD;
-  const float4 xk = __ldg(reinterpret_cast<const float4*>(p.k + row) + lane);
-  const float4 xv = __ldg(reinterpret_cast<const float4*>(p.v + row) + lane);
-
   // K: int8, one scale per 64 dims
   {
-    const float sc = group_scale(group_max(max_abs4(xk), 16), 127.f);
+    const float sc = group_scale(group_max(max_abs4(xk), 16), 127.f), inv = __frcp_rn(sc);
     reinterpret_cast<uint32_t*>(p.k_codes + slot * kD)[lane] =
-        pack_s8(quant_code(xk.x, sc, 127.f), quant_code(xk.y, sc, 127.f), quant_code(xk.z, sc, 127.f),
-                quant_code(xk.w, sc, 127.f));
+        pack_s8(quant_code(xk.x, sc, inv, 127.f), quant_code(xk.y, sc, inv, 127.f), quant_code(xk.z, sc, inv, 127.f),
+                quant_code(xk.w, sc, inv, 127.f));
     if ((lane & 15) == 0) p.k_scales[slot * 2 + (lane >> 4)] = sc;
   }
   if (p.pool.v_bits == 8) {   // V: int8, one scale per 64 dims
-    const float sc = group_scale(group_max(max_abs4(xv), 16), 127.f);
+    const float sc = group_scale(group_max(max_abs4(xv), 16), 127.f), inv = __frcp_rn(sc);
     reinterpret_cast<uint32_t*>(p.v_codes + slot * kD)[lane] =
-        pack_s8(quant_code(xv.x, sc, 127.f), quant_code(xv.y, sc, 127.f), quant_code(xv.z, sc, 127.f),
-                quant_code(xv.w, sc, 127.f));
+        pack_s8(quant_code(xv.x, sc, inv, 127.f), quant_code(xv.y, sc, inv, 127.f), quant_code(xv.z, sc, inv, 127.f),
+                quant_code(xv.w, sc, inv, 127.f));
     if ((lane & 15) == 0) p.v_scales[slot * 2 + (lane >> 4)] = sc;
   } else {                    // V: 4-bit, nibble = code + 8, even dim in the low nibble, one scale per 32 dims
-    const float sc = group_scale(group_max(max_abs4(xv), 8), 7.f);
-    const uint32_t n0 = (uint32_t)(quant_code(xv.x, sc, 7.f) + 8), n1 = (uint32_t)(quant_code(xv.y, sc, 7.f) + 8);
-    const uint32_t n2 = (uint32_t)(quant_code(xv.z, sc, 7.f) + 8), n3 = (uint32_t)(quant_code(xv.w, sc, 7.f) + 8);
+    const float sc = group_scale(group_max(max_abs4(xv), 8), 7.f), inv = __frcp_rn(sc);
+    const uint32_t n0 = (uint32_t)(quant_code(xv.x, sc, inv, 7.f) + 8), n1 = (uint32_t)(quant_code(xv.y, sc, inv, 7.f) + 8);
+    const uint32_t n2 = (uint32_t)(quant_code(xv.z, sc, inv, 7.f) + 8), n3 = (uint32_t)(quant_code(xv.w, sc, inv, 7.f) + 8);
     reinterpret_cast<uint16_t*>(p.v_codes + slot * (kD / 2))[lane] = (uint16_t)(n0 | (n1 << 4) | (n2 << 8) | (n3 << 12));
     if ((lane & 7) == 0) p.v_scales[slot * 4 + (lane >> 3)] = sc;
   }
+}
+
+// One (cell, KV head) item per warp, items cell-major (rows of k and v read in order).
+constexpr int kItemsPerWarp = 1;
+__global__ void __launch_bounds__(32 * kAppendWarps) kv_append_kernel(const AppendParams p) {
+  const int n_items = p.n_new * p.n_kv_heads;
+  const int item0 = (blockIdx.x * kAppendWarps + (threadIdx.x >> 5)) * kItemsPerWarp;
+  const int lane = threadIdx.x & 31;
+  float4 xk[kItemsPerWarp], xv[kItemsPerWarp];
+#pragma unroll
+  for (int j = 0; j < kItemsPerWarp; ++j) {
+    if (item0 + j < n_items) {
+      xk[j] = __ldg(reinterpret_cast<const float4*>(p.k + (size_t)(item0 + j) * kD) + lane);
+      xv[j] = __ldg(reinterpret_cast<const float4*>(p.v + (size_t)(item0 + j) * kD) + lane);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kItemsPerWarp; ++j)
+    if (item0 + j < n_items) append_item(p, item0 + j, xk[j], xv[j], lane);
 }
 
 }  // namespace
@@ -78,7 +98,8 @@ __global__ void __launch_bounds__(32 * kAppendWarps) kv_append_kernel(const Appe
 cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream) {
   const long long items = (long long)p.n_new * p.n_kv_heads;
   if (items == 0) return cudaSuccess;
-  kv_append_kernel<<<(unsigned)((items + kAppendWarps - 1) / kAppendWarps), 32 * kAppendWarps, 0, stream>>>(p);
+  const long long per_cta = (long long)kAppendWarps * kItemsPerWarp;
+  kv_append_kernel<<<(unsigned)((items + per_cta - 1) / per_cta), 32 * kAppendWarps, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

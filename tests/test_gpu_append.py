@@ -59,6 +59,37 @@ def test_append_bit_exact(v_bits, Hkv, page_cells, first, n):
         assert np.array_equal(a.view(np.uint8), b.view(np.uint8)), name
 
 
+def test_append_near_ties_and_tiny_scales():
+    """Values whose quotient by the group scale lies within a few ulps of a half-integer (where a
+    product with the reciprocal and the rounded quotient could round apart), and groups so small that
+    their scales are subnormal: codes still bit-exact."""
+    rng = np.random.default_rng(77)
+    n, Hkv = 512, 2
+    pool = W.make_pool(rng, capacity=1024, n_filled=0, n_kv_heads=Hkv, page_cells=256, v_bits=4)
+    k = np.zeros((n, Hkv, 128), np.float32)
+    v = np.zeros((n, Hkv, 128), np.float32)
+    for i in range(n):
+        for h in range(Hkv):
+            for x, grp, qmax in ((k, 64, 127), (v, 32, 7)):
+                for g0 in range(0, 128, grp):
+                    s = np.float32(10.0 ** rng.uniform(-30, 3))
+                    if i % 7 == 0:
+                        s = np.float32(10.0 ** rng.uniform(-44, -38))     # subnormal scales
+                    steps = rng.integers(-qmax, qmax, size=grp) + 0.5
+                    delta = rng.choice([0.0, 2.0 ** -22, -(2.0 ** -22), 2.0 ** -18, -(2.0 ** -18), 2.0 ** -15], size=grp)
+                    vals = ((steps + delta) * np.float64(s)).astype(np.float32)
+                    vals[int(rng.integers(grp))] = np.float32(qmax * np.float64(s))
+                    x[i, h, g0:g0 + grp] = vals
+    ref = O.append_cells(pool, k, v, 0)
+    dp = qsa.DevicePool.upload(pool)
+    qsa.kv_append(dp, torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda(), 0)
+    torch.cuda.synchronize()
+    got = device_pool_arrays(dp)
+    for name, a, b in zip(("k_codes", "v_codes", "k_scales", "v_scales"), got,
+                          (ref.k_codes, ref.v_codes, ref.k_scales, ref.v_scales)):
+        assert np.array_equal(a.view(np.uint8), b.view(np.uint8)), name
+
+
 def test_append_then_prompt_matches_oracle():
     """A prompt chunk appended to a pool and then attended (prompt path over the new cells) equals
     the oracle's attention over the oracle's appended pool."""
