@@ -249,15 +249,13 @@ struct Stage {
   int valid[kSub];
 };
 
-// Copies of sub-tile `st` of the split into `sg`: thread (cell c = tid / 2, half) copies half of
-// the cell's K and V pieces and one of its scale rows; invisible cells copy nothing.
-// Every filled page's V codes and scales into L2, in pieces of at most 16 KB spread over the first
-// lane of every warp of the grid.  Issued before the wait for the selection: the reads overlap
-// the top-k, and the attention then finds the V of its cells in L2.
+// Every filled page's V codes and scales into L2, in pieces of at most 16 KB spread over one thread
+// of every CTA of the grid.  Issued before the wait for the selection: the reads overlap the
+// top-k, and the attention then finds the V of its cells in L2.
 __device__ __noinline__ void prefetch_v_pages(const WinAttnParams& p) {
   constexpr uint32_t kPiece = 16384;
-  const int n_issuers = gridDim.x * (kAttnThreads / 32);
-  const int issuer = blockIdx.x * (kAttnThreads / 32) + (threadIdx.x >> 5);
+  const int n_issuers = gridDim.x;
+  const int issuer = blockIdx.x;
   int base = 0;   // index of the pool's first piece
   for (int pi = 0; pi < p.n_pools; ++pi) {
     const PoolDev& pool = p.pools[pi];
@@ -282,6 +280,8 @@ __device__ __noinline__ void prefetch_v_pages(const WinAttnParams& p) {
   }
 }
 
+// Copies of sub-tile `st` of the split into `sg`: thread (cell c = tid / 2, half) copies half of
+// the cell's K and V pieces and one of its scale rows; invisible cells copy nothing.
 __device__ __forceinline__ void prefetch_sub(const WinAttnParams& p, const PoolDev& pool, Stage& sg, int base, int n_cells,
                                              int st, int t, int h, int pos, bool v4) {
   const int c = threadIdx.x >> 1, half = threadIdx.x & 1;
@@ -368,7 +368,7 @@ __global__ void __launch_bounds__(kAttnThreads, 5) win_attn_kernel(const WinAttn
     lam_hi = __shfl_sync(0xffffffffu, lam, 4 * (2 * tq + 1));
   }
 
-  if (p.prefetch_v && lane == 0) prefetch_v_pages(p);
+  if (p.prefetch_v && tid == 0) prefetch_v_pages(p);
   pdl_wait();   // ids and n_sel of the preceding launch
   const int n_sel = min(__ldg(p.n_sel + t), p.k_cells);
   const int n_act = (n_sel + p.split_cells - 1) / p.split_cells;
@@ -649,16 +649,19 @@ __global__ void __launch_bounds__(kAttnThreads, 4) win_attn8_kernel(const WinAtt
   __shared__ __align__(16) float pbuf[4][8][kSlice];
   __shared__ float wm[4][8], wl[4][8];
   __shared__ int32_t pt_s[kPageCache];
+  __shared__ uint4 qf_s[8][32];    // warp 0's q fragments: (hi pair, lo pair) per k-step and lane
+  __shared__ float2 lam_s[32];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, tq = lane & 3;
 
   // ---- q of head g: for k-step s = 4 gr + w the dims 64 gr + 16 tq + 4 w .. + 3, scaled by 2^fe
   // (max |q 2^fe| in [64, 128)) and split into fp16 hi + lo.  q is an input of the window, so
-  // this runs before the wait for the selection.
+  // this runs before the wait for the selection; warp 0 makes the fragments, the other warps of
+  // the CTA (the same row and KV head) take them from shared memory.
   uint32_t qh[8][2], ql[8][2];
   float lam0, lam1;   // base-2 logit scale of heads 2tq and 2tq+1
-  {
+  if (warp == 0) {
     float qv[8][4];
     float amax = 0.f;
     const float* qrow = p.q + ((size_t)t * p.n_q_heads + h * G + min(g, G - 1)) * kD + 16 * tq;
@@ -681,6 +684,9 @@ __global__ void __launch_bounds__(kAttnThreads, 4) win_attn8_kernel(const WinAtt
     const float lam = kInvSqrtD * kLog2e * pow2i(-fe);
     lam0 = __shfl_sync(0xffffffffu, lam, 4 * (2 * tq));
     lam1 = __shfl_sync(0xffffffffu, lam, 4 * (2 * tq + 1));
+#pragma unroll
+    for (int s = 0; s < 8; ++s) qf_s[s][lane] = make_uint4(qh[s][0], qh[s][1], ql[s][0], ql[s][1]);
+    lam_s[lane] = make_float2(lam0, lam1);
   }
 
   // The pool's page table (an input of the window) into shared memory when it fits.
@@ -691,7 +697,20 @@ __global__ void __launch_bounds__(kAttnThreads, 4) win_attn8_kernel(const WinAtt
     pt = pt_s;
   }
   __syncthreads();
-  if (p.prefetch_v && lane == 0) prefetch_v_pages(p);
+  if (warp != 0) {
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      const uint4 f = qf_s[s][lane];
+      qh[s][0] = f.x;
+      qh[s][1] = f.y;
+      ql[s][0] = f.z;
+      ql[s][1] = f.w;
+    }
+    const float2 lm = lam_s[lane];
+    lam0 = lm.x;
+    lam1 = lm.y;
+  }
+  if (p.prefetch_v && tid == 0) prefetch_v_pages(p);
   pdl_wait();   // ids and n_sel of the preceding launch
   const int base = split * p.split_cells;
   const int32_t* row_ids = p.ids + (size_t)t * p.k_cells + base;
