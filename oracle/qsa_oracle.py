@@ -64,16 +64,28 @@ def _page_slots(pool, cells: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
     return pool.page_table[cells // pool.page_cells].astype(np.int64), cells % pool.page_cells
 
 
+def _unpack_nibbles(raw: np.ndarray, head_dim: int) -> np.ndarray:
+    """Bytes [n, D/2] -> codes float64 [n, D]: byte j holds dim 2j in its low nibble and 2j + 1 in
+    its high nibble, code = nibble - 8 (reading R8)."""
+    codes = np.empty((raw.shape[0], head_dim), dtype=np.float64)
+    codes[:, 0::2] = (raw & 0x0F).astype(np.int64) - 8
+    codes[:, 1::2] = (raw >> 4).astype(np.int64) - 8
+    return codes
+
+
 def dequantise_k(pool, h: int, cells: Sequence[int]) -> np.ndarray:
-    """K[c, h, d] = kcode[c, h, d] * kscale[c, h, d // 64], float64 [n, D].
+    """K[c, h, d] = kcode[c, h, d] * kscale[c, h, d // kgroup], float64 [n, D].
 
     Per-(cell, KV head, 64-dim group) fp32 scale: [600] description ("one
     64-dim group (= one int8 scale group)"); [1367] Operands (int8 K codes used
-    as stored)."""
+    as stored).  4-bit K (the q4_0 KV format of [2075] Bit for bit): codes and
+    32-dim groups as for 4-bit V."""
     phys, off = _page_slots(pool, np.asarray(cells))
-    codes = pool.k_codes[phys, h, off, :].astype(np.float64)             # [n, D]
-    scales = pool.k_scales[phys, h, off, :].astype(np.float64)           # [n, D/64]
-    return codes * np.repeat(scales, 64, axis=1)
+    raw = pool.k_codes[phys, h, off, :]
+    k_bits = getattr(pool, "k_bits", 8)
+    codes = raw.astype(np.float64) if k_bits == 8 else _unpack_nibbles(raw, pool.head_dim)   # [n, D]
+    scales = pool.k_scales[phys, h, off, :].astype(np.float64)                               # [n, D/kgroup]
+    return codes * np.repeat(scales, pool.head_dim // scales.shape[1], axis=1)
 
 
 def dequantise_v(pool, h: int, cells: Sequence[int]) -> np.ndarray:
@@ -83,14 +95,7 @@ def dequantise_v(pool, h: int, cells: Sequence[int]) -> np.ndarray:
     code = nibble - 8, low nibble holds the even dim, group 32 (reading R8)."""
     phys, off = _page_slots(pool, np.asarray(cells))
     raw = pool.v_codes[phys, h, off, :]
-    if pool.v_bits == 8:
-        codes = raw.astype(np.float64)
-    else:
-        lo = (raw & 0x0F).astype(np.int64) - 8
-        hi = (raw >> 4).astype(np.int64) - 8
-        codes = np.empty((raw.shape[0], pool.head_dim), dtype=np.float64)
-        codes[:, 0::2] = lo
-        codes[:, 1::2] = hi
+    codes = raw.astype(np.float64) if pool.v_bits == 8 else _unpack_nibbles(raw, pool.head_dim)
     scales = pool.v_scales[phys, h, off, :].astype(np.float64)
     return codes * np.repeat(scales, pool.v_group, axis=1)
 
@@ -117,8 +122,8 @@ def quantise_group(x, qmax: int) -> Tuple[np.ndarray, np.float32]:
 
 def append_cells(pool, k_new: np.ndarray, v_new: np.ndarray, first_cell: int):
     """A copy of `pool` with cells first_cell .. first_cell + n - 1 written from k_new, v_new (fp32
-    [n][Hkv][D]): K in int8 with one scale per 64 dims; V likewise, or in 4-bit (code + 8 in a
-    nibble, the even dim in the low nibble) with one scale per 32 dims.  n_filled becomes
+    [n][Hkv][D]): each of K and V in int8 with one scale per 64 dims, or in 4-bit (code + 8 in a
+    nibble, the even dim in the low nibble) with one scale per 32 dims, as the pool stores it.  n_filled becomes
     max(n_filled, first_cell + n)."""
     import copy
     out = copy.deepcopy(pool)
@@ -128,21 +133,19 @@ def append_cells(pool, k_new: np.ndarray, v_new: np.ndarray, first_cell: int):
         phys = int(pool.page_table[cell // pool.page_cells])
         off = cell % pool.page_cells
         for h in range(pool.n_kv_heads):
-            for g in range(pool.head_dim // 64):
-                codes, scale = quantise_group(k_new[i, h, 64 * g:64 * (g + 1)], 127)
-                out.k_codes[phys, h, off, 64 * g:64 * (g + 1)] = codes
-                out.k_scales[phys, h, off, g] = scale
-            vg = pool.v_group
-            for g in range(pool.head_dim // vg):
-                codes, scale = quantise_group(v_new[i, h, vg * g:vg * (g + 1)], 127 if pool.v_bits == 8 else 7)
-                out.v_scales[phys, h, off, g] = scale
-                if pool.v_bits == 8:
-                    out.v_codes[phys, h, off, vg * g:vg * (g + 1)] = codes
-                else:
-                    nib = (codes + 8).astype(np.uint8)
-                    for j in range(0, vg, 2):
-                        d = vg * g + j
-                        out.v_codes[phys, h, off, d // 2] = nib[j] | (nib[j + 1] << 4)
+            for x_new, bits, grp, codes_arr, scales_arr in (
+                    (k_new, getattr(pool, "k_bits", 8), getattr(pool, "k_group", 64), out.k_codes, out.k_scales),
+                    (v_new, pool.v_bits, pool.v_group, out.v_codes, out.v_scales)):
+                for g in range(pool.head_dim // grp):
+                    codes, scale = quantise_group(x_new[i, h, grp * g:grp * (g + 1)], 127 if bits == 8 else 7)
+                    scales_arr[phys, h, off, g] = scale
+                    if bits == 8:
+                        codes_arr[phys, h, off, grp * g:grp * (g + 1)] = codes
+                    else:
+                        nib = (codes + 8).astype(np.uint8)
+                        for j in range(0, grp, 2):
+                            d = grp * g + j
+                            codes_arr[phys, h, off, d // 2] = nib[j] | (nib[j + 1] << 4)
     out.n_filled = max(pool.n_filled, first_cell + n)
     return out
 

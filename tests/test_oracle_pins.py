@@ -393,3 +393,63 @@ def test_append_cells_round_trip_across_pages(v_bits):
         touched[pool.page_table[c // 64], :, c % 64] = True
     for a, b in zip(before, (out.k_codes, out.v_codes, out.k_scales, out.v_scales)):
         assert np.array_equal(a[~touched], b[~touched])
+
+
+# ---------------------------------------------------------------- 4-bit K (the q4_0 layout)
+
+def _k4_twin(rng, n_cells=130, Hkv=2):
+    """A pool with 4-bit K and V (q4_0 layout) whose two 32-dim K-scale groups inside each 64-dim half
+    are equal, and the int8-K twin holding the same codes with one scale per 64 dims."""
+    k4 = W.make_pool(rng, capacity=192, n_filled=n_cells, n_kv_heads=Hkv, page_cells=64, v_bits=4, k_bits=4)
+    k4.k_scales[..., 1] = k4.k_scales[..., 0]
+    k4.k_scales[..., 3] = k4.k_scales[..., 2]
+    raw = np.empty(k4.k_codes.shape[:-1] + (128,), np.int8)
+    raw[..., 0::2] = (k4.k_codes & 0x0F).astype(np.int8) - 8
+    raw[..., 1::2] = (k4.k_codes >> 4).astype(np.int8) - 8
+    k8 = W.Pool(raw, k4.v_codes.copy(), k4.k_scales[..., 0::2].copy(), k4.v_scales.copy(), k4.page_table.copy(),
+                k4.capacity, k4.n_filled, k4.page_cells, k4.n_kv_heads, k4.head_dim, k4.v_bits, k4.v_group)
+    return k4, k8
+
+
+def test_k4_dequantise_worked_by_hand():
+    """Bytes 0x8F, 0x07, 0xF0 of a 4-bit K row are dims 0..5 with codes 7, 0, -1, -8, -8, 7 (the nibble
+    fixture), times the scale of their 32-dim group; dims 32.. take the second group's scale."""
+    g = json.load(open(os.path.join(GOLD, "nibbles.json")))
+    pool = W.make_pool(np.random.default_rng(0), capacity=64, n_filled=64, n_kv_heads=1, page_cells=64,
+                       v_bits=4, k_bits=4)
+    phys = pool.page_table[0]
+    pool.k_codes[phys, 0, 3, :] = 0x88                         # every code 0
+    pool.k_codes[phys, 0, 3, :3] = g["bytes"]
+    pool.k_codes[phys, 0, 3, 16] = 0xF1                        # dims 32, 33: codes -7, 7
+    pool.k_scales[phys, 0, 3, :] = [0.5, 0.25, 2.0, 4.0]
+    k = O.dequantise_k(pool, 0, [3])[0]
+    assert k[:6].tolist() == [0.5 * c for c in g["expect_codes"]]
+    assert k[32:34].tolist() == [-7 * 0.25, 7 * 0.25]
+    assert not k[6:32].any() and not k[34:].any()
+
+
+def test_k4_pool_equals_its_int8_twin():
+    """The same codes read as 4-bit K (two equal 32-dim scales) or as int8 K (one 64-dim scale): block
+    scores, attention and a prompt row agree to rounding."""
+    k4, k8 = _k4_twin(np.random.default_rng(9))
+    cells = list(range(130))
+    for h in range(2):
+        assert np.array_equal(O.dequantise_k(k4, h, cells), O.dequantise_k(k8, h, cells))
+    q = np.random.default_rng(10).standard_normal((2, 6, 128)).astype(np.float32)
+    np.testing.assert_allclose(O.block_scores(k4, q, 64), O.block_scores(k8, q, 64), rtol=1e-12, atol=1e-12)
+    o4, l4 = O.attention(k4, q[0], 129, cells)
+    o8, l8 = O.attention(k8, q[0], 129, cells)
+    np.testing.assert_allclose(o4, o8, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(l4, l8, rtol=1e-12, atol=1e-12)
+
+
+def test_k4_append_round_trip():
+    """4-bit K appended comes back within half a step of its 32-dim group (qmax 7)."""
+    pool = W.make_pool(np.random.default_rng(2), capacity=128, n_filled=10, n_kv_heads=1, page_cells=64,
+                       v_bits=4, k_bits=4)
+    k_new = np.random.default_rng(3).standard_normal((20, 1, 128)).astype(np.float32)
+    out = O.append_cells(pool, k_new, k_new, 10)
+    back = O.dequantise_k(out, 0, list(range(10, 30)))
+    step = np.repeat(np.abs(k_new[:, 0].reshape(20, 4, 32)).max(axis=2) / 7, 32, axis=1)
+    assert (np.abs(back - k_new[:, 0]) <= 0.5 * step * (1 + 1e-5)).all()
+    assert out.k_scales.shape[-1] == 4

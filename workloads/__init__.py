@@ -43,6 +43,7 @@ K_GROUP = 64
 SCALE_LO = 0.005
 SCALE_HI = 0.02
 CODE_SIGMA = math.sqrt((255.0 ** 2 - 1.0) / 12.0)
+CODE_SIGMA_4 = math.sqrt((16.0 ** 2 - 1.0) / 12.0)   # spread of 4-bit codes uniform in [-8, 7]
 
 
 @dataclasses.dataclass
@@ -59,36 +60,48 @@ class Pool:
     head_dim: int
     v_bits: int
     v_group: int
+    k_bits: int = 8
+    k_group: int = 64
 
     @property
     def n_pages(self) -> int:
         return int(self.k_codes.shape[0])
 
 
+def _pack_nibbles(raw: np.ndarray) -> np.ndarray:
+    """4-bit codes in [-8, 7] -> bytes: nibble = code + 8, the even dim in the low nibble."""
+    nib = (raw.astype(np.int16) + 8).astype(np.uint8)
+    return (nib[..., 0::2] | (nib[..., 1::2] << 4)).astype(np.uint8)
+
+
 def make_pool(rng: np.random.Generator, *, capacity: int, n_filled: int, n_kv_heads: int,
               head_dim: int = HEAD_DIM, page_cells: int = 256, v_bits: int = 8,
-              bias_prob: float = 0.0) -> Pool:
+              bias_prob: float = 0.0, k_bits: int = 8) -> Pool:
     """Draw one paged pool.  Draw order: page table, K codes, K scales, V codes,
-    V scales, then (if bias_prob > 0) the bias mask and the bias directions."""
+    V scales, then (if bias_prob > 0) the bias mask and the bias directions.
+    k_bits = 4 (with v_bits = 4: the q4_0 layout) draws K codes in [-8, 7] with
+    one scale per 32 dims, packed as the 4-bit V codes are."""
     assert 0 <= n_filled <= capacity
-    assert head_dim % K_GROUP == 0 and v_bits in (4, 8)
+    assert head_dim % K_GROUP == 0 and v_bits in (4, 8) and k_bits in (4, 8)
     n_pages = (capacity + page_cells - 1) // page_cells
     v_group = 64 if v_bits == 8 else 32
+    k_group = 64 if k_bits == 8 else 32
     page_table = rng.permutation(n_pages).astype(np.int32)
     shape = (n_pages, n_kv_heads, page_cells, head_dim)
-    k_codes = rng.integers(-127, 128, size=shape, dtype=np.int8)
+    if k_bits == 8:
+        k_codes = rng.integers(-127, 128, size=shape, dtype=np.int8)
+    else:
+        k_codes = _pack_nibbles(rng.integers(-8, 8, size=shape, dtype=np.int8))
     k_scales = rng.uniform(SCALE_LO, SCALE_HI,
-                           size=(n_pages, n_kv_heads, page_cells, head_dim // K_GROUP)).astype(np.float32)
+                           size=(n_pages, n_kv_heads, page_cells, head_dim // k_group)).astype(np.float32)
     if v_bits == 8:
         v_codes = rng.integers(-127, 128, size=shape, dtype=np.int8)
     else:
-        raw = rng.integers(-8, 8, size=shape, dtype=np.int8)
-        nib = (raw.astype(np.int16) + 8).astype(np.uint8)
-        v_codes = (nib[..., 0::2] | (nib[..., 1::2] << 4)).astype(np.uint8)
+        v_codes = _pack_nibbles(rng.integers(-8, 8, size=shape, dtype=np.int8))
     v_scales = rng.uniform(SCALE_LO, SCALE_HI,
                            size=(n_pages, n_kv_heads, page_cells, head_dim // v_group)).astype(np.float32)
     pool = Pool(k_codes, v_codes, k_scales, v_scales, page_table, capacity, n_filled,
-                page_cells, n_kv_heads, head_dim, v_bits, v_group)
+                page_cells, n_kv_heads, head_dim, v_bits, v_group, k_bits, k_group)
     if bias_prob > 0.0 and n_filled > 0:
         biased = rng.random(n_filled) < bias_prob
         u = rng.standard_normal((n_kv_heads, head_dim))
@@ -98,8 +111,16 @@ def make_pool(rng: np.random.Generator, *, capacity: int, n_filled: int, n_kv_he
         phys = page_table[cells // page_cells]
         off = cells % page_cells
         for h in range(n_kv_heads):
-            cur = k_codes[phys, h, off, :].astype(np.int16) + add[h][None, :]
-            k_codes[phys, h, off, :] = np.clip(cur, -127, 127).astype(np.int8)
+            if k_bits == 8:
+                cur = k_codes[phys, h, off, :].astype(np.int16) + add[h][None, :]
+                k_codes[phys, h, off, :] = np.clip(cur, -127, 127).astype(np.int8)
+            else:   # the same direction at the 4-bit code spread
+                b = k_codes[phys, h, off, :]
+                raw = np.empty(b.shape[:-1] + (head_dim,), np.int16)
+                raw[..., 0::2] = (b & 0x0F).astype(np.int16) - 8
+                raw[..., 1::2] = (b >> 4).astype(np.int16) - 8
+                add4 = np.rint(3.0 * CODE_SIGMA_4 * u[h]).astype(np.int16)
+                k_codes[phys, h, off, :] = _pack_nibbles(np.clip(raw + add4[None, :], -8, 7))
     _poison_stale_cells(pool)
     return pool
 
