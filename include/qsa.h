@@ -62,14 +62,20 @@ typedef enum {
 
 /*
  * One slot's paged KV pool.  All pointers (dev), 16-byte aligned, caller-owned.
- *   k_codes    int8   [n_pages][n_kv_heads][page_cells][128]
+ *   k_codes    k_bits 8: int8 [n_pages][n_kv_heads][page_cells][128]
+ *              k_bits 4: uint8 [n_pages][n_kv_heads][page_cells][64], packed as
+ *              4-bit V codes are (the q4_0 layout with v_bits 4)
  *   v_codes    v_bits 8: int8 [n_pages][n_kv_heads][page_cells][128]
  *              v_bits 4: uint8 [n_pages][n_kv_heads][page_cells][64]; byte j
  *              holds dim 2j in its low nibble and dim 2j+1 in its high nibble,
  *              nibble = code + 8 (code in [-8, 7])
- *   k_scales   fp32   [n_pages][n_kv_heads][page_cells][2]   (64-dim groups)
+ *   k_scales   fp32   [n_pages][n_kv_heads][page_cells][128 / k_group],
+ *              k_group = 64 (k_bits 8) or 32 (k_bits 4)
  *   v_scales   fp32   [n_pages][n_kv_heads][page_cells][128 / v_group],
  *              v_group = 64 (v_bits 8) or 32 (v_bits 4)
+ * 4-bit K is served by qsa_decode_window, qsa_prompt_attn and qsa_kv_append;
+ * qsa_block_scores, qsa_decode_attn and qsa_decode_attn_noalloc answer
+ * QSA_ERR_UNSUPPORTED for it.  The pools of one decode window share k_bits.
  *   page_table int32  [ceil(capacity / page_cells)] logical -> physical page
  * Logical cell c is at physical page page_table[c / page_cells], offset
  * c % page_cells.  Cells 0 .. n_filled-1 hold data; others are never read.
@@ -88,6 +94,7 @@ typedef struct {
   int32_t n_kv_heads;   /* 1..16 */
   int32_t head_dim;     /* must be 128 */
   int32_t v_bits;       /* 8 or 4 */
+  int32_t k_bits;       /* 8, or 4 for 4-bit K (the q4_0 layout; decode window, prompt and append) */
 } qsa_pool;
 
 /*

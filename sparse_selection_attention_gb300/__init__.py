@@ -43,6 +43,7 @@ class QsaPoolC(ctypes.Structure):
         ("v_scales", ctypes.c_void_p), ("page_table", ctypes.c_void_p),
         ("n_filled", ctypes.c_int32), ("capacity", ctypes.c_int32), ("page_cells", ctypes.c_int32),
         ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("v_bits", ctypes.c_int32),
+        ("k_bits", ctypes.c_int32),
     ]
 
 
@@ -122,11 +123,12 @@ class DevicePool:
     """One slot's paged KV pool resident on the GPU (layout of include/qsa.h)."""
 
     def __init__(self, k_codes, v_codes, k_scales, v_scales, page_table, *, n_filled, capacity, page_cells,
-                 n_kv_heads, v_bits, head_dim=HEAD_DIM):
+                 n_kv_heads, v_bits, head_dim=HEAD_DIM, k_bits=8):
         self.k_codes, self.v_codes = k_codes, v_codes
         self.k_scales, self.v_scales, self.page_table = k_scales, v_scales, page_table
         self.n_filled, self.capacity, self.page_cells = int(n_filled), int(capacity), int(page_cells)
         self.n_kv_heads, self.v_bits, self.head_dim = int(n_kv_heads), int(v_bits), int(head_dim)
+        self.k_bits = int(k_bits)
 
     @classmethod
     def upload(cls, pool, device="cuda") -> "DevicePool":
@@ -134,12 +136,13 @@ class DevicePool:
         t = lambda a: torch.from_numpy(a).to(device)
         return cls(t(pool.k_codes), t(pool.v_codes), t(pool.k_scales), t(pool.v_scales), t(pool.page_table),
                    n_filled=pool.n_filled, capacity=pool.capacity, page_cells=pool.page_cells,
-                   n_kv_heads=pool.n_kv_heads, v_bits=pool.v_bits, head_dim=pool.head_dim)
+                   n_kv_heads=pool.n_kv_heads, v_bits=pool.v_bits, head_dim=pool.head_dim,
+                   k_bits=getattr(pool, "k_bits", 8))
 
     def c(self) -> QsaPoolC:
         return QsaPoolC(_ptr(self.k_codes), _ptr(self.v_codes), _ptr(self.k_scales), _ptr(self.v_scales),
                         _ptr(self.page_table), self.n_filled, self.capacity, self.page_cells, self.n_kv_heads,
-                        self.head_dim, self.v_bits)
+                        self.head_dim, self.v_bits, self.k_bits)
 
 
 def kv_append(pool: DevicePool, k: torch.Tensor, v: torch.Tensor, first_cell: int, stream=None) -> None:

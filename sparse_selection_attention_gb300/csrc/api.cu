@@ -46,6 +46,7 @@ qsa_status check_pool(const qsa_pool& p, bool need_v) {
     return QSA_ERR_ARG;
   if (p.head_dim != QSA_HEAD_DIM) return QSA_ERR_UNSUPPORTED;
   if (p.v_bits != 8 && p.v_bits != 4) return QSA_ERR_ARG;
+  if (p.k_bits != 8 && p.k_bits != 4) return QSA_ERR_ARG;
   if (p.page_cells <= 0 || p.page_cells % 64 != 0) return QSA_ERR_ARG;
   if (p.n_kv_heads < 1 || p.n_kv_heads > 16) return QSA_ERR_UNSUPPORTED;
   if (p.capacity < 0 || p.n_filled < 0 || p.n_filled > p.capacity) return QSA_ERR_ARG;
@@ -63,6 +64,7 @@ PoolDev to_dev(const qsa_pool& p) {
   d.page_cells = p.page_cells;
   d.page_shift = (p.page_cells & (p.page_cells - 1)) == 0 ? __builtin_ctz((unsigned)p.page_cells) : -1;
   d.v_bits = p.v_bits;
+  d.k_bits = p.k_bits;
   return d;
 }
 
@@ -76,7 +78,7 @@ qsa_status check_window(const qsa_pool* pools, int n_pools, const int32_t* row_p
   for (int i = 0; i < n_pools; ++i) {
     const qsa_status s = check_pool(pools[i], need_v);
     if (s != QSA_OK) return s;
-    if (pools[i].n_kv_heads != pools[0].n_kv_heads) return QSA_ERR_ARG;
+    if (pools[i].n_kv_heads != pools[0].n_kv_heads || pools[i].k_bits != pools[0].k_bits) return QSA_ERR_ARG;
   }
   for (int t = 0; t < n_rows; ++t)
     if (row_pool[t] < 0 || row_pool[t] >= n_pools) return QSA_ERR_ARG;
@@ -124,6 +126,7 @@ qsa_status qsa_block_scores(const qsa_pool* pools, int n_pools, const int32_t* r
                             void* stream) {
   qsa_status s = check_window(pools, n_pools, row_pool, n_rows, n_q_heads, false);
   if (s != QSA_OK) return s;
+  if (pools[0].k_bits != 8) return QSA_ERR_UNSUPPORTED;   // 4-bit K: the decode window serves it
   if (!q || !scores || !aligned16(q)) return QSA_ERR_ARG;
   if (block_cells != 32 && block_cells != 64 && block_cells != 128 && block_cells != 256) return QSA_ERR_ARG;
   ScoresParams p{};
@@ -193,6 +196,7 @@ qsa_status qsa_decode_attn(const qsa_pool* pools, int n_pools, const int32_t* ro
                            size_t partials_bytes, void* stream) {
   qsa_status s = check_window(pools, n_pools, row_pool, n_rows, n_q_heads, true);
   if (s != QSA_OK) return s;
+  if (pools[0].k_bits != 8) return QSA_ERR_UNSUPPORTED;   // 4-bit K: the decode window serves it
   if (!q || !row_pos || !ids || !n_sel || !partials) return QSA_ERR_ARG;
   if (!aligned16(partials) || !aligned16(q)) return QSA_ERR_ARG;
   if (k_cells < 0 || chunk_cells < 16 || chunk_cells > 1024 || chunk_cells % 16 != 0) return QSA_ERR_ARG;
@@ -444,6 +448,6 @@ qsa_status qsa_kv_append(const qsa_pool* pool, const float* k, const float* v, i
   return from_cuda(launch_kv_append(p, static_cast<cudaStream_t>(stream)));
 }
 
-int qsa_abi_version(void) { return 104; }
+int qsa_abi_version(void) { return 105; }
 
 }  // extern "C"

@@ -23,6 +23,7 @@ struct PoolDev {
   int page_cells;
   int page_shift;   // log2(page_cells) when page_cells is a power of two, else -1
   int v_bits;
+  int k_bits;
 };
 
 // Linear (page, head, cell) slot of logical cell c of KV head h.

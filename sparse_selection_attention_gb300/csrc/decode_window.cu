@@ -50,11 +50,13 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int w) {
 
 // ------------------------------------------------------------------------------------------ 1
 // Fragment layout (uint4 per lane): frag[((h * NT + nt) * 8 + s) * 32 + lane] holds, for row
-// 8 nt + lane / 4, the dims 64 grp + 16 (lane % 4) + 4 sp .. + 3 of k-step s = 4 grp + sp as
-// {hi(d0, d0+1), hi(d0+2, d0+3), lo(d0, d0+1), lo(d0+2, d0+3)}: the B operand of
-// mma.m16n8k16 for the same permutation of dims that the A fragments of the codes use.
+// 8 nt + lane / 4, four dims d0 .. d0 + 3 of k-step s as {hi(d0, d0+1), hi(d0+2, d0+3),
+// lo(d0, d0+1), lo(d0+2, d0+3)}: the B operand of mma.m16n8k16 for the same permutation of dims
+// that the A fragments of the codes use.  int8 K: k-step s = 4 grp + sp takes, in lane column
+// group tq = lane % 4, dims 64 grp + 16 tq + 4 sp (inside one 64-dim scale group).  4-bit K
+// (k4): k-step s = 2 gq + j takes dims 32 gq + 8 tq + 4 j (inside one 32-dim scale group).
 __global__ void __launch_bounds__(32) win_qprep_kernel(const float* __restrict__ q, int n_rows, int n_q_heads,
-                                                       int n_kv_heads, int NT, uint4* frag, float* inv_f) {
+                                                       int n_kv_heads, int NT, int k4, uint4* frag, float* inv_f) {
   const int t = blockIdx.x, h = blockIdx.y, lane = threadIdx.x;
   const int G = n_q_heads / n_kv_heads;
   pdl_trigger();
@@ -73,8 +75,10 @@ __global__ void __launch_bounds__(32) win_qprep_kernel(const float* __restrict__
   const int fe = scale_exp_128(amax);
   const float f = pow2i(fe);
   if (lane == 0 && t < n_rows) inv_f[t * n_kv_heads + h] = pow2i(-fe);
-  const int d0 = 4 * lane, grp = d0 >> 6, tqp = (d0 >> 4) & 3, sp = (d0 >> 2) & 3;
-  const int s = 4 * grp + sp, nt = t >> 3, gp = t & 7;
+  const int d0 = 4 * lane;
+  const int s = k4 ? 2 * (d0 >> 5) + ((d0 >> 2) & 1) : 4 * (d0 >> 6) + ((d0 >> 2) & 3);
+  const int tqp = k4 ? (d0 >> 3) & 3 : (d0 >> 4) & 3;
+  const int nt = t >> 3, gp = t & 7;
   uint32_t h01, l01, h23, l23;
   split_pair(v[0] * f, v[1] * f, h01, l01);
   split_pair(v[2] * f, v[3] * f, h23, l23);
@@ -90,17 +94,19 @@ constexpr int kScoreThreads = 256;
 constexpr size_t kFragSmemMax = 16384;   // q fragments staged in shared memory up to this size
 constexpr int kMaxInvF = 2 * kScoreThreads;   // (row, KV head) factors in shared memory (R * Hkv <= 32 * 16)
 
-template <int NT>
+// K4: 4-bit K codes (the q4_0 layout): rows of 64 bytes, four scales per cell.
+template <int NT, bool K4>
 __global__ void __launch_bounds__(kScoreThreads, 4) win_scores_kernel(const ScoresParams p,
                                                                        const uint4* __restrict__ frag,
                                                                        const float* __restrict__ inv_f) {
   extern __shared__ __align__(16) uint8_t sm[];
+  constexpr int kRow = K4 ? kD / 2 : kD, kNs = K4 ? 4 : 2;   // code bytes and scales per (head, cell)
   const int B = p.block_cells, Hkv = p.n_kv_heads, R = p.n_rows;
   const int lgB = 31 - __clz(B);   // B is a power of two
   const int mts = B >> 4, tpu = Hkv * mts;
-  uint8_t* codes = sm;                                                    // [Hkv][B][128]
-  float* kscale = reinterpret_cast<float*>(sm + (size_t)Hkv * B * kD);    // [Hkv][B][2]
-  float* part = kscale + (size_t)Hkv * B * 2;                             // [tpu][NT * 8]
+  uint8_t* codes = sm;                                                    // [Hkv][B][kRow]
+  float* kscale = reinterpret_cast<float*>(sm + (size_t)Hkv * B * kRow);  // [Hkv][B][kNs]
+  float* part = kscale + (size_t)Hkv * B * kNs;                           // [tpu][NT * 8]
   float* invf_s = part + (size_t)tpu * NT * 8;                            // [R][Hkv]
   uint4* frag_s = reinterpret_cast<uint4*>(invf_s + kMaxInvF);            // [Hkv][NT][8][32] (frag_smem)
   const int unit = blockIdx.x;
@@ -118,14 +124,22 @@ __global__ void __launch_bounds__(kScoreThreads, 4) win_scores_kernel(const Scor
       const int half = item & 1, hc = item >> 1, h = hc >> lgB, c = hc & (B - 1);
       if (c < n_b) {
         const long long slot = slot00 + (long long)h * pool.page_cells + c;
-        const int8_t* src = pool.k_codes + slot * kD + 64 * half;
-        uint8_t* dst = codes + (size_t)hc * kD + 64 * (half ^ (c & 1));   // odd rows: halves swapped
+        if constexpr (K4) {
+          const int8_t* src = pool.k_codes + slot * kRow + 32 * half;
+          uint8_t* dst = codes + (size_t)hc * kRow + 32 * half;
+          cp_async16(dst, src);
+          cp_async16(dst + 16, src + 16);
+          if (!half) cp_async16(kscale + 4 * hc, pool.k_scales + slot * 4);
+        } else {
+          const int8_t* src = pool.k_codes + slot * kD + 64 * half;
+          uint8_t* dst = codes + (size_t)hc * kD + 64 * (half ^ (c & 1));   // odd rows: halves swapped
 #pragma unroll
-        for (int k = 0; k < 4; ++k) cp_async16(dst + 16 * k, src + 16 * k);
-        if (!half) cp_async8(kscale + 2 * hc, pool.k_scales + slot * 2);
+          for (int k = 0; k < 4; ++k) cp_async16(dst + 16 * k, src + 16 * k);
+          if (!half) cp_async8(kscale + 2 * hc, pool.k_scales + slot * 2);
+        }
       } else if (!half) {
-        kscale[2 * hc] = 0.f;   // cells past the fill weigh nothing
-        kscale[2 * hc + 1] = 0.f;
+#pragma unroll
+        for (int k = 0; k < kNs; ++k) kscale[kNs * hc + k] = 0.f;   // cells past the fill weigh nothing
       }
     }
     cp_async_commit();
@@ -146,6 +160,7 @@ __global__ void __launch_bounds__(kScoreThreads, 4) win_scores_kernel(const Scor
   if (tid + kScoreThreads < R * Hkv) invf_s[tid + kScoreThreads] = invf1;
   __syncthreads();
 
+  if constexpr (!K4) {
   // Warp work item: TPW consecutive m-tiles of one KV head, which share every fragment load.
   constexpr int TPW = NT == 1 ? 2 : 1;
   const int ipb = (mts + TPW - 1) / TPW;   // items per head
@@ -230,6 +245,104 @@ __global__ void __launch_bounds__(kScoreThreads, 4) win_scores_kernel(const Scor
       }
     }
   }
+  } else {
+  // 4-bit K: lane column group tq holds, in 32-dim scale group gq, dims 32 gq + 8 tq .. + 7 (one 32-bit
+  // word: byte 16 gq + 4 tq of the 64-byte row); k-step s = 2 gq + j takes its dims 4 j .. 4 j + 3.
+  constexpr int TPW = NT == 1 ? 2 : 1;
+  const int ipb = (mts + TPW - 1) / TPW;   // items per head
+  for (int item = warp; item < Hkv * ipb; item += kScoreThreads / 32) {
+    const int h = item / ipb, mt0 = TPW * (item % ipb);
+    const int cnt = min(TPW, mts - mt0);
+    float d[TPW][NT][4][4];   // [m-tile][n-tile][32-dim K-scale group]
+#pragma unroll
+    for (int tt = 0; tt < TPW; ++tt)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int gq = 0; gq < 4; ++gq)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) d[tt][nt][gq][i] = 0.f;
+    const size_t fo = (size_t)h * NT * 8 * 32 + lane;
+#pragma unroll
+    for (int gq = 0; gq < 4; ++gq) {
+      uint32_t c[TPW][2];
+#pragma unroll
+      for (int tt = 0; tt < TPW; ++tt)
+#pragma unroll
+        for (int ab = 0; ab < 2; ++ab) {
+          const int row = h * B + 16 * (mt0 + tt) + g + 8 * ab;
+          c[tt][ab] = tt < cnt ? *reinterpret_cast<const uint32_t*>(codes + (size_t)row * kRow + 16 * gq + 4 * tq) : 0u;
+        }
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int s = 2 * gq + j;
+        uint32_t a[TPW][4];
+#pragma unroll
+        for (int tt = 0; tt < TPW; ++tt)
+#pragma unroll
+          for (int ab = 0; ab < 2; ++ab) {
+            // low nibbles = even dims, high nibbles = odd dims; bytes in dim order for this k-step
+            const uint32_t lo = c[tt][ab] & 0x0F0F0F0Fu, hi = (c[tt][ab] >> 4) & 0x0F0F0F0Fu;
+            const uint32_t pr = __byte_perm(lo, hi, j ? 0x7362 : 0x5140);
+            a[tt][ab] = byte_pair_h2(pr, 0x4140, kBiasNibble);
+            a[tt][2 + ab] = byte_pair_h2(pr, 0x4342, kBiasNibble);
+          }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const uint4 bf = fsm ? frag_s[fo + (nt * 8 + s) * 32] : __ldg(frag + fo + (nt * 8 + s) * 32);
+#pragma unroll
+          for (int tt = 0; tt < TPW; ++tt) {
+            if (tt < cnt) {
+              mma16816(d[tt][nt][gq], a[tt], bf.x, bf.y);
+              mma16816(d[tt][nt][gq], a[tt], bf.z, bf.w);
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int tt = 0; tt < TPW; ++tt) {
+      if (tt < cnt) {
+        const int task = h * mts + mt0 + tt;
+        const int row0 = h * B + 16 * (mt0 + tt) + g;
+        const float4 ks0 = *reinterpret_cast<const float4*>(kscale + 4 * row0);
+        const float4 ks1 = *reinterpret_cast<const float4*>(kscale + 4 * (row0 + 8));
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const float(&x)[4][4] = d[tt][nt];
+          float e0 = ks0.x * x[0][0];
+          e0 = fmaf(ks0.y, x[1][0], e0);
+          e0 = fmaf(ks0.z, x[2][0], e0);
+          e0 = fmaf(ks0.w, x[3][0], e0);
+          float e0b = ks1.x * x[0][2];
+          e0b = fmaf(ks1.y, x[1][2], e0b);
+          e0b = fmaf(ks1.z, x[2][2], e0b);
+          e0b = fmaf(ks1.w, x[3][2], e0b);
+          e0 += e0b;
+          float e1 = ks0.x * x[0][1];
+          e1 = fmaf(ks0.y, x[1][1], e1);
+          e1 = fmaf(ks0.z, x[2][1], e1);
+          e1 = fmaf(ks0.w, x[3][1], e1);
+          float e1b = ks1.x * x[0][3];
+          e1b = fmaf(ks1.y, x[1][3], e1b);
+          e1b = fmaf(ks1.z, x[2][3], e1b);
+          e1b = fmaf(ks1.w, x[3][3], e1b);
+          e1 += e1b;
+#pragma unroll
+          for (int o = 4; o < 32; o <<= 1) {
+            e0 += __shfl_xor_sync(0xffffffffu, e0, o);
+            e1 += __shfl_xor_sync(0xffffffffu, e1, o);
+          }
+          if (g == 0) {
+            const int rw = nt * 8 + 2 * tq;
+            part[task * NT * 8 + rw] = rw < R ? e0 * invf_s[rw * Hkv + h] : 0.f;
+            part[task * NT * 8 + rw + 1] = rw + 1 < R ? e1 * invf_s[(rw + 1) * Hkv + h] : 0.f;
+          }
+        }
+      }
+    }
+  }
+  }
   __syncthreads();
   // S[t, b] for the rows of this pool: lane l holds task l (head-major), then a fixed butterfly.
   for (int t = warp; t < R; t += kScoreThreads / 32) {
@@ -242,9 +355,9 @@ __global__ void __launch_bounds__(kScoreThreads, 4) win_scores_kernel(const Scor
 
 // ------------------------------------------------------------------------------------------ 4
 struct Stage {
-  int8_t k[kSub * kD];
+  int8_t k[kSub * kD];   // int8 K rows, or 64-byte 4-bit K rows at the same stride
   uint8_t v[kSub * kD];
-  float ks[kSub * 2];
+  float ks[kSub * 4];    // 2 (int8 K) or 4 (4-bit K) scales per cell
   float vs[kSub * 4];
   int valid[kSub];
 };
@@ -293,11 +406,20 @@ __device__ __forceinline__ void prefetch_sub(const WinAttnParams& p, const PoolD
     valid = cell <= pos && cell >= 0 && cell < pool.n_filled;
     if (valid) slot = cell_slot(pool, p.n_kv_heads, h, cell);
   }
+  const bool k4 = pool.k_bits == 4;
   if (valid) {
+    if (!k4) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int pc = 4 * half + k;
-      cp_async16(sg.k + c * kD + pc * 16, pool.k_codes + slot * kD + pc * 16);
+      for (int k = 0; k < 4; ++k) {
+        const int pc = 4 * half + k;
+        cp_async16(sg.k + c * kD + pc * 16, pool.k_codes + slot * kD + pc * 16);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int pc = 2 * half + k;
+        cp_async16(sg.k + c * kD + pc * 16, pool.k_codes + slot * (kD / 2) + pc * 16);
+      }
     }
     if (!v4) {
 #pragma unroll
@@ -314,7 +436,10 @@ __device__ __forceinline__ void prefetch_sub(const WinAttnParams& p, const PoolD
       }
       if (half) cp_async16(sg.vs + 4 * c, pool.v_scales + slot * 4);
     }
-    if (!half) cp_async8(sg.ks + 2 * c, pool.k_scales + slot * 2);
+    if (!half) {
+      if (k4) cp_async16(sg.ks + 4 * c, pool.k_scales + slot * 4);
+      else cp_async8(sg.ks + 4 * c, pool.k_scales + slot * 2);
+    }
   }
   if (!half) sg.valid[c] = valid;
   cp_async_commit();
@@ -329,6 +454,7 @@ __global__ void __launch_bounds__(kAttnThreads, 5) win_attn_kernel(const WinAttn
   const int pos = __ldg(p.row_pos + t);
   const PoolDev& pool = p.pools[p.row_pool[t]];
   const bool v4 = pool.v_bits == 4;
+  const bool k4 = pool.k_bits == 4;   // the same for every pool of the window
   const int n_vg = v4 ? 4 : 2;
 
   __shared__ __align__(16) Stage stages[2];
@@ -338,7 +464,8 @@ __global__ void __launch_bounds__(kAttnThreads, 5) win_attn_kernel(const WinAttn
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, tq = lane & 3;
 
-  // ---- q of head g (this thread's B columns): dims 16s + 4tq .. +3, s = 0..7, scaled by 2^fe
+  // ---- q of head g (this thread's B columns) for k-step s = 0..7: int8 K, dims 16s + 4tq .. +3;
+  // 4-bit K, dims 32 (s/2) + 8 tq + 4 (s%2) .. +3 (inside one 32-dim scale group), scaled by 2^fe
   // (max |q 2^fe| in [64, 128)) and split into fp16 hi + lo.  q is an input of the window, so this
   // runs before the wait for the selection.
   uint32_t qh[8][2], ql[8][2];
@@ -346,11 +473,12 @@ __global__ void __launch_bounds__(kAttnThreads, 5) win_attn_kernel(const WinAttn
   {
     float qv[8][4];
     float amax = 0.f;
-    const float* qrow = p.q + ((size_t)t * p.n_q_heads + h * G + min(g, G - 1)) * kD + 4 * tq;
+    const float* qrow = p.q + ((size_t)t * p.n_q_heads + h * G + min(g, G - 1)) * kD;
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
       float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (g < G) v = __ldg(reinterpret_cast<const float4*>(qrow + 16 * s));
+      const int d0 = k4 ? 32 * (s >> 1) + 8 * tq + 4 * (s & 1) : 16 * s + 4 * tq;
+      if (g < G) v = __ldg(reinterpret_cast<const float4*>(qrow + d0));
       qv[s][0] = v.x; qv[s][1] = v.y; qv[s][2] = v.z; qv[s][3] = v.w;
       amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
     }
@@ -391,36 +519,67 @@ __global__ void __launch_bounds__(kAttnThreads, 5) win_attn_kernel(const WinAttn
     }
     __syncthreads();
 
-    // ---- S^T = Kcode . (q f)^T on this warp's 16 cells, per K-scale group.
+    // ---- S^T = Kcode . (q f)^T on this warp's 16 cells, one accumulator per K-scale group (two
+    // 64-dim groups for int8 K, four 32-dim groups for 4-bit K).
     const int cb = 16 * warp;
-    float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+    float dk[4][4];
 #pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      const uint32_t w0 = *reinterpret_cast<const uint32_t*>(S.k + (cb + g) * kD + 16 * s + 4 * tq) ^ 0x80808080u;
-      const uint32_t w1 = *reinterpret_cast<const uint32_t*>(S.k + (cb + g + 8) * kD + 16 * s + 4 * tq) ^ 0x80808080u;
-      uint32_t a[4];
-      a[0] = byte_pair_h2(w0, 0x4140, kBiasS8);
-      a[2] = byte_pair_h2(w0, 0x4342, kBiasS8);
-      a[1] = byte_pair_h2(w1, 0x4140, kBiasS8);
-      a[3] = byte_pair_h2(w1, 0x4342, kBiasS8);
-      if (s < 4) {
-        mma16816(d0, a, qh[s][0], qh[s][1]);
-        mma16816(d0, a, ql[s][0], ql[s][1]);
-      } else {
-        mma16816(d1, a, qh[s][0], qh[s][1]);
-        mma16816(d1, a, ql[s][0], ql[s][1]);
+    for (int gq = 0; gq < 4; ++gq)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) dk[gq][i] = 0.f;
+    if (!k4) {
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(S.k + (cb + g) * kD + 16 * s + 4 * tq) ^ 0x80808080u;
+        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(S.k + (cb + g + 8) * kD + 16 * s + 4 * tq) ^ 0x80808080u;
+        uint32_t a[4];
+        a[0] = byte_pair_h2(w0, 0x4140, kBiasS8);
+        a[2] = byte_pair_h2(w0, 0x4342, kBiasS8);
+        a[1] = byte_pair_h2(w1, 0x4140, kBiasS8);
+        a[3] = byte_pair_h2(w1, 0x4342, kBiasS8);
+        mma16816(dk[s >> 2], a, qh[s][0], qh[s][1]);
+        mma16816(dk[s >> 2], a, ql[s][0], ql[s][1]);
+      }
+    } else {
+#pragma unroll
+      for (int gq = 0; gq < 4; ++gq) {
+        // one word per row: dims 32 gq + 8 tq .. + 7 (low nibble = even dim)
+        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(S.k + (cb + g) * kD + 16 * gq + 4 * tq);
+        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(S.k + (cb + g + 8) * kD + 16 * gq + 4 * tq);
+        const uint32_t lo0 = w0 & 0x0F0F0F0Fu, hi0 = (w0 >> 4) & 0x0F0F0F0Fu;
+        const uint32_t lo1 = w1 & 0x0F0F0F0Fu, hi1 = (w1 >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int s = 2 * gq + j;
+          const uint32_t p0 = __byte_perm(lo0, hi0, j ? 0x7362 : 0x5140);
+          const uint32_t p1 = __byte_perm(lo1, hi1, j ? 0x7362 : 0x5140);
+          uint32_t a[4];
+          a[0] = byte_pair_h2(p0, 0x4140, kBiasNibble);
+          a[2] = byte_pair_h2(p0, 0x4342, kBiasNibble);
+          a[1] = byte_pair_h2(p1, 0x4140, kBiasNibble);
+          a[3] = byte_pair_h2(p1, 0x4342, kBiasNibble);
+          mma16816(dk[gq], a, qh[s][0], qh[s][1]);
+          mma16816(dk[gq], a, ql[s][0], ql[s][1]);
+        }
       }
     }
     // ---- logits of cells cb+g, cb+g+8 for heads 2tq, 2tq+1; masked cells -> -inf.
     float z[4];
     {
       const bool va = S.valid[cb + g], vb = S.valid[cb + g + 8];
-      const float2 ka = *reinterpret_cast<const float2*>(S.ks + 2 * (cb + g));
-      const float2 kb = *reinterpret_cast<const float2*>(S.ks + 2 * (cb + g + 8));
-      z[0] = va ? fmaf(d1[0], ka.y, d0[0] * ka.x) * lam_lo : -INFINITY;
-      z[1] = va ? fmaf(d1[1], ka.y, d0[1] * ka.x) * lam_hi : -INFINITY;
-      z[2] = vb ? fmaf(d1[2], kb.y, d0[2] * kb.x) * lam_lo : -INFINITY;
-      z[3] = vb ? fmaf(d1[3], kb.y, d0[3] * kb.x) * lam_hi : -INFINITY;
+      const float4 ka = *reinterpret_cast<const float4*>(S.ks + 4 * (cb + g));
+      const float4 kb = *reinterpret_cast<const float4*>(S.ks + 4 * (cb + g + 8));
+      float x[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4 k = i < 2 ? ka : kb;
+        x[i] = fmaf(dk[1][i], k.y, dk[0][i] * k.x);
+        if (k4) x[i] = fmaf(dk[3][i], k.w, fmaf(dk[2][i], k.z, x[i]));
+      }
+      z[0] = va ? x[0] * lam_lo : -INFINITY;
+      z[1] = va ? x[1] * lam_hi : -INFINITY;
+      z[2] = vb ? x[2] * lam_lo : -INFINITY;
+      z[3] = vb ? x[3] * lam_hi : -INFINITY;
     }
     float mx0 = fmaxf(z[0], z[2]), mx1 = fmaxf(z[1], z[3]);
 #pragma unroll
@@ -1051,8 +1210,9 @@ cudaError_t launch_decode_window(const WindowArgs& a, cudaStream_t stream, cudaE
   //    previous window may still read the workspace).
   cudaError_t e = mark(0);
   if (e != cudaSuccess) return e;
-  e = launch_ex(win_qprep_kernel, dim3(NT * 8, Hkv), dim3(32), 0, stream, false, sp.q, R, sp.n_q_heads, Hkv, NT, frag,
-                inv_f);
+  const int k4 = sp.pools[0].k_bits == 4 ? 1 : 0;   // the pools of a window share k_bits
+  e = launch_ex(win_qprep_kernel, dim3(NT * 8, Hkv), dim3(32), 0, stream, false, sp.q, R, sp.n_q_heads, Hkv, NT, k4,
+                frag, inv_f);
   if (e != cudaSuccess) return e;
   e = mark(1);
   if (e != cudaSuccess) return e;
@@ -1062,11 +1222,15 @@ cudaError_t launch_decode_window(const WindowArgs& a, cudaStream_t stream, cudaE
     const size_t frag_bytes = (size_t)Hkv * NT * 8 * 32 * sizeof(uint4);
     ScoresParams spx = sp;
     spx.frag_smem = frag_bytes <= kFragSmemMax;
-    const size_t smem = (size_t)Hkv * sp.block_cells * (kD + 8) + sizeof(float) * ((size_t)tpu * NT * 8 + kMaxInvF) +
+    const size_t row_bytes = k4 ? kD / 2 + 16 : kD + 8;   // codes + scales of one (head, cell)
+    const size_t smem = (size_t)Hkv * sp.block_cells * row_bytes + sizeof(float) * ((size_t)tpu * NT * 8 + kMaxInvF) +
                         (spx.frag_smem ? frag_bytes : 0);
-    void (*kern)(ScoresParams, const uint4*, const float*) =
-        NT == 1 ? win_scores_kernel<1> : NT == 2 ? win_scores_kernel<2> : NT == 3 ? win_scores_kernel<3>
-                                                                         : win_scores_kernel<4>;
+    using Kern = void (*)(ScoresParams, const uint4*, const float*);
+    const Kern k8_kerns[4] = {win_scores_kernel<1, false>, win_scores_kernel<2, false>, win_scores_kernel<3, false>,
+                              win_scores_kernel<4, false>};
+    const Kern k4_kerns[4] = {win_scores_kernel<1, true>, win_scores_kernel<2, true>, win_scores_kernel<3, true>,
+                              win_scores_kernel<4, true>};
+    const Kern kern = k4 ? k4_kerns[NT - 1] : k8_kerns[NT - 1];
     e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
     e = launch_ex(kern, dim3(sp.total_units), dim3(kScoreThreads), smem, stream, pdl, spx, (const uint4*)frag,
@@ -1080,9 +1244,10 @@ cudaError_t launch_decode_window(const WindowArgs& a, cudaStream_t stream, cudaE
   if (e != cudaSuccess) return e;
   e = mark(3);
   if (e != cudaSuccess) return e;
-  // 4. split attention (warp-owned cells for int8 V; the chunk-style kernel when a pool has 4-bit V)
+  // 4. split attention (warp-owned cells for int8 K and V; the chunk-style kernel when a pool has 4-bit
+  //    V or 4-bit K)
   bool all_int8 = true;
-  for (int i = 0; i < sp.n_pools; ++i) all_int8 = all_int8 && sp.pools[i].v_bits == 8;
+  for (int i = 0; i < sp.n_pools; ++i) all_int8 = all_int8 && sp.pools[i].v_bits == 8 && sp.pools[i].k_bits == 8;
   if (all_int8)
     e = launch_ex(win_attn8_kernel, dim3(n_pairs * ap.n_splits), dim3(kAttnThreads), 0, stream, pdl, ap);
   else

@@ -1,11 +1,11 @@
 // Quantise-on-append of new K/V cells into a paged pool (qsa_kv_append).
 //
-// The pages store the cache as int8 codes (4-bit for the V of the K8V4 format) with one fp32
-// scale per (cell, KV head, group) ("#1367 prompt attention", Operands; "#2075 QSA decode
+// The pages store the cache as int8 codes (4-bit for the V of the K8V4 format, and for K and V of
+// the q4_0 format) with one fp32 scale per (cell, KV head, group) ("#1367 prompt attention", Operands; "#2075 QSA decode
 // attention", Bit for bit) and append the new cells of each row to it ("#2806 sycl: decode QSA
 // selection and attention in fewer, shorter launches", What it leaves alone).  They give no
 // quantiser; this one is symmetric by the group's largest magnitude:
-//   scale = amax / 127 (int8) or amax / 7 (4-bit V),
+//   scale = amax / 127 (int8) or amax / 7 (4-bit),
 //   code  = x / scale rounded to nearest, ties to even, clamped to +-127 (+-7),
 // with amax = 0 giving scale 0 and codes 0.  The division and the rounding are IEEE fp32
 // (round to nearest; the library is built without fast-math), so the codes are exact integers.
@@ -45,33 +45,32 @@ __device__ __forceinline__ uint32_t pack_s8(int a, int b, int c, int d) {
   return (uint32_t)(a & 0xFF) | ((uint32_t)(b & 0xFF) << 8) | ((uint32_t)(c & 0xFF) << 16) | ((uint32_t)(d & 0xFF) << 24);
 }
 
-// Quantises one (cell, KV head) whose K and V rows this warp holds (lane l: dims 4l .. 4l + 3).
-// int8 groups of 64 dims are 16 lanes, 4-bit V groups of 32 dims are 8 lanes.
+// Quantises one row (lane l: dims 4l .. 4l + 3) into a code row and its scales at `slot`: int8 with
+// one scale per 64 dims (16 lanes), or 4-bit (nibble = code + 8, the even dim in the low nibble)
+// with one scale per 32 dims (8 lanes).
+__device__ __forceinline__ void store_row(float4 x, int bits, uint8_t* codes, float* scales, long long slot, int lane) {
+  if (bits == 8) {
+    const float sc = group_scale(group_max(max_abs4(x), 16), 127.f), inv = __frcp_rn(sc);
+    reinterpret_cast<uint32_t*>(codes + slot * kD)[lane] =
+        pack_s8(quant_code(x.x, sc, inv, 127.f), quant_code(x.y, sc, inv, 127.f), quant_code(x.z, sc, inv, 127.f),
+                quant_code(x.w, sc, inv, 127.f));
+    if ((lane & 15) == 0) scales[slot * 2 + (lane >> 4)] = sc;
+  } else {
+    const float sc = group_scale(group_max(max_abs4(x), 8), 7.f), inv = __frcp_rn(sc);
+    const uint32_t n0 = (uint32_t)(quant_code(x.x, sc, inv, 7.f) + 8), n1 = (uint32_t)(quant_code(x.y, sc, inv, 7.f) + 8);
+    const uint32_t n2 = (uint32_t)(quant_code(x.z, sc, inv, 7.f) + 8), n3 = (uint32_t)(quant_code(x.w, sc, inv, 7.f) + 8);
+    reinterpret_cast<uint16_t*>(codes + slot * (kD / 2))[lane] = (uint16_t)(n0 | (n1 << 4) | (n2 << 8) | (n3 << 12));
+    if ((lane & 7) == 0) scales[slot * 4 + (lane >> 3)] = sc;
+  }
+}
+
+// Quantises one (cell, KV head) whose K and V rows this warp holds.
 __device__ __forceinline__ void append_item(const AppendParams& p, int item, float4 xk, float4 xv, int lane) {
   const int Hkv = p.n_kv_heads;
   const int i = item / Hkv, h = item % Hkv;
   const long long slot = cell_slot(p.pool, Hkv, h, p.first_cell + i);
-  // K: int8, one scale per 64 dims
-  {
-    const float sc = group_scale(group_max(max_abs4(xk), 16), 127.f), inv = __frcp_rn(sc);
-    reinterpret_cast<uint32_t*>(p.k_codes + slot * kD)[lane] =
-        pack_s8(quant_code(xk.x, sc, inv, 127.f), quant_code(xk.y, sc, inv, 127.f), quant_code(xk.z, sc, inv, 127.f),
-                quant_code(xk.w, sc, inv, 127.f));
-    if ((lane & 15) == 0) p.k_scales[slot * 2 + (lane >> 4)] = sc;
-  }
-  if (p.pool.v_bits == 8) {   // V: int8, one scale per 64 dims
-    const float sc = group_scale(group_max(max_abs4(xv), 16), 127.f), inv = __frcp_rn(sc);
-    reinterpret_cast<uint32_t*>(p.v_codes + slot * kD)[lane] =
-        pack_s8(quant_code(xv.x, sc, inv, 127.f), quant_code(xv.y, sc, inv, 127.f), quant_code(xv.z, sc, inv, 127.f),
-                quant_code(xv.w, sc, inv, 127.f));
-    if ((lane & 15) == 0) p.v_scales[slot * 2 + (lane >> 4)] = sc;
-  } else {                    // V: 4-bit, nibble = code + 8, even dim in the low nibble, one scale per 32 dims
-    const float sc = group_scale(group_max(max_abs4(xv), 8), 7.f), inv = __frcp_rn(sc);
-    const uint32_t n0 = (uint32_t)(quant_code(xv.x, sc, inv, 7.f) + 8), n1 = (uint32_t)(quant_code(xv.y, sc, inv, 7.f) + 8);
-    const uint32_t n2 = (uint32_t)(quant_code(xv.z, sc, inv, 7.f) + 8), n3 = (uint32_t)(quant_code(xv.w, sc, inv, 7.f) + 8);
-    reinterpret_cast<uint16_t*>(p.v_codes + slot * (kD / 2))[lane] = (uint16_t)(n0 | (n1 << 4) | (n2 << 8) | (n3 << 12));
-    if ((lane & 7) == 0) p.v_scales[slot * 4 + (lane >> 3)] = sc;
-  }
+  store_row(xk, p.pool.k_bits, reinterpret_cast<uint8_t*>(p.k_codes), p.k_scales, slot, lane);
+  store_row(xv, p.pool.v_bits, p.v_codes, p.v_scales, slot, lane);
 }
 
 // One (cell, KV head) item per warp, items cell-major (rows of k and v read in order).

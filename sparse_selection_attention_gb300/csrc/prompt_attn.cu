@@ -183,8 +183,13 @@ __global__ void __launch_bounds__(64) prompt_vmax_kernel(const PoolDev pool, int
       const float4 vs = __ldg(reinterpret_cast<const float4*>(pool.v_scales) + slot);
       mv = fmaxf(fmaxf(fabsf(vs.x), fabsf(vs.y)), fmaxf(fabsf(vs.z), fabsf(vs.w)));
     }
-    const float2 ks = __ldg(reinterpret_cast<const float2*>(pool.k_scales) + slot);
-    mk = fmaxf(fabsf(ks.x), fabsf(ks.y));
+    if (pool.k_bits == 8) {
+      const float2 ks = __ldg(reinterpret_cast<const float2*>(pool.k_scales) + slot);
+      mk = fmaxf(fabsf(ks.x), fabsf(ks.y));
+    } else {
+      const float4 ks = __ldg(reinterpret_cast<const float4*>(pool.k_scales) + slot);
+      mk = fmaxf(fmaxf(fabsf(ks.x), fabsf(ks.y)), fmaxf(fabsf(ks.z), fabsf(ks.w)));
+    }
   }
   mv = warp_max(mv);
   mk = warp_max(mk);
@@ -225,16 +230,18 @@ __global__ void __launch_bounds__(256) prompt_stage_kernel(const PoolDev pool, i
     const bool valid = cell0 + row < pool.n_filled;
     const long long slot = slot0 + row;
     float x[8];
-    if (blk < 2 || pool.v_bits == 8) {     // int8 codes, one scale per 64 dims
+    if ((blk < 2 ? pool.k_bits : pool.v_bits) == 8) {   // int8 codes, one scale per 64 dims
       const int8_t* codes = blk < 2 ? pool.k_codes : reinterpret_cast<const int8_t*>(pool.v_codes);
       const float* scales = blk < 2 ? pool.k_scales : pool.v_scales;
       const uint2 w = valid ? __ldg(reinterpret_cast<const uint2*>(codes + slot * kD + d0)) : make_uint2(0u, 0u);
       const float sc = valid ? __ldg(scales + slot * 2 + hf) * (blk < 2 ? ksh : vsh) : 0.f;
 #pragma unroll
       for (int k = 0; k < 8; ++k) x[k] = (float)(int8_t)((((k < 4) ? w.x : w.y) >> (8 * (k & 3))) & 0xFFu) * sc;
-    } else {                               // 4-bit V: byte j = dims 2j (low nibble), 2j + 1; one scale per 32 dims
-      const uint32_t w = valid ? __ldg(reinterpret_cast<const uint32_t*>(pool.v_codes + slot * (kD / 2) + d0 / 2)) : 0u;
-      const float sc = valid ? __ldg(pool.v_scales + slot * 4 + d0 / 32) * vsh : 0.f;
+    } else {   // 4-bit codes (V, or K of the q4_0 layout): byte j = dims 2j (low nibble), 2j + 1; one scale per 32 dims
+      const uint8_t* codes = blk < 2 ? reinterpret_cast<const uint8_t*>(pool.k_codes) : pool.v_codes;
+      const float* scales = blk < 2 ? pool.k_scales : pool.v_scales;
+      const uint32_t w = valid ? __ldg(reinterpret_cast<const uint32_t*>(codes + slot * (kD / 2) + d0 / 2)) : 0u;
+      const float sc = valid ? __ldg(scales + slot * 4 + d0 / 32) * (blk < 2 ? ksh : vsh) : 0.f;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const uint32_t b = (w >> (8 * k)) & 0xFFu;

@@ -3,6 +3,7 @@ path through the C ABI, and compare with the oracle."""
 import numpy as np
 import torch
 
+import oracle as O
 import sparse_selection_attention_gb300 as qsa
 
 # Gate for float outputs: max |gpu - oracle| / max |oracle| per tensor.
@@ -43,3 +44,24 @@ def gpu_ids(win):
     ids = win.ids.cpu().numpy()
     n_sel = win.n_sel.cpu().numpy()
     return [ids[t, :n_sel[t]].copy() for t in range(win.n_rows)], n_sel
+
+
+def run_window_and_check(case):
+    win, q, row_pos = upload_case(case)
+    win.out.fill_(float("nan"))
+    win.lse.fill_(float("nan"))
+    win.run_window(q, row_pos)
+    torch.cuda.synchronize()
+    R = case.n_rows
+    scores_gpu = win.scores.cpu().numpy()
+    ref = O.decode_window(case, scores_f32=scores_gpu)
+    for t in range(R):
+        nb = len(ref["scores"][t])
+        assert_close(scores_gpu[t, :nb], ref["scores"][t], f"scores row {t}")
+    ids, n_sel = gpu_ids(win)
+    for t in range(R):
+        assert n_sel[t] == ref["n_sel"][t], f"n_sel row {t}"
+        assert np.array_equal(ids[t], ref["ids"][t]), f"ids row {t}"
+    assert_close(win.out.cpu().numpy(), ref["out"], "out")
+    assert_close(win.lse.cpu().numpy(), ref["lse"], "lse")
+    return win, q, row_pos

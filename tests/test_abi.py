@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_pure_host_calls(lib):
-    assert qsa.abi_version() == 104
+    assert qsa.abi_version() == 105
     assert qsa.status_str(qsa.QSA_ERR_SCRATCH) == "scratch buffer too small"
     assert qsa.decode_partials_bytes(5, 24, 64) == 4 * 5 * 24 * 64 * 130
     assert qsa.decode_partials_bytes(0, 24, 64) == 0
@@ -46,7 +46,7 @@ def test_pure_host_calls(lib):
 
 def _pool(**kw):
     base = dict(k_codes=16, v_codes=32, k_scales=48, v_scales=64, page_table=80, n_filled=100, capacity=256,
-                page_cells=256, n_kv_heads=4, head_dim=128, v_bits=8)
+                page_cells=256, n_kv_heads=4, head_dim=128, v_bits=8, k_bits=8)
     base.update(kw)
     return qsa.QsaPoolC(*[base[f] for f, _ in qsa.QsaPoolC._fields_])
 
@@ -129,3 +129,17 @@ def test_kv_append_validation(lib):
     assert call(_pool(page_cells=96), 0, 1) == qsa.QSA_ERR_ARG       # pages of a multiple of 64 cells only
     assert call(_pool(head_dim=64), 0, 1) == qsa.QSA_ERR_UNSUPPORTED
     assert call(pool, 200, 0) == qsa.QSA_OK                          # nothing to append: nothing launched
+
+
+def test_four_bit_k_validation(lib):
+    """4-bit K (k_bits 4) is served by the decode window, the prompt and the append; the standalone
+    decode calls answer UNSUPPORTED; k_bits other than 8 and 4 is an argument error; the pools of one
+    window share k_bits."""
+    k4 = _pool(k_bits=4, v_bits=4)
+    assert _scores_call(lib, [k4], [0, 0]) == qsa.QSA_ERR_UNSUPPORTED
+    assert _scores_call(lib, [_pool(k_bits=5)], [0, 0]) == qsa.QSA_ERR_ARG
+    assert _scores_call(lib, [_pool(), k4], [0, 1]) == qsa.QSA_ERR_ARG          # mixed k_bits in one call
+    arr = (qsa.QsaPoolC * 1)(k4)
+    rp = (ctypes.c_int32 * 2)(0, 0)
+    assert lib.qsa_decode_attn(arr, 1, rp, 16, 32, 48, 64, 2, 24, 64, 64, 1, 256, 1 << 20, None) == \
+        qsa.QSA_ERR_UNSUPPORTED

@@ -9,33 +9,11 @@ import numpy as np
 import pytest
 import torch
 
-import oracle as O
 import sparse_selection_attention_gb300 as qsa
 import workloads as W
-from _parity import assert_close, gpu_ids, upload_case
+from _parity import assert_close, gpu_ids, run_window_and_check, upload_case
 
 pytestmark = pytest.mark.gpu
-
-
-def run_window_and_check(case):
-    win, q, row_pos = upload_case(case)
-    win.out.fill_(float("nan"))
-    win.lse.fill_(float("nan"))
-    win.run_window(q, row_pos)
-    torch.cuda.synchronize()
-    R = case.n_rows
-    scores_gpu = win.scores.cpu().numpy()
-    ref = O.decode_window(case, scores_f32=scores_gpu)
-    for t in range(R):
-        nb = len(ref["scores"][t])
-        assert_close(scores_gpu[t, :nb], ref["scores"][t], f"scores row {t}")
-    ids, n_sel = gpu_ids(win)
-    for t in range(R):
-        assert n_sel[t] == ref["n_sel"][t], f"n_sel row {t}"
-        assert np.array_equal(ids[t], ref["ids"][t]), f"ids row {t}"
-    assert_close(win.out.cpu().numpy(), ref["out"], "out")
-    assert_close(win.lse.cpu().numpy(), ref["lse"], "lse")
-    return win, q, row_pos
 
 
 def test_window_tiny_dense_decode():

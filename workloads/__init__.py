@@ -178,12 +178,12 @@ def decode_case(*, name: str, seed: int, fills: List[int], capacity: int, rows_p
                 n_q_heads: int, n_kv_heads: int, k_cells: int, chunk_cells: int,
                 block_cells: int = 64, page_cells: int = 256, bias_prob: float = 0.0,
                 n_chunks: Optional[int] = None, v_bits: int = 8,
-                row_pos: Optional[List[int]] = None) -> DecodeCase:
+                row_pos: Optional[List[int]] = None, k_bits: int = 8) -> DecodeCase:
     """Pools are drawn slot by slot, then q.  Rows of a slot are contiguous and
     sit at the last positions of its fill unless row_pos is given."""
     rng = np.random.default_rng(seed)
     pools = [make_pool(rng, capacity=capacity, n_filled=f, n_kv_heads=n_kv_heads,
-                       page_cells=page_cells, v_bits=v_bits, bias_prob=bias_prob) for f in fills]
+                       page_cells=page_cells, v_bits=v_bits, bias_prob=bias_prob, k_bits=k_bits) for f in fills]
     row_pool, pos = [], []
     for s, f in enumerate(fills):
         for r in range(rows_per_slot):
@@ -201,11 +201,11 @@ def decode_case(*, name: str, seed: int, fills: List[int], capacity: int, rows_p
 
 def prompt_case(*, name: str, seed: int, n_ctx: int, n_q: int, n_q_heads: int, n_kv_heads: int,
                 v_bits: int = 8, calls_of: Optional[int] = None, page_cells: int = 256,
-                capacity: Optional[int] = None) -> PromptCase:
+                capacity: Optional[int] = None, k_bits: int = 8) -> PromptCase:
     """Queries sit at the last n_q positions of the context (causal over them)."""
     rng = np.random.default_rng(seed)
     pool = make_pool(rng, capacity=capacity or n_ctx, n_filled=n_ctx, n_kv_heads=n_kv_heads,
-                     page_cells=page_cells, v_bits=v_bits)
+                     page_cells=page_cells, v_bits=v_bits, k_bits=k_bits)
     q = make_q(rng, n_q, n_q_heads)
     per = calls_of or n_q
     pos0 = n_ctx - n_q
