@@ -67,10 +67,17 @@ def peaks():
         return 6800.0, 1900.0, "fallback"
 
 
+def row_bytes(pool):
+    """(K code + scale bytes, V code + scale bytes) of one (cell, KV head) in the pool's layout."""
+    k = (K_ROW + KS_ROW) if getattr(pool, "k_bits", 8) == 8 else (K_ROW // 2 + 2 * KS_ROW)
+    v = (V_ROW + VS_ROW) if pool.v_bits == 8 else (V_ROW // 2 + 2 * VS_ROW)
+    return k, v
+
+
 def algorithmic_bytes(case, ids, n_sel):
     """(a1 bytes, a3 bytes) of one window: every filled K code + scale once; the union over rows
     of each pool's selected visible cells, K+V codes + scales, once per KV head."""
-    a1 = sum(p.n_filled * p.n_kv_heads * (K_ROW + KS_ROW) for p in case.pools)
+    a1 = sum(p.n_filled * p.n_kv_heads * row_bytes(p)[0] for p in case.pools)
     a3 = 0
     for pi, pool in enumerate(case.pools):
         cells = set()
@@ -79,7 +86,7 @@ def algorithmic_bytes(case, ids, n_sel):
                 continue
             sel = np.asarray(ids[t][: n_sel[t]])
             cells.update(sel[sel <= case.row_pos[t]].tolist())
-        a3 += len(cells) * pool.n_kv_heads * (K_ROW + KS_ROW + V_ROW + VS_ROW)
+        a3 += len(cells) * pool.n_kv_heads * sum(row_bytes(pool))
     return a1, a3
 
 
@@ -537,6 +544,31 @@ def run_ours(args):
             prompt["k8v4"] = run_prompt_k8v4(dev, stream, flush_l2, tc_peak, ws)
 
     kv_append = None if args.no_append else run_kv_append(dev, stream, flush_l2, hbm_peak, ws)
+    decode_q4_0 = None
+    if not args.no_long and args.case == "verify":
+        qcase = W.decode_case(name="q4_0 verify window", seed=11, fills=[32768], capacity=32768, rows_per_slot=5,
+                              n_q_heads=24, n_kv_heads=4, k_cells=4096, chunk_cells=64, v_bits=4, k_bits=4,
+                              bias_prob=0.05)
+        qwin, qq, qpos = window_of(qcase, dev)
+        for _ in range(3):
+            qwin.run_window(qq, qpos)
+        torch.cuda.synchronize()
+        qids, qsel = qwin.ids.cpu().numpy(), qwin.n_sel.cpu().numpy()
+        q1, q3 = algorithmic_bytes(qcase, [qids[t] for t in range(qcase.n_rows)], qsel)
+        qt = []
+        for _ in range(P):
+            flush_l2()
+            gpu_sleep()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            qwin.run_window(qq, qpos)
+            b.record(stream)
+            torch.cuda.synchronize()
+            qt.append(a.elapsed_time(b))
+        qms = max_over_ranks(float(np.mean(qt)), ws)
+        decode_q4_0 = {"workload": "decode verify window in the q4_0 layout (4-bit K and V, 32-dim scale groups): 5 rows, "
+                                   "24/4 heads, 32,768 cells, top-k 4,096", "ms_per_step": qms,
+                       "value": (q1 + q3) * ws / (qms * 1e-3) / 1e9, "unit": "GB/s", "bytes_per_step": q1 + q3}
 
     clocks.__exit__()
     line = {
@@ -556,6 +588,7 @@ def run_ours(args):
         "separate_calls_ms": float(np.mean(sep)),
         "graph_replay": graph_replay,
         "kv_append": kv_append,
+        "decode_q4_0": decode_q4_0,
         "e2e": {"value": bytes_step * ws / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 5 * K,
