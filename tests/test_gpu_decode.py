@@ -128,7 +128,8 @@ def test_topk_on_oracle_scores_and_adversarial_keys():
     for t in range(case.n_rows):
         rows.append((s64[t].astype(np.float32), 32768, 4096))
     specials = np.array([-np.inf, -1.0, -0.0, 0.0, 1.0, np.inf, np.nan, 2.0], np.float32)
-    for n_filled, k in [(64 * 3000, 64 * 700), (64 * 2000 - 5, 64 * 1999), (64 * 37 + 1, 64 * 38), (64 * 500, 64 * 3)]:
+    for n_filled, k in [(64 * 3000, 64 * 700), (64 * 2000 - 5, 64 * 1999), (64 * 37 + 1, 64 * 38), (64 * 500, 64 * 3),
+                        (64 * 16384, 64 * 4096), (64 * 16384 - 63, 64 * 1)]:   # QSA_MAX_TOPK_BLOCKS candidates
         nb = (n_filled + B - 1) // B
         rows.append((rng.choice(specials, nb).astype(np.float32), n_filled, k))
         rows.append((rng.integers(-3, 4, nb).astype(np.float32), n_filled, k))

@@ -34,6 +34,7 @@ def run_prompt(case, call):
     (64, 64, 2, 1, 8, 64),         # one tile, queries from position 0
     (1000, 37, 6, 6, 8, 128),      # G = 1
     (333, 333, 16, 1, 4, 64),      # G = 16, whole context is the prompt
+    (300, 12, 128, 1, 8, 64),      # G = 128 (the largest group): one query per CTA
     # fewer units than SMs: each unit cut into tile ranges merged by log-sum-exp
     (2000, 300, 2, 1, 8, 64),      # G = 2: 5 units of 27..32 tiles, 3 ranges each (ragged range ends)
     (3000, 64, 8, 2, 4, 128),      # 4-bit V, G = 4: 4 units of 47 tiles, 5 ranges each

@@ -52,6 +52,13 @@ def test_window_many_rows_two_pools():
     run_window_and_check(case)
 
 
+def test_window_max_rows():
+    """QSA_MAX_DECODE_ROWS (32) rows over two pools: four 8-row n-tiles in the block scores."""
+    case = W.decode_case(name="wmax", seed=32, fills=[3000, 2600], capacity=3072, rows_per_slot=16,
+                         n_q_heads=16, n_kv_heads=4, k_cells=512, chunk_cells=64, page_cells=256, bias_prob=0.05)
+    run_window_and_check(case)
+
+
 def test_window_many_waves_of_blocks_two_pools():
     """1,250 32-cell blocks over two pools (two waves and more of block-score CTAs) and 12 rows (two 8-row
     n-tiles, one q-fragment load per m-tile)."""
