@@ -259,6 +259,13 @@ def window_of(case, dev):
 
 
 KERNELS = ["q_prep", "block_scores", "topk", "split_attn", "merge"]
+
+
+def workload_config(case, a1, a3, workload):
+    """The workload part of the JSON line's config, the same for both arms."""
+    return {"workload": workload, "rows": case.n_rows, "q_heads": case.n_q_heads, "kv_heads": case.pools[0].n_kv_heads,
+            "cells": [p.n_filled for p in case.pools], "k_cells": case.k_cells, "block_cells": case.block_cells,
+            "bytes_per_step": a1 + a3, "scores_bytes": a1, "attention_union_bytes": a3}
 K8V4_WORKLOAD = ("large prompt with mixed KV: 8,192 queries at 122,880..131,071 over 131,072 cells, 32/8 heads, "
                  "int8 K / 4-bit V, four calls of 2,048 queries in one stream")
 
@@ -575,10 +582,7 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
         "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded; shapes of the pages' workloads)",
-        "config": {"workload": WORKLOAD if args.case == "verify" else LONG_WORKLOAD, "rows": case.n_rows,
-                   "q_heads": case.n_q_heads, "kv_heads": 4, "cells": [p.n_filled for p in case.pools],
-                   "k_cells": case.k_cells, "block_cells": case.block_cells,
-                   "bytes_per_step": bytes_step, "scores_bytes": a1, "attention_union_bytes": a3,
+        "config": {**workload_config(case, a1, a3, WORKLOAD if args.case == "verify" else LONG_WORKLOAD),
                    "call": "qsa_decode_window (5 launches chained by programmatic dependent launch)",
                    "l2": "flushed before every timed step, outside the events: 256 MB write, then 256 MB read",
                    "parallelism": f"{ws} independent replica(s)" if ws > 1 else "1 GPU"},
@@ -625,7 +629,8 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic (seeded; shapes of the pages' workloads)",
-        "config": {"workload": WORKLOAD, "bytes_per_step": bytes_step},
+        "config": {**workload_config(case, a1, a3, WORKLOAD),
+                   "call": "the oracle's decode window (oracle/qsa_oracle.py: decode_window)", "parallelism": "1 host core"},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": "full decode window per step (block scores, full-sort top-k, chunk partials, "
                                    "merge; FP64 numpy, one thread)"},
