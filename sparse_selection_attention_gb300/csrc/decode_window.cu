@@ -1138,14 +1138,16 @@ __global__ void __launch_bounds__(kAttnThreads, 4) win_attn8_kernel(const WinAtt
 // Host side
 
 int window_split_cells(int n_rows, int n_kv_heads, int k_cells, int n_sm) {
-  // about four 128-thread CTAs per SM in one wave, splits a multiple of the 16-cell slice, at most
-  // kMaxSplits splits per (row, KV head)
+  // at most four 128-thread CTAs per SM (one wave), at most kMaxSplits splits per (row, KV head), and
+  // splits a multiple of 64 cells: one 16-cell slice per warp per round, so the four warps of a CTA
+  // reach its closing barrier together
+  constexpr long long kUnit = 64;
   const long long total = (long long)n_rows * n_kv_heads * (k_cells > 0 ? k_cells : 1);
   const long long target = 4LL * (n_sm > 0 ? n_sm : 1);
-  long long sc = 16 * ((total + 16 * target - 1) / (16 * target));
-  const long long min_sc = 16 * (((long long)k_cells + 16LL * kMaxSplits - 1) / (16LL * kMaxSplits));
+  long long sc = kUnit * ((total + kUnit * target - 1) / (kUnit * target));
+  const long long min_sc = kUnit * (((long long)k_cells + kUnit * kMaxSplits - 1) / (kUnit * kMaxSplits));
   if (sc < min_sc) sc = min_sc;
-  if (sc < 16) sc = 16;
+  if (sc < kUnit) sc = kUnit;
   return (int)sc;
 }
 
