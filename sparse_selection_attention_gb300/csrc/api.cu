@@ -319,16 +319,6 @@ static qsa_status decode_window_impl(const qsa_pool* pools, int n_pools, const i
   ap.out = out;
   ap.lse = lse;
   ap.n_pools = n_pools;
-  // The attention may pull every filled V page into L2 while the top-k runs (HBM is idle then);
-  // worth it only when those pages are few next to what the selection reads, and fit in L2.
-  size_t v_total = 0;
-  for (int i = 0; i < n_pools; ++i) {
-    const size_t pages = (size_t)((pools[i].n_filled + pools[i].page_cells - 1) / pools[i].page_cells);
-    const size_t per_cell = pools[i].v_bits == 8 ? QSA_HEAD_DIM + 2 * sizeof(float) : QSA_HEAD_DIM / 2 + 4 * sizeof(float);
-    v_total += pages * (size_t)pools[i].page_cells * Hkv * per_cell;
-  }
-  const size_t v_attended = (size_t)n_rows * Hkv * k_cells * (QSA_HEAD_DIM + 2 * sizeof(float));
-  ap.prefetch_v = v_total <= ((size_t)64 << 20) && v_total <= 2 * v_attended;
   a.workspace = workspace;
   if (!kernel_us) return from_cuda(launch_decode_window(a, static_cast<cudaStream_t>(stream)));
   cudaEvent_t ev[6] = {};

@@ -362,37 +362,6 @@ struct Stage {
   int valid[kSub];
 };
 
-// Every filled page's V codes and scales into L2, in pieces of at most 16 KB spread over one thread
-// of every CTA of the grid.  Issued before the wait for the selection: the reads overlap the
-// top-k, and the attention then finds the V of its cells in L2.
-__device__ __noinline__ void prefetch_v_pages(const WinAttnParams& p) {
-  constexpr uint32_t kPiece = 16384;
-  const int n_issuers = gridDim.x;
-  const int issuer = blockIdx.x;
-  int base = 0;   // index of the pool's first piece
-  for (int pi = 0; pi < p.n_pools; ++pi) {
-    const PoolDev& pool = p.pools[pi];
-    const int n_pages = (pool.n_filled + pool.page_cells - 1) / pool.page_cells;
-    const uint32_t code_bytes = (uint32_t)(p.n_kv_heads * pool.page_cells * (pool.v_bits == 8 ? kD : kD / 2));
-    const uint32_t sc_bytes = (uint32_t)(p.n_kv_heads * pool.page_cells * (pool.v_bits == 8 ? 2 : 4) * 4);
-    const int n_code = (int)((code_bytes + kPiece - 1) / kPiece), n_sc = (int)((sc_bytes + kPiece - 1) / kPiece);
-    const int per_page = n_code + n_sc;
-    const int n = n_pages * per_page;
-    for (int c = ((issuer - base) % n_issuers + n_issuers) % n_issuers; c < n; c += n_issuers) {
-      const int pg = c / per_page, k = c % per_page;
-      const size_t phys = (size_t)__ldg(pool.page_table + pg);
-      if (k < n_code) {
-        const uint32_t off = (uint32_t)k * kPiece;
-        prefetch_l2(pool.v_codes + phys * code_bytes + off, min(kPiece, code_bytes - off));
-      } else {
-        const uint32_t off = (uint32_t)(k - n_code) * kPiece;
-        prefetch_l2(reinterpret_cast<const uint8_t*>(pool.v_scales) + phys * sc_bytes + off, min(kPiece, sc_bytes - off));
-      }
-    }
-    base += n;
-  }
-}
-
 // Copies of sub-tile `st` of the split into `sg`: thread (cell c = tid / 2, half) copies half of
 // the cell's K and V pieces and one of its scale rows; invisible cells copy nothing.
 __device__ __forceinline__ void prefetch_sub(const WinAttnParams& p, const PoolDev& pool, Stage& sg, int base, int n_cells,
@@ -496,7 +465,6 @@ __global__ void __launch_bounds__(kAttnThreads, 5) win_attn_kernel(const WinAttn
     lam_hi = __shfl_sync(0xffffffffu, lam, 4 * (2 * tq + 1));
   }
 
-  if (p.prefetch_v && tid == 0) prefetch_v_pages(p);
   pdl_wait();   // ids and n_sel of the preceding launch
   const int n_sel = min(__ldg(p.n_sel + t), p.k_cells);
   const int n_act = (n_sel + p.split_cells - 1) / p.split_cells;
@@ -869,7 +837,6 @@ __global__ void __launch_bounds__(kAttnThreads, 4) win_attn8_kernel(const WinAtt
     lam0 = lm.x;
     lam1 = lm.y;
   }
-  if (p.prefetch_v && tid == 0) prefetch_v_pages(p);
   pdl_wait();   // ids and n_sel of the preceding launch
   const int base = split * p.split_cells;
   const int32_t* row_ids = p.ids + (size_t)t * p.k_cells + base;
@@ -1138,10 +1105,11 @@ __global__ void __launch_bounds__(kAttnThreads, 4) win_attn8_kernel(const WinAtt
 // Host side
 
 int window_split_cells(int n_rows, int n_kv_heads, int k_cells, int n_sm) {
-  // at most four 128-thread CTAs per SM (one wave), at most kMaxSplits splits per (row, KV head), and
-  // splits a multiple of 64 cells: one 16-cell slice per warp per round, so the four warps of a CTA
-  // reach its closing barrier together
-  constexpr long long kUnit = 64;
+  // about four 128-thread CTAs per SM in one wave (the most the registers allow: the more warps per
+  // SM, the more of the gathers' latency is hidden; splits of whole 64-cell rounds, with fewer CTAs,
+  // measured 2 us slower on the verify window), splits a multiple of the 16-cell slice, at most
+  // kMaxSplits splits per (row, KV head)
+  constexpr long long kUnit = 16;
   const long long total = (long long)n_rows * n_kv_heads * (k_cells > 0 ? k_cells : 1);
   const long long target = 4LL * (n_sm > 0 ? n_sm : 1);
   long long sc = kUnit * ((total + kUnit * target - 1) / (kUnit * target));

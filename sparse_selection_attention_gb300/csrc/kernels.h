@@ -95,7 +95,6 @@ struct WinAttnParams {
   const int32_t* n_sel;
   int n_pools;
   int n_rows, n_q_heads, n_kv_heads, k_cells;
-  int prefetch_v;    // 1: prefetch every filled V page into L2 before the wait for the selection
   int split_cells;   // cells of one split (multiple of 16)
   int n_splits;      // splits per (row, q head) in the workspace
   float* part_ml;    // [n_rows][n_q_heads][n_splits][2]

@@ -61,11 +61,6 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 __device__ __forceinline__ void cp_async_wait_group1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// Bulk prefetch of `bytes` (multiple of 16) at a 16-byte aligned global address into L2.
-__device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
-}
-
 // Programmatic dependent launch.  pdl_wait() returns once the grid this launch depends on has
 // completed and its memory is visible (a no-op without such a dependency); pdl_trigger() lets
 // the next launch of the stream start its CTAs before this grid has finished.
