@@ -318,7 +318,6 @@ static qsa_status decode_window_impl(const qsa_pool* pools, int n_pools, const i
   ap.k_cells = k_cells;
   ap.out = out;
   ap.lse = lse;
-  ap.n_pools = n_pools;
   a.workspace = workspace;
   if (!kernel_us) return from_cuda(launch_decode_window(a, static_cast<cudaStream_t>(stream)));
   cudaEvent_t ev[6] = {};

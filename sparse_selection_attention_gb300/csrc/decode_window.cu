@@ -1,30 +1,27 @@
-// One decode window in one call (qsa_decode_window): block scores -> top-k ->
-// split-KV attention with the log-sum-exp merge fused in, as four launches
-// chained on one stream with programmatic dependent launch, so that each
-// launch's start-up and prologue overlap the tail of the one before
-// ("#2806 sycl: decode QSA selection and attention in fewer, shorter
-// launches", Summary and What changed: selection and attention of a window in
-// fewer launches; "#1888 QSA decode attention: split each query's cells
-// across blocks", Summary: each query's cells split among blocks and merged by
-// the log-sum-exp rescale in split order).
+// One decode window in one call (qsa_decode_window): q fragments -> block scores -> top-k ->
+// split-KV attention -> log-sum-exp merge, as five launches chained on one stream with
+// programmatic dependent launch, so that each launch's start-up and prologue overlap the tail of
+// the one before ("#2806 sycl: decode QSA selection and attention in fewer, shorter launches",
+// Summary and What changed: selection and attention of a window in fewer launches; "#1888 QSA
+// decode attention: split each query's cells across blocks", Summary: each query's cells split
+// among blocks and merged by the log-sum-exp rescale in split order).
 //
-//  1. win_qprep_kernel: per (row, KV head) qbar = sum of the group's q heads,
-//     scaled by a power of two and split into fp16 hi + lo, laid out as the
-//     block-score kernel's mma B fragments (computed once per window instead
-//     of once per CTA).
-//  2. win_scores_kernel: one CTA per (pool, block); all of the block's K
-//     codes and scales are copied into shared memory (cp.async) before the
-//     kernel waits for step 1; one warp task per (KV head, 16-cell m-tile).  S^T = Kcode .
-//     qbar on mma.sync; cell weights by K scale, fixed butterflies over cells,
-//     then over heads and m-tiles.  The result is the qsa_block_scores
-//     definition.
+//  1. win_qprep_kernel: per (row, KV head) qbar = sum of the group's q heads, scaled by a power
+//     of two and split into fp16 hi + lo, laid out as the block-score kernel's mma B fragments
+//     (computed once per window instead of once per CTA).
+//  2. win_scores_kernel: one CTA per (pool, block); all of the block's K codes and scales are
+//     copied into shared memory (cp.async) before the kernel waits for step 1; warp items of two
+//     16-cell m-tiles of one KV head share every fragment load.  S^T = Kcode . qbar on mma.sync
+//     (int8 codes, or 4-bit codes of the q4_0 layout); cell weights by K scale, fixed butterflies
+//     over cells, then over heads and m-tiles.  The result is the qsa_block_scores definition.
 //  3. topk_kernel (topk.cu), unchanged arithmetic.
-//  4. win_attn_kernel: one CTA per (row, KV head, split of the selection);
-//     each split's partial (m, l, o) per q head goes to the workspace in the
-//     qsa_decode_attn partials layout (a split of the window is a chunk of
-//     that layout).  Splits past the selection launch no work.
-//  5. attn_merge_kernel (decode_attn.cu): the log-sum-exp merge in split
-//     order, skipping empty splits; bitwise reproducible.
+//  4. win_attn8_kernel (int8 K and V: each warp owns its 16-cell slices) or win_attn_kernel
+//     (4-bit V or 4-bit K: the warps share 64-cell sub-tiles): one CTA per (row, KV head, split
+//     of the selection); each split's partial (m, l, o) per q head goes to the workspace in the
+//     qsa_decode_attn partials layout (a split of the window is a chunk of that layout).  Splits
+//     past the selection launch no work.
+//  5. attn_merge_kernel (decode_attn.cu): the log-sum-exp merge in split order, skipping empty
+//     splits; bitwise reproducible.
 #include "kernels.h"
 #include "mma_sync.cuh"
 

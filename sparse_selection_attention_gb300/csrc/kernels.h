@@ -93,7 +93,6 @@ struct WinAttnParams {
   const int32_t* row_pos;
   const int32_t* ids;
   const int32_t* n_sel;
-  int n_pools;
   int n_rows, n_q_heads, n_kv_heads, k_cells;
   int split_cells;   // cells of one split (multiple of 16)
   int n_splits;      // splits per (row, q head) in the workspace
