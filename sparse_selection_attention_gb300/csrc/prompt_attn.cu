@@ -8,7 +8,8 @@
 // K' = kcode * kscale and V' = vcode * vscale (scaled per KV head by a power
 // of two into fp16 range) are split once per tile into operand images, q and
 // p inside the kernel; each product is issued as hi.hi + hi.lo + lo.hi.
-// int8 and 4-bit V codes take the same path (the image holds V').
+// int8 and 4-bit codes (4-bit V; 4-bit K of the q4_0 layout) take the same
+// path (the images hold K' and V').
 #include <cuda_fp16.h>
 
 #include <algorithm>
@@ -41,7 +42,8 @@ __device__ __forceinline__ void raise_device_error(int code) { atomicCAS(&g_devi
 
 namespace ws {
 
-// Warp-specialised prompt attention for int8 V, in three launches.
+// Warp-specialised prompt attention, in three launches (four when the units of a partly empty last
+// round are cut into tile ranges).
 //
 // 1. prompt_vmax_kernel takes each KV head's largest |V scale| and |K scale| over the cells the
 //    call reads (atomic max on their bits): exponents kv_h, kk_h with max |scale| 2^k in [8, 16).
@@ -49,7 +51,7 @@ namespace ws {
 //    shared-memory image the tensor cores read: K' = kcode * kscale * 2^kk_h and V' = vcode *
 //    vscale * 2^kv_h, each split into fp16 hi + lo (22 significant bits), in the stored
 //    [cell][dim] order as two 64-dim blocks in the 128-byte swizzle (0 past n_filled).
-// 3. prompt_attn_ws_kernel, one CTA per (128 rows, KV head), 8 warps:
+// 3. prompt_attn_ws_kernel, one CTA per (128 rows, KV head), or per tile range of one, 8 warps:
 //      warp 0      one thread copies each tile image (one bulk copy) into a 3-stage ring;
 //      warp 1      issues every tcgen05.mma from one elected lane: S(i) = Q K'(i)^T as hi.hi +
 //                  hi.lo + lo.hi (Q in tensor memory) into one of two S slots of tensor memory;
@@ -66,7 +68,8 @@ namespace ws {
 //    round to nearest).  out = O 2^-(kv_h + 5) / l.  No thread barrier sits in the loop: every
 //    hand-off is an mbarrier with a bounded wait.  A wait that runs out sets the device error
 //    word; every role then stops at its next wait and the CTA drains its copies and MMAs before
-//    it exits.
+//    it exits.  A tile range writes its rows unnormalised with (m, l) instead.
+// 4. prompt_merge_kernel combines the ranges of each cut unit by log-sum-exp, in range order.
 constexpr int kThreads = 256;
 constexpr int kM = 128;
 constexpr int kN = 64;
