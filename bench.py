@@ -551,6 +551,26 @@ def run_ours(args):
             prompt["k8v4"] = run_prompt_k8v4(dev, stream, flush_l2, tc_peak, ws)
 
     kv_append = None if args.no_append else run_kv_append(dev, stream, flush_l2, hbm_peak, ws)
+    decode_tiny = None
+    if not args.no_long and args.case == "verify":
+        tcase = W.tiny_dense_decode()
+        twin, tq, tpos = window_of(tcase, dev)
+        for _ in range(3):
+            twin.run_window(tq, tpos)
+        torch.cuda.synchronize()
+        tt = []
+        for _ in range(P):
+            flush_l2()
+            gpu_sleep()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            twin.run_window(tq, tpos)
+            b.record(stream)
+            torch.cuda.synchronize()
+            tt.append(a.elapsed_time(b))
+        decode_tiny = {"workload": "tiny dense decode: 1 row, 2 q heads / 1 KV head, 1,024 int8 K/V cells, top-k = all "
+                                   "cells (latency-bound: microseconds per call)",
+                       "us_per_call": max_over_ranks(float(np.median(tt)), ws) * 1e3}
     decode_q4_0 = None
     if not args.no_long and args.case == "verify":
         qcase = W.decode_case(name="q4_0 verify window", seed=11, fills=[32768], capacity=32768, rows_per_slot=5,
@@ -593,6 +613,7 @@ def run_ours(args):
         "graph_replay": graph_replay,
         "kv_append": kv_append,
         "decode_q4_0": decode_q4_0,
+        "decode_tiny": decode_tiny,
         "e2e": {"value": bytes_step * ws / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 5 * K,
