@@ -298,7 +298,7 @@ def run_kv_append(dev, stream, flush_l2, hbm_peak, ws):
             b.record(stream)
             torch.cuda.synchronize()
             ts.append(a.elapsed_time(b))
-        us = max_over_ranks(float(np.median(ts)), ws) * 1e3
+        us = max_over_ranks(float(np.mean(ts)), ws) * 1e3
         nbytes = n * Hkv * (1024 + 136 + (136 if v_bits == 8 else 80))
         gbs = nbytes / (us * 1e-6) / 1e9
         res[name] = {"us": us, "algorithmic_bytes": nbytes, "GB/s": gbs * ws, "frac_hbm": gbs / hbm_peak}
@@ -420,7 +420,7 @@ def run_ours(args):
         flush_l2()
         gpu_sleep()
         per.append(win.run_window_profile(q, row_pos))
-    kern_us = np.median(np.array(per), axis=0)
+    kern_us = np.mean(np.array(per), axis=0)
     byte_of = {"block_scores": a1, "split_attn": a3}
     kernels = {}
     for j, n in enumerate(KERNELS):
@@ -503,7 +503,7 @@ def run_ours(args):
             b.record(stream)
             torch.cuda.synchronize()
             lt.append(a.elapsed_time(b))
-        lper = np.median(np.array([lwin.run_window_profile(lq, lpos) for _ in range(5)]), axis=0)
+        lper = np.mean(np.array([lwin.run_window_profile(lq, lpos) for _ in range(5)]), axis=0)
         lms = float(np.mean(lt))
         decode_long = {"workload": LONG_WORKLOAD, "ms_per_step": lms,
                        "value": (l1 + l3) / (lms * 1e-3) / 1e9, "unit": "GB/s",
@@ -570,7 +570,7 @@ def run_ours(args):
             tt.append(a.elapsed_time(b))
         decode_tiny = {"workload": "tiny dense decode: 1 row, 2 q heads / 1 KV head, 1,024 int8 K/V cells, top-k = all "
                                    "cells (latency-bound: microseconds per call)",
-                       "us_per_call": max_over_ranks(float(np.median(tt)), ws) * 1e3}
+                       "us_per_call": max_over_ranks(float(np.mean(tt)), ws) * 1e3}
     decode_q4_0 = None
     if not args.no_long and args.case == "verify":
         qcase = W.decode_case(name="q4_0 verify window", seed=11, fills=[32768], capacity=32768, rows_per_slot=5,
