@@ -302,6 +302,8 @@ def run_kv_append(dev, stream, flush_l2, hbm_peak, ws):
         nbytes = n * Hkv * (1024 + 136 + (136 if v_bits == 8 else 80))
         gbs = nbytes / (us * 1e-6) / 1e9
         res[name] = {"us": us, "algorithmic_bytes": nbytes, "GB/s": gbs * ws, "frac_hbm": gbs / hbm_peak}
+        if name == "cells_32768x8_k8v4":
+            res[name]["traffic"] = kernel_traffic("kv_append")   # DRAM bytes per launch (ncu), or None
     return res
 
 
