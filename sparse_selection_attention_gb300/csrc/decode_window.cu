@@ -15,11 +15,11 @@
 //     (int8 codes, or 4-bit codes of the q4_0 layout); cell weights by K scale, fixed butterflies
 //     over cells, then over heads and m-tiles.  The result is the qsa_block_scores definition.
 //  3. topk_kernel (topk.cu), unchanged arithmetic.
-//  4. win_attn8_kernel (int8 K and V: each warp owns its 16-cell slices) or win_attn_kernel
-//     (4-bit V or 4-bit K: the warps share 64-cell sub-tiles): one CTA per (row, KV head, split
-//     of the selection); each split's partial (m, l, o) per q head goes to the workspace in the
-//     qsa_decode_attn partials layout (a split of the window is a chunk of that layout).  Splits
-//     past the selection launch no work.
+//  4. win_attn8_kernel<K4, V4> (each warp owns its 16-cell slices; int8 or 4-bit K and V, one
+//     format per launch) or, for a window whose pools mix V formats, win_attn_kernel (the warps
+//     share 64-cell sub-tiles): one CTA per (row, KV head, split of the selection); each split's
+//     partial (m, l, o) per q head goes to the workspace in the qsa_decode_attn partials layout (a
+//     split of the window is a chunk of that layout).  Splits past the selection launch no work.
 //  5. attn_merge_kernel (decode_attn.cu): the log-sum-exp merge in split order, skipping empty
 //     splits; bitwise reproducible.
 #include "kernels.h"
@@ -683,27 +683,34 @@ __global__ void __launch_bounds__(kAttnThreads, 5) win_attn_kernel(const WinAttn
 }
 
 // ------------------------------------------------------------------------------------------ 4'
-// int8 V: the four warps of a CTA own their cells.  Warp w walks the 16-cell slices w, w + 4, ...
+// Warp-owned cells (int8 or 4-bit K, int8 or 4-bit V; one format per launch): the four warps of a
+// CTA own their cells.  Warp w walks the 16-cell slices w, w + 4, ...
 // of the split through its own two-stage cp.async ring and keeps its own online softmax (base-2
 // logits) and O^T accumulators, so no CTA barrier sits in the loop; the W = p * vscale operand is
 // formed once per (cell, head, V group).  The warps' states are combined in warp order at the end
 // of the split.
 //   QK^T: A = K codes of the slice (16 cells x 16 dims per k-step, converted exactly to fp16),
 //         B = q of the 8 heads scaled by 2^fe and split into fp16 hi + lo; one accumulator per
-//         64-dim K-scale group.
-//   PV:   A = V^T (16 dims x 16 cells), B = W of the slice in fp16 hi + lo per 64-dim V-scale
-//         group, accumulated in O^T (dims x heads).  m-tile mt holds the dims 64 (mt / 4) + 8 r +
-//         2 (mt % 4) (row r) and + 1 (row r + 8), so every m-tile lies in one V-scale group.
+//         K-scale group: int8 K, k-step s = 4 gr + w takes dims 64 gr + 16 tq + 4 w .. + 3 (two
+//         64-dim groups); 4-bit K, s = 2 gq + j takes dims 32 gq + 8 tq + 4 j .. + 3 (four 32-dim
+//         groups).
+//   PV:   A = V^T (16 dims x 16 cells), B = W of the slice in fp16 hi + lo per V-scale group,
+//         accumulated in O^T (dims x heads).  m-tile mt holds, in row r (and r + 8, the next dim):
+//         int8 V, dim 64 (mt / 4) + 8 r + 2 (mt % 4); 4-bit V, dim 32 (mt / 2) + 4 r + 2 (mt % 2);
+//         so every m-tile lies in one V-scale group.
 //   W is scaled by 2^kv[group] (max |vscale| 2^kv in [8, 16) over the slices seen so far; kv only
 //   decreases, and O's rows of that group are rescaled when it does).
 constexpr int kSlice = 16;
-constexpr int kPageCache = 1024;   // page-table entries the int8-V attention keeps in shared memory
+constexpr int kPageCache = 1024;   // page-table entries the attention keeps in shared memory
 
+// Code rows at a 128-byte stride (a 4-bit row uses 64 bytes of it); 2 (int8) or 4 (4-bit) scales
+// per cell.
+template <bool K4, bool V4>
 struct WarpStage {
   int8_t k[kSlice * kD];
   int8_t v[kSlice * kD];
-  float ks[kSlice * 2];
-  float vs[kSlice * 2];
+  float ks[kSlice * (K4 ? 4 : 2)];
+  float vs[kSlice * (V4 ? 4 : 2)];
 };
 
 // Id of this lane's cell (lane / 2) of the slice starting at split entry `first`, or -1 past the
@@ -717,8 +724,9 @@ __device__ __forceinline__ int slice_cell_id(const WinAttnParams& p, const int32
 // Copies the slice's cells (ids from slice_cell_id; lane: cell lane / 2, half lane % 2) into `sg`,
 // pages looked up in `pt` (the pool's page table, in shared memory when it fits); returns the warp's
 // ballot of visible cells (bit 2c + half for cell c).
+template <bool K4, bool V4>
 __device__ __forceinline__ uint32_t prefetch_slice(const WinAttnParams& p, const PoolDev& pool, const int32_t* pt,
-                                                   WarpStage& sg, int cell, int h, int pos) {
+                                                   WarpStage<K4, V4>& sg, int cell, int h, int pos) {
   const int lane = threadIdx.x & 31, c = lane >> 1, half = lane & 1;
   const bool valid = cell >= 0 && cell <= pos && cell < pool.n_filled;
   long long slot = 0;
@@ -735,17 +743,45 @@ __device__ __forceinline__ uint32_t prefetch_slice(const WinAttnParams& p, const
   }
   if (valid) {
     // 16-byte chunks swizzled within the 128-byte row so that the fragment reads below are free of
-    // bank conflicts: K chunk pc of cell c at pc ^ 4 (c & 1), V chunk pc at pc ^ 2 ((c >> 1) & 3).
+    // bank conflicts: int8 K chunk pc of cell c at pc ^ 4 (c & 1), 4-bit K chunk pc at pc ^ (c & 7);
+    // int8 V chunk pc at pc ^ 2 ((c >> 1) & 3), 4-bit V chunk pc at pc ^ ((c >> 1) & 3).
+    if constexpr (!K4) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int pc = 4 * half + k;
-      cp_async16(sg.k + c * kD + ((pc ^ (4 * (c & 1))) << 4), pool.k_codes + slot * kD + pc * 16);
-      cp_async16(sg.v + c * kD + ((pc ^ (2 * ((c >> 1) & 3))) << 4), pool.v_codes + slot * kD + pc * 16);
+      for (int k = 0; k < 4; ++k) {
+        const int pc = 4 * half + k;
+        cp_async16(sg.k + c * kD + ((pc ^ (4 * (c & 1))) << 4), pool.k_codes + slot * kD + pc * 16);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int pc = 2 * half + k;
+        cp_async16(sg.k + c * kD + ((pc ^ (c & 7)) << 4), pool.k_codes + slot * (kD / 2) + pc * 16);
+      }
     }
-    if (!half)
-      cp_async8(sg.ks + 2 * c, pool.k_scales + slot * 2);
-    else
-      cp_async8(sg.vs + 2 * c, pool.v_scales + slot * 2);
+    if constexpr (!V4) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int pc = 4 * half + k;
+        cp_async16(sg.v + c * kD + ((pc ^ (2 * ((c >> 1) & 3))) << 4), pool.v_codes + slot * kD + pc * 16);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int pc = 2 * half + k;
+        cp_async16(sg.v + c * kD + ((pc ^ ((c >> 1) & 3)) << 4), pool.v_codes + slot * (kD / 2) + pc * 16);
+      }
+    }
+    if (!half) {
+      if constexpr (K4)
+        cp_async16(sg.ks + 4 * c, pool.k_scales + slot * 4);
+      else
+        cp_async8(sg.ks + 2 * c, pool.k_scales + slot * 2);
+    } else {
+      if constexpr (V4)
+        cp_async16(sg.vs + 4 * c, pool.v_scales + slot * 4);
+      else
+        cp_async8(sg.vs + 2 * c, pool.v_scales + slot * 2);
+    }
   }
   cp_async_commit();
   return __ballot_sync(0xffffffffu, valid);
@@ -760,6 +796,91 @@ __device__ __forceinline__ float ex2f(float x) {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+__device__ __forceinline__ float f4_at(const float4& v, int i) {
+  return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+// P.V of one slice for 4-bit V (four 32-dim V-scale groups): the V-scale exponents kv (max |vscale|
+// 2^kv in [8, 16) over the slices seen so far, only decreasing), O rescaled by alpha (columns) and
+// by the change of kv (rows of the group), then per group W = p vscale 2^kv in fp16 hi + lo (b0 =
+// cells 2tq, 2tq+1, b1 = cells 2tq+8, 2tq+9) and O^T += V^T . W over its two m-tiles.  Lane (g, tq)
+// reads, of each of those cells, the two bytes of dims 32 gv + 4 g .. + 3 (chunk gv at gv ^ tq).
+template <typename StageT>
+__device__ __forceinline__ void pv_slice_v4(const StageT& S, float2 pA, float2 pB, bool c0, bool c1, bool c2,
+                                            bool c3, float al0, float al1, int g, int tq, int (&kv)[4],
+                                            bool (&have_kv)[4], float (&O)[8][4]) {
+  const float4 vs0 = *reinterpret_cast<const float4*>(S.vs + 4 * (2 * tq));
+  const float4 vs1 = *reinterpret_cast<const float4*>(S.vs + 4 * (2 * tq + 1));
+  const float4 vs2 = *reinterpret_cast<const float4*>(S.vs + 4 * (2 * tq + 8));
+  const float4 vs3 = *reinterpret_cast<const float4*>(S.vs + 4 * (2 * tq + 9));
+  float fac[4] = {1.f, 1.f, 1.f, 1.f};
+#pragma unroll
+  for (int gv = 0; gv < 4; ++gv) {
+    float vx = 0.f;
+    if (c0) vx = fmaxf(vx, fabsf(f4_at(vs0, gv)));
+    if (c1) vx = fmaxf(vx, fabsf(f4_at(vs1, gv)));
+    if (c2) vx = fmaxf(vx, fabsf(f4_at(vs2, gv)));
+    if (c3) vx = fmaxf(vx, fabsf(f4_at(vs3, gv)));
+    vx = fmaxf(vx, __shfl_xor_sync(0xffffffffu, vx, 1));
+    vx = fmaxf(vx, __shfl_xor_sync(0xffffffffu, vx, 2));
+    if (vx > 0.f) {   // warp-uniform: the lanes of one tq see the same cells
+      int e = 0;
+      frexpf(vx, &e);
+      const int k = max(-126, min(127, 4 - e));
+      if (!have_kv[gv]) {
+        kv[gv] = k;
+        have_kv[gv] = true;
+      } else if (k < kv[gv]) {
+        fac[gv] = pow2i(k - kv[gv]);
+        kv[gv] = k;
+      }
+    }
+  }
+  if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f) || fac[0] != 1.f || fac[1] != 1.f || fac[2] != 1.f ||
+      fac[3] != 1.f) {
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      const float f = fac[mt >> 1];
+      O[mt][0] *= al0 * f;
+      O[mt][1] *= al1 * f;
+      O[mt][2] *= al0 * f;
+      O[mt][3] *= al1 * f;
+    }
+  }
+#pragma unroll
+  for (int gv = 0; gv < 4; ++gv) {
+    const float sv = pow2i(kv[gv]);
+    uint32_t bh0, bl0, bh1, bl1;
+    split_pair(c0 ? pA.x * (f4_at(vs0, gv) * sv) : 0.f, c1 ? pA.y * (f4_at(vs1, gv) * sv) : 0.f, bh0, bl0);
+    split_pair(c2 ? pB.x * (f4_at(vs2, gv) * sv) : 0.f, c3 ? pB.y * (f4_at(vs3, gv) * sv) : 0.f, bh1, bl1);
+    const int off = ((gv ^ tq) << 4) + 2 * g;
+    uint32_t x[4];
+#pragma unroll
+    for (int q2 = 0; q2 < 4; ++q2) {
+      const int cell = 2 * tq + (q2 & 1) + 8 * (q2 >> 1);
+      const uint32_t bb = *reinterpret_cast<const uint16_t*>(S.v + cell * kD + off);
+      x[q2] = __byte_perm(bb & 0x0F0Fu, (bb >> 4) & 0x0F0Fu, 0x5140);   // nibbles -> bytes, dim order
+    }
+    // m-tile 2 gv: dims 32 gv + 4 g + {0, 1}; m-tile 2 gv + 1: + {2, 3}
+    const uint32_t y01l = __byte_perm(x[0], x[1], 0x5140), y01h = __byte_perm(x[0], x[1], 0x7362);
+    const uint32_t y23l = __byte_perm(x[2], x[3], 0x5140), y23h = __byte_perm(x[2], x[3], 0x7362);
+    uint32_t a0[4], a1[4];
+    a0[0] = byte_pair_h2(y01l, 0x4140, kBiasNibble);
+    a0[1] = byte_pair_h2(y01l, 0x4342, kBiasNibble);
+    a0[2] = byte_pair_h2(y23l, 0x4140, kBiasNibble);
+    a0[3] = byte_pair_h2(y23l, 0x4342, kBiasNibble);
+    a1[0] = byte_pair_h2(y01h, 0x4140, kBiasNibble);
+    a1[1] = byte_pair_h2(y01h, 0x4342, kBiasNibble);
+    a1[2] = byte_pair_h2(y23h, 0x4140, kBiasNibble);
+    a1[3] = byte_pair_h2(y23h, 0x4342, kBiasNibble);
+    mma16816(O[2 * gv], a0, bh0, bh1);
+    mma16816(O[2 * gv], a0, bl0, bl1);
+    mma16816(O[2 * gv + 1], a1, bh0, bh1);
+    mma16816(O[2 * gv + 1], a1, bl0, bl1);
+  }
+}
+
+template <bool K4, bool V4>
 __global__ void __launch_bounds__(kAttnThreads, 4) win_attn8_kernel(const WinAttnParams p) {
   const int R = p.n_rows, Hkv = p.n_kv_heads;
   const int n_pairs = R * Hkv;
@@ -769,7 +890,8 @@ __global__ void __launch_bounds__(kAttnThreads, 4) win_attn8_kernel(const WinAtt
   const int pos = __ldg(p.row_pos + t);
   const PoolDev& pool = p.pools[p.row_pool[t]];
 
-  __shared__ __align__(16) WarpStage ring[4][2];
+  using Stage8 = WarpStage<K4, V4>;
+  __shared__ __align__(16) Stage8 ring[4][2];
   __shared__ __align__(16) float pbuf[4][8][kSlice];
   __shared__ float wm[4][8], wl[4][8];
   __shared__ int32_t pt_s[kPageCache];
@@ -779,8 +901,9 @@ __global__ void __launch_bounds__(kAttnThreads, 4) win_attn8_kernel(const WinAtt
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, tq = lane & 3;
 
-  // ---- q of head g: for k-step s = 4 gr + w the dims 64 gr + 16 tq + 4 w .. + 3, scaled by 2^fe
-  // (max |q 2^fe| in [64, 128)) and split into fp16 hi + lo.  q is an input of the window, so
+  // ---- q of head g: for k-step s the dims of the K layout (int8: 64 gr + 16 tq + 4 w .. + 3 for
+  // s = 4 gr + w; 4-bit: 32 gq + 8 tq + 4 j .. + 3 for s = 2 gq + j), scaled by 2^fe (max |q 2^fe|
+  // in [64, 128)) and split into fp16 hi + lo.  q is an input of the window, so
   // this runs before the wait for the selection; warp 0 makes the fragments, the other warps of
   // the CTA (the same row and KV head) take them from shared memory.
   uint32_t qh[8][2], ql[8][2];
@@ -788,11 +911,12 @@ __global__ void __launch_bounds__(kAttnThreads, 4) win_attn8_kernel(const WinAtt
   if (warp == 0) {
     float qv[8][4];
     float amax = 0.f;
-    const float* qrow = p.q + ((size_t)t * p.n_q_heads + h * G + min(g, G - 1)) * kD + 16 * tq;
+    const float* qrow = p.q + ((size_t)t * p.n_q_heads + h * G + min(g, G - 1)) * kD;
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
       float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (g < G) v = __ldg(reinterpret_cast<const float4*>(qrow + 64 * (s >> 2) + 4 * (s & 3)));
+      const int d0 = K4 ? 32 * (s >> 1) + 8 * tq + 4 * (s & 1) : 64 * (s >> 2) + 16 * tq + 4 * (s & 3);
+      if (g < G) v = __ldg(reinterpret_cast<const float4*>(qrow + d0));
       qv[s][0] = v.x; qv[s][1] = v.y; qv[s][2] = v.z; qv[s][3] = v.w;
       amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
     }
@@ -849,7 +973,7 @@ __global__ void __launch_bounds__(kAttnThreads, 4) win_attn8_kernel(const WinAtt
   const int my_n = n_slices > warp ? (n_slices - warp + 3) / 4 : 0;
   if (kSlice * warp + (lane >> 1) >= n_cells) id_a = -1;
   if (kSlice * (warp + 4) + (lane >> 1) >= n_cells) id_b = -1;
-  WarpStage* rg = ring[warp];
+  Stage8* rg = ring[warp];
   float(*pb)[kSlice] = pbuf[warp];
 
   float m2[2] = {-INFINITY, -INFINITY};   // running max (base 2) of heads 2tq, 2tq+1
@@ -859,8 +983,14 @@ __global__ void __launch_bounds__(kAttnThreads, 4) win_attn8_kernel(const WinAtt
   for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
     for (int i = 0; i < 4; ++i) O[mt][i] = 0.f;
-  int kv[2] = {0, 0};
-  bool have_kv[2] = {false, false};
+  constexpr int kVG = V4 ? 4 : 2;   // V-scale groups
+  int kv[kVG];
+  bool have_kv[kVG];
+#pragma unroll
+  for (int gv = 0; gv < kVG; ++gv) {
+    kv[gv] = 0;
+    have_kv[gv] = false;
+  }
   uint32_t vmask[2] = {0u, 0u};
   if (my_n > 0) vmask[0] = prefetch_slice(p, pool, pt, rg[0], id_a, h, pos);
 
@@ -874,12 +1004,43 @@ __global__ void __launch_bounds__(kAttnThreads, 4) win_attn8_kernel(const WinAtt
       cp_async_wait_all();
     }
     __syncwarp();
-    const WarpStage& S = rg[st];
+    const Stage8& S = rg[st];
     const uint32_t vm = vmask[st];
 
     // ---- S^T = Kcode . (q f)^T, one accumulator per K-scale group
-    float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
-    {
+    constexpr int kKG = K4 ? 4 : 2;
+    float dk[kKG][4];
+#pragma unroll
+    for (int gq = 0; gq < kKG; ++gq)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) dk[gq][i] = 0.f;
+    if constexpr (K4) {
+#pragma unroll
+      for (int gq = 0; gq < 4; ++gq) {
+        // one word per row: dims 32 gq + 8 tq .. + 7 (low nibble = even dim); rows g and g + 8 share
+        // the swizzle (chunk gq at gq ^ g)
+        const int off = ((gq ^ g) << 4) + 4 * tq;
+        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(S.k + g * kD + off);
+        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(S.k + (g + 8) * kD + off);
+        const uint32_t lo0 = w0 & 0x0F0F0F0Fu, hi0 = (w0 >> 4) & 0x0F0F0F0Fu;
+        const uint32_t lo1 = w1 & 0x0F0F0F0Fu, hi1 = (w1 >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int s = 2 * gq + j;
+          const uint32_t p0 = __byte_perm(lo0, hi0, j ? 0x7362 : 0x5140);
+          const uint32_t p1 = __byte_perm(lo1, hi1, j ? 0x7362 : 0x5140);
+          uint32_t a[4];
+          a[0] = byte_pair_h2(p0, 0x4140, kBiasNibble);
+          a[2] = byte_pair_h2(p0, 0x4342, kBiasNibble);
+          a[1] = byte_pair_h2(p1, 0x4140, kBiasNibble);
+          a[3] = byte_pair_h2(p1, 0x4342, kBiasNibble);
+          mma16816(dk[gq], a, qh[s][0], qh[s][1]);
+          mma16816(dk[gq], a, ql[s][0], ql[s][1]);
+        }
+      }
+    } else {
+      float(&d0)[4] = dk[0];
+      float(&d1)[4] = dk[kKG - 1];
       const int sk = 4 * (g & 1);   // rows g and g + 8 share the swizzle
       const uint4 ca0 = *reinterpret_cast<const uint4*>(S.k + g * kD + ((tq ^ sk) << 4));
       const uint4 ca1 = *reinterpret_cast<const uint4*>(S.k + g * kD + (((4 + tq) ^ sk) << 4));
@@ -907,13 +1068,26 @@ __global__ void __launch_bounds__(kAttnThreads, 4) win_attn8_kernel(const WinAtt
     // ---- base-2 logits of cells g, g+8 for heads 2tq, 2tq+1; masked cells -> -inf
     const bool va = (vm >> (2 * g)) & 1u, vb = (vm >> (2 * g + 16)) & 1u;
     float z[4];
-    {
+    if constexpr (K4) {
+      const float4 ka = *reinterpret_cast<const float4*>(S.ks + 4 * g);
+      const float4 kb = *reinterpret_cast<const float4*>(S.ks + 4 * (g + 8));
+      float x[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4 k = i < 2 ? ka : kb;
+        x[i] = fmaf(dk[3][i], k.w, fmaf(dk[2][i], k.z, fmaf(dk[1][i], k.y, dk[0][i] * k.x)));
+      }
+      z[0] = va ? x[0] * lam0 : -INFINITY;
+      z[1] = va ? x[1] * lam1 : -INFINITY;
+      z[2] = vb ? x[2] * lam0 : -INFINITY;
+      z[3] = vb ? x[3] * lam1 : -INFINITY;
+    } else {
       const float2 ka = *reinterpret_cast<const float2*>(S.ks + 2 * g);
       const float2 kb = *reinterpret_cast<const float2*>(S.ks + 2 * (g + 8));
-      z[0] = va ? fmaf(d1[0], ka.y, d0[0] * ka.x) * lam0 : -INFINITY;
-      z[1] = va ? fmaf(d1[1], ka.y, d0[1] * ka.x) * lam1 : -INFINITY;
-      z[2] = vb ? fmaf(d1[2], kb.y, d0[2] * kb.x) * lam0 : -INFINITY;
-      z[3] = vb ? fmaf(d1[3], kb.y, d0[3] * kb.x) * lam1 : -INFINITY;
+      z[0] = va ? fmaf(dk[1][0], ka.y, dk[0][0] * ka.x) * lam0 : -INFINITY;
+      z[1] = va ? fmaf(dk[1][1], ka.y, dk[0][1] * ka.x) * lam1 : -INFINITY;
+      z[2] = vb ? fmaf(dk[1][2], kb.y, dk[0][2] * kb.x) * lam0 : -INFINITY;
+      z[3] = vb ? fmaf(dk[1][3], kb.y, dk[0][3] * kb.x) * lam1 : -INFINITY;
     }
     float mx0 = fmaxf(z[0], z[2]), mx1 = fmaxf(z[1], z[3]);
 #pragma unroll
@@ -941,10 +1115,13 @@ __global__ void __launch_bounds__(kAttnThreads, 4) win_attn8_kernel(const WinAtt
     __syncwarp();
     const float2 pA = *reinterpret_cast<const float2*>(&pb[g][2 * tq]);
     const float2 pB = *reinterpret_cast<const float2*>(&pb[g][2 * tq + 8]);
-    const float4 vsA = *reinterpret_cast<const float4*>(S.vs + 4 * tq);         // cells 2tq, 2tq+1: (g0, g1)
-    const float4 vsB = *reinterpret_cast<const float4*>(S.vs + 4 * tq + 16);    // cells 2tq+8, 2tq+9
     const bool c0 = (vm >> (4 * tq)) & 1u, c1 = (vm >> (4 * tq + 2)) & 1u;
     const bool c2 = (vm >> (4 * tq + 16)) & 1u, c3 = (vm >> (4 * tq + 18)) & 1u;
+    if constexpr (V4) {
+      pv_slice_v4(S, pA, pB, c0, c1, c2, c3, al0, al1, g, tq, kv, have_kv, O);
+    } else {
+    const float4 vsA = *reinterpret_cast<const float4*>(S.vs + 4 * tq);         // cells 2tq, 2tq+1: (g0, g1)
+    const float4 vsB = *reinterpret_cast<const float4*>(S.vs + 4 * tq + 16);    // cells 2tq+8, 2tq+9
 
     // ---- V-scale exponent per group (slice maximum over visible cells; kv only decreases)
     float fac[2] = {1.f, 1.f};
@@ -1043,6 +1220,7 @@ __global__ void __launch_bounds__(kAttnThreads, 4) win_attn8_kernel(const WinAtt
         }
       }
     }
+    }   // int8 V
     __syncwarp();   // the stage and pb are rewritten by the slice after next
   }
 
@@ -1057,11 +1235,10 @@ __global__ void __launch_bounds__(kAttnThreads, 4) win_attn8_kernel(const WinAtt
   __syncwarp();
   float* wo = reinterpret_cast<float*>(rg);   // this warp's ring: O^T as [head][128]
   {
-    const float u0 = pow2i(-kv[0]), u1 = pow2i(-kv[1]);
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
-      const float u = mt < 4 ? u0 : u1;
-      const int dim = 64 * (mt >> 2) + 8 * g + 2 * (mt & 3);
+      const float u = pow2i(-kv[V4 ? mt >> 1 : mt >> 2]);
+      const int dim = V4 ? 32 * (mt >> 1) + 4 * g + 2 * (mt & 1) : 64 * (mt >> 2) + 8 * g + 2 * (mt & 3);
       wo[(2 * tq) * kD + dim] = O[mt][0] * u;
       wo[(2 * tq + 1) * kD + dim] = O[mt][1] * u;
       wo[(2 * tq) * kD + dim + 1] = O[mt][2] * u;
@@ -1211,14 +1388,19 @@ cudaError_t launch_decode_window(const WindowArgs& a, cudaStream_t stream, cudaE
   if (e != cudaSuccess) return e;
   e = mark(3);
   if (e != cudaSuccess) return e;
-  // 4. split attention (warp-owned cells for int8 K and V; the chunk-style kernel when a pool has 4-bit
-  //    V or 4-bit K)
-  bool all_int8 = true;
-  for (int i = 0; i < sp.n_pools; ++i) all_int8 = all_int8 && sp.pools[i].v_bits == 8 && sp.pools[i].k_bits == 8;
-  if (all_int8)
-    e = launch_ex(win_attn8_kernel, dim3(n_pairs * ap.n_splits), dim3(kAttnThreads), 0, stream, pdl, ap);
+  // 4. split attention: warp-owned cells when the window's pools share one V format (the K format
+  //    is shared by validation); the chunk-style kernel for pools of mixed V formats
+  bool same_v = true;
+  for (int i = 1; i < sp.n_pools; ++i) same_v = same_v && sp.pools[i].v_bits == sp.pools[0].v_bits;
+  const dim3 agrid(n_pairs * ap.n_splits);
+  if (!same_v)
+    e = launch_ex(win_attn_kernel, agrid, dim3(kAttnThreads), 0, stream, pdl, ap);
+  else if (sp.pools[0].v_bits == 8)
+    e = k4 ? launch_ex(win_attn8_kernel<true, false>, agrid, dim3(kAttnThreads), 0, stream, pdl, ap)
+           : launch_ex(win_attn8_kernel<false, false>, agrid, dim3(kAttnThreads), 0, stream, pdl, ap);
   else
-    e = launch_ex(win_attn_kernel, dim3(n_pairs * ap.n_splits), dim3(kAttnThreads), 0, stream, pdl, ap);
+    e = k4 ? launch_ex(win_attn8_kernel<true, true>, agrid, dim3(kAttnThreads), 0, stream, pdl, ap)
+           : launch_ex(win_attn8_kernel<false, true>, agrid, dim3(kAttnThreads), 0, stream, pdl, ap);
   if (e != cudaSuccess) return e;
   e = mark(4);
   if (e != cudaSuccess) return e;
