@@ -5,6 +5,8 @@ launches) against the FP64 oracle, through the C ABI.
 Gates as for the four separate calls: ids bit-exact given the GPU's own fp32
 scores; scores, out and lse within max |gpu - oracle| / max |oracle| <= 1e-5;
 bitwise run-to-run determinism."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -48,6 +50,24 @@ def test_window_many_rows_two_pools():
     """20 rows (three 8-row n-tiles) over two pools in one call."""
     case = W.decode_case(name="wmany", seed=77, fills=[2000, 1500], capacity=2048, rows_per_slot=10,
                          n_q_heads=16, n_kv_heads=8, k_cells=256, chunk_cells=64, page_cells=256,
+                         bias_prob=0.05)
+    run_window_and_check(case)
+
+
+def test_window_pools_of_mixed_v_formats():
+    """An int8-V pool and a 4-bit-V pool in one call: the attention takes the kernel whose warps
+    share sub-tiles, which reads each pool in its own format."""
+    case = W.decode_case(name="wmixv", seed=55, fills=[1500, 1200], capacity=1536, rows_per_slot=3,
+                         n_q_heads=8, n_kv_heads=2, k_cells=256, chunk_cells=64, page_cells=256, bias_prob=0.05)
+    rng = np.random.default_rng(56)
+    pool4 = W.make_pool(rng, capacity=1536, n_filled=1200, n_kv_heads=2, page_cells=256, v_bits=4, bias_prob=0.05)
+    run_window_and_check(dataclasses.replace(case, pools=[case.pools[0], pool4]))
+
+
+def test_window_4bit_k_with_int8_v():
+    """4-bit K (32-dim K-scale groups) with int8 V."""
+    case = W.decode_case(name="wk4v8", seed=57, fills=[1800], capacity=1900, rows_per_slot=4, n_q_heads=12,
+                         n_kv_heads=2, k_cells=384, chunk_cells=64, page_cells=128, v_bits=8, k_bits=4,
                          bias_prob=0.05)
     run_window_and_check(case)
 
