@@ -407,20 +407,24 @@ __global__ void __launch_bounds__(kMergeThreads) attn_merge_kernel(const MergePa
   const int d = tid & (kD - 1), qtr = tid >> 7;
   ms::pdl_wait();   // partials of the preceding launch (a no-op without that dependency)
   const int n_sel = __ldg(p.n_sel + t);
-  const int n_act = min(p.n_chunks, (max(n_sel, 0) + p.chunk_cells - 1) / p.chunk_cells);
   const size_t base = ((size_t)t * p.n_q_heads + g) * p.n_chunks;
-  // Chunk partials of this quarter's first chunks, loaded before their weights are known.
+  // Chunk partials of this quarter's first chunks and this thread's (m, l), loaded before their
+  // weights are known and, inside the partials buffer, before n_sel is: chunks past the selection
+  // are dropped below without being read for anything.
   constexpr int kPre = 16;
   float o_pre[kPre];
   const float* o = p.o + base * kD + d;
 #pragma unroll
   for (int i = 0; i < kPre; ++i) {
     const int jj = qtr + 4 * i;
-    o_pre[i] = jj < n_act ? __ldg(o + (size_t)jj * kD) : 0.f;
+    o_pre[i] = jj < p.n_chunks ? __ldg(o + (size_t)jj * kD) : 0.f;
   }
+  const float2 ml_first =
+      tid < p.n_chunks ? __ldg(reinterpret_cast<const float2*>(p.ml) + base + tid) : make_float2(-INFINITY, 0.f);
+  const int n_act = min(p.n_chunks, (max(n_sel, 0) + p.chunk_cells - 1) / p.chunk_cells);
   float M = -INFINITY, lsum_self = 0.f, m_self = -INFINITY;
   for (int jj = tid; jj < n_act; jj += kMergeThreads) {
-    const float2 ml = __ldg(reinterpret_cast<const float2*>(p.ml) + base + jj);
+    const float2 ml = jj == tid ? ml_first : __ldg(reinterpret_cast<const float2*>(p.ml) + base + jj);
     w_s[jj] = ml.x;
     M = fmaxf(M, ml.x);
     if (jj == tid) { m_self = ml.x; lsum_self = ml.y; }
