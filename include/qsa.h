@@ -59,6 +59,7 @@ typedef enum {
 #define QSA_MAX_DECODE_ROWS 32   /* rows of one decode window */
 #define QSA_MAX_GROUP 8          /* q heads per KV head on the decode side */
 #define QSA_MAX_TOPK_BLOCKS 16384
+#define QSA_MAX_CHUNKS 8192      /* chunks per (row, q head) of the chunk partials */
 
 /*
  * One slot's paged KV pool.  All pointers (dev), 16-byte aligned, caller-owned.
@@ -139,11 +140,14 @@ qsa_status qsa_topk(const float* scores, int max_blocks, const int32_t* n_filled
 
 /*
  * Partials of the decode attention (caller scratch).  For n_rows rows,
- * n_q_heads heads and n_chunks chunks per (row, head) the buffer holds
- *   float ml[n_rows][n_q_heads][n_chunks][2]      (m, l) of each chunk
- *   float o [n_rows][n_q_heads][n_chunks][128]    unnormalised sum p * V
- * back to back (o starts at byte offset 8 * n_rows * n_q_heads * n_chunks).
- * An empty chunk (no visible cell) has m = -inf, l = 0, o = 0.
+ * n_q_heads heads and n_chunks chunks per (row, head), N = n_rows *
+ * n_q_heads * n_chunks, the buffer holds
+ *   float ml[n_rows][n_q_heads][n_chunks][2]      (m, l) of each chunk, at byte 0
+ *   float o [n_rows][n_q_heads][n_chunks][128]    unnormalised sum p * V, at
+ *                                                 byte 8 * N rounded up to a
+ *                                                 multiple of 256
+ * The buffer must be 16-byte aligned.  An empty chunk (no visible cell) has
+ * m = -inf, l = 0, o = 0.  Returns 0 for sizes below 1.
  */
 size_t qsa_decode_partials_bytes(int n_rows, int n_q_heads, int n_chunks);
 
@@ -167,7 +171,8 @@ size_t qsa_decode_partials_bytes(int n_rows, int n_q_heads, int n_chunks);
  *   n_chunks   chunks per (row, head) in the partials, >= ceil(k_cells / C)
  *   partials   (dev)  scratch, partials_bytes >= qsa_decode_partials_bytes()
  * Errors: QSA_ERR_ARG, QSA_ERR_UNSUPPORTED (group > QSA_MAX_GROUP, rows >
- * QSA_MAX_DECODE_ROWS), QSA_ERR_SCRATCH (partials too small).
+ * QSA_MAX_DECODE_ROWS, n_chunks > QSA_MAX_CHUNKS), QSA_ERR_SCRATCH
+ * (partials too small).
  */
 qsa_status qsa_decode_attn(const qsa_pool* pools, int n_pools, const int32_t* row_pool,
                            const float* q, const int32_t* row_pos, const int32_t* ids,
@@ -187,6 +192,9 @@ qsa_status qsa_decode_attn(const qsa_pool* pools, int n_pools, const int32_t* ro
  *   n_sel      (dev)  int32 [n_rows]
  *   out        (dev)  fp32 [n_rows][n_q_heads][128]
  *   lse        (dev)  fp32 [n_rows][n_q_heads], may be NULL
+ * Errors: QSA_ERR_ARG (null or misaligned pointers, bad sizes),
+ * QSA_ERR_UNSUPPORTED (n_rows > QSA_MAX_DECODE_ROWS, n_chunks >
+ * QSA_MAX_CHUNKS).
  */
 qsa_status qsa_attn_merge(const void* partials, const int32_t* n_sel, int n_rows, int n_q_heads,
                           int chunk_cells, int n_chunks, float* out, float* lse, void* stream);
@@ -325,8 +333,10 @@ qsa_status qsa_kv_append(const qsa_pool* pool, const float* k, const float* v, i
  * and for plugins whose interface carries no allocator.
  *   Arguments as qsa_decode_attn and qsa_attn_merge, with
  *   n_chunks = ceil(k_cells / chunk_cells) (at least 1).
- *   Requires n_rows * n_q_heads * n_chunks * 130 * 4 <= QSA_NOALLOC_SCRATCH_BYTES,
- *   else QSA_ERR_SCRATCH with nothing enqueued.  No cudaMalloc / cudaFree.
+ *   Requires qsa_decode_partials_bytes(n_rows, n_q_heads, n_chunks) <=
+ *   QSA_NOALLOC_SCRATCH_BYTES, else QSA_ERR_SCRATCH.  Every refusal (ARG,
+ *   UNSUPPORTED, SCRATCH) comes with nothing enqueued.  No cudaMalloc /
+ *   cudaFree.
  *   The first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress); make that first call before any stream capture.
  *   All calls share the one array: calls that overlap on the GPU (other

@@ -18,6 +18,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libqsa_gb300.so")
 
 QSA_OK, QSA_ERR_ARG, QSA_ERR_UNSUPPORTED, QSA_ERR_SCRATCH, QSA_ERR_CUDA, QSA_ERR_DEVICE = range(6)
+QSA_MAX_CHUNKS = 8192   # chunks per (row, q head) of the chunk partials (qsa.h)
 HEAD_DIM = 128
 MAX_POOLS = 4
 MAX_DECODE_ROWS = 32
@@ -174,6 +175,11 @@ def topk(scores: torch.Tensor, n_filled: Sequence[int], block_cells: int, k_cell
                            _ptr(ids), _ptr(n_sel), _stream(stream)), "qsa_topk")
 
 
+def partials_o_offset(n: int) -> int:
+    """Byte offset of o in a chunk-partials buffer of n (row, head, chunk) entries (qsa.h layout)."""
+    return (8 * n + 255) // 256 * 256
+
+
 def decode_partials_bytes(n_rows: int, n_q_heads: int, n_chunks: int) -> int:
     return int(load().qsa_decode_partials_bytes(n_rows, n_q_heads, n_chunks))
 
@@ -328,6 +334,7 @@ class DecodeWindow:
     def partial_views(self):
         """(ml [R, Hq, n_chunks, 2], o [R, Hq, n_chunks, 128]) views of the partials buffer."""
         R, H, n = self.n_rows, self.n_q_heads, self.n_chunks
+        o0 = partials_o_offset(R * H * n) // 4
         ml = self.partials[: R * H * n * 2].view(R, H, n, 2)
-        o = self.partials[R * H * n * 2:].view(R, H, n, HEAD_DIM)
+        o = self.partials[o0:o0 + R * H * n * HEAD_DIM].view(R, H, n, HEAD_DIM)
         return ml, o

@@ -187,7 +187,8 @@ qsa_status qsa_topk(const float* scores, int max_blocks, const int32_t* n_filled
 
 size_t qsa_decode_partials_bytes(int n_rows, int n_q_heads, int n_chunks) {
   if (n_rows <= 0 || n_q_heads <= 0 || n_chunks <= 0) return 0;
-  return sizeof(float) * (size_t)n_rows * n_q_heads * n_chunks * (2 + QSA_HEAD_DIM);
+  const size_t n = (size_t)n_rows * n_q_heads * n_chunks;
+  return partials_o_offset(n) + sizeof(float) * n * QSA_HEAD_DIM;
 }
 
 qsa_status qsa_decode_attn(const qsa_pool* pools, int n_pools, const int32_t* row_pool, const float* q,
@@ -200,8 +201,9 @@ qsa_status qsa_decode_attn(const qsa_pool* pools, int n_pools, const int32_t* ro
   if (!q || !row_pos || !ids || !n_sel || !partials) return QSA_ERR_ARG;
   if (!aligned16(partials) || !aligned16(q)) return QSA_ERR_ARG;
   if (k_cells < 0 || chunk_cells < 16 || chunk_cells > 1024 || chunk_cells % 16 != 0) return QSA_ERR_ARG;
-  const int need_chunks = (k_cells + chunk_cells - 1) / chunk_cells;
+  const long long need_chunks = ((long long)k_cells + chunk_cells - 1) / chunk_cells;
   if (n_chunks < need_chunks || n_chunks < 1) return QSA_ERR_ARG;
+  if (n_chunks > QSA_MAX_CHUNKS) return QSA_ERR_UNSUPPORTED;
   if (partials_bytes < qsa_decode_partials_bytes(n_rows, n_q_heads, n_chunks)) return QSA_ERR_SCRATCH;
   AttnParams p{};
   for (int i = 0; i < n_pools; ++i) p.pools[i] = to_dev(pools[i]);
@@ -217,19 +219,22 @@ qsa_status qsa_decode_attn(const qsa_pool* pools, int n_pools, const int32_t* ro
   p.chunk_cells = chunk_cells;
   p.n_chunks = n_chunks;
   p.ml = static_cast<float*>(partials);
-  p.o = p.ml + (size_t)n_rows * n_q_heads * n_chunks * 2;
+  p.o = reinterpret_cast<float*>(static_cast<uint8_t*>(partials) +
+                                 partials_o_offset((size_t)n_rows * n_q_heads * n_chunks));
   return from_cuda(launch_decode_attn(p, static_cast<cudaStream_t>(stream)));
 }
 
 qsa_status qsa_attn_merge(const void* partials, const int32_t* n_sel, int n_rows, int n_q_heads,
                           int chunk_cells, int n_chunks, float* out, float* lse, void* stream) {
   if (!partials || !n_sel || !out) return QSA_ERR_ARG;
+  if (!aligned16(partials)) return QSA_ERR_ARG;
   if (n_rows < 1 || n_q_heads < 1 || n_chunks < 1) return QSA_ERR_ARG;
-  if (n_rows > QSA_MAX_DECODE_ROWS) return QSA_ERR_UNSUPPORTED;
+  if (n_rows > QSA_MAX_DECODE_ROWS || n_chunks > QSA_MAX_CHUNKS) return QSA_ERR_UNSUPPORTED;
   if (chunk_cells < 16 || chunk_cells > 1024 || chunk_cells % 16 != 0) return QSA_ERR_ARG;
   MergeParams p{};
   p.ml = static_cast<const float*>(partials);
-  p.o = p.ml + (size_t)n_rows * n_q_heads * n_chunks * 2;
+  p.o = reinterpret_cast<const float*>(static_cast<const uint8_t*>(partials) +
+                                       partials_o_offset((size_t)n_rows * n_q_heads * n_chunks));
   p.n_sel = n_sel;
   p.n_rows = n_rows;
   p.n_q_heads = n_q_heads;
@@ -437,6 +442,6 @@ qsa_status qsa_kv_append(const qsa_pool* pool, const float* k, const float* v, i
   return from_cuda(launch_kv_append(p, static_cast<cudaStream_t>(stream)));
 }
 
-int qsa_abi_version(void) { return 105; }
+int qsa_abi_version(void) { return 106; }
 
 }  // extern "C"

@@ -40,6 +40,11 @@ struct AttnParams {
   float* o;   // [n_rows][n_q_heads][n_chunks][128]
 };
 
+// Byte offset of the o region in a chunk-partials buffer of n (row, head, chunk) entries: the
+// (m, l) pairs first, then o from the next 256-byte boundary, so that o is aligned for vector
+// stores whatever n is.
+inline size_t partials_o_offset(size_t n) { return (sizeof(float) * 2 * n + 255) & ~(size_t)255; }
+
 struct MergeParams {
   const float* ml;
   const float* o;

@@ -50,13 +50,15 @@ extern "C" qsa_status qsa_decode_attn_noalloc(const qsa_pool* pools, int n_pools
                                               const float* q, const int32_t* row_pos, const int32_t* ids,
                                               const int32_t* n_sel, int n_rows, int n_q_heads, int k_cells,
                                               int chunk_cells, float* out, float* lse, void* stream) {
+  // Every check of both steps comes first: a refused call enqueues nothing.
+  if (!out || !n_sel) return QSA_ERR_ARG;
   if (k_cells < 0 || chunk_cells < 16 || chunk_cells > 1024 || chunk_cells % 16 != 0) return QSA_ERR_ARG;
   if (n_rows < 1 || n_q_heads < 1) return QSA_ERR_ARG;
-  int n_chunks = (k_cells + chunk_cells - 1) / chunk_cells;
+  long long n_chunks = ((long long)k_cells + chunk_cells - 1) / chunk_cells;
   if (n_chunks < 1) n_chunks = 1;
+  if (n_rows > QSA_MAX_DECODE_ROWS || n_chunks > QSA_MAX_CHUNKS) return QSA_ERR_UNSUPPORTED;
   // Sizes past the fixed scratch are refused before anything is looked up or enqueued.
-  if ((unsigned long long)n_rows * n_q_heads * n_chunks * (2 + QSA_HEAD_DIM) * sizeof(float) >
-      (unsigned long long)QSA_NOALLOC_SCRATCH_BYTES)
+  if (qsa_decode_partials_bytes(n_rows, n_q_heads, (int)n_chunks) > (size_t)QSA_NOALLOC_SCRATCH_BYTES)
     return QSA_ERR_SCRATCH;
   void* scratch = nullptr;
   qsa_status s = qsa::noalloc_scratch(&scratch);
@@ -64,7 +66,7 @@ extern "C" qsa_status qsa_decode_attn_noalloc(const qsa_pool* pools, int n_pools
   // Nothing in the scratch has to start at zero: every chunk the merge reads
   // was written by the attention launch just before it on the same stream.
   s = qsa_decode_attn(pools, n_pools, row_pool, q, row_pos, ids, n_sel, n_rows, n_q_heads, k_cells, chunk_cells,
-                      n_chunks, scratch, QSA_NOALLOC_SCRATCH_BYTES, stream);
+                      (int)n_chunks, scratch, QSA_NOALLOC_SCRATCH_BYTES, stream);
   if (s != QSA_OK) return s;
-  return qsa_attn_merge(scratch, n_sel, n_rows, n_q_heads, chunk_cells, n_chunks, out, lse, stream);
+  return qsa_attn_merge(scratch, n_sel, n_rows, n_q_heads, chunk_cells, (int)n_chunks, out, lse, stream);
 }

@@ -38,9 +38,12 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_pure_host_calls(lib):
-    assert qsa.abi_version() == 105
+    assert qsa.abi_version() == 106
     assert qsa.status_str(qsa.QSA_ERR_SCRATCH) == "scratch buffer too small"
     assert qsa.decode_partials_bytes(5, 24, 64) == 4 * 5 * 24 * 64 * 130
+    # o starts at the next 256-byte boundary after the (m, l) pairs, whatever their count
+    assert qsa.decode_partials_bytes(1, 1, 1) == 256 + 4 * 128
+    assert qsa.decode_partials_bytes(1, 3, 3) == 256 + 4 * 9 * 128
     assert qsa.decode_partials_bytes(0, 24, 64) == 0
 
 
@@ -143,3 +146,24 @@ def test_four_bit_k_validation(lib):
     rp = (ctypes.c_int32 * 2)(0, 0)
     assert lib.qsa_decode_attn(arr, 1, rp, 16, 32, 48, 64, 2, 24, 64, 64, 1, 256, 1 << 20, None) == \
         qsa.QSA_ERR_UNSUPPORTED
+
+
+def test_chunk_cap_and_noalloc_refusals(lib):
+    """Chunk counts past QSA_MAX_CHUNKS are refused by the attention, the merge and the no-allocation
+    entry point alike; the no-allocation call checks every argument of both of its steps (a NULL out
+    among them) before it looks anything up or enqueues anything."""
+    pools = (qsa.QsaPoolC * 1)(_pool(n_filled=256, capacity=256))
+    rp = (ctypes.c_int32 * 1)(0)
+    cap = qsa.QSA_MAX_CHUNKS
+    k = 16 * (cap + 1)
+    need = qsa.decode_partials_bytes(1, 4, cap + 1)
+    assert lib.qsa_decode_attn(pools, 1, rp, 16, 32, 48, 64, 1, 4, k, 16, cap + 1, 256, need, None) == \
+        qsa.QSA_ERR_UNSUPPORTED
+    assert lib.qsa_attn_merge(256, 64, 1, 4, 16, cap + 1, 512, None, None) == qsa.QSA_ERR_UNSUPPORTED
+    assert lib.qsa_attn_merge(260, 64, 1, 4, 16, 4, 512, None, None) == qsa.QSA_ERR_ARG   # misaligned partials
+    noalloc = lambda out, k_cells, C=16, Hq=4: lib.qsa_decode_attn_noalloc(pools, 1, rp, 16, 32, 48, 64, 1, Hq,
+                                                                        k_cells, C, out, None, None)
+    assert noalloc(None, 256) == qsa.QSA_ERR_ARG
+    assert noalloc(512, 200000) == qsa.QSA_ERR_UNSUPPORTED      # 12,500 chunks of 16 cells
+    assert noalloc(512, 2 ** 31 - 1, C=1024) == qsa.QSA_ERR_UNSUPPORTED   # no int overflow in the chunk count
+    assert noalloc(512, 16 * cap, Hq=8) == qsa.QSA_ERR_SCRATCH  # 8 x 8,192 chunks of partials > 8 MiB

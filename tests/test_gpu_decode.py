@@ -63,6 +63,20 @@ def test_small_ragged(fill, page_cells, Hq, Hkv, k, C, v_bits):
     run_and_check(case)
 
 
+@pytest.mark.parametrize("fill,Hq,Hkv,k,C", [
+    (64, 1, 1, 64, 64),        # one row, one head, one chunk: 1 (row, head, chunk) entry of partials
+    (700, 3, 1, 192, 64),      # three q heads on one KV head, three chunks: 9 entries
+    (500, 3, 1, 320, 48),      # ragged chunks of 48 over a selection of 320
+])
+def test_odd_partial_counts(fill, Hq, Hkv, k, C):
+    """An odd number of (row, head, chunk) entries: the o region of the partials still starts on a
+    16-byte boundary (it starts at the next 256-byte boundary after the (m, l) pairs)."""
+    case = W.decode_case(name="odd", seed=fill + Hq, fills=[fill], capacity=fill + 64, rows_per_slot=1,
+                         n_q_heads=Hq, n_kv_heads=Hkv, k_cells=k, chunk_cells=C, page_cells=64,
+                         bias_prob=0.05)
+    run_and_check(case)
+
+
 @pytest.mark.parametrize("rows_per_slot,Hq,Hkv,B", [
     (10, 16, 8, 64),    # 20 rows (three 8-row tiles), 8 KV heads: two warp tasks per warp
     (6, 8, 2, 128),     # 12 rows, 128-cell blocks

@@ -35,6 +35,32 @@ def test_noalloc_matches_caller_scratch_twice(make):
         assert_close(lse.cpu().numpy(), ref_lse, "noalloc lse")
 
 
+def _noalloc_vs_caller_scratch(case):
+    """One no-allocation call on a fresh pair of outputs, checked against the caller-scratch path."""
+    win, q, row_pos = upload_case(case)
+    win.run(q, row_pos)
+    torch.cuda.synchronize()
+    out = torch.full_like(win.out, float("nan"))
+    lse = torch.full_like(win.lse, float("nan"))
+    qsa.decode_attn_noalloc(win.pools, win.row_pool, q, row_pos, win.ids, win.n_sel, case.k_cells,
+                            case.chunk_cells, out, lse)
+    torch.cuda.synchronize()
+    assert_close(out.cpu().numpy(), win.out.cpu().numpy(), f"noalloc out ({case.name})")
+    assert_close(lse.cpu().numpy(), win.lse.cpu().numpy(), f"noalloc lse ({case.name})")
+
+
+def test_noalloc_ragged_odd_sizes_back_to_back():
+    """Odd q-head counts, a last chunk that is only partly filled, and two calls in a row of which the
+    second is the smaller: partials the first call left behind in the shared array must not leak into
+    the second result."""
+    big = W.decode_case(name="odd-big", seed=31, fills=[1500], capacity=1600, rows_per_slot=3, n_q_heads=3,
+                        n_kv_heads=1, k_cells=704, chunk_cells=48, page_cells=64, bias_prob=0.05)
+    small = W.decode_case(name="odd-small", seed=32, fills=[333], capacity=384, rows_per_slot=1, n_q_heads=1,
+                          n_kv_heads=1, k_cells=192, chunk_cells=80, page_cells=64, bias_prob=0.05)
+    _noalloc_vs_caller_scratch(big)
+    _noalloc_vs_caller_scratch(small)
+
+
 def test_noalloc_refuses_windows_past_its_scratch():
     case = W.verify_window()
     win, q, row_pos = upload_case(case)
