@@ -202,12 +202,14 @@ qsa_status qsa_attn_merge(const void* partials, const int32_t* n_sel, int n_rows
 /*
  * qsa_decode_window -- one whole decode window in one call: block scores ->
  * top-k -> split-KV attention -> log-sum-exp merge (the four steps above),
- * enqueued as four chained launches on `stream` ("#2806 sycl: decode QSA
- * selection and attention in fewer, shorter launches", Summary: selection
- * and attention of a window in fewer, shorter launches).  scores, ids and
- * n_sel are written exactly as qsa_block_scores and qsa_topk write them.
- * The attention splits each (row, KV head)'s selection into splits of a
- * multiple of 64 cells chosen by the library for this GPU, and the merge
+ * enqueued as five launches chained by programmatic dependent launch on
+ * `stream` (q preparation, block scores, top-k, split attention, merge;
+ * "#2806 sycl: decode QSA selection and attention in fewer, shorter
+ * launches", Summary: selection and attention of a window in fewer, shorter
+ * launches).  scores, ids and n_sel are written exactly as qsa_block_scores
+ * and qsa_topk write them.  The attention splits each (row, KV head)'s
+ * selection into splits of a multiple of 16 cells chosen by the library for
+ * this GPU (about four CTAs per SM, at most 256 splits), and the merge
  * folds the splits in split order, skipping empty ones; out and lse follow
  * the qsa_attn_merge definition (equal to the chunked result up to
  * rounding; bitwise reproducible run to run on the same GPU).

@@ -304,34 +304,46 @@ def merge_partials(m: np.ndarray, l: np.ndarray, o: np.ndarray) -> Tuple[np.ndar
 
 # ---------------------------------------------------------------- prompt
 
-def prompt_attention(pool, q: np.ndarray, q_pos0: int, rows: Sequence[int] = None):
+def prompt_attention(pool, q: np.ndarray, q_pos0: int, rows: Sequence[int] = None, heads: Sequence[int] = None,
+                     row_block: int = 64):
     """Dense causal prompt attention of a chunk of queries ([1367] What it does;
     [600] description: a chunk of queries against the whole cached context).
 
     Query i sits at position q_pos0 + i and sees cells 0..q_pos0+i (R5).  The
     computation is the exact attention of the fp32 q on the dequantised K/V;
-    the GPU's operand split is rounding inside its error budget.
+    the GPU's operand split is rounding inside its error budget.  For each q
+    head the logits of up to `row_block` rows come from one matrix product
+    with the head's dequantised K; a row's cells past its position are masked
+    to -inf before the softmax (so they weigh exactly 0), and the weights
+    multiply V in a second product.  `heads` limits the q heads computed
+    (others are left at out = 0, lse = -inf).
     Returns out [len(rows), Hq, D] and lse [len(rows), Hq], float64."""
     n_q, Hq, D = q.shape
     Hkv = pool.n_kv_heads
     rows = list(range(n_q)) if rows is None else list(rows)
+    heads = list(range(Hq)) if heads is None else list(heads)
     last = q_pos0 + max(rows) + 1 if rows else 0
     out = np.zeros((len(rows), Hq, D))
     lse = np.full((len(rows), Hq), -np.inf)
     for h in range(Hkv):
+        group = [g for g in heads if kv_head(g, Hq, Hkv) == h]
+        if not group:
+            continue
         K = dequantise_k(pool, h, np.arange(last))
         V = dequantise_v(pool, h, np.arange(last))
-        for g in range(Hq):
-            if kv_head(g, Hq, Hkv) != h:
-                continue
-            for r, i in enumerate(rows):
-                n = q_pos0 + i + 1
-                z = K[:n] @ q[i, g].astype(np.float64) / math.sqrt(D)
-                mx = z.max()
+        for b0 in range(0, len(rows), row_block):
+            blk = rows[b0:b0 + row_block]
+            pos = q_pos0 + np.asarray(blk)                     # each row's own cell
+            n = int(pos.max()) + 1
+            hidden = np.arange(n)[None, :] > pos[:, None]      # cells past the row's position
+            for g in group:
+                z = q[blk, g].astype(np.float64) @ K[:n].T / math.sqrt(D)   # [rows, n]
+                z[hidden] = -np.inf
+                mx = z.max(axis=1, keepdims=True)
                 p = np.exp(z - mx)
-                s = p.sum()
-                out[r, g] = (p @ V[:n]) / s
-                lse[r, g] = mx + math.log(s)
+                s = p.sum(axis=1)
+                out[b0:b0 + len(blk), g] = (p @ V[:n]) / s[:, None]
+                lse[b0:b0 + len(blk), g] = mx[:, 0] + np.log(s)
     return out, lse
 
 

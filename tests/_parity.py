@@ -1,5 +1,8 @@
 """Helpers shared by the GPU parity tests: upload seeded cases, run the CUDA
 path through the C ABI, and compare with the oracle."""
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -65,3 +68,24 @@ def run_window_and_check(case):
     assert_close(win.out.cpu().numpy(), ref["out"], "out")
     assert_close(win.lse.cpu().numpy(), ref["lse"], "lse")
     return win, q, row_pos
+
+
+def row_stats(gpu, ref):
+    """Row-wise relative error of an output [rows, heads, D]: for every (query, head) vector
+    ||gpu - ref|| / ||ref||; returns (mean, max) over the vectors with ||ref|| > 0."""
+    gpu = np.asarray(gpu, dtype=np.float64).reshape(-1, np.shape(gpu)[-1])
+    ref = np.asarray(ref, dtype=np.float64).reshape(-1, np.shape(ref)[-1])
+    nr = np.linalg.norm(ref, axis=1)
+    ok = nr > 0
+    r = np.linalg.norm(gpu - ref, axis=1)[ok] / nr[ok]
+    return float(r.mean()), float(r.max())
+
+
+def report(name, **stats):
+    """Prints a parity record; with QSA_PARITY_REPORT set, also appends it to that JSON-lines file."""
+    rec = {"case": name, **stats}
+    print("PARITY", json.dumps(rec))
+    path = os.environ.get("QSA_PARITY_REPORT")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps(rec) + "\n")

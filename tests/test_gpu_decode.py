@@ -77,6 +77,17 @@ def test_odd_partial_counts(fill, Hq, Hkv, k, C):
     run_and_check(case)
 
 
+def test_codes_of_minus_128():
+    """int8 K and V codes drawn in [-128, 127]: scores, selection, partials and outputs stay at parity
+    (the one code without a positive twin goes through the exact fp16 conversions)."""
+    case = W.decode_case(name="m128", seed=128, fills=[1500], capacity=1600, rows_per_slot=3, n_q_heads=12,
+                         n_kv_heads=2, k_cells=512, chunk_cells=64, page_cells=128, bias_prob=0.05, code_lo=-128)
+    assert (case.pools[0].k_codes == -128).any() and (case.pools[0].v_codes == -128).any()
+    run_and_check(case)
+    from _parity import run_window_and_check
+    run_window_and_check(case)
+
+
 @pytest.mark.parametrize("rows_per_slot,Hq,Hkv,B", [
     (10, 16, 8, 64),    # 20 rows (three 8-row tiles), 8 KV heads: two warp tasks per warp
     (6, 8, 2, 128),     # 12 rows, 128-cell blocks

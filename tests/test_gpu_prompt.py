@@ -1,6 +1,7 @@
 """GPU parity of the tensor-core prompt attention against the FP64 oracle,
 through the C ABI: small ragged cases in full, the two full-size prompt
-workloads on sampled rows, the cross-path identity with decode, and the
+workloads on every row (the oracle spread over the host's cores), codes of
+-128, the cross-path identity with decode, and the
 bounded-wait error path (a wait limit of 0 makes the kernel give up at its
 first wait, report through the device error word and leave the context
 usable; no fault, trap or hang is involved)."""
@@ -11,7 +12,8 @@ import torch
 import oracle as O
 import sparse_selection_attention_gb300 as qsa
 import workloads as W
-from _parity import assert_close
+from _parity import assert_close, report, row_stats
+from oracle import parallel as OP
 
 pytestmark = pytest.mark.gpu
 
@@ -75,34 +77,43 @@ def test_prompt_heads_with_far_apart_v_scales():
     assert_close(lse, ref_lse, "lse")
 
 
-def _sample_rows(n_q, k, seed):
-    rng = np.random.default_rng(seed)
-    rows = set(rng.choice(n_q, size=k, replace=False).tolist()) | {0, 1, n_q - 1}
-    return sorted(rows)
-
-
-def test_prompt_int8_full_size_sampled():
-    """2,048 queries against 32,768 cells, 24/4 heads (the prompt workload of the bench)."""
-    case = W.prompt_int8()
-    out, lse = run_prompt(case, case.calls[0])
-    rows = _sample_rows(2048, 40, 0)
-    ref_out, ref_lse = O.prompt_attention(case.pool, case.q, case.calls[0][2], rows=rows)
-    assert_close(out[rows], ref_out, "out")
-    assert_close(lse[rows], ref_lse, "lse")
+def check_all_rows(name, builder, call_index):
+    """Every row of one call of a named prompt workload against the oracle, element-wise at the gate,
+    with the row-wise error reported."""
+    case = getattr(W, builder)()
+    out, lse = run_prompt(case, case.calls[call_index])
+    ref_out, ref_lse = OP.prompt_call(builder, {}, call_index)
+    e_out = assert_close(out, ref_out, f"{name} out")
+    e_lse = assert_close(lse, ref_lse, f"{name} lse")
+    mean_row, max_row = row_stats(out, ref_out)
+    report(name, rows=int(out.shape[0]), heads=int(out.shape[1]), max_rel_out=e_out, max_rel_lse=e_lse,
+           mean_row_rel_out=mean_row, max_row_rel_out=max_row)
     assert np.isfinite(out).all() and np.isfinite(lse).all()
 
 
-def test_prompt_k8v4_last_call_sampled():
-    """8,192 queries against 131,072 cells in four calls; the last call checked on sampled rows."""
-    case = W.prompt_k8v4()
-    call = case.calls[-1]
-    out, lse = run_prompt(case, call)
-    rows = _sample_rows(call[1], 24, 1)
-    q_call = case.q[call[0]:call[0] + call[1]]
-    ref_out, ref_lse = O.prompt_attention(case.pool, q_call, call[2], rows=rows)
-    assert_close(out[rows], ref_out, "out")
-    assert_close(lse[rows], ref_lse, "lse")
-    assert np.isfinite(out).all()
+def test_prompt_int8_full_size_all_rows():
+    """2,048 queries against 32,768 cells, 24/4 heads (the prompt workload of the bench), every row."""
+    check_all_rows("prompt int8 2048 x 32768", "prompt_int8", 0)
+
+
+@pytest.mark.parametrize("call_index", [0, 1, 2, 3])
+def test_prompt_k8v4_all_calls_all_rows(call_index):
+    """8,192 queries against 131,072 cells (32/8 heads, int8 K, 4-bit V) in four calls of 2,048: every
+    row of every call."""
+    check_all_rows(f"prompt k8v4 call {call_index}", "prompt_k8v4", call_index)
+
+
+@pytest.mark.parametrize("v_bits", [8, 4])
+def test_prompt_codes_of_minus_128(v_bits):
+    """int8 codes drawn in [-128, 127] (K, and V when int8): the code without a positive twin goes
+    through the exact conversions like every other."""
+    case = W.prompt_case(name="m128", seed=128 + v_bits, n_ctx=900, n_q=120, n_q_heads=12, n_kv_heads=3,
+                         v_bits=v_bits, page_cells=128, capacity=1024, code_lo=-128)
+    assert (case.pool.k_codes == -128).any()
+    out, lse = run_prompt(case, case.calls[0])
+    ref_out, ref_lse = O.prompt_attention(case.pool, case.q, case.calls[0][2])
+    assert_close(out, ref_out, "out")
+    assert_close(lse, ref_lse, "lse")
 
 
 def test_prompt_row_equals_decode_with_all_cells():

@@ -306,6 +306,27 @@ def test_decode_with_all_cells_equals_prompt_row():
         assert np.allclose(dout, pout[t], atol=1e-12) and np.allclose(dlse, plse[t], atol=1e-12)
 
 
+def test_prompt_row_blocks_and_head_subsets_match_single_rows():
+    """The prompt oracle's row blocks (causal mask per row inside a block) and head subsets give, row by
+    row, the single-row attention over cells 0 .. position, computed without any mask."""
+    case = _small_case(fill=640)
+    pool = case.pools[0]
+    pos0 = 590
+    rows = [0, 3, 4, 9, 10, 11, 49]
+    Hq = case.q.shape[1]
+    heads = [1, 2, Hq - 1]
+    q = np.concatenate([case.q] * 20)[:50]
+    out, lse = O.prompt_attention(pool, q, pos0, rows=rows, heads=heads, row_block=3)
+    for r, i in enumerate(rows):
+        dout, dlse = O.attention(pool, q[i], pos0 + i, list(range(pos0 + i + 1)))
+        for g in range(Hq):
+            if g in heads:
+                assert np.allclose(out[r, g], dout[g], rtol=0, atol=1e-12)
+                assert abs(lse[r, g] - dlse[g]) <= 1e-12
+            else:
+                assert np.all(out[r, g] == 0.0) and lse[r, g] == -np.inf
+
+
 def test_stale_cells_are_never_read():
     """Cells past the fill carry NaN scales; the whole decode chain stays finite."""
     case = _small_case(fill=700)

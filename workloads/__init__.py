@@ -76,11 +76,13 @@ def _pack_nibbles(raw: np.ndarray) -> np.ndarray:
 
 def make_pool(rng: np.random.Generator, *, capacity: int, n_filled: int, n_kv_heads: int,
               head_dim: int = HEAD_DIM, page_cells: int = 256, v_bits: int = 8,
-              bias_prob: float = 0.0, k_bits: int = 8) -> Pool:
+              bias_prob: float = 0.0, k_bits: int = 8, code_lo: int = -127) -> Pool:
     """Draw one paged pool.  Draw order: page table, K codes, K scales, V codes,
     V scales, then (if bias_prob > 0) the bias mask and the bias directions.
     k_bits = 4 (with v_bits = 4: the q4_0 layout) draws K codes in [-8, 7] with
-    one scale per 32 dims, packed as the 4-bit V codes are."""
+    one scale per 32 dims, packed as the 4-bit V codes are.  int8 codes are
+    drawn in [code_lo, 127] (code_lo -128 includes the one code without a
+    positive twin)."""
     assert 0 <= n_filled <= capacity
     assert head_dim % K_GROUP == 0 and v_bits in (4, 8) and k_bits in (4, 8)
     n_pages = (capacity + page_cells - 1) // page_cells
@@ -89,13 +91,13 @@ def make_pool(rng: np.random.Generator, *, capacity: int, n_filled: int, n_kv_he
     page_table = rng.permutation(n_pages).astype(np.int32)
     shape = (n_pages, n_kv_heads, page_cells, head_dim)
     if k_bits == 8:
-        k_codes = rng.integers(-127, 128, size=shape, dtype=np.int8)
+        k_codes = rng.integers(code_lo, 128, size=shape, dtype=np.int8)
     else:
         k_codes = _pack_nibbles(rng.integers(-8, 8, size=shape, dtype=np.int8))
     k_scales = rng.uniform(SCALE_LO, SCALE_HI,
                            size=(n_pages, n_kv_heads, page_cells, head_dim // k_group)).astype(np.float32)
     if v_bits == 8:
-        v_codes = rng.integers(-127, 128, size=shape, dtype=np.int8)
+        v_codes = rng.integers(code_lo, 128, size=shape, dtype=np.int8)
     else:
         v_codes = _pack_nibbles(rng.integers(-8, 8, size=shape, dtype=np.int8))
     v_scales = rng.uniform(SCALE_LO, SCALE_HI,
@@ -178,12 +180,13 @@ def decode_case(*, name: str, seed: int, fills: List[int], capacity: int, rows_p
                 n_q_heads: int, n_kv_heads: int, k_cells: int, chunk_cells: int,
                 block_cells: int = 64, page_cells: int = 256, bias_prob: float = 0.0,
                 n_chunks: Optional[int] = None, v_bits: int = 8,
-                row_pos: Optional[List[int]] = None, k_bits: int = 8) -> DecodeCase:
+                row_pos: Optional[List[int]] = None, k_bits: int = 8, code_lo: int = -127) -> DecodeCase:
     """Pools are drawn slot by slot, then q.  Rows of a slot are contiguous and
     sit at the last positions of its fill unless row_pos is given."""
     rng = np.random.default_rng(seed)
     pools = [make_pool(rng, capacity=capacity, n_filled=f, n_kv_heads=n_kv_heads,
-                       page_cells=page_cells, v_bits=v_bits, bias_prob=bias_prob, k_bits=k_bits) for f in fills]
+                       page_cells=page_cells, v_bits=v_bits, bias_prob=bias_prob, k_bits=k_bits,
+                       code_lo=code_lo) for f in fills]
     row_pool, pos = [], []
     for s, f in enumerate(fills):
         for r in range(rows_per_slot):
@@ -201,11 +204,11 @@ def decode_case(*, name: str, seed: int, fills: List[int], capacity: int, rows_p
 
 def prompt_case(*, name: str, seed: int, n_ctx: int, n_q: int, n_q_heads: int, n_kv_heads: int,
                 v_bits: int = 8, calls_of: Optional[int] = None, page_cells: int = 256,
-                capacity: Optional[int] = None, k_bits: int = 8) -> PromptCase:
+                capacity: Optional[int] = None, k_bits: int = 8, code_lo: int = -127) -> PromptCase:
     """Queries sit at the last n_q positions of the context (causal over them)."""
     rng = np.random.default_rng(seed)
     pool = make_pool(rng, capacity=capacity or n_ctx, n_filled=n_ctx, n_kv_heads=n_kv_heads,
-                     page_cells=page_cells, v_bits=v_bits, k_bits=k_bits)
+                     page_cells=page_cells, v_bits=v_bits, k_bits=k_bits, code_lo=code_lo)
     q = make_q(rng, n_q, n_q_heads)
     per = calls_of or n_q
     pos0 = n_ctx - n_q
