@@ -363,6 +363,25 @@ qsa_status qsa_get_device_error(int32_t* code, void* stream);
  * error path without a hang.  Affects later launches on all devices. */
 void qsa_set_wait_limit_ns(uint64_t ns);
 
+/*
+ * qsa_measure_tc_rate -- measurement utility (the pages have no counterpart):
+ * the dense tensor-core rate of the current GPU for one operand kind, timed
+ * with CUDA events on the legacy default stream after one warm-up launch.
+ *   QSA_TC_KIND_F16: one CTA per SM issues `passes` x 4 back-to-back
+ *     tcgen05.mma kind::f16 (f16 x f16 -> f32, M = 128, N = 256, K = 16)
+ *     from shared memory into tensor memory (about 1 ms per 3,000 passes);
+ *   QSA_TC_KIND_I8: tcgen05 has no int8 kind on sm_103a, so 16 warps per SM
+ *     each issue `passes` x 8 independent mma.sync.m16n8k32 s8 x s8 -> s32
+ *     (about 1 ms per 10 passes).
+ * Writes 2 * M * N * K * MMAs / seconds to *ops_per_second (host).
+ * Synchronous; occupies every SM for the launch.  Errors: QSA_ERR_ARG (kind,
+ * passes outside 1 .. 2^20, NULL output), QSA_ERR_CUDA, QSA_ERR_DEVICE (the
+ * f16 launch's bounded wait ran out).
+ */
+#define QSA_TC_KIND_F16 0
+#define QSA_TC_KIND_I8 1
+qsa_status qsa_measure_tc_rate(int kind, int passes, double* ops_per_second);
+
 const char* qsa_status_str(qsa_status s);
 
 /* ABI version of this header (major * 100 + minor). */

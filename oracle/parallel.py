@@ -42,23 +42,27 @@ def workers(n: int = 0) -> int:
     return n if n > 0 else (os.cpu_count() or 1)
 
 
-def prompt_call(builder: str, kwargs: Dict, call_index: int, n_workers: int = 0, row_block: int = 128
-                ) -> Tuple[np.ndarray, np.ndarray]:
-    """out [n_q, Hq, 128] and lse [n_q, Hq] (float64) of every row of one prompt call of the case
-    `workloads.<builder>(**kwargs)`, by oracle.prompt_attention over tasks (row block, KV head)."""
+def prompt_call(builder: str, kwargs: Dict, call_index: int, n_workers: int = 0, row_block: int = 128,
+                rows: List[int] = None) -> Tuple[np.ndarray, np.ndarray]:
+    """out [n, Hq, 128] and lse [n, Hq] (float64) of the given rows (default: every row) of one prompt
+    call of the case `workloads.<builder>(**kwargs)`, by oracle.prompt_attention over tasks (row block,
+    KV head)."""
     case = _build(builder, kwargs)
     _, n_q, _ = case.calls[call_index]
+    rows = list(range(n_q)) if rows is None else list(rows)
     Hq, Hkv = case.n_q_heads, case.pool.n_kv_heads
     G = Hq // Hkv
-    tasks = [(call_index, list(range(r0, min(n_q, r0 + row_block))), list(range(h * G, (h + 1) * G)))
-             for h in range(Hkv) for r0 in range(0, n_q, row_block)]
-    out = np.zeros((n_q, Hq, case.q.shape[2]))
-    lse = np.full((n_q, Hq), -np.inf)
+    tasks = [(call_index, rows[r0:r0 + row_block], list(range(h * G, (h + 1) * G)))
+             for h in range(Hkv) for r0 in range(0, len(rows), row_block)]
+    where = {r: i for i, r in enumerate(rows)}
+    out = np.zeros((len(rows), Hq, case.q.shape[2]))
+    lse = np.full((len(rows), Hq), -np.inf)
     ctx = mp.get_context("spawn")
     with ctx.Pool(workers(n_workers), initializer=_init, initargs=(builder, kwargs)) as pool:
-        for rows, heads, o, l in pool.imap_unordered(_prompt_task, tasks):
-            out[np.ix_(rows, heads)] = o
-            lse[np.ix_(rows, heads)] = l
+        for rws, heads, o, l in pool.imap_unordered(_prompt_task, tasks):
+            idx = [where[r] for r in rws]
+            out[np.ix_(idx, heads)] = o
+            lse[np.ix_(idx, heads)] = l
     return out, lse
 
 

@@ -27,8 +27,9 @@ EXPORTS = [
     "qsa_block_scores", "qsa_topk", "qsa_decode_partials_bytes", "qsa_decode_attn", "qsa_attn_merge",
     "qsa_prompt_attn", "qsa_prompt_scratch_bytes", "qsa_get_device_error", "qsa_set_wait_limit_ns", "qsa_status_str", "qsa_abi_version",
     "qsa_decode_attn_noalloc", "qsa_decode_window", "qsa_decode_window_workspace_bytes",
-    "qsa_decode_window_profile", "qsa_kv_append",
+    "qsa_decode_window_profile", "qsa_kv_append", "qsa_measure_tc_rate",
 ]
+QSA_TC_KIND_F16, QSA_TC_KIND_I8 = 0, 1
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -84,9 +85,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qsa_status_str.argtypes = [i]
     lib.qsa_status_str.restype = ctypes.c_char_p
     lib.qsa_abi_version.argtypes = []
+    lib.qsa_measure_tc_rate.argtypes = [i, i, ctypes.POINTER(ctypes.c_double)]
     for name in ("qsa_block_scores", "qsa_topk", "qsa_decode_attn", "qsa_attn_merge", "qsa_prompt_attn",
                  "qsa_get_device_error", "qsa_abi_version", "qsa_decode_attn_noalloc", "qsa_decode_window",
-                 "qsa_decode_window_profile"):
+                 "qsa_decode_window_profile", "qsa_measure_tc_rate"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -242,6 +244,14 @@ def get_device_error(stream=None) -> int:
 
 def set_wait_limit_ns(ns: int) -> None:
     load().qsa_set_wait_limit_ns(int(ns))
+
+
+def measure_tc_rate(kind: int, passes: int = 10000) -> float:
+    """qsa_measure_tc_rate: dense tcgen05 operations per second of this GPU for QSA_TC_KIND_I8 or
+    QSA_TC_KIND_F16 (synchronous; a few milliseconds)."""
+    r = ctypes.c_double(0.0)
+    _check(load().qsa_measure_tc_rate(int(kind), int(passes), ctypes.byref(r)), "qsa_measure_tc_rate")
+    return float(r.value)
 
 
 def abi_version() -> int:

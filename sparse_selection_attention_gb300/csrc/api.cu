@@ -442,6 +442,20 @@ qsa_status qsa_kv_append(const qsa_pool* pool, const float* k, const float* v, i
   return from_cuda(launch_kv_append(p, static_cast<cudaStream_t>(stream)));
 }
 
-int qsa_abi_version(void) { return 106; }
+qsa_status qsa_measure_tc_rate(int kind, int passes, double* ops_per_second) {
+  if (!ops_per_second || (kind != QSA_TC_KIND_F16 && kind != QSA_TC_KIND_I8) || passes < 1 || passes > (1 << 20))
+    return QSA_ERR_ARG;
+  float ms = 0.f;
+  double ops = 0.0;
+  const qsa_status s = from_cuda(run_tc_rate(kind == QSA_TC_KIND_I8, passes, &ms, &ops));
+  if (s != QSA_OK) return s;
+  int32_t code = 0;
+  if (read_and_clear_device_error(&code, nullptr) != cudaSuccess) return QSA_ERR_CUDA;
+  if (code != 0) return QSA_ERR_DEVICE;
+  *ops_per_second = ms > 0.f ? ops / (1e-3 * ms) : 0.0;
+  return QSA_OK;
+}
+
+int qsa_abi_version(void) { return 107; }
 
 }  // extern "C"

@@ -141,6 +141,10 @@ cudaError_t launch_attn_merge_ex(const MergeParams& p, cudaStream_t stream, bool
 cudaError_t launch_prompt_attn(const PromptParams& p, cudaStream_t stream);
 cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream);
 cudaError_t read_and_clear_device_error(int32_t* code, cudaStream_t stream);
+// Dense tcgen05 rate (tc_rate.cu): times `passes` x 4 MMAs of M = 128, N = 256 per SM on the
+// legacy default stream; *ms the launch's event time, *ops the operations it performed.
+cudaError_t run_tc_rate(int kind_i8, int passes, float* ms, double* ops);
+unsigned long long wait_limit_ns();
 // Device address of the library's error word on the current device (for kernels of other
 // translation units), or nullptr.
 int* device_error_word();

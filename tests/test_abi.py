@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_pure_host_calls(lib):
-    assert qsa.abi_version() == 106
+    assert qsa.abi_version() == 107
     assert qsa.status_str(qsa.QSA_ERR_SCRATCH) == "scratch buffer too small"
     assert qsa.decode_partials_bytes(5, 24, 64) == 4 * 5 * 24 * 64 * 130
     # o starts at the next 256-byte boundary after the (m, l) pairs, whatever their count
@@ -167,3 +167,11 @@ def test_chunk_cap_and_noalloc_refusals(lib):
     assert noalloc(512, 200000) == qsa.QSA_ERR_UNSUPPORTED      # 12,500 chunks of 16 cells
     assert noalloc(512, 2 ** 31 - 1, C=1024) == qsa.QSA_ERR_UNSUPPORTED   # no int overflow in the chunk count
     assert noalloc(512, 16 * cap, Hq=8) == qsa.QSA_ERR_SCRATCH  # 8 x 8,192 chunks of partials > 8 MiB
+
+
+def test_tc_rate_validation(lib):
+    """Argument checks of the rate measurement, taken before anything is launched."""
+    r = ctypes.c_double(0.0)
+    assert lib.qsa_measure_tc_rate(2, 10, ctypes.byref(r)) == qsa.QSA_ERR_ARG
+    assert lib.qsa_measure_tc_rate(qsa.QSA_TC_KIND_I8, 0, ctypes.byref(r)) == qsa.QSA_ERR_ARG
+    assert lib.qsa_measure_tc_rate(qsa.QSA_TC_KIND_F16, 10, None) == qsa.QSA_ERR_ARG
