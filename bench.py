@@ -164,7 +164,8 @@ class ClockSampler:
 
 
 def kernel_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged since."""
+    """DRAM bytes per launch from the committed ncu summary (key "kernel" or "kernel@workload"), if the
+    kernel source is unchanged since."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             d = json.load(f)[kernel]
@@ -479,7 +480,7 @@ def run_ours(args):
     ach = byte_of[dom] / (kern_us[KERNELS.index(dom)] * 1e-6) / 1e9
     roofline = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
                 "frac": ach / hbm_peak, "peak_source": f"{peak_src} hbm_gbs (burst copy; kernel timed alone)",
-                "algorithmic_bytes": byte_of[dom], "traffic": kernel_traffic(dom),
+                "algorithmic_bytes": byte_of[dom], "traffic": kernel_traffic(f"{dom}@{args.case}"),
                 "timing": "qsa_decode_window_profile: CUDA events around the launch, no overlap with its neighbours"}
 
     # ---- the four separate calls (qsa_block_scores, qsa_topk, qsa_decode_attn, qsa_attn_merge), for context

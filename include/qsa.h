@@ -74,9 +74,7 @@ typedef enum {
  *              k_group = 64 (k_bits 8) or 32 (k_bits 4)
  *   v_scales   fp32   [n_pages][n_kv_heads][page_cells][128 / v_group],
  *              v_group = 64 (v_bits 8) or 32 (v_bits 4)
- * 4-bit K is served by qsa_decode_window, qsa_prompt_attn and qsa_kv_append;
- * qsa_block_scores, qsa_decode_attn and qsa_decode_attn_noalloc answer
- * QSA_ERR_UNSUPPORTED for it.  The pools of one decode window share k_bits.
+ * Every call serves 4-bit K.  The pools of one call share k_bits.
  *   page_table int32  [ceil(capacity / page_cells)] logical -> physical page
  * Logical cell c is at physical page page_table[c / page_cells], offset
  * c % page_cells.  Cells 0 .. n_filled-1 hold data; others are never read.
@@ -95,7 +93,7 @@ typedef struct {
   int32_t n_kv_heads;   /* 1..16 */
   int32_t head_dim;     /* must be 128 */
   int32_t v_bits;       /* 8 or 4 */
-  int32_t k_bits;       /* 8, or 4 for 4-bit K (the q4_0 layout; decode window, prompt and append) */
+  int32_t k_bits;       /* 8, or 4 for 4-bit K (the q4_0 layout) */
 } qsa_pool;
 
 /*

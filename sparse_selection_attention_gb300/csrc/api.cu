@@ -126,7 +126,6 @@ qsa_status qsa_block_scores(const qsa_pool* pools, int n_pools, const int32_t* r
                             void* stream) {
   qsa_status s = check_window(pools, n_pools, row_pool, n_rows, n_q_heads, false);
   if (s != QSA_OK) return s;
-  if (pools[0].k_bits != 8) return QSA_ERR_UNSUPPORTED;   // 4-bit K: the decode window serves it
   if (!q || !scores || !aligned16(q)) return QSA_ERR_ARG;
   if (block_cells != 32 && block_cells != 64 && block_cells != 128 && block_cells != 256) return QSA_ERR_ARG;
   ScoresParams p{};
@@ -151,6 +150,7 @@ qsa_status qsa_block_scores(const qsa_pool* pools, int n_pools, const int32_t* r
   p.err = device_error_word();
   p.wait_limit_ns = wait_limit_ns();
   if (!p.err) return QSA_ERR_CUDA;
+  if (pools[0].k_bits == 4) return from_cuda(launch_block_scores(p, static_cast<cudaStream_t>(stream)));
   if (!block_scores_supported(p.n_kv_heads, block_cells)) return QSA_ERR_UNSUPPORTED;
   p.q_rows_per_batch = block_scores_q_rows_per_batch(n_rows, n_q_heads, p.n_kv_heads, block_cells);
   if (block_scores_smem_bytes(n_rows, n_q_heads, p.n_kv_heads, block_cells) > (size_t)device_max_smem_optin())
@@ -197,7 +197,6 @@ qsa_status qsa_decode_attn(const qsa_pool* pools, int n_pools, const int32_t* ro
                            size_t partials_bytes, void* stream) {
   qsa_status s = check_window(pools, n_pools, row_pool, n_rows, n_q_heads, true);
   if (s != QSA_OK) return s;
-  if (pools[0].k_bits != 8) return QSA_ERR_UNSUPPORTED;   // 4-bit K: the decode window serves it
   if (!q || !row_pos || !ids || !n_sel || !partials) return QSA_ERR_ARG;
   if (!aligned16(partials) || !aligned16(q)) return QSA_ERR_ARG;
   if (k_cells < 0 || chunk_cells < 16 || chunk_cells > 1024 || chunk_cells % 16 != 0) return QSA_ERR_ARG;
@@ -221,6 +220,7 @@ qsa_status qsa_decode_attn(const qsa_pool* pools, int n_pools, const int32_t* ro
   p.ml = static_cast<float*>(partials);
   p.o = reinterpret_cast<float*>(static_cast<uint8_t*>(partials) +
                                  partials_o_offset((size_t)n_rows * n_q_heads * n_chunks));
+  if (pools[0].k_bits == 4) return from_cuda(launch_chunk_attn_window_kernels(p, static_cast<cudaStream_t>(stream)));
   return from_cuda(launch_decode_attn(p, static_cast<cudaStream_t>(stream)));
 }
 

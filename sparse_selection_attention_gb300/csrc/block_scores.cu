@@ -578,6 +578,85 @@ int n_stages_for(int R, int Hkv, int B, int total_units, int grid, int smem_max)
 
 }  // namespace staged
 
+// 4-bit K (the q4_0 layout: 64-byte rows, low nibble = even dim, code = nibble - 8, one scale per
+// 32 dims).  One 256-thread CTA per (pool, block); per KV head, qbar of every row is formed in
+// shared memory, then thread (cell tid / 4 + 64 m, 32-dim group tid % 4) takes the dot products of
+// its group with each row's qbar, weighted by the group's scale; sums over lanes, warps and KV heads
+// run in a fixed order.  fp32 arithmetic.
+constexpr int kK4Threads = 256;
+
+__global__ void __launch_bounds__(kK4Threads) block_scores_k4_kernel(const ScoresParams p) {
+  __shared__ float qb[QSA_MAX_DECODE_ROWS * kD];   // qbar of one KV head, [row][dim]
+  __shared__ float red[kK4Threads / 32][QSA_MAX_DECODE_ROWS];
+  __shared__ float acc_s[QSA_MAX_DECODE_ROWS];
+  const int unit = blockIdx.x;
+  int pi = 0;
+  while (pi + 1 < p.n_pools && unit >= p.unit_begin[pi + 1]) ++pi;
+  const PoolDev& pool = p.pools[pi];
+  const int B = p.block_cells, Hkv = p.n_kv_heads, R = p.n_rows, G = p.n_q_heads / Hkv;
+  const int b = unit - p.unit_begin[pi];
+  const int cell0 = b * B;
+  const int n_b = min(B, pool.n_filled - cell0);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int grp = tid & 3;
+  if (tid < QSA_MAX_DECODE_ROWS) acc_s[tid] = 0.f;
+  const int page = __ldg(pool.page_table + cell0 / pool.page_cells);
+  const long long slot0 = (long long)page * Hkv * pool.page_cells + cell0 % pool.page_cells;
+  for (int h = 0; h < Hkv; ++h) {
+    __syncthreads();   // qb and red of the previous head fully read
+    for (int i = tid; i < R * kD; i += kK4Threads) {
+      const int t = i / kD, d = i - t * kD;
+      const float* qg = p.q + ((size_t)t * p.n_q_heads + (size_t)h * G) * kD + d;
+      float s = 0.f;
+      for (int g = 0; g < G; ++g) s += __ldg(qg + (size_t)g * kD);
+      qb[i] = s;
+    }
+    __syncthreads();
+    float part[QSA_MAX_DECODE_ROWS];
+#pragma unroll
+    for (int t = 0; t < QSA_MAX_DECODE_ROWS; ++t) part[t] = 0.f;
+    for (int c = tid >> 2; c < n_b; c += kK4Threads / 4) {
+      const long long slot = slot0 + (long long)h * pool.page_cells + c;
+      const uint4 w = __ldg(reinterpret_cast<const uint4*>(pool.k_codes + slot * (kD / 2)) + grp);
+      const float scale = __ldg(pool.k_scales + slot * 4 + grp);
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+      float code[32];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const uint32_t byte = (ws[j >> 2] >> (8 * (j & 3))) & 0xFFu;
+        code[2 * j] = (float)((int)(byte & 15u) - 8);
+        code[2 * j + 1] = (float)((int)(byte >> 4) - 8);
+      }
+#pragma unroll
+      for (int t = 0; t < QSA_MAX_DECODE_ROWS; ++t) {
+        if (t < R && p.row_pool[t] == pi) {
+          const float* qr = qb + t * kD + 32 * grp;
+          float dot = 0.f;
+#pragma unroll
+          for (int d = 0; d < 32; ++d) dot = fmaf(code[d], qr[d], dot);
+          part[t] = fmaf(scale, dot, part[t]);
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < QSA_MAX_DECODE_ROWS; ++t) {
+      if (t < R) {
+        const float v = warp_sum(part[t]);
+        if (lane == 0) red[warp][t] = v;
+      }
+    }
+    __syncthreads();
+    if (tid < R) {
+      float s = 0.f;
+      for (int w = 0; w < kK4Threads / 32; ++w) s += red[w][tid];
+      acc_s[tid] += s;
+    }
+  }
+  __syncthreads();
+  if (tid < R && p.row_pool[tid] == pi)
+    p.scores[(size_t)tid * p.max_blocks + b] = acc_s[tid] * (kInvSqrtD / (float)n_b);
+}
+
 }  // namespace
 
 int block_scores_q_rows_per_batch(int n_rows, int n_q_heads, int n_kv_heads, int block_cells) {
@@ -622,6 +701,10 @@ static cudaError_t launch_staged(const ScoresParams& p, int grid, int n_stages, 
 
 cudaError_t launch_block_scores(const ScoresParams& p, cudaStream_t stream) {
   if (p.total_units == 0) return cudaSuccess;
+  if (p.pools[0].k_bits == 4) {   // the pools of one call share k_bits
+    block_scores_k4_kernel<<<p.total_units, kK4Threads, 0, stream>>>(p);
+    return cudaGetLastError();
+  }
   const int nt = (p.n_rows + 7) / 8;
   if (nt > kNtMax) return cudaErrorInvalidValue;
   {

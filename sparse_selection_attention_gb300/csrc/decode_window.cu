@@ -1333,6 +1333,39 @@ static cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, si
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+cudaError_t launch_chunk_attn_window_kernels(const AttnParams& a, cudaStream_t stream) {
+  // A chunk of qsa_decode_attn is a split of this file's attention kernels: same (m, l, o) per
+  // (row, q head, chunk) in the same layout, chunks past the selection not written.
+  WinAttnParams p{};
+  for (int i = 0; i < QSA_MAX_POOLS; ++i) p.pools[i] = a.pools[i];
+  bool same_v = true;
+  for (int t = 0; t < a.n_rows; ++t) {
+    p.row_pool[t] = a.row_pool[t];
+    same_v = same_v && a.pools[a.row_pool[t]].v_bits == a.pools[a.row_pool[0]].v_bits;
+  }
+  p.q = a.q;
+  p.row_pos = a.row_pos;
+  p.ids = a.ids;
+  p.n_sel = a.n_sel;
+  p.n_rows = a.n_rows;
+  p.n_q_heads = a.n_q_heads;
+  p.n_kv_heads = a.n_kv_heads;
+  p.k_cells = a.k_cells;
+  p.split_cells = a.chunk_cells;
+  p.n_splits = a.n_chunks;
+  p.part_ml = a.ml;
+  p.part_o = a.o;
+  const bool k4 = a.pools[a.row_pool[0]].k_bits == 4;
+  const bool v4 = a.pools[a.row_pool[0]].v_bits == 4;
+  const dim3 grid(a.n_rows * a.n_kv_heads * a.n_chunks);
+  if (!same_v) return launch_ex(win_attn_kernel, grid, dim3(kAttnThreads), 0, stream, false, p);
+  if (k4)
+    return v4 ? launch_ex(win_attn8_kernel<true, true>, grid, dim3(kAttnThreads), 0, stream, false, p)
+              : launch_ex(win_attn8_kernel<true, false>, grid, dim3(kAttnThreads), 0, stream, false, p);
+  return v4 ? launch_ex(win_attn8_kernel<false, true>, grid, dim3(kAttnThreads), 0, stream, false, p)
+            : launch_ex(win_attn8_kernel<false, false>, grid, dim3(kAttnThreads), 0, stream, false, p);
+}
+
 cudaError_t launch_decode_window(const WindowArgs& a, cudaStream_t stream, cudaEvent_t* ev) {
   // With `ev` (6 events) the launches are not chained (each starts after the previous one ends) and
   // ev[i] is recorded before launch i, ev[5] after the last: per-kernel times.

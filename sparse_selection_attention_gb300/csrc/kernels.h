@@ -136,6 +136,8 @@ size_t topk_smem_bytes(int max_nb);
 cudaError_t launch_block_scores(const ScoresParams& p, cudaStream_t stream);
 cudaError_t launch_topk(const TopkParams& p, int max_nb, cudaStream_t stream);
 cudaError_t launch_decode_attn(const AttnParams& p, cudaStream_t stream);
+// qsa_decode_attn through the decode window's attention kernels (4-bit K; decode_window.cu).
+cudaError_t launch_chunk_attn_window_kernels(const AttnParams& p, cudaStream_t stream);
 cudaError_t launch_attn_merge(const MergeParams& p, cudaStream_t stream);
 cudaError_t launch_attn_merge_ex(const MergeParams& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_prompt_attn(const PromptParams& p, cudaStream_t stream);

@@ -135,17 +135,11 @@ def test_kv_append_validation(lib):
 
 
 def test_four_bit_k_validation(lib):
-    """4-bit K (k_bits 4) is served by the decode window, the prompt and the append; the standalone
-    decode calls answer UNSUPPORTED; k_bits other than 8 and 4 is an argument error; the pools of one
-    window share k_bits."""
+    """4-bit K (k_bits 4) is served by every call; k_bits other than 8 and 4 is an argument error; the
+    pools of one call share k_bits (checked before anything is launched)."""
     k4 = _pool(k_bits=4, v_bits=4)
-    assert _scores_call(lib, [k4], [0, 0]) == qsa.QSA_ERR_UNSUPPORTED
     assert _scores_call(lib, [_pool(k_bits=5)], [0, 0]) == qsa.QSA_ERR_ARG
     assert _scores_call(lib, [_pool(), k4], [0, 1]) == qsa.QSA_ERR_ARG          # mixed k_bits in one call
-    arr = (qsa.QsaPoolC * 1)(k4)
-    rp = (ctypes.c_int32 * 2)(0, 0)
-    assert lib.qsa_decode_attn(arr, 1, rp, 16, 32, 48, 64, 2, 24, 64, 64, 1, 256, 1 << 20, None) == \
-        qsa.QSA_ERR_UNSUPPORTED
 
 
 def test_chunk_cap_and_noalloc_refusals(lib):

@@ -50,16 +50,18 @@ def test_tiny_dense_decode():
     assert int(win.n_sel[0]) == 1024
 
 
-@pytest.mark.parametrize("fill,page_cells,Hq,Hkv,k,C,v_bits", [
-    (1000, 128, 6, 2, 256, 64, 8),      # ragged last block, 4 blocks chosen of 16
-    (1000, 256, 8, 1, 2048, 48, 8),     # k > all cells: take all; ragged chunks of 48
-    (777, 64, 4, 4, 320, 112, 4),       # 4-bit V, group 1, odd chunk size
-    (300, 64, 24, 4, 64, 16, 8),        # one block, 16-cell chunks
+@pytest.mark.parametrize("fill,page_cells,Hq,Hkv,k,C,v_bits,k_bits", [
+    (1000, 128, 6, 2, 256, 64, 8, 8),      # ragged last block, 4 blocks chosen of 16
+    (1000, 256, 8, 1, 2048, 48, 8, 8),     # k > all cells: take all; ragged chunks of 48
+    (777, 64, 4, 4, 320, 112, 4, 8),       # 4-bit V, group 1, odd chunk size
+    (300, 64, 24, 4, 64, 16, 8, 8),        # one block, 16-cell chunks
+    (1000, 128, 6, 2, 256, 64, 4, 4),      # q4_0 (4-bit K and V): ragged last block
+    (777, 64, 8, 2, 320, 48, 8, 4),        # 4-bit K with int8 V, ragged chunks of 48
 ])
-def test_small_ragged(fill, page_cells, Hq, Hkv, k, C, v_bits):
+def test_small_ragged(fill, page_cells, Hq, Hkv, k, C, v_bits, k_bits):
     case = W.decode_case(name="ragged", seed=fill + k, fills=[fill], capacity=fill + 100, rows_per_slot=3,
                          n_q_heads=Hq, n_kv_heads=Hkv, k_cells=k, chunk_cells=C, page_cells=page_cells,
-                         v_bits=v_bits, bias_prob=0.05)
+                         v_bits=v_bits, bias_prob=0.05, k_bits=k_bits)
     run_and_check(case)
 
 
