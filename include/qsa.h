@@ -362,6 +362,55 @@ qsa_status qsa_get_device_error(int32_t* code, void* stream);
 void qsa_set_wait_limit_ns(uint64_t ns);
 
 /*
+ * Context-sharded decode (several GPUs, each holding a range of every slot's
+ * cells).  The split and its merge follow "#1888 QSA decode attention: split
+ * each query's cells across blocks on the int8 mma path", Summary: the cells
+ * of a query are split, each split yields (m, l, o) partials, and the splits
+ * are merged by the log-sum-exp rescale in split order.  Here a split is a
+ * rank's cell range.  A rank describes its range [lo, hi) of a slot as a pool
+ * view (page_table advanced by lo / page_cells pages, n_filled = min(hi,
+ * n_filled) - lo; lo and hi multiples of page_cells) and runs:
+ *   qsa_block_scores on its views; an all-gather of the scores (the caller's
+ *   collective); qsa_topk over the gathered scores (one global selection,
+ *   the same on every rank and equal to a single GPU's); qsa_ids_in_range;
+ *   qsa_decode_attn on its views; an all-gather of the chunk partials and of
+ *   the ranks' n_sel; qsa_attn_merge_shards.
+ */
+
+/*
+ * qsa_ids_in_range -- per row t, the selected ids in [lo[t], hi[t]) (the
+ * rank's range of the row's slot), shifted by -lo[t] (the range's own cell
+ * numbering), and the row's position shifted by -lo[t].
+ *   ids        (dev)  int32 [n_rows][k_cells], ascending in [0, n_sel)
+ *   n_sel      (dev)  int32 [n_rows]
+ *   row_pos    (dev)  int32 [n_rows]
+ *   lo, hi     (host) int32 [n_rows], 0 <= lo <= hi
+ *   ids_out    (dev)  int32 [n_rows][k_cells]: entries [0, n_sel_out) written
+ *   n_sel_out, row_pos_out (dev) int32 [n_rows]
+ * Errors: QSA_ERR_ARG, QSA_ERR_UNSUPPORTED (n_rows > QSA_MAX_DECODE_ROWS).
+ */
+qsa_status qsa_ids_in_range(const int32_t* ids, const int32_t* n_sel, const int32_t* row_pos, int n_rows,
+                            int k_cells, const int32_t* lo, const int32_t* hi, int32_t* ids_out,
+                            int32_t* n_sel_out, int32_t* row_pos_out, void* stream);
+
+/*
+ * qsa_attn_merge_shards -- the log-sum-exp merge of qsa_attn_merge over the
+ * chunk partials of n_shards ranks, folded in rank order, then chunk order,
+ * visiting for rank s only chunks j < ceil(n_sel[s][t] / C) and skipping
+ * empty ones.  out and lse as qsa_attn_merge.
+ *   partials   (dev)  n_shards buffers back to back, each
+ *                     qsa_decode_partials_bytes(n_rows, n_q_heads, n_chunks)
+ *                     bytes in the chunk-partials layout (as written by
+ *                     qsa_decode_attn with these sizes), 16-byte aligned
+ *   n_sel      (dev)  int32 [n_shards][n_rows]: each rank's n_sel_out
+ * Errors: QSA_ERR_ARG, QSA_ERR_UNSUPPORTED (n_rows > QSA_MAX_DECODE_ROWS,
+ * n_chunks > QSA_MAX_CHUNKS).
+ */
+qsa_status qsa_attn_merge_shards(const void* partials, int n_shards, const int32_t* n_sel, int n_rows,
+                                 int n_q_heads, int chunk_cells, int n_chunks, float* out, float* lse,
+                                 void* stream);
+
+/*
  * qsa_measure_tc_rate -- measurement utility (the pages have no counterpart):
  * the dense tensor-core rate of the current GPU for one operand kind, timed
  * with CUDA events on the legacy default stream after one warm-up launch.

@@ -36,6 +36,11 @@ notes of the repository):
   R7  chunk j of a row is entries [j*C, (j+1)*C) of its selected-id list;
   R8  4-bit V: code = nibble - 8, low nibble = even dim, one scale per
       32-dim group; int8 V and int8 K: one scale per 64-dim group;
+  R15 context-sharded decode (a slot's cells split into ranges held by
+      different GPUs) selects once per row over the block scores of all
+      ranges (one global top-k): the selection, and so the result of
+      decode_window, does not depend on the split; each range contributes the
+      chunk partials of the selected cells it holds, merged by log-sum-exp;
   R14 appending a cell quantises each group of its K and V rows symmetrically
       by the group's largest magnitude: scale = amax / 127 (int8) or amax / 7
       (4-bit V), code = round-half-to-even(x / scale) clamped to +-127 (+-7),

@@ -27,7 +27,8 @@ EXPORTS = [
     "qsa_block_scores", "qsa_topk", "qsa_decode_partials_bytes", "qsa_decode_attn", "qsa_attn_merge",
     "qsa_prompt_attn", "qsa_prompt_scratch_bytes", "qsa_get_device_error", "qsa_set_wait_limit_ns", "qsa_status_str", "qsa_abi_version",
     "qsa_decode_attn_noalloc", "qsa_decode_window", "qsa_decode_window_workspace_bytes",
-    "qsa_decode_window_profile", "qsa_kv_append", "qsa_measure_tc_rate",
+    "qsa_decode_window_profile", "qsa_kv_append", "qsa_measure_tc_rate", "qsa_ids_in_range",
+    "qsa_attn_merge_shards",
 ]
 QSA_TC_KIND_F16, QSA_TC_KIND_I8 = 0, 1
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -86,9 +87,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qsa_status_str.restype = ctypes.c_char_p
     lib.qsa_abi_version.argtypes = []
     lib.qsa_measure_tc_rate.argtypes = [i, i, ctypes.POINTER(ctypes.c_double)]
+    lib.qsa_ids_in_range.argtypes = [p, p, p, i, i, i32p, i32p, p, p, p, p]
+    lib.qsa_attn_merge_shards.argtypes = [p, i, p, i, i, i, i, p, p, p]
     for name in ("qsa_block_scores", "qsa_topk", "qsa_decode_attn", "qsa_attn_merge", "qsa_prompt_attn",
                  "qsa_get_device_error", "qsa_abi_version", "qsa_decode_attn_noalloc", "qsa_decode_window",
-                 "qsa_decode_window_profile", "qsa_measure_tc_rate"):
+                 "qsa_decode_window_profile", "qsa_measure_tc_rate", "qsa_ids_in_range", "qsa_attn_merge_shards"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
