@@ -59,6 +59,7 @@ typedef enum {
 #define QSA_MAX_DECODE_ROWS 32   /* rows of one decode window */
 #define QSA_MAX_GROUP 8          /* q heads per KV head on the decode side */
 #define QSA_MAX_TOPK_BLOCKS 16384
+#define QSA_MAX_KV_HEADS 16      /* KV heads of a pool */
 #define QSA_MAX_CHUNKS 8192      /* chunks per (row, q head) of the chunk partials */
 
 /*
@@ -76,6 +77,16 @@ typedef enum {
  *              v_group = 64 (v_bits 8) or 32 (v_bits 4)
  * Every call serves 4-bit K.  The pools of one call share k_bits.
  *   page_table int32  [ceil(capacity / page_cells)] logical -> physical page
+ *   k_sums     fp32   [n_pages][n_kv_heads][page_cells / 64][128], or NULL:
+ *              optional block summaries, for each 64-cell block of a page the
+ *              sum over its cells of the dequantised K rows (kcode * kscale),
+ *              in ascending cell order.  When every pool of a call keeps them
+ *              and block_cells is a multiple of 64, qsa_block_scores and
+ *              qsa_decode_window score blocks from them (the same S[t,b],
+ *              512 bytes per 64 cells and KV head read instead of the codes
+ *              and scales).  They must describe exactly cells 0 .. n_filled-1:
+ *              qsa_kv_append keeps them so for in-order appends;
+ *              qsa_kv_summarise (re)builds them.
  * Logical cell c is at physical page page_table[c / page_cells], offset
  * c % page_cells.  Cells 0 .. n_filled-1 hold data; others are never read.
  * (Per-(cell, KV head, 64-dim group) scales: #600 description; paged pool and
@@ -94,6 +105,7 @@ typedef struct {
   int32_t head_dim;     /* must be 128 */
   int32_t v_bits;       /* 8 or 4 */
   int32_t k_bits;       /* 8, or 4 for 4-bit K (the q4_0 layout) */
+  const float* k_sums;  /* optional block summaries (see above), 16-byte aligned, or NULL */
 } qsa_pool;
 
 /*
@@ -307,6 +319,8 @@ size_t qsa_prompt_scratch_bytes(const qsa_pool* pool, int n_q, int q_pos0, int n
  *           (+-7; stored as the nibble code + 8, the even dim in the low
  *           nibble); amax = 0 gives scale 0 and codes 0.
  * The division and rounding are IEEE fp32, so the codes are exact integers.
+ * A pool with k_sums has the summaries of the 64-cell blocks the new cells
+ * fall in rewritten, each over its cells below first_cell + n_new.
  *   pool        (host) descriptor; the call WRITES its code and scale arrays
  *                      for the appended cells (the const in qsa_pool marks
  *                      the attention calls' read-only use).  n_filled is the
@@ -319,6 +333,20 @@ size_t qsa_prompt_scratch_bytes(const qsa_pool* pool, int n_q, int q_pos0, int n
  */
 qsa_status qsa_kv_append(const qsa_pool* pool, const float* k, const float* v, int first_cell,
                          int n_new, void* stream);
+
+/*
+ * qsa_kv_summarise -- (re)writes a pool's block summaries (qsa_pool.k_sums)
+ * of the 64-cell blocks that cells first_cell .. first_cell + n_cells - 1
+ * fall in, each over its cells below first_cell + n_cells (so a call with
+ * first_cell 0 and n_cells = n_filled builds them for the whole fill).  An
+ * index of the pool's blocks kept beside the K/V cells ("#2806 sycl: decode
+ * QSA selection and attention in fewer, shorter launches", What it leaves
+ * alone: the K/V and indexer appends).
+ *   pool   (host) descriptor with k_sums set; the call WRITES k_sums
+ *   first_cell >= 0, n_cells >= 0, first_cell + n_cells <= capacity
+ * Errors: QSA_ERR_ARG (no k_sums, bad range), QSA_ERR_UNSUPPORTED.
+ */
+qsa_status qsa_kv_summarise(const qsa_pool* pool, int first_cell, int n_cells, void* stream);
 
 /* Size of the library-owned scratch of qsa_decode_attn_noalloc (8 MiB). */
 #define QSA_NOALLOC_SCRATCH_BYTES (8u << 20)

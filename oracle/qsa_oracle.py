@@ -58,7 +58,7 @@ import numpy as np
 __all__ = [
     "dequantise_k", "dequantise_v", "kv_head", "block_scores", "score_key",
     "topk_select", "attention", "chunk_partials", "merge_partials",
-    "prompt_attention", "decode_window", "quantise_group", "append_cells",
+    "prompt_attention", "decode_window", "quantise_group", "append_cells", "block_summaries",
 ]
 
 
@@ -185,6 +185,21 @@ def block_scores(pool, q_rows: np.ndarray, block_cells: int) -> np.ndarray:
                 qg = q64[t, h * G:(h + 1) * G, :]                    # [G, D]
                 logits = qg @ K.T / math.sqrt(D)                     # [G, n_b]
                 out[t, b] += logits.sum() / n_b
+    return out
+
+
+def block_summaries(pool, summary_cells: int = 64) -> np.ndarray:
+    """Sum of the dequantised K rows over the filled cells of each summary block of
+    `summary_cells` cells, float64 [n_blocks, Hkv, D] (the index of blocks a pool may keep
+    beside its cells; by R3's linearity the block score is
+    S[t,b] = sum_h qbar[t,h] . (sum of b's summaries)[h] / (n_b sqrt(D)))."""
+    Hkv, D = pool.n_kv_heads, pool.head_dim
+    nb = (pool.n_filled + summary_cells - 1) // summary_cells
+    out = np.zeros((nb, Hkv, D))
+    for b in range(nb):
+        cells = np.arange(b * summary_cells, min((b + 1) * summary_cells, pool.n_filled))
+        for h in range(Hkv):
+            out[b, h] = dequantise_k(pool, h, cells).sum(axis=0)
     return out
 
 

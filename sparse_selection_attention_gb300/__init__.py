@@ -28,7 +28,7 @@ EXPORTS = [
     "qsa_prompt_attn", "qsa_prompt_scratch_bytes", "qsa_get_device_error", "qsa_set_wait_limit_ns", "qsa_status_str", "qsa_abi_version",
     "qsa_decode_attn_noalloc", "qsa_decode_window", "qsa_decode_window_workspace_bytes",
     "qsa_decode_window_profile", "qsa_kv_append", "qsa_measure_tc_rate", "qsa_ids_in_range",
-    "qsa_attn_merge_shards",
+    "qsa_attn_merge_shards", "qsa_kv_summarise",
 ]
 QSA_TC_KIND_F16, QSA_TC_KIND_I8 = 0, 1
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -46,7 +46,7 @@ class QsaPoolC(ctypes.Structure):
         ("v_scales", ctypes.c_void_p), ("page_table", ctypes.c_void_p),
         ("n_filled", ctypes.c_int32), ("capacity", ctypes.c_int32), ("page_cells", ctypes.c_int32),
         ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("v_bits", ctypes.c_int32),
-        ("k_bits", ctypes.c_int32),
+        ("k_bits", ctypes.c_int32), ("k_sums", ctypes.c_void_p),
     ]
 
 
@@ -89,9 +89,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qsa_measure_tc_rate.argtypes = [i, i, ctypes.POINTER(ctypes.c_double)]
     lib.qsa_ids_in_range.argtypes = [p, p, p, i, i, i32p, i32p, p, p, p, p]
     lib.qsa_attn_merge_shards.argtypes = [p, i, p, i, i, i, i, p, p, p]
+    lib.qsa_kv_summarise.argtypes = [pool_p, i, i, p]
     for name in ("qsa_block_scores", "qsa_topk", "qsa_decode_attn", "qsa_attn_merge", "qsa_prompt_attn",
                  "qsa_get_device_error", "qsa_abi_version", "qsa_decode_attn_noalloc", "qsa_decode_window",
-                 "qsa_decode_window_profile", "qsa_measure_tc_rate", "qsa_ids_in_range", "qsa_attn_merge_shards"):
+                 "qsa_decode_window_profile", "qsa_measure_tc_rate", "qsa_ids_in_range", "qsa_attn_merge_shards",
+                 "qsa_kv_summarise"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -129,12 +131,23 @@ class DevicePool:
     """One slot's paged KV pool resident on the GPU (layout of include/qsa.h)."""
 
     def __init__(self, k_codes, v_codes, k_scales, v_scales, page_table, *, n_filled, capacity, page_cells,
-                 n_kv_heads, v_bits, head_dim=HEAD_DIM, k_bits=8):
+                 n_kv_heads, v_bits, head_dim=HEAD_DIM, k_bits=8, k_sums=None):
         self.k_codes, self.v_codes = k_codes, v_codes
         self.k_scales, self.v_scales, self.page_table = k_scales, v_scales, page_table
         self.n_filled, self.capacity, self.page_cells = int(n_filled), int(capacity), int(page_cells)
         self.n_kv_heads, self.v_bits, self.head_dim = int(n_kv_heads), int(v_bits), int(head_dim)
         self.k_bits = int(k_bits)
+        self.k_sums = k_sums   # optional block summaries, fp32 [pages][heads][page_cells / 64][128]
+
+    def keep_block_sums(self, stream=None) -> "DevicePool":
+        """Allocates the pool's block summaries and builds them for cells 0 .. n_filled - 1; later
+        qsa_kv_append calls keep them current."""
+        n_pages = self.k_codes.shape[0]
+        self.k_sums = torch.zeros((n_pages, self.n_kv_heads, self.page_cells // 64, HEAD_DIM), dtype=torch.float32,
+                                  device=self.k_codes.device)
+        if self.n_filled > 0:
+            kv_summarise(self, 0, self.n_filled, stream)
+        return self
 
     @classmethod
     def upload(cls, pool, device="cuda") -> "DevicePool":
@@ -148,7 +161,7 @@ class DevicePool:
     def c(self) -> QsaPoolC:
         return QsaPoolC(_ptr(self.k_codes), _ptr(self.v_codes), _ptr(self.k_scales), _ptr(self.v_scales),
                         _ptr(self.page_table), self.n_filled, self.capacity, self.page_cells, self.n_kv_heads,
-                        self.head_dim, self.v_bits, self.k_bits)
+                        self.head_dim, self.v_bits, self.k_bits, _ptr(self.k_sums))
 
 
 def kv_append(pool: DevicePool, k: torch.Tensor, v: torch.Tensor, first_cell: int, stream=None) -> None:
@@ -159,6 +172,14 @@ def kv_append(pool: DevicePool, k: torch.Tensor, v: torch.Tensor, first_cell: in
     _check(load().qsa_kv_append(ctypes.byref(pc), _ptr(k), _ptr(v), int(first_cell), n_new, _stream(stream)),
            "qsa_kv_append")
     pool.n_filled = max(pool.n_filled, int(first_cell) + n_new)
+
+
+def kv_summarise(pool: DevicePool, first_cell: int, n_cells: int, stream=None) -> None:
+    """qsa_kv_summarise: rewrites the pool's block summaries of the 64-cell blocks the cells
+    first_cell .. first_cell + n_cells - 1 fall in."""
+    pc = pool.c()
+    _check(load().qsa_kv_summarise(ctypes.byref(pc), int(first_cell), int(n_cells), _stream(stream)),
+           "qsa_kv_summarise")
 
 
 def _pools_c(pools: Sequence[DevicePool]):

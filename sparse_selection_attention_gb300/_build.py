@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libqsa_gb300.so")
 SOURCES = ["api.cu", "block_scores.cu", "topk.cu", "decode_attn.cu", "decode_window.cu", "prompt_attn.cu",
-           "noalloc.cu", "kv_append.cu", "tc_rate.cu", "shard.cu"]
+           "noalloc.cu", "kv_append.cu", "tc_rate.cu", "shard.cu", "block_sums.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in ("common.cuh", "kernels.h", "tc.cuh", "mma_sync.cuh")] + [
     os.path.join(ROOT, "include", "qsa.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

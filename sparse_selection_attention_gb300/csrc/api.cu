@@ -48,8 +48,9 @@ qsa_status check_pool(const qsa_pool& p, bool need_v) {
   if (p.v_bits != 8 && p.v_bits != 4) return QSA_ERR_ARG;
   if (p.k_bits != 8 && p.k_bits != 4) return QSA_ERR_ARG;
   if (p.page_cells <= 0 || p.page_cells % 64 != 0) return QSA_ERR_ARG;
-  if (p.n_kv_heads < 1 || p.n_kv_heads > 16) return QSA_ERR_UNSUPPORTED;
+  if (p.n_kv_heads < 1 || p.n_kv_heads > QSA_MAX_KV_HEADS) return QSA_ERR_UNSUPPORTED;
   if (p.capacity < 0 || p.n_filled < 0 || p.n_filled > p.capacity) return QSA_ERR_ARG;
+  if (p.k_sums && !aligned16(p.k_sums)) return QSA_ERR_ARG;
   return QSA_OK;
 }
 
@@ -65,6 +66,7 @@ PoolDev to_dev(const qsa_pool& p) {
   d.page_shift = (p.page_cells & (p.page_cells - 1)) == 0 ? __builtin_ctz((unsigned)p.page_cells) : -1;
   d.v_bits = p.v_bits;
   d.k_bits = p.k_bits;
+  d.k_sums = p.k_sums;
   return d;
 }
 
@@ -150,6 +152,7 @@ qsa_status qsa_block_scores(const qsa_pool* pools, int n_pools, const int32_t* r
   p.err = device_error_word();
   p.wait_limit_ns = wait_limit_ns();
   if (!p.err) return QSA_ERR_CUDA;
+  if (block_sums_usable(p)) return from_cuda(launch_sum_scores(p, static_cast<cudaStream_t>(stream), false));
   if (pools[0].k_bits == 4) return from_cuda(launch_block_scores(p, static_cast<cudaStream_t>(stream)));
   if (!block_scores_supported(p.n_kv_heads, block_cells)) return QSA_ERR_UNSUPPORTED;
   p.q_rows_per_batch = block_scores_q_rows_per_batch(n_rows, n_q_heads, p.n_kv_heads, block_cells);
@@ -288,7 +291,7 @@ static qsa_status decode_window_impl(const qsa_pool* pools, int n_pools, const i
   sp.err = device_error_word();
   sp.wait_limit_ns = wait_limit_ns();
   if (!sp.err) return QSA_ERR_CUDA;
-  if (!window_scores_supported(n_rows, Hkv, block_cells)) return QSA_ERR_UNSUPPORTED;
+  if (!block_sums_usable(sp) && !window_scores_supported(n_rows, Hkv, block_cells)) return QSA_ERR_UNSUPPORTED;
   // top-k
   TopkParams& tp = a.topk;
   int max_nb = 1;
@@ -439,7 +442,21 @@ qsa_status qsa_kv_append(const qsa_pool* pool, const float* k, const float* v, i
   p.n_kv_heads = pool->n_kv_heads;
   p.first_cell = first_cell;
   p.n_new = n_new;
-  return from_cuda(launch_kv_append(p, static_cast<cudaStream_t>(stream)));
+  qsa_status st = from_cuda(launch_kv_append(p, static_cast<cudaStream_t>(stream)));
+  if (st != QSA_OK || !pool->k_sums) return st;
+  return from_cuda(launch_summarise(p.pool, const_cast<float*>(pool->k_sums), pool->n_kv_heads, first_cell, n_new,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+qsa_status qsa_kv_summarise(const qsa_pool* pool, int first_cell, int n_cells, void* stream) {
+  if (!pool) return QSA_ERR_ARG;
+  qsa_status s = check_pool(*pool, false);
+  if (s != QSA_OK) return s;
+  if (!pool->k_sums) return QSA_ERR_ARG;
+  if (first_cell < 0 || n_cells < 0 || (long long)first_cell + n_cells > pool->capacity) return QSA_ERR_ARG;
+  if (n_cells == 0) return QSA_OK;
+  return from_cuda(launch_summarise(to_dev(*pool), const_cast<float*>(pool->k_sums), pool->n_kv_heads, first_cell,
+                                    n_cells, static_cast<cudaStream_t>(stream)));
 }
 
 qsa_status qsa_measure_tc_rate(int kind, int passes, double* ops_per_second) {
@@ -456,6 +473,6 @@ qsa_status qsa_measure_tc_rate(int kind, int passes, double* ops_per_second) {
   return QSA_OK;
 }
 
-int qsa_abi_version(void) { return 107; }
+int qsa_abi_version(void) { return 108; }
 
 }  // extern "C"

@@ -24,6 +24,7 @@ struct PoolDev {
   int page_shift;   // log2(page_cells) when page_cells is a power of two, else -1
   int v_bits;
   int k_bits;
+  const float* k_sums;   // per (64-cell summary block, KV head) sums of dequantised K, or nullptr
 };
 
 // Linear (page, head, cell) slot of logical cell c of KV head h.

@@ -1388,13 +1388,18 @@ cudaError_t launch_decode_window(const WindowArgs& a, cudaStream_t stream, cudaE
   cudaError_t e = mark(0);
   if (e != cudaSuccess) return e;
   const int k4 = sp.pools[0].k_bits == 4 ? 1 : 0;   // the pools of a window share k_bits
-  e = launch_ex(win_qprep_kernel, dim3(NT * 8, Hkv), dim3(32), 0, stream, false, sp.q, R, sp.n_q_heads, Hkv, NT, k4,
-                frag, inv_f);
+  const bool sums = block_sums_usable(sp);           // scores from the pools' block summaries: no q prep
+  if (!sums)
+    e = launch_ex(win_qprep_kernel, dim3(NT * 8, Hkv), dim3(32), 0, stream, false, sp.q, R, sp.n_q_heads, Hkv, NT,
+                  k4, frag, inv_f);
   if (e != cudaSuccess) return e;
   e = mark(1);
   if (e != cudaSuccess) return e;
   // 2. block scores
-  if (sp.total_units > 0) {
+  if (sums) {
+    e = launch_sum_scores(sp, stream, false);
+    if (e != cudaSuccess) return e;
+  } else if (sp.total_units > 0) {
     const int tpu = Hkv * (sp.block_cells / 16);
     const size_t frag_bytes = (size_t)Hkv * NT * 8 * 32 * sizeof(uint4);
     ScoresParams spx = sp;

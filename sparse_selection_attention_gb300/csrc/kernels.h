@@ -142,6 +142,13 @@ cudaError_t launch_attn_merge(const MergeParams& p, cudaStream_t stream);
 cudaError_t launch_attn_merge_ex(const MergeParams& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_prompt_attn(const PromptParams& p, cudaStream_t stream);
 cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream);
+// Block summaries (block_sums.cu): (re)writes the summaries of the 64-cell blocks that cells
+// first_cell .. first_cell + n_cells - 1 fall in, each over its cells below first_cell + n_cells;
+// block scores from the summaries when every pool keeps them and block_cells is a multiple of 64.
+cudaError_t launch_summarise(const PoolDev& pool, float* k_sums, int n_kv_heads, int first_cell, int n_cells,
+                             cudaStream_t stream);
+bool block_sums_usable(const ScoresParams& p);
+cudaError_t launch_sum_scores(const ScoresParams& p, cudaStream_t stream, bool pdl);
 cudaError_t read_and_clear_device_error(int32_t* code, cudaStream_t stream);
 // Dense tcgen05 rate (tc_rate.cu): times `passes` x 4 MMAs of M = 128, N = 256 per SM on the
 // legacy default stream; *ms the launch's event time, *ops the operations it performed.

@@ -139,7 +139,7 @@ class LibraryBackend:
         from . import DevicePool
         return DevicePool(pool.k_codes, pool.v_codes, pool.k_scales, pool.v_scales, pool.page_table[first_page:],
                           n_filled=n_cells, capacity=n_cells, page_cells=pool.page_cells, n_kv_heads=pool.n_kv_heads,
-                          v_bits=pool.v_bits, head_dim=pool.head_dim, k_bits=pool.k_bits)
+                          v_bits=pool.v_bits, head_dim=pool.head_dim, k_bits=pool.k_bits, k_sums=pool.k_sums)
 
     def block_scores(self, views, row_pool, q, block_cells: int, local_blocks: int):
         from . import block_scores

@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_pure_host_calls(lib):
-    assert qsa.abi_version() == 107
+    assert qsa.abi_version() == 108
     assert qsa.status_str(qsa.QSA_ERR_SCRATCH) == "scratch buffer too small"
     assert qsa.decode_partials_bytes(5, 24, 64) == 4 * 5 * 24 * 64 * 130
     # o starts at the next 256-byte boundary after the (m, l) pairs, whatever their count
@@ -49,7 +49,7 @@ def test_pure_host_calls(lib):
 
 def _pool(**kw):
     base = dict(k_codes=16, v_codes=32, k_scales=48, v_scales=64, page_table=80, n_filled=100, capacity=256,
-                page_cells=256, n_kv_heads=4, head_dim=128, v_bits=8, k_bits=8)
+                page_cells=256, n_kv_heads=4, head_dim=128, v_bits=8, k_bits=8, k_sums=None)
     base.update(kw)
     return qsa.QsaPoolC(*[base[f] for f, _ in qsa.QsaPoolC._fields_])
 

@@ -327,6 +327,26 @@ def test_prompt_row_blocks_and_head_subsets_match_single_rows():
                 assert np.all(out[r, g] == 0.0) and lse[r, g] == -np.inf
 
 
+@pytest.mark.parametrize("B", [64, 128])
+def test_block_scores_from_block_summaries(B):
+    """R3 is linear in K: the block score equals qbar . (the block's summed K rows) / (n_b sqrt(D)),
+    summed over KV heads, with the block's 64-cell summaries added; a summary that dropped a scale or
+    a cell, or a block score that dropped 1/n_b, fails it."""
+    case = _small_case(fill=700)
+    pool = case.pools[0]
+    S = O.block_scores(pool, case.q, B)
+    sums = O.block_summaries(pool, 64)
+    Hq, Hkv = case.q.shape[1], pool.n_kv_heads
+    G = Hq // Hkv
+    for t in range(case.q.shape[0]):
+        for b in range(S.shape[1]):
+            n_b = min(B, pool.n_filled - b * B)
+            kb = sums[b * B // 64:(b * B + n_b + 63) // 64].sum(axis=0)          # [Hkv, D]
+            qbar = case.q[t].astype(np.float64).reshape(Hkv, G, -1).sum(axis=1)  # [Hkv, D]
+            v = float((qbar * kb).sum()) / (n_b * np.sqrt(128.0))
+            assert abs(v - S[t, b]) <= 1e-12 * max(1.0, abs(S[t, b]))
+
+
 def test_stale_cells_are_never_read():
     """Cells past the fill carry NaN scales; the whole decode chain stays finite."""
     case = _small_case(fill=700)
