@@ -15,8 +15,10 @@ from sparse_selection_attention_gb300 import sharded
 pytestmark = pytest.mark.gpu
 
 
-def run_sharded(case, world):
+def run_sharded(case, world, block_sums=False):
     pools = [qsa.DevicePool.upload(p) for p in case.pools]
+    if block_sums:
+        pools = [p.keep_block_sums() for p in pools]
     q = torch.from_numpy(case.q).cuda()
     row_pos = torch.from_numpy(case.row_pos).cuda()
     be = sharded.LibraryBackend()
@@ -27,8 +29,8 @@ def run_sharded(case, world):
     return be.last_scores.cpu().numpy(), ids.cpu().numpy(), n_sel.cpu().numpy(), out.cpu().numpy(), lse.cpu().numpy()
 
 
-def check(case, world):
-    scores, ids, n_sel, out, lse = run_sharded(case, world)
+def check(case, world, block_sums=False):
+    scores, ids, n_sel, out, lse = run_sharded(case, world, block_sums)
     ref = O.decode_window(case, scores_f32=scores)
     for t in range(case.n_rows):
         nb = len(ref["scores"][t])
@@ -59,3 +61,8 @@ def test_q4_0_sharded():
                          n_kv_heads=2, k_cells=512, chunk_cells=64, page_cells=128, bias_prob=0.05, v_bits=4,
                          k_bits=4)
     check(case, 3)
+
+
+def test_sharded_with_block_summaries():
+    """Rank views keep the pools' block summaries: the ranks score their blocks from them."""
+    check(W.batched_long_context(), 3, block_sums=True)
