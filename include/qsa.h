@@ -247,6 +247,29 @@ qsa_status qsa_decode_window(const qsa_pool* pools, int n_pools, const int32_t* 
                              void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * qsa_decode_window_host -- qsa_decode_window whose per-step inputs and
+ * results live in page-locked host memory: q, row_pos, out and lse (when not
+ * NULL) are host pointers from cudaHostAlloc / cudaMallocHost or a range
+ * registered with cudaHostRegister, in the layouts of qsa_decode_window.  The
+ * window's first launch reads q and row_pos through the device's mapping of
+ * those pages (on Grace-Blackwell, over the coherent host link) into the
+ * workspace, and the later launches read that copy; the merge writes out and
+ * lse straight into host memory.  No DMA copy is enqueued.  Everything else
+ * (pools, scores, ids, n_sel, workspace) is device memory as for
+ * qsa_decode_window, and the workspace size is the same.  The results are in
+ * host memory once `stream` has completed the call.
+ * Errors: QSA_ERR_ARG, with nothing enqueued, when one of the four host
+ * buffers is not page-locked (pageable memory, device memory or NULL; lse may
+ * be NULL); otherwise as qsa_decode_window.
+ */
+qsa_status qsa_decode_window_host(const qsa_pool* pools, int n_pools, const int32_t* row_pool,
+                                  const float* q, const int32_t* row_pos, int n_rows,
+                                  int n_q_heads, int block_cells, int k_cells, float* scores,
+                                  int max_blocks, int32_t* ids, int32_t* n_sel, float* out,
+                                  float* lse, void* workspace, size_t workspace_bytes,
+                                  void* stream);
+
+/*
  * qsa_decode_window_profile -- qsa_decode_window for measurement: the same
  * five launches (q fragments, block scores, top-k, split attention, merge),
  * each started only after the previous one has finished, with CUDA events

@@ -28,7 +28,7 @@ EXPORTS = [
     "qsa_prompt_attn", "qsa_prompt_scratch_bytes", "qsa_get_device_error", "qsa_set_wait_limit_ns", "qsa_status_str", "qsa_abi_version",
     "qsa_decode_attn_noalloc", "qsa_decode_window", "qsa_decode_window_workspace_bytes",
     "qsa_decode_window_profile", "qsa_kv_append", "qsa_measure_tc_rate", "qsa_ids_in_range",
-    "qsa_attn_merge_shards", "qsa_kv_summarise",
+    "qsa_attn_merge_shards", "qsa_kv_summarise", "qsa_decode_window_host",
 ]
 QSA_TC_KIND_F16, QSA_TC_KIND_I8 = 0, 1
 NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -77,6 +77,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qsa_decode_window.argtypes = [pool_p, i, i32p, p, p, i, i, i, i, p, i, p, p, p, p, p, sz, p]
     lib.qsa_decode_window_profile.argtypes = [pool_p, i, i32p, p, p, i, i, i, i, p, i, p, p, p, p, p, sz, p,
                                               ctypes.POINTER(ctypes.c_float)]
+    lib.qsa_decode_window_host.argtypes = [pool_p, i, i32p, p, p, i, i, i, i, p, i, p, p, p, p, p, sz, p]
     lib.qsa_decode_window_workspace_bytes.argtypes = [i, i, i, i]
     lib.qsa_decode_window_workspace_bytes.restype = sz
     lib.qsa_kv_append.argtypes = [pool_p, p, p, i, i, p]
@@ -93,7 +94,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     for name in ("qsa_block_scores", "qsa_topk", "qsa_decode_attn", "qsa_attn_merge", "qsa_prompt_attn",
                  "qsa_get_device_error", "qsa_abi_version", "qsa_decode_attn_noalloc", "qsa_decode_window",
                  "qsa_decode_window_profile", "qsa_measure_tc_rate", "qsa_ids_in_range", "qsa_attn_merge_shards",
-                 "qsa_kv_summarise"):
+                 "qsa_kv_summarise", "qsa_decode_window_host"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -336,6 +337,19 @@ class DecodeWindow:
     def run_window(self, q: torch.Tensor, row_pos: torch.Tensor, stream=None) -> None:
         """The whole window in one call (qsa_decode_window): scores, ids, n_sel, out and lse."""
         _check(load().qsa_decode_window(*self._window_args(q, row_pos, stream)), "qsa_decode_window")
+
+    def run_window_host(self, q_host: torch.Tensor, row_pos_host: torch.Tensor, out_host: torch.Tensor,
+                        lse_host: Optional[torch.Tensor] = None, stream=None) -> None:
+        """qsa_decode_window_host: the window with q, row_pos, out and lse in page-locked host memory
+        (CPU tensors with pin_memory()); scores, ids and n_sel stay on the device.  The results are in
+        out_host / lse_host once the stream has run the call."""
+        for t in (q_host, row_pos_host, out_host) + ((lse_host,) if lse_host is not None else ()):
+            if t.device.type != "cpu" or not t.is_pinned() or not t.is_contiguous():
+                raise ValueError("run_window_host takes contiguous page-locked CPU tensors")
+        args = list(self._window_args(self.out, self.out, stream))
+        args[3], args[4] = q_host.data_ptr(), row_pos_host.data_ptr()
+        args[13], args[14] = out_host.data_ptr(), (lse_host.data_ptr() if lse_host is not None else None)
+        _check(load().qsa_decode_window_host(*args), "qsa_decode_window_host")
 
     def _window_args(self, q, row_pos, stream):
         if self._ws is None:

@@ -258,7 +258,8 @@ size_t qsa_decode_window_workspace_bytes(int n_rows, int n_q_heads, int n_kv_hea
 static qsa_status decode_window_impl(const qsa_pool* pools, int n_pools, const int32_t* row_pool, const float* q,
                               const int32_t* row_pos, int n_rows, int n_q_heads, int block_cells, int k_cells,
                               float* scores, int max_blocks, int32_t* ids, int32_t* n_sel, float* out, float* lse,
-                              void* workspace, size_t workspace_bytes, void* stream, float* kernel_us) {
+                              void* workspace, size_t workspace_bytes, void* stream, float* kernel_us,
+                              bool host_inputs = false) {
   qsa_status s = check_window(pools, n_pools, row_pool, n_rows, n_q_heads, true);
   if (s != QSA_OK) return s;
   if (!q || !row_pos || !scores || !ids || !n_sel || !out || !workspace) return QSA_ERR_ARG;
@@ -327,6 +328,12 @@ static qsa_status decode_window_impl(const qsa_pool* pools, int n_pools, const i
   ap.out = out;
   ap.lse = lse;
   a.workspace = workspace;
+  if (host_inputs) {   // q and row_pos are staged into the workspace by the window's first launch
+    a.q_src = q;
+    a.pos_src = row_pos;
+    sp.q = ap.q = reinterpret_cast<const float*>(static_cast<uint8_t*>(workspace) + a.layout.q_in);
+    ap.row_pos = reinterpret_cast<const int32_t*>(static_cast<uint8_t*>(workspace) + a.layout.pos_in);
+  }
   if (!kernel_us) return from_cuda(launch_decode_window(a, static_cast<cudaStream_t>(stream)));
   cudaEvent_t ev[6] = {};
   cudaError_t e = cudaSuccess;
@@ -349,6 +356,30 @@ qsa_status qsa_decode_window(const qsa_pool* pools, int n_pools, const int32_t* 
                              void* workspace, size_t workspace_bytes, void* stream) {
   return decode_window_impl(pools, n_pools, row_pool, q, row_pos, n_rows, n_q_heads, block_cells, k_cells, scores,
                             max_blocks, ids, n_sel, out, lse, workspace, workspace_bytes, stream, nullptr);
+}
+
+// The device's alias of a page-locked host buffer, or NULL for anything else.
+static const void* host_alias(const void* ptr) {
+  if (!ptr) return nullptr;
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, ptr) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+
+qsa_status qsa_decode_window_host(const qsa_pool* pools, int n_pools, const int32_t* row_pool, const float* q,
+                                  const int32_t* row_pos, int n_rows, int n_q_heads, int block_cells, int k_cells,
+                                  float* scores, int max_blocks, int32_t* ids, int32_t* n_sel, float* out, float* lse,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  const float* qd = static_cast<const float*>(host_alias(q));
+  const int32_t* pd = static_cast<const int32_t*>(host_alias(row_pos));
+  float* od = static_cast<float*>(const_cast<void*>(host_alias(out)));
+  float* ld = lse ? static_cast<float*>(const_cast<void*>(host_alias(lse))) : nullptr;
+  if (!qd || !pd || !od || (lse && !ld)) return QSA_ERR_ARG;
+  return decode_window_impl(pools, n_pools, row_pool, qd, pd, n_rows, n_q_heads, block_cells, k_cells, scores,
+                            max_blocks, ids, n_sel, od, ld, workspace, workspace_bytes, stream, nullptr, true);
 }
 
 qsa_status qsa_decode_window_profile(const qsa_pool* pools, int n_pools, const int32_t* row_pool, const float* q,
@@ -473,6 +504,6 @@ qsa_status qsa_measure_tc_rate(int kind, int passes, double* ops_per_second) {
   return QSA_OK;
 }
 
-int qsa_abi_version(void) { return 108; }
+int qsa_abi_version(void) { return 109; }
 
 }  // extern "C"

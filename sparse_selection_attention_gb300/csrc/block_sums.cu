@@ -81,6 +81,7 @@ __global__ void __launch_bounds__(32 * QSA_MAX_KV_HEADS) sum_scores_kernel(const
     kb.z += x.z;
     kb.w += x.w;
   }
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // q staged by a preceding launch (else a no-op)
   for (int t = 0; t < R; ++t) {
     if (p.row_pool[t] != pi) continue;
     const float4* qg = reinterpret_cast<const float4*>(p.q + ((size_t)t * p.n_q_heads + (size_t)h * G) * kD) + lane;

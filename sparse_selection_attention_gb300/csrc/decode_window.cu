@@ -57,6 +57,7 @@ __global__ void __launch_bounds__(32) win_qprep_kernel(const float* __restrict__
   const int t = blockIdx.x, h = blockIdx.y, lane = threadIdx.x;
   const int G = n_q_heads / n_kv_heads;
   pdl_trigger();
+  pdl_wait();   // q staged by the preceding launch (a no-op without that dependency)
   float v[4] = {0.f, 0.f, 0.f, 0.f};
   if (t < n_rows) {
     const float* qg = q + ((size_t)t * n_q_heads + (size_t)h * G) * kD + 4 * lane;
@@ -1293,6 +1294,18 @@ int window_split_cells(int n_rows, int n_kv_heads, int k_cells, int n_sm) {
   return (int)sc;
 }
 
+// ------------------------------------------------------------------------------------------ 0
+// Inputs in page-locked host memory: one load of each 16 bytes of q and of the row positions across
+// the host link, stored into the workspace, so that no later launch of the window (the split
+// attention reads q and row_pos in every CTA) waits on the host link.
+__global__ void __launch_bounds__(256) stage_inputs_kernel(const float4* __restrict__ q_src, int n_q4,
+                                                           const int32_t* __restrict__ pos_src, int n_rows,
+                                                           float4* q_dst, int32_t* pos_dst) {
+  pdl_trigger();   // the next launch may start its CTAs; it waits for this grid before reading q
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_q4; i += gridDim.x * blockDim.x) q_dst[i] = q_src[i];
+  if (blockIdx.x == 0 && threadIdx.x < n_rows) pos_dst[threadIdx.x] = pos_src[threadIdx.x];
+}
+
 WindowLayout window_layout(int n_rows, int n_q_heads, int n_kv_heads, int k_cells, int n_sm) {
   WindowLayout L{};
   const int NT = (n_rows + 7) / 8;
@@ -1309,6 +1322,10 @@ WindowLayout window_layout(int n_rows, int n_q_heads, int n_kv_heads, int k_cell
   off = up(off + sizeof(float) * 2 * (size_t)n_rows * n_q_heads * L.n_splits);
   L.part_o = off;
   off = up(off + sizeof(float) * kD * (size_t)n_rows * n_q_heads * L.n_splits);
+  L.q_in = off;   // staged q and row positions (calls with host inputs)
+  off = up(off + sizeof(float) * kD * (size_t)n_rows * n_q_heads);
+  L.pos_in = off;
+  off = up(off + sizeof(int32_t) * (size_t)n_rows);
   L.total = off;
   return L;
 }
@@ -1384,20 +1401,31 @@ cudaError_t launch_decode_window(const WindowArgs& a, cudaStream_t stream, cudaE
   const int n_pairs = R * Hkv;
 
   // 1. q fragments: an ordinary launch, ordered after everything before it on the stream (the
-  //    previous window may still read the workspace).
+  //    previous window may still read the workspace).  With host inputs an ordinary launch first
+  //    stages q and row_pos into the workspace, and the q fragments follow it chained.
   cudaError_t e = mark(0);
   if (e != cudaSuccess) return e;
+  const bool staged = a.q_src != nullptr;
+  if (staged) {
+    const int n_q4 = R * sp.n_q_heads * (kD / 4);
+    const int blocks = (n_q4 + 255) / 256;
+    stage_inputs_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(a.q_src), n_q4, a.pos_src, R,
+                                                    reinterpret_cast<float4*>(ws + a.layout.q_in),
+                                                    reinterpret_cast<int32_t*>(ws + a.layout.pos_in));
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   const int k4 = sp.pools[0].k_bits == 4 ? 1 : 0;   // the pools of a window share k_bits
   const bool sums = block_sums_usable(sp);           // scores from the pools' block summaries: no q prep
   if (!sums)
-    e = launch_ex(win_qprep_kernel, dim3(NT * 8, Hkv), dim3(32), 0, stream, false, sp.q, R, sp.n_q_heads, Hkv, NT,
-                  k4, frag, inv_f);
+    e = launch_ex(win_qprep_kernel, dim3(NT * 8, Hkv), dim3(32), 0, stream, pdl && staged, sp.q, R, sp.n_q_heads, Hkv,
+                  NT, k4, frag, inv_f);
   if (e != cudaSuccess) return e;
   e = mark(1);
   if (e != cudaSuccess) return e;
   // 2. block scores
   if (sums) {
-    e = launch_sum_scores(sp, stream, false);
+    e = launch_sum_scores(sp, stream, pdl && staged);
     if (e != cudaSuccess) return e;
   } else if (sp.total_units > 0) {
     const int tpu = Hkv * (sp.block_cells / 16);

@@ -109,7 +109,7 @@ struct WinAttnParams {
 
 // Byte offsets of the parts of a decode-window workspace.
 struct WindowLayout {
-  size_t frag, inv_f, part_ml, part_o, total;
+  size_t frag, inv_f, part_ml, part_o, q_in, pos_in, total;
   int split_cells, n_splits;
 };
 
@@ -120,6 +120,11 @@ struct WindowArgs {
   WinAttnParams attn;
   WindowLayout layout;
   void* workspace;
+  // Inputs in page-locked host memory (device aliases), staged into the workspace's q_in / pos_in by
+  // the window's first launch; the other launches then read the staged copies.  NULL: q and row_pos
+  // are device memory, read in place.
+  const float* q_src;
+  const int32_t* pos_src;
 };
 
 WindowLayout window_layout(int n_rows, int n_q_heads, int n_kv_heads, int k_cells, int n_sm);

@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_pure_host_calls(lib):
-    assert qsa.abi_version() == 108
+    assert qsa.abi_version() == 109
     assert qsa.status_str(qsa.QSA_ERR_SCRATCH) == "scratch buffer too small"
     assert qsa.decode_partials_bytes(5, 24, 64) == 4 * 5 * 24 * 64 * 130
     # o starts at the next 256-byte boundary after the (m, l) pairs, whatever their count

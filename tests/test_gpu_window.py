@@ -166,3 +166,41 @@ def test_window_refuses_small_workspace():
     with pytest.raises(qsa.QsaError) as e:
         win.run_window(q, row_pos)
     assert e.value.status == qsa.QSA_ERR_SCRATCH
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("sums", [False, True])
+def test_window_with_page_locked_host_buffers(sums):
+    """qsa_decode_window_host (q, row positions, out and lse in page-locked host memory, staged by the
+    window's first launch) gives the device-buffer call's results bit for bit, on a two-pool ragged
+    window, with scores from the codes and from block summaries; pageable host tensors and device
+    tensors in the host slots are refused before anything runs."""
+    case = W.decode_case(name="host", seed=77, fills=[1000, 3333], capacity=4096, rows_per_slot=2, n_q_heads=12,
+                         n_kv_heads=2, k_cells=512, chunk_cells=64)
+    dev = torch.device("cuda")
+    pools = [qsa.DevicePool.upload(p, dev) for p in case.pools]
+    if sums:
+        pools = [p.keep_block_sums() for p in pools]
+    win = qsa.DecodeWindow(pools, case.row_pool, case.n_q_heads, case.block_cells, case.k_cells, case.chunk_cells,
+                           case.n_chunks)
+    q = torch.from_numpy(case.q).to(dev)
+    pos = torch.from_numpy(case.row_pos.astype(np.int32)).to(dev)
+    win.run_window(q, pos)
+    torch.cuda.synchronize()
+    out_d, lse_d, ids_d = win.out.cpu(), win.lse.cpu(), win.ids.cpu()
+    q_h = torch.from_numpy(np.ascontiguousarray(case.q)).pin_memory()
+    pos_h = torch.from_numpy(case.row_pos.astype(np.int32)).pin_memory()
+    out_h = torch.full(tuple(win.out.shape), float("nan")).pin_memory()
+    lse_h = torch.full(tuple(win.lse.shape), float("nan")).pin_memory()
+    win.ids.zero_()
+    win.run_window_host(q_h, pos_h, out_h, lse_h)
+    torch.cuda.synchronize()
+    assert torch.equal(out_h, out_d) and torch.equal(lse_h, lse_d) and torch.equal(win.ids.cpu(), ids_d)
+    # refusals: a pageable q, a device out
+    lib = qsa.load()
+    args = list(win._window_args(win.out, win.out, None))
+    args[3], args[4], args[13], args[14] = torch.from_numpy(np.ascontiguousarray(case.q)).data_ptr(), \
+        pos_h.data_ptr(), out_h.data_ptr(), lse_h.data_ptr()
+    assert lib.qsa_decode_window_host(*args) == qsa.QSA_ERR_ARG
+    args[3], args[13] = q_h.data_ptr(), win.out.data_ptr()
+    assert lib.qsa_decode_window_host(*args) == qsa.QSA_ERR_ARG
