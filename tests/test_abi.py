@@ -169,3 +169,17 @@ def test_tc_rate_validation(lib):
     assert lib.qsa_measure_tc_rate(2, 10, ctypes.byref(r)) == qsa.QSA_ERR_ARG
     assert lib.qsa_measure_tc_rate(qsa.QSA_TC_KIND_I8, 0, ctypes.byref(r)) == qsa.QSA_ERR_ARG
     assert lib.qsa_measure_tc_rate(qsa.QSA_TC_KIND_F16, 10, None) == qsa.QSA_ERR_ARG
+
+
+def test_window_host_refuses_buffers_that_are_not_page_locked(lib):
+    """qsa_decode_window_host takes q, row_pos, out and lse in page-locked host memory only: pageable
+    host arrays (and NULL) are refused with QSA_ERR_ARG before the pools are even looked at."""
+    q = (ctypes.c_float * (2 * 128))()
+    pos = (ctypes.c_int32 * 1)()
+    out = (ctypes.c_float * (2 * 128))()
+    addr = lambda a: ctypes.cast(a, ctypes.c_void_p).value
+    call = lambda qq, pp, oo: lib.qsa_decode_window_host(None, 1, None, qq, pp, 1, 2, 64, 64, None, 1, None, None, oo,
+                                                         None, None, 0, None)
+    assert call(addr(q), addr(pos), addr(out)) == qsa.QSA_ERR_ARG
+    assert call(None, addr(pos), addr(out)) == qsa.QSA_ERR_ARG
+    assert call(addr(q), addr(pos), None) == qsa.QSA_ERR_ARG
