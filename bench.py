@@ -144,6 +144,14 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
+    def slowdown_since(self, n0: int) -> bool:
+        """A hardware, hardware-thermal or software-thermal slowdown in the samples taken since sample n0."""
+        for ln in self.lines[n0:]:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) == 6 and any(v.lower() == "active" for v in parts[2:5]):
+                return True
+        return False
+
     def summary(self):
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
@@ -423,18 +431,27 @@ def run_ours(args):
     bytes_step = a1 + a3
 
     # ---- device-timed steps: one qsa_decode_window call each, events on the launching stream
+    # A run whose clock samples show a hardware or thermal slowdown is taken once more.
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    barrier(ws)
-    torch.cuda.synchronize()
-    for k in range(K):
-        flush_l2()
-        gpu_sleep()   # the GPU idles here, outside the events, while the CPU enqueues the step
-        ev[k][0].record(stream)
-        win.run_window(q, row_pos)
-        ev[k][1].record(stream)
-    torch.cuda.synchronize()
-    barrier(ws)
+    remeasured = False
+    for attempt in range(2):
+        n0 = len(clocks.lines)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        barrier(ws)
+        torch.cuda.synchronize()
+        for k in range(K):
+            flush_l2()
+            gpu_sleep()   # the GPU idles here, outside the events, while the CPU enqueues the step
+            ev[k][0].record(stream)
+            win.run_window(q, row_pos)
+            ev[k][1].record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+        time.sleep(0.05)   # the sampler's last samples of the timed region
+        slow = max_over_ranks(1.0 if clocks.slowdown_since(n0) else 0.0, ws) > 0.0   # the ranks decide together
+        if attempt == 1 or not slow:
+            break
+        remeasured = True
     step_ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
     step_ms = max_over_ranks(step_ms, ws)
     value = bytes_step * ws / (step_ms * 1e-3) / 1e9
@@ -715,7 +732,7 @@ def run_ours(args):
                 "call": "qsa_decode_window_host: q and row positions staged from page-locked host memory by the "
                         "window's first launch, out and lse written back to host memory by its merge"},
         "gpu_launches": 5 * K,
-        "clocks": clocks.summary(),
+        "clocks": dict(clocks.summary(), remeasured_after_slowdown=remeasured),
         other_key: decode_other,
         "decode_block_sums": decode_sums,
         other_key + "_block_sums": decode_other_sums,
