@@ -52,12 +52,12 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int w) {
 // that the A fragments of the codes use.  int8 K: k-step s = 4 grp + sp takes, in lane column
 // group tq = lane % 4, dims 64 grp + 16 tq + 4 sp (inside one 64-dim scale group).  4-bit K
 // (k4): k-step s = 2 gq + j takes dims 32 gq + 8 tq + 4 j (inside one 32-dim scale group).
-__global__ void __launch_bounds__(32) win_qprep_kernel(const float* __restrict__ q, int n_rows, int n_q_heads,
-                                                       int n_kv_heads, int NT, int k4, uint4* frag, float* inv_f) {
-  const int t = blockIdx.x, h = blockIdx.y, lane = threadIdx.x;
+// The fragment of row t and KV head h for this lane (a whole warp calls it): qbar = the sum of the
+// head's q heads (dims 4 lane .. + 3), max |qbar 2^fe| in [64, 128), split into fp16 hi + lo; rows
+// at or past n_rows give zero fragments.
+__device__ __forceinline__ void q_fragment(const float* __restrict__ q, int t, int h, int n_rows, int n_q_heads,
+                                           int n_kv_heads, int NT, int k4, int lane, uint4* frag, float* inv_f) {
   const int G = n_q_heads / n_kv_heads;
-  pdl_trigger();
-  pdl_wait();   // q staged by the preceding launch (a no-op without that dependency)
   float v[4] = {0.f, 0.f, 0.f, 0.f};
   if (t < n_rows) {
     const float* qg = q + ((size_t)t * n_q_heads + (size_t)h * G) * kD + 4 * lane;
@@ -83,6 +83,13 @@ __global__ void __launch_bounds__(32) win_qprep_kernel(const float* __restrict__
   frag[((h * NT + nt) * 8 + s) * 32 + gp * 4 + tqp] = make_uint4(h01, h23, l01, l23);
 }
 
+__global__ void __launch_bounds__(32) win_qprep_kernel(const float* __restrict__ q, int n_rows, int n_q_heads,
+                                                       int n_kv_heads, int NT, int k4, uint4* frag, float* inv_f) {
+  pdl_trigger();
+  pdl_wait();   // q staged by the preceding launch (a no-op without that dependency)
+  q_fragment(q, blockIdx.x, blockIdx.y, n_rows, n_q_heads, n_kv_heads, NT, k4, threadIdx.x, frag, inv_f);
+}
+
 // ------------------------------------------------------------------------------------------ 2
 // One 256-thread CTA per unit (pool, block).  Thread i copies 64 bytes of one cell's K codes (and
 // half 0 its two K scales) into shared memory with cp.async before the kernel waits for step 1, so
@@ -90,6 +97,10 @@ __global__ void __launch_bounds__(32) win_qprep_kernel(const float* __restrict__
 // (KV head, 16-cell m-tile) then take their operands from shared memory.
 constexpr int kScoreThreads = 256;
 constexpr size_t kFragSmemMax = 16384;   // q fragments staged in shared memory up to this size
+// Score CTAs make their own q fragments in windows of up to this many blocks (at most one CTA per
+// SM): the tiny dense window takes 15.6 instead of 17.7 us; at 512 blocks (the verify window) the
+// per-CTA fragment work costs more than the launch it saves (31.8 against 29.7 us).
+constexpr int kOwnFragUnits = 152;
 constexpr int kMaxInvF = 2 * kScoreThreads;   // (row, KV head) factors in shared memory (R * Hkv <= 32 * 16)
 
 // K4: 4-bit K codes (the q4_0 layout): rows of 64 bytes, four scales per cell.
@@ -143,19 +154,27 @@ __global__ void __launch_bounds__(kScoreThreads, 4) win_scores_kernel(const Scor
     cp_async_commit();
   }
   pdl_trigger();
-  pdl_wait();   // q fragments of the preceding launch
-  // The fragments every task reads, copied once into shared memory while the codes are in flight.
+  pdl_wait();   // q fragments (or, with host inputs, q) of the preceding launch
   const bool fsm = p.frag_smem != 0;
-  if (fsm) {
-    for (int i = tid; i < Hkv * NT * 8 * 32; i += kScoreThreads) cp_async16(frag_s + i, frag + i);
-    cp_async_commit();
+  if (p.own_frag) {
+    // Small windows: every CTA makes the q fragments and factors itself, from q, while its codes
+    // are in flight (the values of win_qprep_kernel, without its launch).
+    for (int task = warp; task < NT * 8 * Hkv; task += kScoreThreads / 32)
+      q_fragment(p.q, task / Hkv, task % Hkv, R, p.n_q_heads, Hkv, NT, K4 ? 1 : 0, lane, frag_s, invf_s);
+    cp_async_wait_all();
+  } else {
+    // The fragments every task reads, copied once into shared memory while the codes are in flight.
+    if (fsm) {
+      for (int i = tid; i < Hkv * NT * 8 * 32; i += kScoreThreads) cp_async16(frag_s + i, frag + i);
+      cp_async_commit();
+    }
+    // per-(row, head) factors 2^-fe of the fragments, read while the codes arrive
+    const float invf0 = tid < R * Hkv ? __ldg(inv_f + tid) : 0.f;
+    const float invf1 = tid + kScoreThreads < R * Hkv ? __ldg(inv_f + tid + kScoreThreads) : 0.f;
+    cp_async_wait_all();
+    if (tid < R * Hkv) invf_s[tid] = invf0;
+    if (tid + kScoreThreads < R * Hkv) invf_s[tid + kScoreThreads] = invf1;
   }
-  // per-(row, head) factors 2^-fe of the fragments, read while the codes arrive
-  const float invf0 = tid < R * Hkv ? __ldg(inv_f + tid) : 0.f;
-  const float invf1 = tid + kScoreThreads < R * Hkv ? __ldg(inv_f + tid + kScoreThreads) : 0.f;
-  cp_async_wait_all();
-  if (tid < R * Hkv) invf_s[tid] = invf0;
-  if (tid + kScoreThreads < R * Hkv) invf_s[tid + kScoreThreads] = invf1;
   __syncthreads();
 
   if constexpr (!K4) {
@@ -1417,7 +1436,11 @@ cudaError_t launch_decode_window(const WindowArgs& a, cudaStream_t stream, cudaE
   }
   const int k4 = sp.pools[0].k_bits == 4 ? 1 : 0;   // the pools of a window share k_bits
   const bool sums = block_sums_usable(sp);           // scores from the pools' block summaries: no q prep
-  if (!sums)
+  const size_t frag_bytes = (size_t)Hkv * NT * 8 * 32 * sizeof(uint4);
+  // Windows of at most kOwnFragUnits blocks: the score CTAs make the q fragments themselves (each
+  // reads all of q), which takes the q-preparation launch out of the chain.
+  const bool own_frag = !sums && frag_bytes <= kFragSmemMax && sp.total_units <= kOwnFragUnits;
+  if (!sums && !own_frag)
     e = launch_ex(win_qprep_kernel, dim3(NT * 8, Hkv), dim3(32), 0, stream, pdl && staged, sp.q, R, sp.n_q_heads, Hkv,
                   NT, k4, frag, inv_f);
   if (e != cudaSuccess) return e;
@@ -1429,9 +1452,9 @@ cudaError_t launch_decode_window(const WindowArgs& a, cudaStream_t stream, cudaE
     if (e != cudaSuccess) return e;
   } else if (sp.total_units > 0) {
     const int tpu = Hkv * (sp.block_cells / 16);
-    const size_t frag_bytes = (size_t)Hkv * NT * 8 * 32 * sizeof(uint4);
     ScoresParams spx = sp;
     spx.frag_smem = frag_bytes <= kFragSmemMax;
+    spx.own_frag = own_frag ? 1 : 0;
     const size_t row_bytes = k4 ? kD / 2 + 16 : kD + 8;   // codes + scales of one (head, cell)
     const size_t smem = (size_t)Hkv * sp.block_cells * row_bytes + sizeof(float) * ((size_t)tpu * NT * 8 + kMaxInvF) +
                         (spx.frag_smem ? frag_bytes : 0);
@@ -1443,8 +1466,8 @@ cudaError_t launch_decode_window(const WindowArgs& a, cudaStream_t stream, cudaE
     const Kern kern = k4 ? k4_kerns[NT - 1] : k8_kerns[NT - 1];
     e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
-    e = launch_ex(kern, dim3(sp.total_units), dim3(kScoreThreads), smem, stream, pdl, spx, (const uint4*)frag,
-                  (const float*)inv_f);
+    e = launch_ex(kern, dim3(sp.total_units), dim3(kScoreThreads), smem, stream, own_frag ? pdl && staged : pdl, spx,
+                  (const uint4*)frag, (const float*)inv_f);
     if (e != cudaSuccess) return e;
   }
   e = mark(2);

@@ -13,6 +13,7 @@ struct ScoresParams {
   int n_rows, n_q_heads, n_kv_heads, block_cells, max_blocks;
   int q_rows_per_batch;   // rows of q staged in shared memory at a time
   int frag_smem;          // decode window: 1 when the scores kernel stages the q fragments in shared memory
+  int own_frag;           // decode window: 1 when each scores CTA makes the q fragments itself (small windows)
   const float* q;
   float* scores;
   int* err;               // device error word (bounded waits of the staged kernel)
