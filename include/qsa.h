@@ -213,7 +213,10 @@ qsa_status qsa_attn_merge(const void* partials, const int32_t* n_sel, int n_rows
  * qsa_decode_window -- one whole decode window in one call: block scores ->
  * top-k -> split-KV attention -> log-sum-exp merge (the four steps above),
  * enqueued as five launches chained by programmatic dependent launch on
- * `stream` (q preparation, block scores, top-k, split attention, merge;
+ * `stream` (q preparation, block scores, top-k, split attention, merge; in
+ * windows of at most 152 blocks the block-score launch prepares q itself and
+ * there are four; when the pools keep block summaries the scores come from
+ * them and there are four;
  * "#2806 sycl: decode QSA selection and attention in fewer, shorter
  * launches", Summary: selection and attention of a window in fewer, shorter
  * launches).  scores, ids and n_sel are written exactly as qsa_block_scores
