@@ -274,10 +274,12 @@ qsa_status qsa_decode_window_host(const qsa_pool* pools, int n_pools, const int3
 
 /*
  * qsa_decode_window_profile -- qsa_decode_window for measurement: the same
- * five launches (q fragments, block scores, top-k, split attention, merge),
- * each started only after the previous one has finished, with CUDA events
- * between them.  Synchronises `stream`, then writes the launches' times in
- * microseconds to kernel_us (host, 5 floats).  Outputs as qsa_decode_window.
+ * launches (q fragments, block scores, top-k, split attention, merge), each
+ * started only after the previous one has finished, with CUDA events between
+ * them.  Synchronises `stream`, then writes the five steps' times in
+ * microseconds to kernel_us (host, 5 floats; a step without a launch of its
+ * own, such as the q fragments of a small window, reads about 0).  Outputs as
+ * qsa_decode_window.
  * Errors: as qsa_decode_window; QSA_ERR_ARG when kernel_us is NULL.
  */
 qsa_status qsa_decode_window_profile(const qsa_pool* pools, int n_pools, const int32_t* row_pool,
